@@ -1,0 +1,145 @@
+"""ctypes binding and build step for ``oracle_gemm.c``.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "oracle_gemm.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
+
+_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2}
+GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread"]
+
+_lock = threading.Lock()
+_default = None
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc-compile one oracle source file into a shared library."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp.%d" % os.getpid()
+    subprocess.run(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no GPU needed).  Returns the .so path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, _LIB)
+    return _LIB
+
+
+def _check_storage(x, dtype: str, name: str) -> np.ndarray:
+    x = np.asarray(x)
+    want = np.float32 if dtype == "tf32" else np.uint16
+    if x.dtype != want:
+        raise TypeError(f"{name}: {dtype} storage must be {np.dtype(want).name}, got {x.dtype}")
+    return np.ascontiguousarray(x)
+
+
+class Oracle:
+    """One loaded copy of the oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, dbl, vp, ip = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+        lib.orc_gemm.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, ip, ip, vp, i64, vp, ip]
+        lib.orc_gemm.restype = ip
+        lib.orc_gemm_entries.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, ip, ip, vp, vp, i64,
+                                         vp, vp, ip]
+        lib.orc_gemm_entries.restype = ip
+        lib.orc_decode_array.argtypes = [vp, i64, ip, vp]
+        lib.orc_decode_array.restype = None
+        lib.orc_num_host_threads.argtypes = []
+        lib.orc_num_host_threads.restype = ip
+        self.lib = lib
+        self.path = path
+
+    def host_threads(self) -> int:
+        return int(self.lib.orc_num_host_threads())
+
+    def gemm(self, M, N, K, alpha, A, lda, B, ldb, dtype, relu, with_scale=False, threads=0):
+        """Full D_ref as a (M, N) float64 array (and |alpha|*sum|a||b| if asked).
+
+        ``A``/``B`` are flat or 2-D storage arrays: a(i,k) = A.flat[i*lda + k],
+        b(k,j) = B.flat[k + j*ldb].  bf16/fp16 storage is uint16 bit patterns,
+        tf32 storage is float32.
+        """
+        A = _check_storage(A, dtype, "A")
+        B = _check_storage(B, dtype, "B")
+        if M and K and A.size < (M - 1) * lda + K:
+            raise ValueError("A too small for (M, K, lda)")
+        if N and K and B.size < (N - 1) * ldb + K:
+            raise ValueError("B too small for (K, N, ldb)")
+        Dt = np.zeros((max(N, 0), max(M, 0)), dtype=np.float64)  # column-major (M, N)
+        St = np.zeros_like(Dt) if with_scale else None
+        rc = self.lib.orc_gemm(M, N, K, float(alpha), A.ctypes.data, lda, B.ctypes.data, ldb,
+                               _DTYPE_CODE[dtype], int(bool(relu)), Dt.ctypes.data, max(M, 1),
+                               St.ctypes.data if St is not None else None, int(threads))
+        if rc != 0:
+            raise ValueError(f"orc_gemm failed with {rc}")
+        return (Dt.T, St.T) if with_scale else Dt.T
+
+    def gemm_entries(self, M, N, K, alpha, A, lda, B, ldb, dtype, relu, I, J, threads=0):
+        """D_ref and |alpha|*sum|a||b| at coordinates (I[q], J[q])."""
+        A = _check_storage(A, dtype, "A")
+        B = _check_storage(B, dtype, "B")
+        I = np.ascontiguousarray(I, dtype=np.int64)
+        J = np.ascontiguousarray(J, dtype=np.int64)
+        if I.shape != J.shape:
+            raise ValueError("I and J differ in shape")
+        out = np.zeros(I.shape, dtype=np.float64)
+        scale = np.zeros(I.shape, dtype=np.float64)
+        rc = self.lib.orc_gemm_entries(M, N, K, float(alpha), A.ctypes.data, lda, B.ctypes.data, ldb,
+                                       _DTYPE_CODE[dtype], int(bool(relu)), I.ctypes.data,
+                                       J.ctypes.data, I.size, out.ctypes.data, scale.ctypes.data,
+                                       int(threads))
+        if rc != 0:
+            raise ValueError(f"orc_gemm_entries failed with {rc}")
+        return out, scale
+
+    def decode(self, bits, dtype: str) -> np.ndarray:
+        """The oracle's own decode of storage elements to float64."""
+        x = _check_storage(bits, dtype, "bits")
+        out = np.zeros(x.shape, dtype=np.float64)
+        self.lib.orc_decode_array(x.ctypes.data, x.size, _DTYPE_CODE[dtype], out.ctypes.data)
+        return out
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def host_threads() -> int:
+    return default().host_threads()
+
+
+def gemm(*args, **kw):
+    return default().gemm(*args, **kw)
+
+
+def gemm_entries(*args, **kw):
+    return default().gemm_entries(*args, **kw)
+
+
+def decode(bits, dtype):
+    return default().decode(bits, dtype)

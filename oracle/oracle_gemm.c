@@ -1,0 +1,289 @@
+/*
+ * Oracle for the dense GEMM with a pointwise epilogue, D = epi(alpha * A * B).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * CUDA path is checked against.  Only the tests, the package's smoke check and
+ * the benchmark's CPU-baseline leg may build, load or call it; the library
+ * path never does.  It shares no code, header, table or helper with the CUDA
+ * sources.
+ *
+ * What it computes (for every 0 <= i < M, 0 <= j < N):
+ *   1. decode each operand element exactly from its storage format
+ *      (bf16 / fp16 bit patterns, or fp32 narrowed to tf32);
+ *   2. s = sum_{k=0}^{K-1} a(i,k) * b(k,j), in double, k ascending
+ *      ("Matrix Multiplication", Step 3 "Looping over K": C[i,j] is the sum
+ *      over k of A[i,k]*B[k,j]; accumulate wider than the inputs);
+ *   3. y = alpha * s  ("Walk through GEMM", section 5 "Apply the epilogue":
+ *      alpha is applied first ...);
+ *   4. if ReLU: y = max(y, 0) with Julia's max semantics (... then the max
+ *      with zero): NaN stays NaN, -0 becomes +0;
+ *   5. D_ref[i + j*ldd] = y, as double.
+ *
+ * Storage ("Walk through GEMM", section 2 "Bind runtime global arrays"):
+ *   A logical (M,K), K-contiguous:  a(i,k) = A[i*lda + k]
+ *   B logical (K,N), K-contiguous:  b(k,j) = B[k + j*ldb]
+ * Elements outside k < K, i < M, j < N (stride padding) are never read.
+ *
+ * The multithreaded entry splits output columns j over threads; every
+ * element's summation order is the same whatever the thread count.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread.
+ * -ffp-contract=off keeps s += a*b as a rounded product and a rounded add
+ * (no fused multiply-add), so the result is the same on every host.
+ */
+#define _GNU_SOURCE
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* Operand storage formats understood by the oracle. */
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_TF32 = 2 };
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double orc_decode_bf16(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 7) & 0xFF;
+    int f = h & 0x7F;
+    double v;
+    if (e == 0xFF) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, -126 - 7);            /* subnormal: 0.f * 2^-126 */
+    } else {
+        v = ldexp((double)(128 + f), e - 127 - 7); /* 1.f * 2^(e-127) */
+    }
+    return s ? -v : v;
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_decode_fp16(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0x1F) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, -14 - 10);
+    } else {
+        v = ldexp((double)(1024 + f), e - 15 - 10);
+    }
+    return s ? -v : v;
+}
+
+/*
+ * fp32 -> tf32 narrowing ("Matrix Multiplication", Step 4 "Using the tensor
+ * cores": TFloat32 keeps fp32's sign and 8-bit exponent and a 10-bit
+ * fraction).  The conversion rounds the 24-bit significand to 11 bits, to
+ * nearest with ties away from zero (the usual fp32->tf32 conversion), keeping
+ * the exponent range; a value whose rounded magnitude exceeds the largest
+ * finite tf32, (2 - 2^-10) * 2^127, becomes infinity.  Inf and NaN pass
+ * through.  Works on the magnitude as an integer significand times a power of
+ * two, which covers subnormals with the same rounding position.
+ */
+double orc_decode_tf32(uint32_t u) {
+    int s = (u >> 31) & 1;
+    int e = (u >> 23) & 0xFF;
+    uint32_t f = u & 0x7FFFFF;
+    double v;
+    if (e == 0xFF) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        uint32_t sig = (e == 0) ? f : (f | 0x800000u); /* value = sig * 2^(ee-23) */
+        int ee = (e == 0) ? -126 : e - 127;
+        uint32_t q = sig >> 13;           /* kept: 11 (or fewer) leading bits */
+        uint32_t r = sig & 0x1FFFu;       /* dropped: 13 bits */
+        if (r >= 0x1000u) q += 1;         /* half or more: away from zero */
+        v = ldexp((double)q, ee - 23 + 13);
+        if (v > ldexp(2047.0, 127 - 10)) v = INFINITY;
+    }
+    return s ? -v : v;
+}
+
+static double decode_elem(const void *base, int64_t idx, int dtype) {
+    switch (dtype) {
+    case ORC_BF16: return orc_decode_bf16(((const uint16_t *)base)[idx]);
+    case ORC_FP16: return orc_decode_fp16(((const uint16_t *)base)[idx]);
+    default: {
+        uint32_t u;
+        memcpy(&u, (const unsigned char *)base + 4 * idx, 4);
+        return orc_decode_tf32(u);
+    }
+    }
+}
+
+/* Julia's max(y, 0): NaN propagates; -0 and negatives give +0. */
+static double relu_max(double y) {
+    if (isnan(y)) return y;
+    return (y > 0.0) ? y : 0.0;
+}
+
+static double epilogue(double alpha, double s, int relu) {
+    double y = alpha * s;
+    return relu ? relu_max(y) : y;
+}
+
+int orc_num_host_threads(void) {
+    cpu_set_t set;
+    if (sched_getaffinity(0, sizeof(set), &set) == 0) {
+        int c = CPU_COUNT(&set);
+        if (c > 0) return c;
+    }
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* ---------------- full product over decoded operands ---------------- */
+
+typedef struct {
+    int64_t M, N, K;
+    double alpha;
+    int relu;
+    const double *Ad; /* decoded A, (M, K) row-major */
+    const double *Bd; /* decoded B, (N, K) row-major: Bd[j*K + k] = b(k,j) */
+    double *D;
+    int64_t ldd;
+    double *scale;    /* optional |alpha| * sum_k |a||b| */
+    int64_t j0, j1;
+} full_job;
+
+static void *full_worker(void *p) {
+    full_job *jb = (full_job *)p;
+    for (int64_t j = jb->j0; j < jb->j1; ++j) {
+        const double *bj = jb->Bd + j * jb->K;
+        for (int64_t i = 0; i < jb->M; ++i) {
+            const double *ai = jb->Ad + i * jb->K;
+            double s = 0.0;
+            for (int64_t k = 0; k < jb->K; ++k) s += ai[k] * bj[k];
+            jb->D[i + j * jb->ldd] = epilogue(jb->alpha, s, jb->relu);
+            if (jb->scale) {
+                double t = 0.0;
+                for (int64_t k = 0; k < jb->K; ++k) t += fabs(ai[k]) * fabs(bj[k]);
+                jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;
+            }
+        }
+    }
+    return NULL;
+}
+
+/*
+ * D_ref (double, element (i,j) at D[i + j*ldd]) for the whole M x N output.
+ * Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
+ */
+int orc_gemm(int64_t M, int64_t N, int64_t K, double alpha,
+             const void *A, int64_t lda, const void *B, int64_t ldb,
+             int dtype, int relu, double *D, int64_t ldd, double *scale,
+             int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldd < M) return -1;
+    if (dtype < ORC_BF16 || dtype > ORC_TF32) return -1;
+    if (M == 0 || N == 0) return 0;
+    double *Ad = (double *)malloc(sizeof(double) * (size_t)(M * (K ? K : 1)));
+    double *Bd = (double *)malloc(sizeof(double) * (size_t)(N * (K ? K : 1)));
+    if (!Ad || !Bd) { free(Ad); free(Bd); return -2; }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t k = 0; k < K; ++k) Ad[i * K + k] = decode_elem(A, i * lda + k, dtype);
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode_elem(B, k + j * ldb, dtype);
+
+    if (nthreads <= 0) nthreads = orc_num_host_threads();
+    if (nthreads > N) nthreads = (int)N;
+    full_job *jobs = (full_job *)calloc((size_t)nthreads, sizeof(full_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(Ad); free(Bd); free(jobs); free(tids); return -2; }
+    for (int t = 0; t < nthreads; ++t) {
+        full_job *jb = &jobs[t];
+        jb->M = M; jb->N = N; jb->K = K; jb->alpha = alpha; jb->relu = relu;
+        jb->Ad = Ad; jb->Bd = Bd; jb->D = D; jb->ldd = ldd; jb->scale = scale;
+        jb->j0 = N * t / nthreads;
+        jb->j1 = N * (t + 1) / nthreads;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, full_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    full_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+    /* Columns whose thread could not start are done here. */
+    for (int t = started + 1; t < nthreads; ++t) full_worker(&jobs[t]);
+    free(jobs); free(tids); free(Ad); free(Bd);
+    return 0;
+}
+
+/* ---------------- selected entries, decoded on the fly ---------------- */
+
+typedef struct {
+    int64_t K;
+    double alpha;
+    int relu, dtype;
+    const void *A, *B;
+    int64_t lda, ldb;
+    const int64_t *I, *J;
+    double *out, *scale;
+    int64_t p0, p1;
+} entry_job;
+
+static void *entry_worker(void *p) {
+    entry_job *jb = (entry_job *)p;
+    for (int64_t q = jb->p0; q < jb->p1; ++q) {
+        int64_t i = jb->I[q], j = jb->J[q];
+        double s = 0.0, t = 0.0;
+        for (int64_t k = 0; k < jb->K; ++k) {
+            double a = decode_elem(jb->A, i * jb->lda + k, jb->dtype);
+            double b = decode_elem(jb->B, k + j * jb->ldb, jb->dtype);
+            s += a * b;
+            t += fabs(a) * fabs(b);
+        }
+        jb->out[q] = epilogue(jb->alpha, s, jb->relu);
+        if (jb->scale) jb->scale[q] = fabs(jb->alpha) * t;
+    }
+    return NULL;
+}
+
+/*
+ * D_ref at the listed coordinates (I[q], J[q]), q < count, into out[q];
+ * the same arithmetic as orc_gemm, one element at a time.  Coordinates must
+ * satisfy 0 <= I < M and 0 <= J < N (checked).
+ */
+int orc_gemm_entries(int64_t M, int64_t N, int64_t K, double alpha,
+                     const void *A, int64_t lda, const void *B, int64_t ldb,
+                     int dtype, int relu, const int64_t *I, const int64_t *J,
+                     int64_t count, double *out, double *scale, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || count < 0) return -1;
+    if (dtype < ORC_BF16 || dtype > ORC_TF32) return -1;
+    for (int64_t q = 0; q < count; ++q)
+        if (I[q] < 0 || I[q] >= M || J[q] < 0 || J[q] >= N) return -1;
+    if (count == 0) return 0;
+    if (nthreads <= 0) nthreads = orc_num_host_threads();
+    if (nthreads > count) nthreads = (int)count;
+    entry_job *jobs = (entry_job *)calloc((size_t)nthreads, sizeof(entry_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -2; }
+    for (int t = 0; t < nthreads; ++t) {
+        entry_job *jb = &jobs[t];
+        jb->K = K; jb->alpha = alpha; jb->relu = relu; jb->dtype = dtype;
+        jb->A = A; jb->B = B; jb->lda = lda; jb->ldb = ldb;
+        jb->I = I; jb->J = J; jb->out = out; jb->scale = scale;
+        jb->p0 = count * t / nthreads;
+        jb->p1 = count * (t + 1) / nthreads;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, entry_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    entry_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t) entry_worker(&jobs[t]);
+    free(jobs); free(tids);
+    return 0;
+}
+
+/* Decode a whole array of storage elements (for the decode pins). */
+void orc_decode_array(const void *src, int64_t n, int dtype, double *dst) {
+    for (int64_t q = 0; q < n; ++q) dst[q] = decode_elem(src, q, dtype);
+}

@@ -1,0 +1,227 @@
+"""Seeded synthetic operands for the dense GEMM workloads.
+
+This module is shared by the tests, the benchmark and the oracle's callers.
+It only makes input bytes: it holds none of the GEMM's arithmetic (no
+products, sums, scaling or epilogue).  Both the CUDA path and the oracle read
+the very same buffers, so parity never depends on how a value was drawn.
+
+Generator (defined here, not taken from any library so that it is the same
+on every machine and every numpy version):
+
+* ``splitmix64``: the 64-bit mixing function of Steele, Lea and Flood's
+  SplitMix generator ("Fast splittable pseudorandom number generators",
+  OOPSLA 2014): ``z = x + 0x9E3779B97F4A7C15; z = (z ^ z>>30) * 0xBF58476D1CE4E5B9;
+  z = (z ^ z>>27) * 0x94D049BB133111EB; z ^ z>>31``.
+* Element ``n`` of stream ``s`` under seed ``seed`` is
+  ``splitmix64(key(seed, s) + n * 0x9E3779B97F4A7C15)`` with
+  ``key(seed, s) = splitmix64(seed * 2**20 + s)``; it is counter-based, so any
+  element can be regenerated on its own.
+* A uniform in [0, 1) takes the top 24 bits: ``(x >> 40) * 2**-24`` (exact in
+  float32).  ``[lo, hi)`` maps by ``lo + (hi - lo) * u`` in float64 then
+  rounds to float32 (exact for [-1, 1) and [0, 1)).
+* A standard normal uses Box-Muller on two uniforms of one element:
+  ``u1`` from counter ``2n``, ``u2`` from ``2n + 1``,
+  ``sqrt(-2 ln(1 - u1)) * cos(2 pi u2)`` in float64, then float32.
+
+Operands are "rounded to BF16/FP16" from float32 by IEEE round to nearest,
+ties to even.  TF32 workloads keep float32 storage; the narrowing is the
+method's own step and happens inside the GEMM, not here.
+
+Storage follows the GEMM's conventions (Walk through GEMM, section 2 "Bind
+runtime global arrays"): A is logically (M, K) and K-contiguous with leading
+stride ``lda`` (numpy array of shape (M, lda)); B is logically (K, N) and
+K-contiguous with ``ldb`` (numpy shape (N, ldb)); D is (M, N) M-contiguous
+with ``ldc`` (numpy shape (N, ldc)).  Stride padding is filled with a NaN
+sentinel so that a kernel reading it shows up at once.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# NaN sentinels written into stride padding (quiet NaNs of each storage type).
+PAD_BF16 = 0x7FC1
+PAD_FP16 = 0x7E01
+PAD_F32_BITS = 0x7FC00001
+
+STREAM_A = 0
+STREAM_B = 1
+
+
+def splitmix64(x: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    with np.errstate(over="ignore"):
+        z = (x + _GAMMA).astype(np.uint64)
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        return z ^ (z >> np.uint64(31))
+
+
+def _stream_key(seed: int, stream: int) -> np.uint64:
+    base = np.array([(int(seed) << 20) + int(stream)], dtype=np.uint64)
+    return splitmix64(base)[0]
+
+
+def raw_u64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Counter-based 64-bit draws ``start .. start+count-1`` of one stream."""
+    key = _stream_key(seed, stream)
+    n = np.arange(start, start + count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return splitmix64(key + n * _GAMMA)
+
+
+def uniform01(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Uniform float64 values on the 2**-24 grid of [0, 1)."""
+    x = raw_u64(seed, stream, start, count)
+    return (x >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
+
+
+def uniform_f32(seed: int, stream: int, count: int, lo: float, hi: float) -> np.ndarray:
+    u = uniform01(seed, stream, 0, count)
+    return (lo + (hi - lo) * u).astype(np.float32)
+
+
+def normal_f32(seed: int, stream: int, count: int, scale: float = 1.0) -> np.ndarray:
+    u = uniform01(seed, stream, 0, 2 * count)
+    u1 = u[0::2]
+    u2 = u[1::2]
+    z = np.sqrt(-2.0 * np.log1p(-u1)) * np.cos((2.0 * np.pi) * u2)
+    return (z * scale).astype(np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """IEEE round-to-nearest-even float32 -> bfloat16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+    r[nan] = ((u[nan] >> 16) | 0x40).astype(np.uint16)
+    return r
+
+
+def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
+    """IEEE round-to-nearest-even float32 -> binary16 bit patterns."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+DTYPES = ("bf16", "fp16", "tf32")
+
+
+def element_bytes(dtype: str) -> int:
+    return {"bf16": 2, "fp16": 2, "tf32": 4}[dtype]
+
+
+def storage_numpy_dtype(dtype: str):
+    return {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32}[dtype]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One GEMM problem: shapes, strides, operand type, scalars and the
+    distribution its entries are drawn from."""
+
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: str
+    alpha: float
+    relu: bool
+    seed: int
+    dist: str  # "uniform" or "normal"
+    lo: float = -1.0
+    hi: float = 1.0
+    scale: float = 1.0
+    lda: int | None = None
+    ldb: int | None = None
+    ldc: int | None = None
+
+    @property
+    def strides(self):
+        return (self.lda or max(self.K, 1), self.ldb or max(self.K, 1), self.ldc or max(self.M, 1))
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> float:
+        e = element_bytes(self.dtype)
+        return float((self.M * self.K + self.K * self.N) * e + 4 * self.M * self.N)
+
+
+# The problems the pages and their configurations fix.
+WORKLOADS = {
+    # Walk through GEMM example run 65 x 97 x 73 (bounded edge tiles, TMA-illegal strides).
+    "c1_bf16_65x97x73": Workload("c1_bf16_65x97x73", 65, 97, 73, "bf16", 1.5, True, 0, "uniform", -1.0, 1.0),
+    # cuTile tutorial step-3/4 shape, FP32 operands narrowed to TF32.
+    "c2_tf32_256x128x512": Workload("c2_tf32_256x128x512", 256, 128, 512, "tf32", 1.0, False, 1, "uniform", 0.0, 1.0),
+    "c3_fp16_4096": Workload("c3_fp16_4096", 4096, 4096, 4096, "fp16", 0.5, True, 2, "normal", scale=0.1),
+    "c4_bf16_8192": Workload("c4_bf16_8192", 8192, 8192, 8192, "bf16", 1.0, True, 3, "normal"),
+    "c5a_bf16_16384x64x4096": Workload("c5a_bf16_16384x64x4096", 16384, 64, 4096, "bf16", 1.0, True, 4, "uniform",
+                                       lda=4104, ldb=4104, ldc=16392),
+    "c5b_bf16_64x16384x4096": Workload("c5b_bf16_64x16384x4096", 64, 16384, 4096, "bf16", 1.0, True, 4, "uniform",
+                                       lda=4104, ldb=4104, ldc=72),
+    "c5c_bf16_8191x4097x1000": Workload("c5c_bf16_8191x4097x1000", 8191, 4097, 1000, "bf16", 1.0, True, 4, "uniform",
+                                        lda=1008, ldb=1008, ldc=8199),
+}
+
+
+def _draw(w: Workload, stream: int, count: int) -> np.ndarray:
+    if w.dist == "uniform":
+        return uniform_f32(w.seed, stream, count, w.lo, w.hi)
+    if w.dist == "normal":
+        return normal_f32(w.seed, stream, count, w.scale)
+    raise ValueError(w.dist)
+
+
+def _to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x32)
+    if dtype == "fp16":
+        return f32_to_fp16_bits(x32)
+    if dtype == "tf32":
+        return np.ascontiguousarray(x32, dtype=np.float32)
+    raise ValueError(dtype)
+
+
+def pad_value(dtype: str):
+    if dtype == "bf16":
+        return np.uint16(PAD_BF16)
+    if dtype == "fp16":
+        return np.uint16(PAD_FP16)
+    return np.array([PAD_F32_BITS], dtype=np.uint32).view(np.float32)[0]
+
+
+def make_operands(w: Workload):
+    """Return (A, B) storage arrays for workload ``w``.
+
+    A has shape (M, lda): row i holds A[i, 0:K] then NaN padding.
+    B has shape (N, ldb): row j holds B[0:K, j] then NaN padding.
+    A's logical entries use stream 0 in row-major (i, k) order, B's use
+    stream 1 in (j, k) order.
+    """
+    lda, ldb, _ = w.strides
+    A = np.full((w.M, lda), pad_value(w.dtype), dtype=storage_numpy_dtype(w.dtype))
+    B = np.full((w.N, ldb), pad_value(w.dtype), dtype=storage_numpy_dtype(w.dtype))
+    if w.M * w.K:
+        A[:, : w.K] = _to_storage(_draw(w, STREAM_A, w.M * w.K), w.dtype).reshape(w.M, w.K)
+    if w.N * w.K:
+        B[:, : w.K] = _to_storage(_draw(w, STREAM_B, w.N * w.K), w.dtype).reshape(w.N, w.K)
+    return A, B
+
+
+def make_output(w: Workload, fill_bits: int = 0x7FC00002) -> np.ndarray:
+    """D storage of shape (N, ldc) filled with a float32 NaN sentinel, so the
+    rows i >= M of each column (stride padding) can be checked untouched."""
+    _, _, ldc = w.strides
+    return np.full((w.N, ldc), fill_bits, dtype=np.uint32).view(np.float32)
+
+
+def with_shape(w: Workload, **kw) -> Workload:
+    return dataclasses.replace(w, **kw)

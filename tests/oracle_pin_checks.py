@@ -1,0 +1,364 @@
+"""Checks that pin the oracle to what the definition and the formats fix.
+
+Each ``check_*`` takes an ``oracle.Oracle`` instance and raises
+``AssertionError`` on a mismatch.  ``test_oracle_pins.py`` runs them on the
+real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle
+with a planted mistake and expects a failure.
+
+None of these checks re-types the oracle's arithmetic: the expected values
+come from closed forms, invariants, hand-worked examples, a second decode
+written from numpy's own float types, and exact rational arithmetic
+(``fractions.Fraction``) on tiny problems.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import seeded_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+
+def bf16_bits_exact(x) -> np.ndarray:
+    """float -> bf16 bits for values known to be exactly representable."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def fp16_bits_exact(x) -> np.ndarray:
+    f = np.asarray(x, dtype=np.float64)
+    h = f.astype(np.float16)
+    assert np.array_equal(h.astype(np.float64), f), "value not exact in fp16"
+    return h.view(np.uint16)
+
+
+def storage_of(x, dtype):
+    if dtype == "bf16":
+        return bf16_bits_exact(x)
+    if dtype == "fp16":
+        return fp16_bits_exact(x)
+    return np.asarray(x, dtype=np.float32)
+
+
+def second_decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Decode via numpy's own float types (independent of the oracle)."""
+    with np.errstate(invalid="ignore"):
+        if dtype == "bf16":
+            return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        if dtype == "fp16":
+            return bits.view(np.float16).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def pack(Alog: np.ndarray, Blog: np.ndarray, dtype: str, lda=None, ldb=None):
+    """Logical A (M,K) and B (K,N) -> K-contiguous storage with strides."""
+    M, K = Alog.shape
+    K2, N = Blog.shape
+    assert K == K2
+    lda = lda or max(K, 1)
+    ldb = ldb or max(K, 1)
+    A = np.full((M, lda), si.pad_value(dtype), dtype=si.storage_numpy_dtype(dtype))
+    B = np.full((N, ldb), si.pad_value(dtype), dtype=si.storage_numpy_dtype(dtype))
+    A[:, :K] = storage_of(Alog, dtype).reshape(M, K)
+    B[:, :K] = storage_of(Blog.T, dtype).reshape(N, K)
+    return A, lda, B, ldb
+
+
+def run(orc, Alog, Blog, dtype, alpha, relu, lda=None, ldb=None, **kw):
+    A, lda, B, ldb = pack(np.asarray(Alog, float), np.asarray(Blog, float), dtype, lda, ldb)
+    M, K = np.asarray(Alog).shape
+    N = np.asarray(Blog).shape[1]
+    return orc.gemm(M, N, K, alpha, A, lda, B, ldb, dtype, relu, **kw)
+
+
+def tf32_reference(x: float) -> float:
+    """fp32 -> tf32 by the reading 'round to nearest, ties away from zero, 10
+    fraction bits, fp32 exponent range', written with frexp and float64
+    arithmetic (a second formulation, not the oracle's integer one)."""
+    if math.isnan(x) or math.isinf(x) or x == 0.0:
+        return x
+    a = abs(x)
+    if a < 2.0 ** -126:          # fp32 subnormal: fixed rounding position
+        unit = 2.0 ** (-126 - 10)
+    else:
+        _, e = math.frexp(a)     # a = m * 2^e, m in [0.5, 1)
+        unit = 2.0 ** (e - 1 - 10)
+    q = a / unit                 # exact: a power-of-two scaling
+    fl = math.floor(q)
+    r = fl + 1 if q - fl >= 0.5 else fl
+    y = r * unit
+    if y > (2.0 - 2.0 ** -10) * 2.0 ** 127:
+        y = math.inf
+    return math.copysign(y, x)
+
+
+# ---------------------------------------------------------------- checks
+
+def check_decode_tables(orc):
+    """All 65 536 bf16 and fp16 patterns against numpy's decode."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dt in ("bf16", "fp16"):
+        got = orc.decode(bits, dt)
+        want = second_decode(bits, dt)
+        nan_g, nan_w = np.isnan(got), np.isnan(want)
+        assert np.array_equal(nan_g, nan_w), dt
+        ok = ~nan_w
+        assert np.array_equal(got[ok], want[ok]), dt
+        assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok])), dt
+
+
+def tf32_probe_patterns(n_random=100_000, seed=11) -> np.ndarray:
+    edge = []
+    for e in (0, 1, 2, 100, 126, 127, 128, 200, 253, 254, 255):
+        for f in (0, 1, 0xFFF, 0x1000, 0x1001, 0x1FFF, 0x2000, 0x3000, 0x7FE000, 0x7FEFFF,
+                  0x7FF000, 0x7FFFFF, 0x400000, 0x401000):
+            for s in (0, 1):
+                edge.append((s << 31) | (e << 23) | f)
+    rnd = si.raw_u64(seed, 0, 0, n_random).astype(np.uint64) & np.uint64(0xFFFFFFFF)
+    return np.concatenate([np.array(edge, dtype=np.uint64), rnd]).astype(np.uint32)
+
+
+def check_tf32_narrowing(orc):
+    pats = tf32_probe_patterns()
+    x = pats.view(np.float32)
+    got = orc.decode(x, "tf32")
+    with np.errstate(invalid="ignore"):
+        x64 = x.astype(np.float64)
+    want = np.array([tf32_reference(float(v)) for v in x64])
+    nan_g, nan_w = np.isnan(got), np.isnan(want)
+    assert np.array_equal(nan_g, nan_w)
+    ok = ~nan_w
+    assert np.array_equal(got[ok], want[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+
+
+def check_golden(orc):
+    with open(os.path.join(GOLDEN, "hand_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        D = run(orc, c["A"], c["B"], c["dtype"], c["alpha"], c["relu"])
+        want = np.array(c["D"], dtype=np.float64)
+        assert D.shape == want.shape, c["name"]
+        assert np.array_equal(D, want), (c["name"], D, want)
+
+
+def check_identity(orc):
+    """A = I (M = K): D = epi(alpha * B) exactly."""
+    rng_vals = si.uniform_f32(21, 0, 7 * 9, -1.0, 1.0)
+    Bq = second_decode(si.f32_to_bf16_bits(rng_vals), "bf16").reshape(7, 9)
+    for alpha, relu in ((1.5, True), (-2.0, True), (0.75, False)):
+        D = run(orc, np.eye(7), Bq, "bf16", alpha, relu)
+        want = alpha * Bq
+        if relu:
+            want = np.where(want > 0, want, 0.0)
+        assert np.array_equal(D, want)
+
+
+def check_permutation(orc):
+    """A a permutation matrix: row i of D is row p(i) of epi(alpha*B)."""
+    p = np.array([3, 0, 4, 1, 2])
+    P = np.zeros((5, 5))
+    P[np.arange(5), p] = 1.0
+    vals = si.uniform_f32(22, 0, 5 * 6, -1.0, 1.0)
+    Bq = second_decode(si.f32_to_bf16_bits(vals), "bf16").reshape(5, 6)
+    D = run(orc, P, Bq, "bf16", 2.0, False)
+    assert np.array_equal(D, 2.0 * Bq[p, :])
+
+
+def rank1_case():
+    u = np.array([1, -3, 2, 5, -1, 7, 4], dtype=float)               # M = 7
+    v = np.array([2, -1, 3, -6, 1], dtype=float)                      # N = 5
+    s = np.array([0.5, -2, 1, 0.25, 4, -0.125, 2, 1, -1, 8, 0.5])    # K = 11
+    t = np.array([2, 0.5, -1, 4, -0.25, 8, 1, -2, 0.5, 0.125, -4])
+    return u, v, s, t
+
+
+def check_rank1(orc):
+    """a(i,k) = u_i s_k, b(k,j) = t_k v_j  =>  D = alpha (s.t) u v^T, exact.
+    M, N, K all differ, so a transposed operand or output fails."""
+    u, v, s, t = rank1_case()
+    Alog, Blog = np.outer(u, s), np.outer(t, v)
+    st = float(np.dot(s, t))
+    for dt in ("bf16", "fp16", "tf32"):
+        for alpha, relu in ((1.0, False), (1.5, True), (-0.5, True)):
+            D, S = run(orc, Alog, Blog, dt, alpha, relu, with_scale=True)
+            want = alpha * st * np.outer(u, v)
+            if relu:
+                want = np.where(want > 0, want, 0.0)
+            assert np.array_equal(D, want), (dt, alpha, relu)
+            scale = abs(alpha) * float(np.dot(np.abs(s), np.abs(t))) * np.outer(np.abs(u), np.abs(v))
+            assert np.array_equal(S, scale)
+
+
+def check_alpha_zero_and_sign(orc):
+    vals = si.uniform_f32(23, 0, 6 * 5, 0.0, 1.0)
+    Apos = second_decode(si.f32_to_bf16_bits(vals), "bf16").reshape(6, 5)
+    vals = si.uniform_f32(23, 1, 5 * 4, 0.0, 1.0)
+    Bneg = -second_decode(si.f32_to_bf16_bits(vals), "bf16").reshape(5, 4)
+    # alpha = 0 gives zeros, with or without the epilogue.
+    for relu in (False, True):
+        D = run(orc, Apos, Bneg, "bf16", 0.0, relu)
+        assert np.all(D == 0.0)
+    # A >= 0, B <= 0, alpha > 0: every product <= 0, ReLU clears all.
+    D = run(orc, Apos, Bneg, "bf16", 1.25, True)
+    assert np.all(D == 0.0) and not np.any(np.signbit(D))
+    Dn = run(orc, Apos, Bneg, "bf16", 1.25, False)
+    assert np.all(Dn < 0.0)
+    # Negative alpha flips which entries survive: relu(alpha*s) = -alpha*|s| here.
+    Dm = run(orc, Apos, Bneg, "bf16", -1.25, True)
+    assert np.all(Dm > 0.0)
+    assert np.array_equal(Dm, -Dn)
+
+
+def exact_product(Alog, Blog, alpha, relu):
+    """Exact rational D (as Fractions) for logical float inputs."""
+    M, K = Alog.shape
+    N = Blog.shape[1]
+    out = [[None] * N for _ in range(M)]
+    fa = Fraction(alpha)
+    for i in range(M):
+        for j in range(N):
+            s = sum((Fraction(Alog[i, k]) * Fraction(Blog[k, j]) for k in range(K)), Fraction(0))
+            y = fa * s
+            if relu and y < 0:
+                y = Fraction(0)
+            out[i][j] = y
+    return out
+
+
+def check_bruteforce_exact(orc):
+    """Tiny shapes on a dyadic grid (entries c/64, |c| <= 64): every double
+    partial sum is exact, so the oracle must equal the exact rational result
+    bit for bit, whatever the order."""
+    for (M, N, K), seed in (((3, 4, 5), 31), ((5, 2, 9), 32), ((1, 7, 16), 33), ((8, 8, 3), 34)):
+        ca = si.raw_u64(seed, 0, 0, M * K) % np.uint64(129)
+        cb = si.raw_u64(seed, 1, 0, K * N) % np.uint64(129)
+        Alog = (ca.astype(np.float64) - 64.0).reshape(M, K) / 64.0
+        Blog = (cb.astype(np.float64) - 64.0).reshape(K, N) / 64.0
+        for dt in ("bf16", "fp16", "tf32"):
+            for alpha, relu in ((1.0, False), (-1.5, True)):
+                D = run(orc, Alog, Blog, dt, alpha, relu)
+                E = exact_product(Alog, Blog, alpha, relu)
+                for i in range(M):
+                    for j in range(N):
+                        assert Fraction(D[i, j]) == E[i][j], (dt, M, N, K, i, j)
+
+
+def check_bruteforce_bound(orc):
+    """Random bf16 in [-1, 1): the double sum is within K * 2^-53 * sum|ab|
+    of the exact sum (the textbook bound for recursive summation)."""
+    M, N, K = 4, 3, 12
+    A = si.f32_to_bf16_bits(si.uniform_f32(41, 0, M * K, -1.0, 1.0)).reshape(M, K)
+    B = si.f32_to_bf16_bits(si.uniform_f32(41, 1, N * K, -1.0, 1.0)).reshape(N, K)
+    Alog = second_decode(A, "bf16")
+    Blog = second_decode(B, "bf16").T
+    D = orc.gemm(M, N, K, 1.0, A, K, B, K, "bf16", False)
+    E = exact_product(Alog, Blog, 1.0, False)
+    for i in range(M):
+        for j in range(N):
+            mag = sum(abs(Fraction(Alog[i, k]) * Fraction(Blog[k, j])) for k in range(K))
+            assert abs(Fraction(D[i, j]) - E[i][j]) <= Fraction(K, 2 ** 53) * mag
+
+
+def check_zero_padding_neutral(orc):
+    """Embedding in a larger K with zero A columns / B rows changes nothing
+    ('Matrix Multiplication', ragged sizes: zero padding is neutral)."""
+    M, N, K, extra = 6, 5, 10, 7
+    A = si.f32_to_bf16_bits(si.uniform_f32(51, 0, M * K, -1.0, 1.0)).reshape(M, K)
+    B = si.f32_to_bf16_bits(si.uniform_f32(51, 1, N * K, -1.0, 1.0)).reshape(N, K)
+    D0 = orc.gemm(M, N, K, 1.5, A, K, B, K, "bf16", True)
+    Az = np.zeros((M, K + extra), np.uint16)
+    Bz = np.zeros((N, K + extra), np.uint16)
+    Az[:, :K] = A
+    Bz[:, :K] = B
+    D1 = orc.gemm(M, N, K + extra, 1.5, Az, K + extra, Bz, K + extra, "bf16", True)
+    assert np.array_equal(D0, D1)
+
+
+def check_strides_and_padding(orc):
+    """lda > K and ldb > K with NaN padding: padding is never read, and the
+    strided result equals the tight one."""
+    w = si.Workload("t", 9, 7, 13, "bf16", 1.0, True, 52, "uniform", lda=21, ldb=16)
+    A, B = si.make_operands(w)
+    D = orc.gemm(9, 7, 13, 1.0, A, 21, B, 16, "bf16", True)
+    assert not np.any(np.isnan(D))
+    D2 = orc.gemm(9, 7, 13, 1.0, np.ascontiguousarray(A[:, :13]), 13,
+                  np.ascontiguousarray(B[:, :13]), 13, "bf16", True)
+    assert np.array_equal(D, D2)
+
+
+def check_relu_special_values(orc):
+    """Julia max semantics: NaN stays NaN, -0 becomes +0."""
+    D = run(orc, [[1.0], [-1.0]], [[0.0, 1.0]], "bf16", 1.0, True)
+    assert np.array_equal(D, [[0.0, 1.0], [0.0, 0.0]])
+    assert not np.any(np.signbit(D))
+    # A zero sum times a negative alpha is -0; the max with zero gives +0.
+    D = run(orc, [[1.0], [2.0]], [[0.0, 0.0]], "bf16", -1.0, True)
+    assert np.array_equal(D, np.zeros((2, 2))) and not np.any(np.signbit(D))
+    Dn = run(orc, [[1.0], [2.0]], [[0.0, 0.0]], "bf16", -1.0, False)
+    assert np.all(np.signbit(Dn))                 # without the epilogue -0 stays
+    A = np.array([[np.nan, 1.0], [1.0, 1.0]], np.float32)
+    Ab = (A.view(np.uint32) >> 16).astype(np.uint16)
+    B = bf16_bits_exact(np.array([[1.0, 1.0], [-1.0, -1.0]]))  # storage row j = column j of B
+    D = orc.gemm(2, 2, 2, 1.0, Ab, 2, B, 2, "bf16", True)
+    assert np.isnan(D[0, 0]) and np.isnan(D[0, 1])
+    assert D[1, 0] == 2.0 and D[1, 1] == 0.0
+
+
+def check_entries_match_full(orc):
+    w = si.Workload("e", 37, 29, 41, "fp16", 0.5, True, 61, "normal", scale=0.1, lda=45, ldb=48)
+    A, B = si.make_operands(w)
+    D, S = orc.gemm(37, 29, 41, 0.5, A, 45, B, 48, "fp16", True, with_scale=True)
+    I = np.array([0, 36, 5, 17, 36, 0])
+    J = np.array([0, 28, 11, 3, 0, 28])
+    v, s = orc.gemm_entries(37, 29, 41, 0.5, A, 45, B, 48, "fp16", True, I, J)
+    assert np.array_equal(v, D[I, J])
+    assert np.array_equal(s, S[I, J])
+
+
+def check_thread_independent(orc):
+    w = si.Workload("t", 33, 17, 50, "bf16", 1.0, False, 62, "uniform")
+    A, B = si.make_operands(w)
+    D1 = orc.gemm(33, 17, 50, 1.0, A, 50, B, 50, "bf16", False, threads=1)
+    D4 = orc.gemm(33, 17, 50, 1.0, A, 50, B, 50, "bf16", False, threads=4)
+    assert np.array_equal(D1, D4)
+
+
+def check_degenerate(orc):
+    A = np.zeros((3, 1), np.uint16)
+    B = np.zeros((4, 1), np.uint16)
+    D = orc.gemm(3, 4, 0, 2.0, A, 1, B, 1, "bf16", True)
+    assert D.shape == (3, 4) and np.all(D == 0.0)
+    assert orc.gemm(0, 4, 5, 1.0, np.zeros(0, np.uint16), 5, np.zeros(20, np.uint16), 5,
+                    "bf16", True).shape == (0, 4)
+    assert orc.gemm(3, 0, 5, 1.0, np.zeros(15, np.uint16), 5, np.zeros(0, np.uint16), 5,
+                    "bf16", True).shape == (3, 0)
+
+
+ALL_CHECKS = [
+    check_decode_tables,
+    check_tf32_narrowing,
+    check_golden,
+    check_identity,
+    check_permutation,
+    check_rank1,
+    check_alpha_zero_and_sign,
+    check_bruteforce_exact,
+    check_bruteforce_bound,
+    check_zero_padding_neutral,
+    check_strides_and_padding,
+    check_relu_special_values,
+    check_entries_match_full,
+    check_thread_independent,
+    check_degenerate,
+]

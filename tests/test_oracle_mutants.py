@@ -1,0 +1,67 @@
+"""Plant a mistake in a copy of the oracle (on the CPU) and show that the pins
+catch it: each mutant must fail at least one check of ``oracle_pin_checks``.
+
+The mutants are the plausible slips: a dropped term, a wrong sign, a wrong
+index or a transposed operand, a wrong exponent bias, a wrong tie rule, the
+epilogue applied in the wrong order, and lost special values.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pin_checks as pins
+
+MUTANTS = {
+    "drop_last_k": ("for (int64_t k = 0; k < jb->K; ++k) s += ai[k] * bj[k];",
+                    "for (int64_t k = 0; k + 1 < jb->K; ++k) s += ai[k] * bj[k];"),
+    "subtract_products": ("for (int64_t k = 0; k < jb->K; ++k) s += ai[k] * bj[k];",
+                          "for (int64_t k = 0; k < jb->K; ++k) s -= ai[k] * bj[k];"),
+    "reversed_k_in_A": ("Ad[i * K + k] = decode_elem(A, i * lda + k, dtype);",
+                        "Ad[i * K + k] = decode_elem(A, i * lda + (K - 1 - k), dtype);"),
+    "wrong_B_column": ("Bd[j * K + k] = decode_elem(B, k + j * ldb, dtype);",
+                       "Bd[j * K + k] = decode_elem(B, k + (N - 1 - j) * ldb, dtype);"),
+    "bf16_bias": ("v = ldexp((double)(128 + f), e - 127 - 7);",
+                  "v = ldexp((double)(128 + f), e - 126 - 7);"),
+    "fp16_subnormal_scale": ("v = ldexp((double)f, -14 - 10);",
+                             "v = ldexp((double)f, -15 - 10);"),
+    "tf32_ties_to_zero": ("if (r >= 0x1000u) q += 1;", "if (r > 0x1000u) q += 1;"),
+    "tf32_truncate": ("if (r >= 0x1000u) q += 1;", "if (0) q += 1;"),
+    "relu_keeps_negative_zero": ("return (y > 0.0) ? y : 0.0;", "return (y >= 0.0) ? y : 0.0;"),
+    "relu_drops_nan": ("if (isnan(y)) return y;", "if (0) return y;"),
+    "relu_before_alpha": ("double y = alpha * s;\n    return relu ? relu_max(y) : y;",
+                          "return relu ? alpha * relu_max(s) : alpha * s;"),
+    "alpha_dropped": ("double y = alpha * s;", "double y = s;"),
+    "scale_signed_alpha": ("jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;",
+                           "jb->scale[i + j * jb->ldd] = jb->alpha * t;"),
+}
+
+
+def _run_checks(orc):
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except AssertionError:
+            failed.append(check.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(oracle.oracle.SOURCE) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    path = tmp_path / f"oracle_{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(path), str(tmp_path / f"lib_{name}.so"))
+    failed = _run_checks(oracle.Oracle(lib))
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    lib = oracle.compile_source(oracle.oracle.SOURCE, str(tmp_path / "lib_ref.so"))
+    assert _run_checks(oracle.Oracle(lib)) == []
+    assert os.path.exists(lib)
