@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""Benchmark: BF16 GEMM + ReLU at M = N = K = 8192 through the tg_gemm C ABI.
+
+One step is one call of the whole path (plan, TMA descriptors, the persistent
+tcgen05 kernel with its fused alpha/ReLU epilogue) over the 8192^3 workload:
+A, B BF16 (seeded standard normal), D FP32 column-major, alpha = 1.  Inputs
+stay resident in HBM; A + B (268 MB) and D (268 MB) are each larger than the
+129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the only other arm), on a bounded sample of the same workload.
+
+Multi-GPU runs (torchrun) are independent replicas: each rank computes the
+full workload on its own GPU with no collective on the data path; the value
+is the FLOPs of all ranks over the slowest rank's time ("weak" scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+WORKLOAD = "c4_bf16_8192"
+METRIC = "bf16 GEMM+ReLU TFLOP/s at 8192³; % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(w: si.Workload, world: int) -> dict:
+    lda, ldb, ldc = w.strides
+    return {
+        "workload": f"{w.name}: M=N=K={w.M} BF16 operands (seeded N(0,1) rounded to BF16), "
+                    f"alpha={w.alpha}, ReLU epilogue, FP32 accumulate, D FP32 column-major",
+        "M": w.M, "N": w.N, "K": w.K, "lda": lda, "ldb": ldb, "ldc": ldc,
+        "l2": "inputs larger than L2 (A+B 268 MB and D 268 MB vs 129 MB L2); no flush",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_sample_time(w: si.Workload, A, B, cols: int, threads: int = 0) -> float:
+    """Wall time of the oracle on the sample D[:, 0:cols] (all rows, full K)."""
+    import oracle
+
+    lda, ldb, _ = w.strides
+    Bs = np.ascontiguousarray(B[:cols])
+    t0 = time.perf_counter()
+    oracle.gemm(w.M, cols, w.K, w.alpha, A, lda, Bs, ldb, w.dtype, w.relu, threads=threads)
+    return time.perf_counter() - t0
+
+
+def calibrate_cols(w, A, B, target_s: float, max_cols: int) -> int:
+    t = oracle_sample_time(w, A, B, 2)
+    per_col = max(t / 2.0, 1e-6)
+    return int(max(2, min(max_cols, target_s / per_col)))
+
+
+def cpu_baseline(w: si.Workload, A, B, target_s: float = 15.0) -> dict:
+    import oracle
+
+    cols = calibrate_cols(w, A, B, target_s, w.N)
+    t = oracle_sample_time(w, A, B, cols)
+    flops = 2.0 * w.M * cols * w.K
+    return {
+        "value": flops / t / 1e12, "unit": UNIT, "cores": oracle.host_threads(), "kind": "oracle",
+        "sample": f"D[:, 0:{cols}] of the {w.M}x{w.N}x{w.K} workload (all rows, full K), "
+                  f"{t:.1f} s wall on the host cores, double-precision C triple loop",
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = si.WORKLOADS[WORKLOAD]
+    A, B = si.make_operands(w)
+    import oracle
+
+    # Size each step so that (warmup + steps) steps end within ~2.5 minutes.
+    per_step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    cols = calibrate_cols(w, A, B, per_step_target, w.N)
+    for _ in range(args.warmup):
+        oracle_sample_time(w, A, B, cols)
+    times = [oracle_sample_time(w, A, B, cols) for _ in range(args.steps)]
+    total = sum(times)
+    flops = 2.0 * w.M * cols * w.K
+    value = flops * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.host_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: D[:, 0:{cols}] of the 8192^3 workload (all rows, "
+                                   f"full K), double-precision C triple loop on the host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = list(csv.reader(io.StringIO(out)))
+        samples = []
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + r[0].strip().split(".")[1]) if "." in r[0] else 0.0
+                samples.append((ts + frac, [x.strip() for x in r]))
+            except (ValueError, IndexError):
+                continue
+        inside = [s for t, s in samples if self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        use = inside or [s for _, s in samples]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(s[2]) for s in use if s[2].replace(".", "").isdigit()]
+        smax = [float(s[3]) for s in use if s[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in use for i in range(4) if s[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside),
+                "power_w_max": max((float(s[4]) for s in use
+                                    if s[4].replace(".", "").isdigit()), default=None)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel_hash: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the kernel as it is now (same source hash); else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(WORKLOAD)
+    if not e or e.get("source_hash") != kernel_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import dense_gemm_epilogue_gb300 as tg
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    tg.build()
+    tg.load()
+    w = si.WORKLOADS[WORKLOAD]
+    lda, ldb, ldc = w.strides
+    A, B = si.make_operands(w)
+    hA = torch.from_numpy(A.view(np.int16)).pin_memory()
+    hB = torch.from_numpy(B.view(np.int16)).pin_memory()
+    dA = hA.cuda()
+    dB = hB.cuda()
+    dD = torch.empty((w.N, ldc), dtype=torch.float32, device="cuda")
+    hD = torch.empty((w.N, ldc), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+    plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, dD, ldc, w.dtype)
+
+    def step():
+        st = tg.tg_gemm(w.M, w.N, w.K, w.alpha, dA, lda, dB, ldb, dD, ldc, w.dtype, w.relu, stream)
+        if st != tg.TG_OK:
+            raise tg.TgError(st, "tg_gemm")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    region0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    barrier()
+    region_ms = region0.elapsed_time(region1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    st, where = tg.tg_check_device_status(stream)
+    if st != tg.TG_OK:
+        raise tg.TgError(st, f"device status (wait site {where})")
+    clocks = sampler.stop() if sampler else None
+
+    # End to end through the public API: pinned host A, B -> device, the
+    # call, D -> pinned host, every step.
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    with torch.cuda.stream(stream):
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        step()
+        hD.copy_(dD, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            step()
+            hD.copy_(dD, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_wall = time.perf_counter() - t_wall0
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    step_ms = region_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([step_ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank == 0:
+        flops = w.flops
+        value = world * flops / (step_ms * 1e-3) / 1e12
+        peaks, peak_src = load_peaks()
+        launch_avg_ms = statistics.fmean(launch_ms)
+        achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        traffic = load_traffic(tg.source_hash())
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": workload_config(w, world),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                         "kernel": "tg_gemm_kernel<BF16, BN=256, TMA>",
+                         "kernel_ms_avg": launch_avg_ms,
+                         "algorithmic_flops_per_launch": flops},
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
+                    "d2h_bytes_per_step": int(w.N * ldc * 4),
+                    "steps": e2e_steps, "wall_s": e2e_wall},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "plan": plan,
+            "library_source_hash": tg.source_hash(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, A, B)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

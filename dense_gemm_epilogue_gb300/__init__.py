@@ -1,0 +1,220 @@
+"""Python binding of the tg_gemm C ABI (``include/tg_gemm.h``).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library
+``_lib/libtg_gemm.so`` built from ``csrc/`` by ``build.py``.  There is no
+fallback: if the library is missing, ``load()`` raises.
+
+Pointers may be given as integers, as objects with ``data_ptr()`` (torch
+tensors) or as None (NULL).  Streams may be integers (a ``cudaStream_t``),
+objects with a ``cuda_stream`` attribute (``torch.cuda.Stream``) or None (the
+legacy default stream).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB as LIBRARY_PATH
+from .build import build, source_hash  # noqa: F401
+
+TG_OK = 0
+TG_ERR_INVALID_VALUE = 1
+TG_ERR_UNSUPPORTED = 2
+TG_ERR_CUDA = 3
+TG_ERR_DEVICE_TIMEOUT = 4
+
+TG_BF16 = 0
+TG_FP16 = 1
+TG_TF32 = 2
+DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32}
+
+TG_EPILOGUE_NONE = 0
+TG_EPILOGUE_RELU = 1
+
+# Every symbol include/tg_gemm.h declares.
+EXPORTED = (
+    "tg_gemm",
+    "tg_gemm_ex",
+    "tg_plan",
+    "tg_status_string",
+    "tg_check_device_status",
+    "tg_set_wait_limit_ns",
+    "tg_selftest_wait_timeout",
+    "tg_version",
+)
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {tg_status_string(status)} ({status})" if what else
+                         f"{tg_status_string(status)} ({status})")
+
+
+class tg_options(ctypes.Structure):
+    _fields_ = [
+        ("block_n", ctypes.c_int32),
+        ("producer", ctypes.c_int32),
+        ("swap_ab", ctypes.c_int32),
+        ("raster_group", ctypes.c_int32),
+        ("max_ctas", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
+    ]
+
+
+class tg_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("block_m", ctypes.c_int32),
+        ("block_n", ctypes.c_int32),
+        ("block_k", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
+        ("producer", ctypes.c_int32),
+        ("swap_ab", ctypes.c_int32),
+        ("raster_group", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("tiles", ctypes.c_int64),
+        ("threads", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32),
+        ("tmem_cols", ctypes.c_int32),
+        ("vector_store", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIBRARY_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"tg_gemm library not built ({p} missing); run "
+                               "dense_gemm_epilogue_gb300.build.build() first")
+        lib = ctypes.CDLL(p)
+        i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+        lib.tg_gemm.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                ctypes.c_int, vp]
+        lib.tg_gemm.restype = ctypes.c_int
+        lib.tg_gemm_ex.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                   ctypes.c_int, ctypes.POINTER(tg_options), vp]
+        lib.tg_gemm_ex.restype = ctypes.c_int
+        lib.tg_plan.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                ctypes.POINTER(tg_options), i32, ctypes.POINTER(tg_plan_info)]
+        lib.tg_plan.restype = ctypes.c_int
+        lib.tg_status_string.argtypes = [ctypes.c_int]
+        lib.tg_status_string.restype = ctypes.c_char_p
+        lib.tg_check_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        lib.tg_check_device_status.restype = ctypes.c_int
+        lib.tg_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.tg_set_wait_limit_ns.restype = ctypes.c_int
+        lib.tg_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.tg_selftest_wait_timeout.restype = ctypes.c_int
+        lib.tg_version.argtypes = []
+        lib.tg_version.restype = i32
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x).__name__} as a pointer")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    raise TypeError(f"cannot pass {type(s).__name__} as a stream")
+
+
+def _dtype(d):
+    return DTYPE_CODES[d] if isinstance(d, str) else int(d)
+
+
+def _epi(e):
+    if isinstance(e, str):
+        return {"none": TG_EPILOGUE_NONE, "relu": TG_EPILOGUE_RELU}[e]
+    if isinstance(e, bool):
+        return TG_EPILOGUE_RELU if e else TG_EPILOGUE_NONE
+    return int(e)
+
+
+def _options(opts):
+    if opts is None:
+        return None
+    if isinstance(opts, tg_options):
+        return ctypes.byref(opts)
+    o = tg_options()
+    for k, v in dict(opts).items():
+        if k == "reserved":
+            for i, r in enumerate(v):
+                o.reserved[i] = r
+        else:
+            setattr(o, k, int(v))
+    return ctypes.byref(o)
+
+
+def tg_gemm(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, stream=None) -> int:
+    """D = epi(alpha * A * B); returns the tg_status code (enqueue only)."""
+    return load().tg_gemm(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
+                          _dtype(in_dtype), _epi(epilogue), _stream(stream))
+
+
+def tg_gemm_ex(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, opts=None,
+               stream=None) -> int:
+    """tg_gemm with planner overrides (dict of tg_options fields)."""
+    return load().tg_gemm_ex(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
+                             _dtype(in_dtype), _epi(epilogue), _options(opts), _stream(stream))
+
+
+def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):
+    """The planner's choice as a dict; raises TgError on invalid arguments."""
+    info = tg_plan_info()
+    st = load().tg_plan(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc, _dtype(in_dtype),
+                        _options(opts), num_sms, ctypes.byref(info))
+    if st != TG_OK:
+        raise TgError(st, "tg_plan")
+    return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
+
+
+def tg_status_string(status: int) -> str:
+    return load().tg_status_string(int(status)).decode()
+
+
+def tg_check_device_status(stream=None):
+    """(status, where): synchronises the stream and reads/clears the status word."""
+    where = ctypes.c_int32(0)
+    st = load().tg_check_device_status(_stream(stream), ctypes.byref(where))
+    return st, where.value
+
+
+def tg_set_wait_limit_ns(ns: int) -> int:
+    return load().tg_set_wait_limit_ns(int(ns))
+
+
+def tg_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return load().tg_selftest_wait_timeout(int(limit_ns), _stream(stream))
+
+
+def tg_version() -> int:
+    return load().tg_version()
+
+
+def check(status: int, what: str = "tg_gemm") -> None:
+    if status != TG_OK:
+        raise TgError(status, what)

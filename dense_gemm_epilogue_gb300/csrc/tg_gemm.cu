@@ -1,0 +1,441 @@
+// C-ABI front end of tg_gemm: argument validation, the host planner, TMA
+// tensor-map encoding, per-device state and kernel launch.
+//
+// The planner follows "Walk through GEMM" section 1 "Choose the work and the
+// storage separately": the host picks a compiled tile configuration from the
+// problem's shape, while dimensions and leading strides stay runtime kernel
+// arguments.  Host validation mirrors section 3 "Copy one K stage" (the host
+// checks layouts; the caller is responsible for allocation bounds).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tg_gemm.h"
+#include "tg_launch.h"
+
+namespace tg {
+
+// D = epi(alpha * 0) over the M x N output: the K == 0 case (empty sums).
+__global__ void tg_fill_empty_sum_kernel(float *d, int64_t m, int64_t n, int64_t ldc, float alpha,
+                                         int relu) {
+    const float v = apply_epilogue(0.0f, alpha, relu);
+    const int64_t total = m * n;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i % m, c = i / m;
+        d[r + c * ldc] = v;
+    }
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait must
+// run out, record SITE_SELFTEST and return.
+__global__ void tg_selftest_wait_kernel(uint32_t *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t barrier_word;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&barrier_word);
+        mbar_init(b, 1);
+        abort_word = 0;
+        fence_mbar_init();
+        const WaitCtl ctl{reinterpret_cast<volatile int *>(&abort_word), status, limit_ns};
+        wait_phase(b, 0, ctl, SITE_SELFTEST);
+    }
+}
+
+}  // namespace tg
+
+namespace {
+
+using tg::Config;
+using tg::Kind;
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int elem_bytes(tg_dtype t) { return t == TG_TF32 ? 4 : 2; }
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *status = nullptr;  // one word of device memory owned by the library
+};
+
+std::mutex g_dev_mutex;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up on first use: device attributes and the status word.
+tg_status device_state(int *dev_out, DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess)
+            return TG_ERR_CUDA;
+        if (s.cc_major != 10 || s.cc_minor != 3) return TG_ERR_UNSUPPORTED;
+        if (cudaMalloc(&s.status, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
+        if (cudaMemset(s.status, 0, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
+        s.ready = true;
+    }
+    *dev_out = dev;
+    *out = &s;
+    return TG_OK;
+}
+
+// ------------------------------------------------------------------ planner
+
+struct Plan {
+    bool swap = false;
+    int block_n = 0;
+    int producer = 0;  // 1 TMA, 2 plain loads
+    int stages = 0;
+    int group = 0;
+    int grid = 0;
+    int64_t tiles = 0;
+    int threads = 0;
+    int smem = 0;
+    int tmem_cols = 0;
+    bool vector_store = false;
+    int64_t mk = 0, nk = 0;  // role-space rows and cols
+};
+
+template <Kind KD>
+void config_numbers(int bn, int *stages, int *smem, int *threads, int *tmem) {
+    switch (bn) {
+#define TG_CASE(BN)                                   \
+    case BN:                                          \
+        *stages = Config<KD, BN>::STAGES;             \
+        *smem = Config<KD, BN>::SMEM_BYTES;           \
+        *threads = Config<KD, BN>::NUM_THREADS;       \
+        *tmem = Config<KD, BN>::TMEM_COLS;            \
+        break;
+        TG_CASE(64)
+        TG_CASE(128)
+        TG_CASE(256)
+#undef TG_CASE
+    default:
+        *stages = *smem = *threads = *tmem = 0;
+    }
+}
+
+void config_numbers_for(tg_dtype t, int bn, int *stages, int *smem, int *threads, int *tmem) {
+    if (t == TG_BF16) config_numbers<Kind::BF16>(bn, stages, smem, threads, tmem);
+    else if (t == TG_FP16) config_numbers<Kind::FP16>(bn, stages, smem, threads, tmem);
+    else config_numbers<Kind::TF32>(bn, stages, smem, threads, tmem);
+}
+
+bool tma_legal(const void *p, int64_t ld, int esize) {
+    const uint64_t stride = (uint64_t)ld * (uint64_t)esize;
+    return ((uintptr_t)p % 16) == 0 && stride % 16 == 0 && stride < (1ull << 40);
+}
+
+tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, const float *D, int64_t ldc, tg_dtype t, const tg_options *o) {
+    if (t != TG_BF16 && t != TG_FP16 && t != TG_TF32) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_VALUE;
+    if (lda < (K > 1 ? K : 1) || ldb < (K > 1 ? K : 1) || ldc < (M > 1 ? M : 1))
+        return TG_ERR_INVALID_VALUE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TG_ERR_UNSUPPORTED;
+    const int e = elem_bytes(t);
+    if (M * K > 0 && (A == nullptr || (uintptr_t)A % e)) return TG_ERR_INVALID_VALUE;
+    if (K * N > 0 && (B == nullptr || (uintptr_t)B % e)) return TG_ERR_INVALID_VALUE;
+    if (M * N > 0 && (D == nullptr || (uintptr_t)D % 4)) return TG_ERR_INVALID_VALUE;
+    if (o) {
+        if (o->block_n != 0 && o->block_n != 64 && o->block_n != 128 && o->block_n != 256)
+            return TG_ERR_INVALID_VALUE;
+        if (o->producer < 0 || o->producer > 2) return TG_ERR_INVALID_VALUE;
+        if (o->swap_ab < 0 || o->swap_ab > 2) return TG_ERR_INVALID_VALUE;
+        if (o->raster_group < 0 || o->max_ctas < 0) return TG_ERR_INVALID_VALUE;
+        if (o->reserved[0] || o->reserved[1] || o->reserved[2]) return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+// Plan a problem with M, N, K > 0 (arguments already validated).
+tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, const float *D, int64_t ldc, tg_dtype t, const tg_options *o,
+                    int sms, Plan *plan) {
+    static const tg_options kNone = {};
+    if (!o) o = &kNone;
+    Plan p;
+    // Fill the 128-row MMA dimension: a short M with a long N runs with the
+    // operand roles swapped (both are K-major, so nothing is transposed).
+    if (o->swap_ab == 1) p.swap = false;
+    else if (o->swap_ab == 2) p.swap = true;
+    else p.swap = (M < tg::BLOCK_M) && (N >= tg::BLOCK_M) && (N >= 2 * M);
+    p.mk = p.swap ? N : M;
+    p.nk = p.swap ? M : N;
+
+    const int e = elem_bytes(t);
+    const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
+    if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
+    p.producer = o->producer ? o->producer : (legal ? 1 : 2);
+
+    // Tile N: the candidate with the fewest (waves x per-tile cost), where a
+    // tile's cost per K step is modelled as BN + 64 (the A operand's fixed
+    // share of shared-memory traffic makes narrow tiles less efficient).
+    const int64_t mblocks = ceil_div(p.mk, tg::BLOCK_M);
+    if (o->block_n) {
+        p.block_n = o->block_n;
+    } else {
+        int64_t best = -1;
+        for (int bn : {256, 128, 64}) {
+            const int64_t tiles = mblocks * ceil_div(p.nk, bn);
+            const int64_t est = ceil_div(tiles, sms) * (bn + 64);
+            if (best < 0 || est < best) {
+                best = est;
+                p.block_n = bn;
+            }
+        }
+    }
+    p.tiles = mblocks * ceil_div(p.nk, p.block_n);
+    config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    int64_t g = o->raster_group ? o->raster_group : 16;
+    if (g > mblocks) g = mblocks;
+    p.group = (int)g;
+    int64_t grid = p.tiles < sms ? p.tiles : sms;
+    if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
+    p.grid = (int)grid;
+    p.vector_store = p.swap && ((uintptr_t)D % 16 == 0) && (ldc % 4 == 0);
+    *plan = p;
+    return TG_OK;
+}
+
+// ------------------------------------------------------------------ TMA maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// K-major operand with `rows` rows of `k` elements, leading stride `ld`;
+// box = 128-byte rows (block_k elements) x box_rows, 128-byte swizzle, zero
+// fill outside [0,k) x [0,rows).
+bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows, int64_t k,
+                    int64_t ld, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int e = elem_bytes(t);
+    CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                             : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * e)};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+              const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype t, tg_epilogue epi,
+              const tg_options *opts, void *stream_ptr) {
+    if (epi != TG_EPILOGUE_NONE && epi != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
+    tg_status st = validate(M, N, K, A, lda, B, ldb, D, ldc, t, opts);
+    if (st != TG_OK) return st;
+    if (M == 0 || N == 0) return TG_OK;
+    int dev = 0;
+    DeviceState *ds = nullptr;
+    st = device_state(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
+
+    if (K == 0) {
+        const int64_t total = M * N;
+        int64_t blocks = ceil_div(total, 256);
+        const int64_t cap = (int64_t)ds->sms * 8;
+        if (blocks > cap) blocks = cap;
+        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(D, M, N, ldc, alpha,
+                                                                            relu);
+        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
+
+    Plan plan;
+    st = make_plan(M, N, K, A, lda, B, ldb, D, ldc, t, opts, ds->sms, &plan);
+    if (st != TG_OK) return st;
+
+    tg::LaunchArgs la;
+    std::memset(&la, 0, sizeof(la));
+    const void *ar = plan.swap ? B : A;   // A-role operand
+    const void *br = plan.swap ? A : B;   // B-role operand
+    const int64_t ldar = plan.swap ? ldb : lda;
+    const int64_t ldbr = plan.swap ? lda : ldb;
+    la.block_n = plan.block_n;
+    la.plain_loads = plan.producer == 2;
+    if (!la.plain_loads) {
+        const bool ok = encode_operand(&la.map_a, t, ar, plan.mk, K, ldar, tg::BLOCK_M) &&
+                        encode_operand(&la.map_b, t, br, plan.nk, K, ldbr, plan.block_n);
+        if (!ok) {
+            if (opts && opts->producer == 1) return TG_ERR_INVALID_VALUE;
+            la.plain_loads = true;  // shapes the TMA unit cannot describe
+        }
+    }
+    tg::GemmParams &p = la.p;
+    p.m = (int32_t)plan.mk;
+    p.n = (int32_t)plan.nk;
+    p.k = (int32_t)K;
+    p.num_m_blocks = (int32_t)ceil_div(plan.mk, tg::BLOCK_M);
+    p.num_n_blocks = (int32_t)ceil_div(plan.nk, plan.block_n);
+    p.num_k_blocks = (int32_t)ceil_div(K, t == TG_TF32 ? 32 : 64);
+    p.raster_group = plan.group;
+    p.relu = relu;
+    p.num_tiles = plan.tiles;
+    p.alpha = alpha;
+    p.vector_store = plan.vector_store ? 1 : 0;
+    p.d = D;
+    p.d_row_stride = plan.swap ? ldc : 1;
+    p.d_col_stride = plan.swap ? 1 : ldc;
+    p.a_ptr = ar;
+    p.b_ptr = br;
+    p.lda = ldar;
+    p.ldb = ldbr;
+    p.status = ds->status;
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    la.grid = plan.grid;
+    la.device = dev;
+    la.stream = stream;
+
+    cudaError_t e;
+    if (t == TG_BF16) e = tg::launch_bf16(la);
+    else if (t == TG_FP16) e = tg::launch_fp16(la);
+    else e = tg::launch_tf32(la);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+tg_status tg_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                  const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype in_dtype,
+                  tg_epilogue epilogue, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, nullptr, stream);
+}
+
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                     const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype in_dtype,
+                     tg_epilogue epilogue, const tg_options *opts, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, opts, stream);
+}
+
+tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                  int64_t ldb, const float *D, int64_t ldc, tg_dtype in_dtype,
+                  const tg_options *opts, int32_t num_sms, tg_plan_info *out) {
+    if (!out) return TG_ERR_INVALID_VALUE;
+    // NULL operands are planned as 256-byte aligned.
+    const void *a = A ? A : reinterpret_cast<const void *>(256);
+    const void *b = B ? B : reinterpret_cast<const void *>(256);
+    const float *d = D ? D : reinterpret_cast<const float *>(256);
+    tg_status st = validate(M, N, K, a, lda, b, ldb, d, ldc, in_dtype, opts);
+    if (st != TG_OK) return st;
+    int sms = num_sms;
+    if (sms <= 0) {
+        int dev = 0;
+        DeviceState *ds = nullptr;
+        st = device_state(&dev, &ds);
+        if (st != TG_OK) return st;
+        sms = ds->sms;
+    }
+    std::memset(out, 0, sizeof(*out));
+    if (M == 0 || N == 0 || K == 0) return TG_OK;  // nothing to tile
+    Plan p;
+    st = make_plan(M, N, K, a, lda, b, ldb, d, ldc, in_dtype, opts, sms, &p);
+    if (st != TG_OK) return st;
+    out->block_m = tg::BLOCK_M;
+    out->block_n = p.block_n;
+    out->block_k = in_dtype == TG_TF32 ? 32 : 64;
+    out->stages = p.stages;
+    out->producer = p.producer;
+    out->swap_ab = p.swap ? 1 : 0;
+    out->raster_group = p.group;
+    out->grid = p.grid;
+    out->tiles = p.tiles;
+    out->threads = p.threads;
+    out->smem_bytes = p.smem;
+    out->tmem_cols = p.tmem_cols;
+    out->vector_store = p.vector_store ? 1 : 0;
+    return TG_OK;
+}
+
+const char *tg_status_string(tg_status s) {
+    switch (s) {
+    case TG_OK: return "TG_OK";
+    case TG_ERR_INVALID_VALUE: return "TG_ERR_INVALID_VALUE";
+    case TG_ERR_UNSUPPORTED: return "TG_ERR_UNSUPPORTED";
+    case TG_ERR_CUDA: return "TG_ERR_CUDA";
+    case TG_ERR_DEVICE_TIMEOUT: return "TG_ERR_DEVICE_TIMEOUT";
+    default: return "TG_ERR_UNKNOWN";
+    }
+}
+
+tg_status tg_check_device_status(void *stream, int32_t *where) {
+    int dev = 0;
+    DeviceState *ds = nullptr;
+    tg_status st = device_state(&dev, &ds);
+    if (st != TG_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TG_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TG_ERR_CUDA;
+    if (word == 0) return TG_OK;
+    if (cudaMemset(ds->status, 0, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
+    if (where) *where = (int32_t)word;
+    return TG_ERR_DEVICE_TIMEOUT;
+}
+
+tg_status tg_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
+    return TG_OK;
+}
+
+tg_status tg_selftest_wait_timeout(uint64_t limit_ns, void *stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return TG_ERR_INVALID_VALUE;
+    int dev = 0;
+    DeviceState *ds = nullptr;
+    tg_status st = device_state(&dev, &ds);
+    if (st != TG_OK) return st;
+    tg::tg_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ds->status,
+                                                                                 limit_ns);
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+int32_t tg_version(void) { return kVersion; }
+
+}  // extern "C"

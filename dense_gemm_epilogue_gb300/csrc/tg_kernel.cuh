@@ -1,0 +1,455 @@
+// Persistent, warp-specialised tcgen05 GEMM with a fused alpha/ReLU epilogue.
+//
+// Computes, in the kernel's "role space", Dk(r, c) = epi(alpha * sum_k Ak(r,k) * Bk(c,k))
+// where Ak is the A-role operand (rows r, K-contiguous) and Bk the B-role
+// operand (rows c, K-contiguous).  The host either maps A -> Ak, B -> Bk and
+// stores Dk(r,c) at D[r + c*ldc] (the natural orientation), or swaps the
+// roles (Ak = B's storage, Bk = A's storage) and stores Dk(r,c) at
+// D[r*ldc + c]; both operands are K-major, so the swap costs nothing.
+//
+// Roles per CTA (one CTA per SM, persistent over output tiles):
+//   warp 0      producer: TMA 2-D loads (or plain bounds-checked loads that
+//               write the same swizzled layout) into an S-stage ring guarded by
+//               full/empty mbarriers ("Walk through GEMM" sections 3-4: copy a
+//               K stage, consume, then release it; here the release is the
+//               tensor core's own completion signal).
+//   warp 1      tensor-memory allocator and MMA issuer: one thread issues
+//               tcgen05.mma (128 x BN x 16 for 16-bit kinds, x8 for TF32) into
+//               one of two TMEM accumulators, FP32 ("Matrix Multiplication"
+//               step 3: the accumulator is wider than the inputs).
+//   warps 2-5   epilogue: tcgen05.ld TMEM -> registers, y = alpha*x, then the
+//               max with zero when ReLU is on ("Walk through GEMM" section 5),
+//               bounds-checked stores of the rows/columns inside the problem
+//               ("Matrix Multiplication", ragged sizes: the overhang is not
+//               stored).  Two accumulators let tile t's epilogue overlap tile
+//               t+1's main loop.
+//   warps 6-9   (TF32 only) narrow each landed FP32 stage in place to TF32
+//               (round to nearest, ties away from zero) before the MMA reads it
+//               ("Matrix Multiplication" step 4: convert the operand tiles to
+//               TFloat32, keep the accumulator FP32).
+// Out-of-range K columns of A and rows of B are read as zeros (TMA
+// out-of-bounds fill, or the plain loader's bounds check), which adds nothing
+// to the sums ("Matrix Multiplication", ragged sizes: zero padding).
+//
+// Every wait is bounded in time.  A wait that runs out records a code in the
+// per-device status word, raises a CTA-wide abort flag that makes every other
+// role leave its loop, drains the copies and MMAs this CTA still has in
+// flight (with a bounded wait), frees tensor memory and returns.
+#pragma once
+
+#include <cstdint>
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2 };
+
+template <Kind KD>
+struct KindTraits;
+template <>
+struct KindTraits<Kind::BF16> {
+    static constexpr int elem_bytes = 2, block_k = 64, umma_k = 16;
+    static constexpr uint32_t fmt = 1;  // instruction-descriptor operand format: BF16
+};
+template <>
+struct KindTraits<Kind::FP16> {
+    static constexpr int elem_bytes = 2, block_k = 64, umma_k = 16;
+    static constexpr uint32_t fmt = 0;  // F16
+};
+template <>
+struct KindTraits<Kind::TF32> {
+    static constexpr int elem_bytes = 4, block_k = 32, umma_k = 8;
+    static constexpr uint32_t fmt = 2;  // TF32
+};
+
+// Codes written to the status word when a bounded wait runs out.
+enum WaitSite : uint32_t {
+    SITE_FULL = 1,
+    SITE_EMPTY = 2,
+    SITE_ACC_FULL = 3,
+    SITE_ACC_EMPTY = 4,
+    SITE_CONVERTED = 5,
+    SITE_DRAIN = 6,
+    SITE_SELFTEST = 7,
+};
+
+struct GemmParams {
+    int32_t m, n, k;                // role-space problem: rows, cols, reduction
+    int32_t num_m_blocks, num_n_blocks, num_k_blocks;
+    int32_t raster_group;           // M tiles per raster group
+    int32_t relu;
+    int64_t num_tiles;
+    float alpha;
+    int32_t vector_store;           // 1: cols contiguous in D and 16-byte aligned
+    float *d;
+    int64_t d_row_stride;           // D element stride between role-space rows
+    int64_t d_col_stride;           // D element stride between role-space cols
+    const void *a_ptr;              // plain-load producer only
+    const void *b_ptr;
+    int64_t lda, ldb;               // role-space leading strides (elements)
+    uint32_t *status;               // per-device status word
+    uint64_t wait_limit_ns;
+};
+
+constexpr int BLOCK_M = 128;
+constexpr int ROW_BYTES = 128;                   // one K-major smem row: 128 bytes
+constexpr int SMEM_LIMIT = 232448;               // max dynamic smem per CTA (227 KB)
+
+template <int BN>
+struct StageCount {
+    static constexpr int stage_bytes = (BLOCK_M + BN) * ROW_BYTES;
+    static constexpr int fit = (SMEM_LIMIT - 2048) / stage_bytes;
+    static constexpr int value = fit > 8 ? 8 : fit;
+};
+
+template <Kind KD, int BN>
+struct Config {
+    using T = KindTraits<KD>;
+    static constexpr bool TF32 = (KD == Kind::TF32);
+    static constexpr int BK = T::block_k;
+    static constexpr int STAGES = StageCount<BN>::value;
+    static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
+    static constexpr int B_BYTES = BN * ROW_BYTES;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = STAGES * A_BYTES;
+    static constexpr int BAR_OFF = B_OFF + STAGES * B_BYTES;
+    // full[S], empty[S], converted[S], acc_full[2], acc_empty[2], drain
+    static constexpr int FULL0 = 0, EMPTY0 = STAGES, CONV0 = 2 * STAGES;
+    static constexpr int ACCF0 = 3 * STAGES, ACCE0 = 3 * STAGES + 2, DRAIN = 3 * STAGES + 4;
+    static constexpr int NUM_BARS = 3 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int USED_BYTES = MISC_OFF + 16;
+    static constexpr int SMEM_BYTES = USED_BYTES + 1024;  // slack for 1024-byte alignment
+    static constexpr int TMEM_COLS = 2 * BN;               // two FP32 accumulators
+    static constexpr int NUM_WARPS = TF32 ? 10 : 6;
+    static constexpr int NUM_THREADS = NUM_WARPS * 32;
+    static constexpr int MMAS_PER_STAGE = BK / T::umma_k;
+    // Instruction descriptor: D FP32 (bit 4), A/B formats (bits 7-9, 10-12),
+    // both K-major (bits 15, 16 zero), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+    static constexpr uint32_t IDESC = (1u << 4) | (T::fmt << 7) | (T::fmt << 10) |
+                                      ((uint32_t)(BN >> 3) << 17) |
+                                      ((uint32_t)(BLOCK_M >> 4) << 24);
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "tensor-memory allocation is a power of two in [32, 512]");
+    static_assert(BK * T::elem_bytes == ROW_BYTES, "one stage row is one 128-byte swizzle row");
+};
+
+struct WaitCtl {
+    volatile int *abort_flag;
+    uint32_t *status;
+    uint64_t limit_ns;
+};
+
+// Wait for the phase of `bar` with parity `parity`.  Returns false if the CTA
+// is aborting or if this wait ran out of time (then it raises the abort flag
+// and records `site`).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtl &c,
+                                           uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*c.abort_flag) return false;
+        if (globaltimer_ns() - t0 > c.limit_ns) {
+            *c.abort_flag = 1;
+            atomicCAS(c.status, 0u, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, const WaitCtl &c) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > c.limit_ns) {
+            atomicCAS(c.status, 0u, (uint32_t)SITE_DRAIN);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tile_coords(int64_t t, const GemmParams &p, int &mb, int &nb) {
+    const int64_t per_group = (int64_t)p.raster_group * p.num_n_blocks;
+    const int64_t g = t / per_group;
+    const int64_t first_m = g * p.raster_group;
+    const int64_t left = (int64_t)p.num_m_blocks - first_m;
+    const int gsz = (int)(left < p.raster_group ? left : p.raster_group);
+    const int64_t r = t - g * per_group;
+    mb = (int)(first_m + r % gsz);
+    nb = (int)(r / gsz);
+}
+
+__device__ __forceinline__ float apply_epilogue(float x, float alpha, int relu) {
+    float y = alpha * x;
+    if (relu) y = (y > 0.0f || y != y) ? y : 0.0f;  // max(y, 0): NaN stays, -0 -> +0
+    return y;
+}
+
+// Narrow one FP32 bit pattern to TF32: round the magnitude to 10 fraction
+// bits, ties away from zero; Inf passes through, NaN becomes a quiet NaN whose
+// upper fraction bits are set so that it stays NaN without its low 13 bits.
+__device__ __forceinline__ uint32_t narrow_tf32(uint32_t u) {
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        return (u & 0x007FFFFFu) ? ((u & 0x80000000u) | 0x7FC00000u) : u;
+    }
+    return (u + 0x1000u) & 0xFFFFE000u;
+}
+
+// Plain-load producer: one stage of `rows` x BK elements into the 128-byte
+// swizzled K-major layout (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
+template <int ELEM_BYTES, int ROWS>
+__device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, int64_t ld,
+                                                 int32_t row0, int32_t rows_total, int32_t k0,
+                                                 int32_t k_total, int lane) {
+    constexpr int EPC = 16 / ELEM_BYTES;  // elements per 16-byte chunk
+    constexpr int CHUNKS = ROWS * 8;
+    for (int ch = lane; ch < CHUNKS; ch += 32) {
+        const int r = ch >> 3, c = ch & 7;
+        const int32_t gr = row0 + r;
+        uint32_t w[4];
+        if (ELEM_BYTES == 2) {
+            const uint16_t *s = static_cast<const uint16_t *>(src);
+            uint16_t h[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int32_t gk = k0 + c * EPC + e;
+                h[e] = (gr < rows_total && gk < k_total) ? s[(int64_t)gr * ld + gk] : (uint16_t)0;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = (uint32_t)h[2 * e] | ((uint32_t)h[2 * e + 1] << 16);
+        } else {
+            const uint32_t *s = static_cast<const uint32_t *>(src);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int32_t gk = k0 + c * EPC + e;
+                w[e] = (gr < rows_total && gk < k_total) ? s[(int64_t)gr * ld + gk] : 0u;
+            }
+        }
+        uint4 *out = reinterpret_cast<uint4 *>(dst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
+        *out = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <Kind KD, int BN, bool PLAIN_LOADS>
+__global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
+    tg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    using C = Config<KD, BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
+    auto a_stage = [&](int s) -> uint32_t { return sbase + C::A_OFF + s * C::A_BYTES; };
+    auto b_stage = [&](int s) -> uint32_t { return sbase + C::B_OFF + s * C::B_BYTES; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(C::FULL0 + s), PLAIN_LOADS ? 32 : 1);
+            mbar_init(bar(C::EMPTY0 + s), 1);
+            mbar_init(bar(C::CONV0 + s), 128);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(C::ACCF0 + a), 1);
+            mbar_init(bar(C::ACCE0 + a), 128);
+        }
+        mbar_init(bar(C::DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (!PLAIN_LOADS && threadIdx.x == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nkb = p.num_k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (PLAIN_LOADS) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                    load_stage_plain<C::T::elem_bytes, BLOCK_M>(smem + C::A_OFF + s * C::A_BYTES,
+                                                                p.a_ptr, p.lda, mb * BLOCK_M, p.m,
+                                                                kb * C::BK, p.k, lane);
+                    load_stage_plain<C::T::elem_bytes, BN>(smem + C::B_OFF + s * C::B_BYTES,
+                                                           p.b_ptr, p.ldb, nb * BN, p.n,
+                                                           kb * C::BK, p.k, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::FULL0 + s));
+                    if (++s == S) { s = 0; ph ^= 1; }
+                }
+            }
+        } else if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar(C::FULL0 + s), C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M);
+                    tma_load_2d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kb * C::BK, nb * BN);
+                    ++issued;
+                    if (++s == S) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok) {
+                // Let every TMA copy already issued land before the CTA exits.
+                for (int st = 0; st < S && st < issued; ++st) {
+                    const int64_t last = st + (int64_t)S * ((issued - 1 - st) / S);
+                    wait_phase_drain(bar(C::FULL0 + st), (uint32_t)((last / S) & 1), ctl);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t tl = 0;
+            bool ok = true;
+            const int wait_bar0 = C::TF32 ? C::CONV0 : C::FULL0;
+            const uint32_t wait_site = C::TF32 ? SITE_CONVERTED : SITE_FULL;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tl) {
+                const uint32_t acc = tl & 1, use = tl >> 1;
+                if (!wait_phase(bar(C::ACCE0 + acc), (use & 1) ^ 1, ctl, SITE_ACC_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_phase(bar(wait_bar0 + s), ph, ctl, wait_site)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = a_stage(s), b0 = b_stage(s);
+#pragma unroll
+                    for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
+                        const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
+                        const uint32_t accumulate = (kb | kk) != 0;
+                        if (C::TF32) mma_tf32(d_tmem, ad, bd, C::IDESC, accumulate);
+                        else mma_f16(d_tmem, ad, bd, C::IDESC, accumulate);
+                    }
+                    mma_commit(bar(C::EMPTY0 + s));  // stage s is free once these MMAs finish
+                    if (++s == S) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(bar(C::ACCF0 + acc));     // accumulator ready for the epilogue
+            }
+            if (!ok) {
+                mma_commit(bar(C::DRAIN));
+                wait_phase_drain(bar(C::DRAIN), 0, ctl);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int row_in_tile = q * 32 + lane;
+        uint32_t tl = 0;
+        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const uint32_t acc = tl & 1, use = tl >> 1;
+            if (!wait_phase(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
+            tc_fence_after();
+            const int32_t r = mb * BLOCK_M + row_in_tile;
+            const bool row_ok = r < p.m;
+            float *drow = p.d + (int64_t)r * p.d_row_stride;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + c0, v);
+                tmem_ld_wait();
+                const int32_t col0 = nb * BN + c0;
+                if (row_ok) {
+                    if (p.vector_store && col0 + 32 <= p.n) {
+                        float4 *dst = reinterpret_cast<float4 *>(drow + col0);
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            dst[j / 4] = make_float4(
+                                apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
+                                apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
+                                apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
+                                apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu));
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (col0 + j < p.n) {
+                                drow[(int64_t)(col0 + j) * p.d_col_stride] =
+                                    apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::ACCE0 + acc));
+        }
+    } else if (C::TF32) {
+        // ------------------------------------------------------ TF32 narrowing
+        const int ct = threadIdx.x - 6 * 32;  // 0..127
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!wait_phase(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
+                uint4 *a4 = reinterpret_cast<uint4 *>(smem + C::A_OFF + s * C::A_BYTES);
+                for (int i = ct; i < C::A_BYTES / 16; i += 128) {
+                    uint4 x = a4[i];
+                    a4[i] = make_uint4(narrow_tf32(x.x), narrow_tf32(x.y), narrow_tf32(x.z),
+                                       narrow_tf32(x.w));
+                }
+                uint4 *b4 = reinterpret_cast<uint4 *>(smem + C::B_OFF + s * C::B_BYTES);
+                for (int i = ct; i < C::B_BYTES / 16; i += 128) {
+                    uint4 x = b4[i];
+                    b4[i] = make_uint4(narrow_tf32(x.x), narrow_tf32(x.y), narrow_tf32(x.z),
+                                       narrow_tf32(x.w));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::CONV0 + s));
+                if (++s == S) { s = 0; ph ^= 1; }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tg

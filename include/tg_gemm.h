@@ -1,0 +1,184 @@
+/*
+ * tg_gemm: dense GEMM with a fused pointwise epilogue on GB300 (sm_103a).
+ *
+ *   D = epi(alpha * A * B),  epi = identity or ReLU (max with zero)
+ *
+ * The operation is the one defined by "Walk through GEMM" (Tylo.jl manual):
+ * the introduction (D = alpha * A * B, optionally ReLU in the epilogue) and
+ * section 5 "Apply the epilogue and store by ownership" (alpha is applied to
+ * the accumulator first, then the max with zero, with no extra kernel).  The
+ * operand formats and the FP32 accumulator follow "Matrix Multiplication"
+ * (cuTile.jl tutorial), Step 3 "Looping over K" and Step 4 "Using the tensor
+ * cores"; ragged sizes follow its section "Sizes that are not a multiple of
+ * the tile shape" (out-of-range K reads count as zero, out-of-range outputs
+ * are not stored).
+ *
+ * Storage ("Walk through GEMM", section 2 "Bind runtime global arrays"), all
+ * indices zero-based:
+ *   A: logical (M, K), K-contiguous:   a(i,k) = A[i*lda + k],  lda >= max(K,1)
+ *   B: logical (K, N), K-contiguous:   b(k,j) = B[k + j*ldb],  ldb >= max(K,1)
+ *   D: logical (M, N), M-contiguous:   D[i + j*ldc] (float),   ldc >= max(M,1)
+ * Element types: TG_BF16 / TG_FP16 operands are 2-byte storage; TG_TF32
+ * operands are FP32 storage narrowed in the kernel to TF32 (10 fraction bits,
+ * round to nearest, ties away from zero).  Products accumulate in FP32; D is
+ * FP32.  Only D[i + j*ldc] with i < M, j < N is written: stride padding of D
+ * is left untouched, and stride padding of A and B is never read.
+ *
+ * Ownership: every buffer and the stream belong to the caller and are only
+ * borrowed for the call ("Walk through GEMM", section 2: views never copy,
+ * allocate or make data ready).  A, B and D are device pointers (or memory the
+ * device can address); D must not overlap A or B.  The library keeps small
+ * per-device state of its own (a status word, cached device attributes);
+ * it allocates that state on the first call on a device.
+ *
+ * Asynchrony: tg_gemm enqueues its work on `stream` (a cudaStream_t passed as
+ * void*, NULL for the legacy default stream) and returns without waiting;
+ * results are visible after the stream is synchronised.  Calls on one stream
+ * run in order; the kernels use no atomics, so repeated calls with the same
+ * inputs give bitwise identical D.
+ *
+ * Errors: arguments are validated on the host before anything is launched.
+ * A non-OK status means nothing was enqueued, except TG_ERR_CUDA returned by a
+ * failed launch.  Device-side waits have a time limit; a wait that runs out
+ * makes the kernel exit early and sets a per-device status word, which
+ * tg_check_device_status reads.
+ */
+#ifndef TG_GEMM_H
+#define TG_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_VALUE = 1,  /* bad dimension, stride, pointer, enum or option */
+    TG_ERR_UNSUPPORTED = 2,    /* valid request this build cannot run (e.g. no sm_103 device) */
+    TG_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+    TG_ERR_DEVICE_TIMEOUT = 4  /* a kernel's bounded wait ran out (see tg_check_device_status) */
+} tg_status;
+
+typedef enum {
+    TG_BF16 = 0,  /* bfloat16 operands */
+    TG_FP16 = 1,  /* IEEE binary16 operands */
+    TG_TF32 = 2   /* FP32 storage, narrowed to TF32 in the kernel */
+} tg_dtype;
+
+typedef enum {
+    TG_EPILOGUE_NONE = 0,  /* D = alpha * A*B */
+    TG_EPILOGUE_RELU = 1   /* D = max(alpha * A*B, 0); NaN stays NaN, -0 becomes +0 */
+} tg_epilogue;
+
+/*
+ * D = epi(alpha * A * B) on `stream`.
+ *
+ * M, N, K >= 0.  M == 0 or N == 0: returns TG_OK and launches nothing.
+ * K == 0: D = epi(alpha * 0) over the M x N output (the empty sum).
+ * Pointers may be NULL only when the matrix they address is empty
+ * (A: M*K == 0, B: K*N == 0, D: M*N == 0).  A and B must be aligned to their
+ * element size, D to 4 bytes.  Leading strides as in the storage rules above.
+ * Strides or base addresses that the tensor-memory-accelerator (TMA) cannot
+ * address (not multiples of 16 bytes) are not errors: the planner routes them
+ * to a kernel variant whose producer warp loads with plain bounds-checked
+ * loads.
+ *
+ * Returns TG_OK once the work is enqueued; TG_ERR_INVALID_VALUE for bad
+ * arguments (nothing enqueued); TG_ERR_UNSUPPORTED when the current device is
+ * not a compute capability 10.3 GPU; TG_ERR_CUDA when a CUDA call fails.
+ */
+tg_status tg_gemm(int64_t M, int64_t N, int64_t K, float alpha,
+                  const void *A, int64_t lda,
+                  const void *B, int64_t ldb,
+                  float *D, int64_t ldc,
+                  tg_dtype in_dtype, tg_epilogue epilogue, void *stream);
+
+/*
+ * Planner overrides, for tests and tuning.  A zero-initialised struct (or a
+ * NULL pointer) means "the planner decides" for every field.
+ */
+typedef struct {
+    int32_t block_n;      /* 0: planner; else 64, 128 or 256 (tile N of one CTA) */
+    int32_t producer;     /* 0: planner; 1: TMA loads (must be legal); 2: plain loads */
+    int32_t swap_ab;      /* 0: planner; 1: never swap; 2: always swap the A/B roles */
+    int32_t raster_group; /* 0: planner; else number of M tiles per raster group (>= 1) */
+    int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
+    int32_t reserved[3];  /* must be zero */
+} tg_options;
+
+/* What the planner chose for one problem (host only; no CUDA call). */
+typedef struct {
+    int32_t block_m;      /* tile M of one CTA (128) */
+    int32_t block_n;      /* tile N of one CTA */
+    int32_t block_k;      /* K elements per pipeline stage (64 for 2-byte types, 32 for TF32) */
+    int32_t stages;       /* shared-memory ring depth */
+    int32_t producer;     /* 1 TMA, 2 plain loads */
+    int32_t swap_ab;      /* 1 if the kernel computes D^T = B^T A^T with the roles swapped */
+    int32_t raster_group; /* M tiles per raster group */
+    int32_t grid;         /* persistent CTAs launched */
+    int64_t tiles;        /* output tiles */
+    int32_t threads;      /* threads per CTA */
+    int32_t smem_bytes;   /* dynamic shared memory per CTA */
+    int32_t tmem_cols;    /* tensor-memory columns per CTA */
+    int32_t vector_store; /* 1 if the epilogue stores 16-byte vectors (swapped, aligned D) */
+} tg_plan_info;
+
+/* tg_gemm with planner overrides.  Invalid or inapplicable overrides
+ * (e.g. TMA forced on a TMA-illegal stride) return TG_ERR_INVALID_VALUE. */
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                     const void *A, int64_t lda,
+                     const void *B, int64_t ldb,
+                     float *D, int64_t ldc,
+                     tg_dtype in_dtype, tg_epilogue epilogue,
+                     const tg_options *opts, void *stream);
+
+/*
+ * Run the planner only.  `num_sms` > 0 plans for that many SMs without
+ * touching CUDA; `num_sms` <= 0 queries the current device.  A, B, D are used
+ * only for their alignment (may be NULL when M, N or K is 0; a NULL is taken
+ * as 256-byte aligned).  Returns TG_ERR_INVALID_VALUE on the same argument
+ * errors as tg_gemm_ex.
+ */
+tg_status tg_plan(int64_t M, int64_t N, int64_t K,
+                  const void *A, int64_t lda, const void *B, int64_t ldb,
+                  const float *D, int64_t ldc, tg_dtype in_dtype,
+                  const tg_options *opts, int32_t num_sms, tg_plan_info *out);
+
+/* Static text for a status code ("TG_OK", ...); never NULL. */
+const char *tg_status_string(tg_status status);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word
+ * that kernels set when a bounded wait runs out.  Returns TG_OK if no wait ran
+ * out since the last check, TG_ERR_DEVICE_TIMEOUT if one did (then *where, if
+ * not NULL, receives a code naming the wait: 1 stage-full, 2 stage-empty,
+ * 3 accumulator-full, 4 accumulator-empty, 5 converted-stage, 6 drain,
+ * 7 self-test), TG_ERR_CUDA on a CUDA error.
+ */
+tg_status tg_check_device_status(void *stream, int32_t *where);
+
+/*
+ * Set the time limit, in nanoseconds, of every device-side wait of later
+ * launches on all devices (default 4e9 ns; 0 restores the default).
+ */
+tg_status tg_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Failure-detection self-test: launch one CTA whose single thread waits on a
+ * shared-memory barrier that nothing ever completes, with a `limit_ns` time
+ * limit.  The wait runs out, the kernel records code 7 in the status word and
+ * returns normally (no trap, no fault); tg_check_device_status then reports
+ * TG_ERR_DEVICE_TIMEOUT.  limit_ns must be in (0, 1e9].
+ */
+tg_status tg_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_H */

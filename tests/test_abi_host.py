@@ -1,0 +1,131 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every
+symbol the header declares, validates arguments before touching CUDA, and
+its planner makes the documented choices."""
+
+from __future__ import annotations
+
+import os
+import re
+import subprocess
+
+import pytest
+
+import seeded_inputs as si
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import dense_gemm_epilogue_gb300 as tg
+
+    tg.build()
+    tg.load()
+    return tg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names(tg):
+    assert declared_functions() == sorted(tg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(tg):
+    lib = tg.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", tg.LIBRARY_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (tg_[a-z0-9_]+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_strings_and_version(tg):
+    assert tg.tg_status_string(0) == "TG_OK"
+    assert tg.tg_status_string(4) == "TG_ERR_DEVICE_TIMEOUT"
+    assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
+    assert tg.tg_version() == 100
+    assert tg.tg_set_wait_limit_ns(0) == tg.TG_OK
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
+
+
+@pytest.mark.parametrize("args", [
+    dict(M=-1), dict(N=-1), dict(K=-1),
+    dict(lda=9), dict(ldb=9), dict(ldc=9),
+    dict(A=None), dict(B=None), dict(D=None),
+    dict(A=FAKE + 1), dict(D=FAKE + 2),
+    dict(dtype=3), dict(epi=2),
+    dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
+    dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"reserved": [1, 0, 0]}),
+])
+def test_invalid_arguments_rejected_before_cuda(tg, args):
+    a = dict(M=10, N=10, K=10, A=FAKE, lda=10, B=FAKE, ldb=10, D=FAKE, ldc=10, dtype=0, epi=1,
+             opts=None)
+    a.update(args)
+    st = tg.tg_gemm_ex(a["M"], a["N"], a["K"], 1.0, a["A"], a["lda"], a["B"], a["ldb"], a["D"],
+                       a["ldc"], a["dtype"], a["epi"], a["opts"])
+    assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def test_empty_output_is_ok_without_cuda(tg):
+    assert tg.tg_gemm(0, 10, 10, 1.0, None, 10, FAKE, 10, None, 1, "bf16", True) == tg.TG_OK
+    assert tg.tg_gemm(10, 0, 10, 1.0, FAKE, 10, None, 10, None, 10, "bf16", True) == tg.TG_OK
+
+
+def test_tf32_alignment_is_element_size(tg):
+    st = tg.tg_gemm(4, 4, 4, 1.0, FAKE + 2, 4, FAKE, 4, FAKE, 4, "tf32", False)
+    assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def plan(tg, w, opts=None, sms=152, A=FAKE, B=FAKE, D=FAKE):
+    lda, ldb, ldc = w.strides
+    return tg.tg_plan(w.M, w.N, w.K, A, lda, B, ldb, D, ldc, w.dtype, opts, sms)
+
+
+def test_plan_headline_8192(tg):
+    p = plan(tg, si.WORKLOADS["c4_bf16_8192"])
+    assert (p["block_m"], p["block_n"], p["block_k"]) == (128, 256, 64)
+    assert p["producer"] == 1 and p["swap_ab"] == 0
+    assert p["tiles"] == 64 * 32 and p["grid"] == 152
+    assert p["stages"] == 4 and p["tmem_cols"] == 512 and p["threads"] == 192
+    assert p["smem_bytes"] <= 232448
+
+
+def test_plan_tma_illegal_strides_use_plain_loads(tg):
+    p = plan(tg, si.WORKLOADS["c1_bf16_65x97x73"])   # 73 * 2 bytes is not a multiple of 16
+    assert p["producer"] == 2 and p["swap_ab"] == 0
+    with pytest.raises(tg.TgError):
+        plan(tg, si.WORKLOADS["c1_bf16_65x97x73"], opts={"producer": 1})
+    # A misaligned base also rules TMA out.
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"], A=FAKE + 2)["producer"] == 2
+
+
+def test_plan_skinny_shapes(tg):
+    a = plan(tg, si.WORKLOADS["c5a_bf16_16384x64x4096"])
+    assert a["swap_ab"] == 0 and a["block_n"] == 64 and a["tiles"] == 128 and a["producer"] == 1
+    b = plan(tg, si.WORKLOADS["c5b_bf16_64x16384x4096"])
+    assert b["swap_ab"] == 1 and b["block_n"] == 64 and b["tiles"] == 128
+    assert b["vector_store"] == 1                      # ldc = 72 keeps rows 16-byte aligned
+    c = plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])
+    assert c["producer"] == 1 and c["swap_ab"] == 0
+
+
+def test_plan_tf32(tg):
+    p = plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])
+    assert p["block_k"] == 32 and p["threads"] == 320
+
+
+def test_plan_overrides(tg):
+    w = si.WORKLOADS["c3_fp16_4096"]
+    p = plan(tg, w, opts={"block_n": 128, "max_ctas": 10, "raster_group": 4, "swap_ab": 2})
+    assert p["block_n"] == 128 and p["grid"] == 10 and p["raster_group"] == 4 and p["swap_ab"] == 1
+    p = plan(tg, w, opts={"raster_group": 1000})
+    assert p["raster_group"] == 32                     # clamped to the M tile count
+    assert plan(tg, w, sms=7)["grid"] == 7

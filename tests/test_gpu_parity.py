@@ -1,0 +1,165 @@
+"""CUDA path against the oracle, element by element, through the C ABI.
+
+Every workload of the pages' configurations runs at its full size with the
+planner's own choice (the launch configuration the benchmark times) and is
+compared on every output element; smaller problems sweep the ragged edges,
+every compiled tile configuration, both producers, both operand roles and
+the special cases (K = 0, alpha = 0, ReLU of all-negative sums, NaN inputs).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+from gemm_harness import assert_within, check_full, logical, run_tg
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_gemm_epilogue_gb300 as tg
+
+    tg.build()
+    tg.load()
+
+
+@pytest.mark.parametrize("name", ["c1_bf16_65x97x73", "c2_tf32_256x128x512"])
+def test_small_configs_full(name):
+    check_full(si.WORKLOADS[name], repeats=2)
+
+
+def _edge_cases():
+    sizes = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+    rng = np.random.default_rng(7)
+    picks = {(s, s, s) for s in sizes}
+    while len(picks) < 90:
+        picks.add(tuple(int(x) for x in rng.choice(sizes, 3)))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("M,N,K", _edge_cases())
+def test_edge_sweep_bf16(M, N, K):
+    w = si.Workload(f"edge{M}x{N}x{K}", M, N, K, "bf16", 1.5, True, 100 + M + 7 * N + 13 * K,
+                    "uniform")
+    check_full(w)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "tf32"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 65, 33), (257, 255, 129), (17, 300, 70)])
+def test_edge_sweep_other_types(dtype, M, N, K):
+    w = si.Workload(f"edge_{dtype}", M, N, K, dtype, -0.75, dtype == "fp16", 5 + M + N + K,
+                    "uniform")
+    check_full(w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "tf32"])
+@pytest.mark.parametrize("block_n", [64, 128, 256])
+@pytest.mark.parametrize("producer", [1, 2])
+def test_every_config(dtype, block_n, producer):
+    """Each compiled tile configuration and both producers on a ragged
+    problem spanning several tiles in M, N and K."""
+    w = si.Workload("cfg", 300, 520, 200, dtype, 1.25, True, 17, "uniform", lda=208, ldb=216,
+                    ldc=304)
+    check_full(w, opts={"block_n": block_n, "producer": producer})
+
+
+@pytest.mark.parametrize("swap", [1, 2])
+@pytest.mark.parametrize("M,N", [(64, 1000), (200, 333), (5, 700)])
+def test_swap_roles(swap, M, N):
+    w = si.Workload("swap", M, N, 150, "bf16", 0.5, True, 23, "uniform", ldc=M + 4)
+    check_full(w, opts={"swap_ab": swap})
+
+
+def test_swap_scalar_store_unaligned_ldc():
+    w = si.Workload("swap_ldc", 33, 900, 77, "fp16", 1.0, False, 29, "uniform", ldc=35)
+    check_full(w, opts={"swap_ab": 2})
+
+
+def test_persistent_multiple_tiles_per_cta():
+    """A grid smaller than the tile count: each CTA walks several tiles and
+    both tensor-memory accumulators are reused."""
+    w = si.Workload("persist", 1000, 1100, 300, "bf16", 1.0, True, 31, "normal")
+    for g in (1, 3, 7):
+        check_full(w, opts={"max_ctas": g, "raster_group": 2})
+
+
+def test_k_zero_gives_epilogue_of_zero():
+    w = si.Workload("k0", 70, 90, 0, "bf16", 2.0, True, 1, "uniform", lda=1, ldb=1, ldc=72)
+    check_full(w)
+
+
+def test_alpha_zero_and_negative_products():
+    base = si.Workload("az", 200, 180, 96, "bf16", 0.0, True, 41, "uniform")
+    check_full(base)
+    A, B = si.make_operands(si.with_shape(base, lo=0.0, hi=1.0))
+    # A >= 0, B <= 0 (flip B's sign bit): with alpha > 0 every sum is <= 0.
+    Bn = B.copy()
+    Bn[:, : base.K] |= np.uint16(0x8000)
+    w = si.with_shape(base, alpha=1.0)
+    out = run_tg(w, A, Bn)
+    assert np.all(logical(out, w) == 0.0) and not np.any(np.signbit(logical(out, w)))
+    # Negative alpha flips which entries survive.
+    wn = si.with_shape(base, alpha=-1.0)
+    outn = run_tg(wn, A, Bn)
+    assert np.all(logical(outn, wn) > 0.0)
+
+
+def test_nan_input_propagates_through_relu():
+    w = si.Workload("nan", 130, 70, 40, "bf16", 1.0, True, 43, "uniform")
+    A, B = si.make_operands(w)
+    A[5, 3] = np.uint16(0x7FC0)
+    out = logical(run_tg(w, A, B), w)
+    assert np.all(np.isnan(out[5, :]))
+    assert not np.any(np.isnan(np.delete(out, 5, axis=0)))
+
+
+def test_repeated_calls_bitwise_identical():
+    w = si.Workload("rep", 513, 700, 1000, "bf16", 1.0, True, 47, "normal")
+    check_full(w, repeats=3)
+
+
+def test_invalid_arguments_launch_nothing():
+    import torch
+    import dense_gemm_epilogue_gb300 as tg
+
+    D = torch.full((10, 10), 7.0, device="cuda")
+    A = torch.zeros((10, 10), dtype=torch.int16, device="cuda")
+    assert tg.tg_gemm(10, 10, 10, 1.0, A, 9, A, 10, D, 10, "bf16", True) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_gemm(10, 10, 10, 1.0, A, 10, A, 10, D, 9, "bf16", True) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_gemm(10, 10, 10, 1.0, None, 10, A, 10, D, 10, "bf16", True) == \
+        tg.TG_ERR_INVALID_VALUE
+    torch.cuda.synchronize()
+    assert torch.all(D == 7.0)
+
+
+def test_wait_timeout_selftest_reports_status():
+    """A bounded wait on a barrier nothing completes runs out, records its
+    site and returns; the context stays usable."""
+    import torch
+    import dense_gemm_epilogue_gb300 as tg
+
+    assert tg.tg_check_device_status()[0] == tg.TG_OK
+    assert tg.tg_selftest_wait_timeout(2_000_000) == tg.TG_OK
+    st, where = tg.tg_check_device_status()
+    assert st == tg.TG_ERR_DEVICE_TIMEOUT and where == 7
+    assert tg.tg_check_device_status()[0] == tg.TG_OK      # cleared
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0                      # context still fine
+    check_full(si.WORKLOADS["c1_bf16_65x97x73"])
+
+
+@pytest.mark.parametrize("name", ["c5a_bf16_16384x64x4096", "c5b_bf16_64x16384x4096",
+                                  "c5c_bf16_8191x4097x1000", "c3_fp16_4096"])
+def test_large_configs_full(name):
+    check_full(si.WORKLOADS[name])
+
+
+def test_headline_8192_full():
+    """The 8192^3 BF16 + ReLU workload, every element against the oracle."""
+    check_full(si.WORKLOADS["c4_bf16_8192"])
