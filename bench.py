@@ -72,33 +72,38 @@ def workload_config(w: si.Workload, world: int) -> dict:
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_sample_time(w: si.Workload, A, B, cols: int, threads: int = 0) -> float:
-    """Wall time of the oracle on the sample D[:, 0:cols] (all rows, full K)."""
+def oracle_sample_time(w: si.Workload, A, B, rows: int, cols: int, threads: int = 0) -> float:
+    """Wall time of the oracle on the leading block D[0:rows, 0:cols] of the
+    workload (full K): the same arithmetic those entries get in the full
+    problem, since D[i, j] reads only row i of A and column j of B."""
     import oracle
 
     lda, ldb, _ = w.strides
+    As = np.ascontiguousarray(A[:rows])
     Bs = np.ascontiguousarray(B[:cols])
     t0 = time.perf_counter()
-    oracle.gemm(w.M, cols, w.K, w.alpha, A, lda, Bs, ldb, w.dtype, w.relu, threads=threads)
+    oracle.gemm(rows, cols, w.K, w.alpha, As, lda, Bs, ldb, w.dtype, w.relu, threads=threads)
     return time.perf_counter() - t0
 
 
-def calibrate_cols(w, A, B, target_s: float, max_cols: int) -> int:
-    t = oracle_sample_time(w, A, B, 2)
-    per_col = max(t / 2.0, 1e-6)
-    return int(max(2, min(max_cols, target_s / per_col)))
+def calibrate_block(w, A, B, target_s: float) -> int:
+    """Square sample size whose oracle time is about target_s."""
+    t = oracle_sample_time(w, A, B, 128, 128)
+    per_entry = max(t / (128.0 * 128.0), 1e-9)
+    s = int((target_s / per_entry) ** 0.5) // 64 * 64
+    return int(max(64, min(s, w.M, w.N)))
 
 
 def cpu_baseline(w: si.Workload, A, B, target_s: float = 15.0) -> dict:
     import oracle
 
-    cols = calibrate_cols(w, A, B, target_s, w.N)
-    t = oracle_sample_time(w, A, B, cols)
-    flops = 2.0 * w.M * cols * w.K
+    s = calibrate_block(w, A, B, target_s)
+    t = oracle_sample_time(w, A, B, s, s)
+    flops = 2.0 * s * s * w.K
     return {
         "value": flops / t / 1e12, "unit": UNIT, "cores": oracle.host_threads(), "kind": "oracle",
-        "sample": f"D[:, 0:{cols}] of the {w.M}x{w.N}x{w.K} workload (all rows, full K), "
-                  f"{t:.1f} s wall on the host cores, double-precision C triple loop",
+        "sample": f"D[0:{s}, 0:{s}] of the {w.M}x{w.N}x{w.K} workload (full K), {t:.1f} s wall "
+                  f"on the host cores, double-precision C triple loop",
     }
 
 
@@ -111,12 +116,12 @@ def run_reference(args, rank, world):
 
     # Size each step so that (warmup + steps) steps end within ~2.5 minutes.
     per_step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    cols = calibrate_cols(w, A, B, per_step_target, w.N)
+    blk = calibrate_block(w, A, B, per_step_target)
     for _ in range(args.warmup):
-        oracle_sample_time(w, A, B, cols)
-    times = [oracle_sample_time(w, A, B, cols) for _ in range(args.steps)]
+        oracle_sample_time(w, A, B, blk, blk)
+    times = [oracle_sample_time(w, A, B, blk, blk) for _ in range(args.steps)]
     total = sum(times)
-    flops = 2.0 * w.M * cols * w.K
+    flops = 2.0 * blk * blk * w.K
     value = flops * args.steps / total / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
@@ -126,8 +131,8 @@ def run_reference(args, rank, world):
         "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.host_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: D[:, 0:{cols}] of the 8192^3 workload (all rows, "
-                                   f"full K), double-precision C triple loop on the host cores"},
+                         "sample": f"each step: D[0:{blk}, 0:{blk}] of the 8192^3 workload "
+                                   f"(full K), double-precision C triple loop on the host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -81,27 +81,43 @@ def uniform01(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     return (x >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
 
 
+CHUNK = 1 << 20  # elements generated per pass (keeps temporaries in cache)
+
+
 def uniform_f32(seed: int, stream: int, count: int, lo: float, hi: float) -> np.ndarray:
-    u = uniform01(seed, stream, 0, count)
-    return (lo + (hi - lo) * u).astype(np.float32)
+    out = np.empty(count, dtype=np.float32)
+    for s0 in range(0, count, CHUNK):
+        n = min(CHUNK, count - s0)
+        u = uniform01(seed, stream, s0, n)
+        out[s0:s0 + n] = lo + (hi - lo) * u
+    return out
 
 
 def normal_f32(seed: int, stream: int, count: int, scale: float = 1.0) -> np.ndarray:
-    u = uniform01(seed, stream, 0, 2 * count)
-    u1 = u[0::2]
-    u2 = u[1::2]
-    z = np.sqrt(-2.0 * np.log1p(-u1)) * np.cos((2.0 * np.pi) * u2)
-    return (z * scale).astype(np.float32)
+    out = np.empty(count, dtype=np.float32)
+    for s0 in range(0, count, CHUNK):
+        n = min(CHUNK, count - s0)
+        u = uniform01(seed, stream, 2 * s0, 2 * n)
+        u1 = u[0::2]
+        u2 = u[1::2]
+        z = np.sqrt(-2.0 * np.log1p(-u1)) * np.cos((2.0 * np.pi) * u2)
+        out[s0:s0 + n] = z * scale
+    return out
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """IEEE round-to-nearest-even float32 -> bfloat16 bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    nan = (u & 0x7FFFFFFF) > 0x7F800000
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
-    r[nan] = ((u[nan] >> 16) | 0x40).astype(np.uint16)
-    return r
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).reshape(-1)
+    out = np.empty(u.shape, dtype=np.uint16)
+    for s0 in range(0, u.size, CHUNK):
+        c = u[s0:s0 + CHUNK]
+        with np.errstate(over="ignore"):
+            r = (c + np.uint32(0x7FFF) + ((c >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+        nan = (c & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+        if nan.any():
+            r = np.where(nan, (c >> np.uint32(16)) | np.uint32(0x40), r)
+        out[s0:s0 + CHUNK] = r
+    return out.reshape(np.shape(x))
 
 
 def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
