@@ -43,6 +43,7 @@ EXPORTED = (
     "tg_set_wait_limit_ns",
     "tg_selftest_wait_timeout",
     "tg_version",
+    "tg_gemm_noalloc",
 )
 
 
@@ -115,6 +116,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_set_wait_limit_ns.restype = ctypes.c_int
         lib.tg_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.tg_selftest_wait_timeout.restype = ctypes.c_int
+        lib.tg_gemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, vp, i64,
+                                        ctypes.c_int, ctypes.c_int, vp]
+        lib.tg_gemm_noalloc.restype = ctypes.c_int
         lib.tg_version.argtypes = []
         lib.tg_version.restype = i32
         if path is None:
@@ -180,6 +184,14 @@ def tg_gemm_ex(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, opts=
     """tg_gemm with planner overrides (dict of tg_options fields)."""
     return load().tg_gemm_ex(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
                              _dtype(in_dtype), _epi(epilogue), _options(opts), _stream(stream))
+
+
+def tg_gemm_noalloc(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue,
+                    stream=None) -> int:
+    """tg_gemm for callers that cannot allocate device memory (the library
+    allocates nothing in this call; see include/tg_gemm.h)."""
+    return load().tg_gemm_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
+                                  _dtype(in_dtype), _epi(epilogue), _stream(stream))
 
 
 def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):

@@ -174,6 +174,35 @@ tg_status tg_set_wait_limit_ns(uint64_t ns);
  */
 tg_status tg_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 
+/*
+ * tg_gemm for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this call; it exists for callers whose device memory is
+ * all held by their own pool allocator, that must avoid cudaMalloc's
+ * implicit synchronisation, or that run inside a stream capture where
+ * cudaMalloc is not allowed.
+ *
+ * Same arguments, results and errors as tg_gemm, and the same kernel and
+ * planner.  It calls no cudaMalloc, cudaFree or other allocating routine: the
+ * kernel's scratch (its 4-byte status word) lives in a fixed 256-byte,
+ * 256-byte-aligned __device__ array inside the library, which every device
+ * that loads the library holds until the process exits.  A plan needing more
+ * scratch than that returns TG_ERR_UNSUPPORTED before launching anything
+ * (no M, N, K does today: the status word does not grow with the problem).
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  All calls on a device share the array: each call
+ * clears the status word on its own stream first, and calls that overlap on
+ * the GPU (concurrent streams) race on it.  A wait that runs out still ends
+ * the kernel early, but this call does not report it (tg_check_device_status
+ * reads only tg_gemm's word); its waits use the default 4 s limit.
+ */
+tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                          const void *A, int64_t lda,
+                          const void *B, int64_t ldb,
+                          float *D, int64_t ldc,
+                          tg_dtype in_dtype, tg_epilogue epilogue, void *stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t tg_version(void);
 
