@@ -61,7 +61,8 @@ class tg_options(ctypes.Structure):
         ("swap_ab", ctypes.c_int32),
         ("raster_group", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("cta_pair", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -80,6 +81,7 @@ class tg_plan_info(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("tmem_cols", ctypes.c_int32),
         ("vector_store", ctypes.c_int32),
+        ("cta_pair", ctypes.c_int32),
     ]
 
 

@@ -104,6 +104,7 @@ tg_status device_state(int *dev_out, DeviceState **out) {
 // ------------------------------------------------------------------ planner
 
 struct Plan {
+    bool pair = false;  // CTA-pair kernel (256-row tiles over a 2-CTA cluster)
     bool swap = false;
     int block_n = 0;
     int producer = 0;  // 1 TMA, 2 plain loads
@@ -137,6 +138,17 @@ void config_numbers(int bn, int *stages, int *smem, int *threads, int *tmem) {
     }
 }
 
+template <Kind KD>
+void pair_numbers(int bn, int *stages, int *smem, int *threads, int *tmem) {
+    if (bn == 256) {
+        using C = tg::PairConfig<KD, 256>;
+        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
+    } else {
+        using C = tg::PairConfig<KD, 128>;
+        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
+    }
+}
+
 void config_numbers_for(tg_dtype t, int bn, int *stages, int *smem, int *threads, int *tmem) {
     if (t == TG_BF16) config_numbers<Kind::BF16>(bn, stages, smem, threads, tmem);
     else if (t == TG_FP16) config_numbers<Kind::FP16>(bn, stages, smem, threads, tmem);
@@ -165,7 +177,13 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
         if (o->producer < 0 || o->producer > 2) return TG_ERR_INVALID_VALUE;
         if (o->swap_ab < 0 || o->swap_ab > 2) return TG_ERR_INVALID_VALUE;
         if (o->raster_group < 0 || o->max_ctas < 0) return TG_ERR_INVALID_VALUE;
-        if (o->reserved[0] || o->reserved[1] || o->reserved[2]) return TG_ERR_INVALID_VALUE;
+        if (o->cta_pair < 0 || o->cta_pair > 2) return TG_ERR_INVALID_VALUE;
+        if (o->reserved[0] || o->reserved[1]) return TG_ERR_INVALID_VALUE;
+        // Overrides that cannot apply to this problem.
+        const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
+        if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
+        if (o->cta_pair == 2 && (t == TG_TF32 || !legal || o->producer == 2 || o->block_n == 64))
+            return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
 }
@@ -190,30 +208,55 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
     p.producer = o->producer ? o->producer : (legal ? 1 : 2);
 
-    // Tile N: the candidate with the fewest (waves x per-tile cost), where a
-    // tile's cost per K step is modelled as BN + 64 (the A operand's fixed
-    // share of shared-memory traffic makes narrow tiles less efficient).
-    const int64_t mblocks = ceil_div(p.mk, tg::BLOCK_M);
-    if (o->block_n) {
-        p.block_n = o->block_n;
-    } else {
-        int64_t best = -1;
-        for (int bn : {256, 128, 64}) {
-            const int64_t tiles = mblocks * ceil_div(p.nk, bn);
-            const int64_t est = ceil_div(tiles, sms) * (bn + 64);
-            if (best < 0 || est < best) {
-                best = est;
-                p.block_n = bn;
-            }
+    // Tile shape: the candidate with the smallest (waves x cycles per K step
+    // of one tile).  Per 16-wide K step an SM's tensor core needs BN/2 cycles
+    // (128 rows each), and its shared memory moves the A and B bytes twice
+    // (TMA write, tensor-core read) at about 128 B/cycle: 64 + BN/2 cycles for
+    // a single-CTA tile, 64 + BN/4 when a CTA pair splits B.  A tile costs the
+    // larger of the two.  Pair tiles need BF16/FP16 operands on TMA.
+    const bool pair_ok = t != TG_TF32 && p.producer == 1;
+    if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
+    if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
+    struct Cand { bool pair; int bn; };
+    Cand cands[5];
+    int nc = 0;
+    // Ties go to single-CTA tiles, then to the wider tile.
+    for (int bn : {256, 128, 64})
+        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 2) cands[nc++] = {false, bn};
+    for (int bn : {256, 128})
+        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 1 && pair_ok) cands[nc++] = {true, bn};
+    int64_t best = -1;
+    for (int i = 0; i < nc; ++i) {
+        const Cand c = cands[i];
+        const int rows = c.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
+        const int64_t tiles = ceil_div(p.mk, rows) * ceil_div(p.nk, c.bn);
+        const int64_t slots = c.pair ? sms / 2 : sms;
+        const int64_t mma = c.bn / 2;
+        const int64_t smem = c.pair ? 64 + c.bn / 4 : 64 + c.bn / 2;
+        const int64_t est = ceil_div(tiles, slots > 0 ? slots : 1) * (mma > smem ? mma : smem);
+        if (best < 0 || est < best) {
+            best = est;
+            p.pair = c.pair;
+            p.block_n = c.bn;
         }
     }
+    const int rows = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
+    const int64_t mblocks = ceil_div(p.mk, rows);
     p.tiles = mblocks * ceil_div(p.nk, p.block_n);
-    config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    if (p.pair) {
+        if (t == TG_BF16) pair_numbers<Kind::BF16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+        else pair_numbers<Kind::FP16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    } else {
+        config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    }
     int64_t g = o->raster_group ? o->raster_group : 16;
     if (g > mblocks) g = mblocks;
     p.group = (int)g;
-    int64_t grid = p.tiles < sms ? p.tiles : sms;
-    if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
+    const int64_t slots = p.pair ? sms / 2 : sms;
+    int64_t grid = p.tiles < slots ? p.tiles : slots;
+    if (p.pair) grid *= 2;
+    if (o->max_ctas && grid > o->max_ctas) grid = p.pair ? (o->max_ctas & ~1) : o->max_ctas;
+    if (grid < (p.pair ? 2 : 1)) grid = p.pair ? 2 : 1;
     p.grid = (int)grid;
     p.vector_store = p.swap && ((uintptr_t)D % 16 == 0) && (ldc % 4 == 0);
     *plan = p;
@@ -298,19 +341,25 @@ tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64
     const int64_t ldbr = plan.swap ? lda : ldb;
     la.block_n = plan.block_n;
     la.plain_loads = plan.producer == 2;
+    la.pair = plan.pair;
     if (!la.plain_loads) {
+        const int b_box = plan.pair ? plan.block_n / 2 : plan.block_n;
         const bool ok = encode_operand(&la.map_a, t, ar, plan.mk, K, ldar, tg::BLOCK_M) &&
-                        encode_operand(&la.map_b, t, br, plan.nk, K, ldbr, plan.block_n);
+                        encode_operand(&la.map_b, t, br, plan.nk, K, ldbr, b_box);
         if (!ok) {
-            if (opts && opts->producer == 1) return TG_ERR_INVALID_VALUE;
+            if (opts && (opts->producer == 1 || opts->cta_pair == 2)) return TG_ERR_INVALID_VALUE;
             la.plain_loads = true;  // shapes the TMA unit cannot describe
+            la.pair = false;
+            plan.pair = false;
+            plan.tiles = ceil_div(plan.mk, tg::BLOCK_M) * ceil_div(plan.nk, plan.block_n);
+            plan.grid = (int)(plan.tiles < ds->sms ? plan.tiles : ds->sms);
         }
     }
     tg::GemmParams &p = la.p;
     p.m = (int32_t)plan.mk;
     p.n = (int32_t)plan.nk;
     p.k = (int32_t)K;
-    p.num_m_blocks = (int32_t)ceil_div(plan.mk, tg::BLOCK_M);
+    p.num_m_blocks = (int32_t)ceil_div(plan.mk, plan.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
     p.num_n_blocks = (int32_t)ceil_div(plan.nk, plan.block_n);
     p.num_k_blocks = (int32_t)ceil_div(K, t == TG_TF32 ? 32 : 64);
     p.raster_group = plan.group;
@@ -377,7 +426,8 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     Plan p;
     st = make_plan(M, N, K, a, lda, b, ldb, d, ldc, in_dtype, opts, sms, &p);
     if (st != TG_OK) return st;
-    out->block_m = tg::BLOCK_M;
+    out->block_m = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
+    out->cta_pair = p.pair ? 1 : 0;
     out->block_n = p.block_n;
     out->block_k = in_dtype == TG_TF32 ? 32 : 64;
     out->stages = p.stages;

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "tg_kernel.cuh"
+#include "tg_kernel_pair.cuh"
 
 namespace tg {
 
@@ -12,9 +13,10 @@ struct LaunchArgs {
     GemmParams p;
     CUtensorMap map_a;   // A-role operand (unused by the plain-load producer)
     CUtensorMap map_b;   // B-role operand
-    int block_n;         // 64, 128 or 256
-    bool plain_loads;    // plain bounds-checked loads instead of TMA
-    int grid;            // persistent CTAs
+    int block_n;         // tile N: 64, 128 or 256 (single CTA); 128 or 256 (CTA pair)
+    bool plain_loads;    // plain bounds-checked loads instead of TMA (single CTA only)
+    bool pair;           // CTA-pair kernel (cluster of 2, cta_group::2 MMA)
+    int grid;            // persistent CTAs (even for the pair kernel)
     int device;          // current device ordinal (for the per-device attribute cache)
     cudaStream_t stream;
 };

@@ -179,20 +179,29 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     std::memset(&la, 0, sizeof(la));
     la.block_n = info.block_n;
     la.plain_loads = info.producer == 2;
+    la.pair = info.cta_pair != 0;
+    int64_t tiles = info.tiles;
+    int grid = info.grid;
     if (!la.plain_loads &&
         !(noalloc_encode(&la.map_a, in_dtype, ar, mk, K, ldar, tg::BLOCK_M) &&
-          noalloc_encode(&la.map_b, in_dtype, br, nk, K, ldbr, info.block_n)))
+          noalloc_encode(&la.map_b, in_dtype, br, nk, K, ldbr,
+                         la.pair ? info.block_n / 2 : info.block_n))) {
+        // Shapes the TMA unit cannot describe: single-CTA tiles, plain loads.
         la.plain_loads = true;
+        la.pair = false;
+        tiles = cdiv(mk, tg::BLOCK_M) * cdiv(nk, info.block_n);
+        grid = (int)(tiles < nd->sms ? tiles : nd->sms);
+    }
     tg::GemmParams &p = la.p;
     p.m = (int32_t)mk;
     p.n = (int32_t)nk;
     p.k = (int32_t)K;
-    p.num_m_blocks = (int32_t)cdiv(mk, tg::BLOCK_M);
+    p.num_m_blocks = (int32_t)cdiv(mk, la.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
     p.num_n_blocks = (int32_t)cdiv(nk, info.block_n);
     p.num_k_blocks = (int32_t)cdiv(K, info.block_k);
     p.raster_group = info.raster_group;
     p.relu = relu;
-    p.num_tiles = info.tiles;
+    p.num_tiles = tiles;
     p.alpha = alpha;
     p.vector_store = info.vector_store;
     p.d = D;
@@ -204,7 +213,7 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     p.ldb = ldbr;
     p.status = nd->scratch;
     p.wait_limit_ns = kNoAllocWaitLimitNs;
-    la.grid = info.grid;
+    la.grid = grid;
     la.device = dev;
     la.stream = stream;
 

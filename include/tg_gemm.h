@@ -105,13 +105,14 @@ typedef struct {
     int32_t swap_ab;      /* 0: planner; 1: never swap; 2: always swap the A/B roles */
     int32_t raster_group; /* 0: planner; else number of M tiles per raster group (>= 1) */
     int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
-    int32_t reserved[3];  /* must be zero */
+    int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (BF16/FP16, TMA) */
+    int32_t reserved[2];  /* must be zero */
 } tg_options;
 
 /* What the planner chose for one problem (host only; no CUDA call). */
 typedef struct {
-    int32_t block_m;      /* tile M of one CTA (128) */
-    int32_t block_n;      /* tile N of one CTA */
+    int32_t block_m;      /* tile M: 128 (single CTA) or 256 (CTA pair) */
+    int32_t block_n;      /* tile N */
     int32_t block_k;      /* K elements per pipeline stage (64 for 2-byte types, 32 for TF32) */
     int32_t stages;       /* shared-memory ring depth */
     int32_t producer;     /* 1 TMA, 2 plain loads */
@@ -123,6 +124,7 @@ typedef struct {
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
     int32_t tmem_cols;    /* tensor-memory columns per CTA */
     int32_t vector_store; /* 1 if the epilogue stores 16-byte vectors (swapped, aligned D) */
+    int32_t cta_pair;     /* 1 if a pair of CTAs (a 2-CTA cluster) computes each tile */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides

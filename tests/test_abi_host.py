@@ -63,7 +63,9 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(A=FAKE + 1), dict(D=FAKE + 2),
     dict(dtype=3), dict(epi=2),
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
-    dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"reserved": [1, 0, 0]}),
+    dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"reserved": [1, 0]}),
+    dict(opts={"cta_pair": 3}), dict(opts={"cta_pair": 2, "block_n": 64}),
+    dict(dtype=2, opts={"cta_pair": 2}),
 ])
 def test_invalid_arguments_rejected_before_cuda(tg, args):
     a = dict(M=10, N=10, K=10, A=FAKE, lda=10, B=FAKE, ldb=10, D=FAKE, ldc=10, dtype=0, epi=1,
@@ -91,11 +93,15 @@ def plan(tg, w, opts=None, sms=152, A=FAKE, B=FAKE, D=FAKE):
 
 def test_plan_headline_8192(tg):
     p = plan(tg, si.WORKLOADS["c4_bf16_8192"])
-    assert (p["block_m"], p["block_n"], p["block_k"]) == (128, 256, 64)
+    assert p["cta_pair"] == 1                       # 256 x 256 tiles over CTA pairs
+    assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 64)
     assert p["producer"] == 1 and p["swap_ab"] == 0
-    assert p["tiles"] == 64 * 32 and p["grid"] == 152
-    assert p["stages"] == 4 and p["tmem_cols"] == 512 and p["threads"] == 192
+    assert p["tiles"] == 32 * 32 and p["grid"] == 152
+    assert p["stages"] == 7 and p["tmem_cols"] == 512 and p["threads"] == 192
     assert p["smem_bytes"] <= 232448
+    s = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"cta_pair": 1})
+    assert (s["cta_pair"], s["block_m"], s["block_n"], s["tiles"]) == (0, 128, 256, 2048)
+    assert s["stages"] == 4
 
 
 def test_plan_tma_illegal_strides_use_plain_loads(tg):
@@ -119,13 +125,30 @@ def test_plan_skinny_shapes(tg):
 
 def test_plan_tf32(tg):
     p = plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])
-    assert p["block_k"] == 32 and p["threads"] == 320
+    assert p["block_k"] == 32 and p["threads"] == 320 and p["cta_pair"] == 0
+    with pytest.raises(tg.TgError):
+        plan(tg, si.WORKLOADS["c2_tf32_256x128x512"], opts={"cta_pair": 2})
+
+
+def test_plan_pair_grid_is_even_and_capped(tg):
+    w = si.WORKLOADS["c3_fp16_4096"]
+    p = plan(tg, w)
+    assert p["cta_pair"] == 1 and p["block_m"] == 256 and p["grid"] % 2 == 0
+    q = plan(tg, w, opts={"cta_pair": 2, "max_ctas": 7})
+    assert q["grid"] == 6
+    r = plan(tg, si.Workload("tiny", 200, 100, 64, "bf16", 1.0, True, 0, "uniform"),
+             opts={"cta_pair": 2})
+    assert r["tiles"] == 1 and r["grid"] == 2
 
 
 def test_plan_overrides(tg):
     w = si.WORKLOADS["c3_fp16_4096"]
-    p = plan(tg, w, opts={"block_n": 128, "max_ctas": 10, "raster_group": 4, "swap_ab": 2})
+    p = plan(tg, w, opts={"block_n": 128, "max_ctas": 10, "raster_group": 4, "swap_ab": 2,
+                          "cta_pair": 1})
     assert p["block_n"] == 128 and p["grid"] == 10 and p["raster_group"] == 4 and p["swap_ab"] == 1
-    p = plan(tg, w, opts={"raster_group": 1000})
+    p = plan(tg, w, opts={"raster_group": 1000, "cta_pair": 1})
     assert p["raster_group"] == 32                     # clamped to the M tile count
-    assert plan(tg, w, sms=7)["grid"] == 7
+    p = plan(tg, w, opts={"raster_group": 1000, "cta_pair": 2})
+    assert p["raster_group"] == 16                     # 256-row tiles
+    assert plan(tg, w, sms=7, opts={"cta_pair": 1})["grid"] == 7
+    assert plan(tg, w, sms=7)["grid"] == 6             # pairs: 3 clusters of 2

@@ -66,7 +66,25 @@ def test_every_config(dtype, block_n, producer):
     problem spanning several tiles in M, N and K."""
     w = si.Workload("cfg", 300, 520, 200, dtype, 1.25, True, 17, "uniform", lda=208, ldb=216,
                     ldc=304)
-    check_full(w, opts={"block_n": block_n, "producer": producer})
+    check_full(w, opts={"block_n": block_n, "producer": producer, "cta_pair": 1})
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (129, 300, 64), (513, 1000, 1000), (1, 17, 8)])
+def test_cta_pair_configs(dtype, block_n, M, N, K):
+    """CTA-pair tiles (256 rows over a 2-CTA cluster, cta_group::2 MMA):
+    ragged rows that leave the peer's half partly or wholly outside M."""
+    w = si.Workload("pair", M, N, K, dtype, 0.75, True, 19 + M + N, "uniform", ldc=M + 3)
+    check_full(w, opts={"cta_pair": 2, "block_n": block_n})
+
+
+def test_cta_pair_persistent_and_swapped():
+    w = si.Workload("pair_persist", 1100, 900, 320, "bf16", 1.0, True, 37, "normal")
+    for g in (2, 6):
+        check_full(w, opts={"cta_pair": 2, "max_ctas": g, "raster_group": 2})
+    ws = si.Workload("pair_swap", 100, 2000, 256, "fp16", 1.0, False, 38, "uniform", ldc=104)
+    check_full(ws, opts={"cta_pair": 2, "swap_ab": 2})
 
 
 @pytest.mark.parametrize("swap", [1, 2])
@@ -86,7 +104,7 @@ def test_persistent_multiple_tiles_per_cta():
     both tensor-memory accumulators are reused."""
     w = si.Workload("persist", 1000, 1100, 300, "bf16", 1.0, True, 31, "normal")
     for g in (1, 3, 7):
-        check_full(w, opts={"max_ctas": g, "raster_group": 2})
+        check_full(w, opts={"max_ctas": g, "raster_group": 2, "cta_pair": 1})
 
 
 def test_k_zero_gives_epilogue_of_zero():
