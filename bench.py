@@ -338,7 +338,10 @@ def run_gpu(args, rank, world, local):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"bf16_tflops (burst) of {peak_src}",
-                         "kernel": "tg_gemm_kernel<BF16, BN=256, TMA>",
+                         "kernel": ("tg_gemm_pair_kernel" if plan.get("cta_pair") else
+                                    "tg_gemm_kernel") +
+                                   f"<BF16, {plan['block_m']}x{plan['block_n']}, "
+                                   f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>",
                          "kernel_ms_avg": launch_avg_ms,
                          "algorithmic_flops_per_launch": flops},
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
