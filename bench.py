@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -290,27 +290,53 @@ def run_gpu(args, rank, world, local):
         raise tg.TgError(st, f"device status (wait site {where})")
     clocks = sampler.stop() if sampler else None
 
-    # End to end through the public API: pinned host A, B -> device, the
-    # call, D -> pinned host, every step.
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    with torch.cuda.stream(stream):
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        step()
-        hD.copy_(dD, non_blocking=True)
+    # End to end through the public API: every step copies its inputs A, B
+    # from pinned host memory, runs the call and reads D back to pinned host
+    # memory.  Steps are pipelined over two device buffer sets on three
+    # streams (H2D, compute, D2H), so step i+1's upload overlaps step i's
+    # download; the time is from the first upload to the last download.
+    e2e_steps = max(2, args.e2e_steps)
+    bufs = [(dA, dB, dD)]
+    bufs.append((torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dD)))
+    hDs = [hD, torch.empty_like(hD).pin_memory()]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_gemm = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step(i):
+        b = i % 2
+        a_, b_, d_ = bufs[b]
+        if i >= 2:
+            s_in.wait_event(ev_gemm[b])          # step i-2 has finished reading A, B
+        with torch.cuda.stream(s_in):
+            a_.copy_(hA, non_blocking=True)
+            b_.copy_(hB, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])         # step i-2's D has been read back
+        st_ = tg.tg_gemm(w.M, w.N, w.K, w.alpha, a_, lda, b_, ldb, d_, ldc, w.dtype, w.relu,
+                         stream)
+        if st_ != tg.TG_OK:
+            raise tg.TgError(st_, "tg_gemm")
+        ev_gemm[b].record(stream)
+        s_out.wait_event(ev_gemm[b])
+        with torch.cuda.stream(s_out):
+            hDs[b].copy_(d_, non_blocking=True)
+            ev_out[b].record(s_out)
+
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            step()
-            hD.copy_(dD, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_wall = time.perf_counter() - t_wall0
     barrier()
@@ -328,7 +354,15 @@ def run_gpu(args, rank, world, local):
         peaks, peak_src = load_peaks()
         launch_avg_ms = statistics.fmean(launch_ms)
         achieved = flops / (launch_avg_ms * 1e-3) / 1e12
-        peak = float(peaks["bf16_tflops"])
+        # Back-to-back launches for more than ~50 ms run in the power-capped
+        # regime the sustained peak was measured in; a short burst compares
+        # with the burst peak.  Both are reported.
+        sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
+        peak = float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+        first = launch_ms[: min(10, len(launch_ms))]
+        burst_ach = flops / (statistics.fmean(first) * 1e-3) / 1e12
+        burst_peak = float(peaks["bf16_tflops"])
+        qs = sorted(launch_ms)
         traffic = load_traffic(tg.source_hash())
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -337,7 +371,15 @@ def run_gpu(args, rank, world, local):
             "dtype": "bf16", "data": "synthetic", "config": workload_config(w, world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                         "peak_source": (f"bf16_tflops_sustained of {peak_src} (the timed region "
+                                         f"ran {region_ms:.0f} ms of back-to-back launches)"
+                                         if sustained else f"bf16_tflops (burst) of {peak_src}"),
+                         "burst": {"achieved": burst_ach, "peak": burst_peak,
+                                   "frac": burst_ach / burst_peak,
+                                   "launches": len(first),
+                                   "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+                         "kernel_ms_p10_p50_p90": [qs[len(qs) // 10], qs[len(qs) // 2],
+                                                   qs[(9 * len(qs)) // 10]],
                          "kernel": ("tg_gemm_pair_kernel" if plan.get("cta_pair") else
                                     "tg_gemm_kernel") +
                                    f"<BF16, {plan['block_m']}x{plan['block_n']}, "
@@ -347,7 +389,8 @@ def run_gpu(args, rank, world, local):
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
                     "d2h_bytes_per_step": int(w.N * ldc * 4),
-                    "steps": e2e_steps, "wall_s": e2e_wall},
+                    "steps": e2e_steps, "wall_s": e2e_wall,
+                    "pipelining": "2 buffer sets; H2D, compute and D2H on separate streams"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "plan": plan,

@@ -62,7 +62,8 @@ class tg_options(ctypes.Structure):
         ("raster_group", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("split_k", ctypes.c_int32),
+        ("l2_hint", ctypes.c_int32),
     ]
 
 
@@ -82,6 +83,8 @@ class tg_plan_info(ctypes.Structure):
         ("tmem_cols", ctypes.c_int32),
         ("vector_store", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
+        ("split_tiles", ctypes.c_int32),
+        ("split_segs", ctypes.c_int32),
     ]
 
 
@@ -167,11 +170,7 @@ def _options(opts):
         return ctypes.byref(opts)
     o = tg_options()
     for k, v in dict(opts).items():
-        if k == "reserved":
-            for i, r in enumerate(v):
-                o.reserved[i] = r
-        else:
-            setattr(o, k, int(v))
+        setattr(o, k, int(v))
     return ctypes.byref(o)
 
 

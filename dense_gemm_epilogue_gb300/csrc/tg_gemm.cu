@@ -16,6 +16,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/tg_gemm.h"
 #include "tg_launch.h"
@@ -76,6 +77,55 @@ struct DeviceState {
 std::mutex g_dev_mutex;
 DeviceState g_dev[kMaxDevices];
 
+// Split-K workspace of one (device, stream): room for `tiles` partial
+// 256 x 256 FP32 pair tiles and one ready flag per tile half (kept at zero
+// between launches by the kernel itself).
+struct Workspace {
+    int device;
+    cudaStream_t stream;
+    float *ws;
+    uint32_t *flags;
+    int64_t tiles;
+};
+std::mutex g_ws_mutex;
+std::vector<Workspace> g_ws;
+
+constexpr int64_t kPairTileFloats = 256 * 256;
+
+tg_status workspace_for(int dev, cudaStream_t stream, int64_t tiles, Workspace *out) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    for (Workspace &w : g_ws) {
+        if (w.device == dev && w.stream == stream && w.tiles >= tiles) {
+            *out = w;
+            return TG_OK;
+        }
+    }
+    Workspace w{dev, stream, nullptr, nullptr, tiles};
+    if (cudaMalloc(&w.ws, sizeof(float) * kPairTileFloats * tiles) != cudaSuccess) return TG_ERR_CUDA;
+    if (cudaMalloc(&w.flags, sizeof(uint32_t) * 2 * tiles) != cudaSuccess) {
+        cudaFree(w.ws);
+        return TG_ERR_CUDA;
+    }
+    if (cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * tiles) != cudaSuccess) return TG_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
+    // A smaller workspace of the same stream stays allocated (it may still be
+    // in use by queued work); the larger one replaces it for later calls.
+    for (Workspace &old : g_ws)
+        if (old.device == dev && old.stream == stream) old.stream = reinterpret_cast<cudaStream_t>(~uintptr_t(0));
+    g_ws.push_back(w);
+    *out = w;
+    return TG_OK;
+}
+
+// After a bounded wait ran out, flags may be left raised: clear them all.
+tg_status reset_workspace_flags(int dev) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    for (Workspace &w : g_ws)
+        if (w.device == dev && cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * w.tiles) != cudaSuccess)
+            return TG_ERR_CUDA;
+    return TG_OK;
+}
+
 // Per-device set-up on first use: device attributes and the status word.
 tg_status device_state(int *dev_out, DeviceState **out) {
     int dev = 0;
@@ -103,8 +153,33 @@ tg_status device_state(int *dev_out, DeviceState **out) {
 
 // ------------------------------------------------------------------ planner
 
+// Split-K tail: the kernel cuts each of the last R = tiles mod pairs tiles
+// into S = min(pairs / R, split_max, K blocks / 8) K segments (see
+// tg_kernel_pair.cuh); the host mirrors the rule to size and report it.
+// By default the split is used only when there are fewer tiles than pairs:
+// with a full wave or more, the GPU runs at its power limit and idle SMs in
+// the last wave only raise the clock of the others, so splitting adds
+// partial-sum traffic for no gain.
+constexpr int kDefaultSplitMax = 8;
+
+void split_rule(int64_t tiles, int64_t pairs, int64_t nkb, int split_max, int64_t ws_tiles,
+                int64_t *rem_out, int *segs_out) {
+    int64_t rem = tiles % pairs, segs = 1;
+    if (split_max > 1 && rem > 0) {
+        segs = pairs / rem;
+        if (segs > split_max) segs = split_max;
+        if (segs > nkb / tg::SPLIT_MIN_KBLOCKS) segs = nkb / tg::SPLIT_MIN_KBLOCKS;
+        if (segs < 2 || rem * (segs - 1) > ws_tiles) segs = 1;
+    }
+    *rem_out = segs > 1 ? rem : 0;
+    *segs_out = (int)segs;
+}
+
 struct Plan {
     bool pair = false;  // CTA-pair kernel (256-row tiles over a 2-CTA cluster)
+    int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
+    int64_t split_tiles = 0;
+    int split_segs = 1;
     bool swap = false;
     int block_n = 0;
     int producer = 0;  // 1 TMA, 2 plain loads
@@ -178,7 +253,8 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
         if (o->swap_ab < 0 || o->swap_ab > 2) return TG_ERR_INVALID_VALUE;
         if (o->raster_group < 0 || o->max_ctas < 0) return TG_ERR_INVALID_VALUE;
         if (o->cta_pair < 0 || o->cta_pair > 2) return TG_ERR_INVALID_VALUE;
-        if (o->reserved[0] || o->reserved[1]) return TG_ERR_INVALID_VALUE;
+        if (o->split_k < 0 || o->split_k > 64) return TG_ERR_INVALID_VALUE;
+        if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
         // Overrides that cannot apply to this problem.
         const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
         if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
@@ -216,6 +292,9 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     // larger of the two.  Pair tiles need BF16/FP16 operands on TMA.
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
     if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
+    // Pair tiles pay off on long K loops; at short K (few K blocks per tile)
+    // the single-CTA kernel measured as fast or faster.
+    const bool pair_auto = pair_ok && ceil_div(K, 64) >= 24;
     if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     struct Cand { bool pair; int bn; };
     Cand cands[5];
@@ -224,7 +303,9 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     for (int bn : {256, 128, 64})
         if ((!o->block_n || o->block_n == bn) && o->cta_pair != 2) cands[nc++] = {false, bn};
     for (int bn : {256, 128})
-        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 1 && pair_ok) cands[nc++] = {true, bn};
+        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 1 &&
+            (o->cta_pair == 2 ? pair_ok : pair_auto))
+            cands[nc++] = {true, bn};
     int64_t best = -1;
     for (int i = 0; i < nc; ++i) {
         const Cand c = cands[i];
@@ -249,15 +330,38 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     } else {
         config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
     }
-    int64_t g = o->raster_group ? o->raster_group : 16;
+    // Raster group: M tiles per group.  For 256-row pair tiles, 8 (a window
+    // of about 8 x 9.5 tiles per wave of 76 pairs) measured the least DRAM
+    // traffic at 8192^3 (1.07 GB per launch, against 1.25 GB for 16 and
+    // 1.48 GB for 4).
+    int64_t g = o->raster_group ? o->raster_group : (p.pair ? 8 : 16);
     if (g > mblocks) g = mblocks;
     p.group = (int)g;
-    const int64_t slots = p.pair ? sms / 2 : sms;
-    int64_t grid = p.tiles < slots ? p.tiles : slots;
-    if (p.pair) grid *= 2;
-    if (o->max_ctas && grid > o->max_ctas) grid = p.pair ? (o->max_ctas & ~1) : o->max_ctas;
-    if (grid < (p.pair ? 2 : 1)) grid = p.pair ? 2 : 1;
-    p.grid = (int)grid;
+    if (p.pair) {
+        // Pairs available, then the split: with fewer tiles than pairs the
+        // grid is sized for the tiles' K segments (so every segment gets a
+        // pair); otherwise for all pairs, and only the last partial wave can
+        // be split.  The kernel applies the same rule to its actual grid.
+        int64_t pairs_max = sms / 2;
+        if (o->max_ctas && pairs_max > o->max_ctas / 2) pairs_max = o->max_ctas / 2;
+        if (pairs_max < 1) pairs_max = 1;
+        p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 1);
+        const int64_t nkb = ceil_div(K, 64);
+        int64_t pairs = pairs_max;
+        if (p.tiles < pairs_max) {
+            int64_t segs = pairs_max / p.tiles;
+            if (segs > p.split_max) segs = p.split_max;
+            if (segs > nkb / tg::SPLIT_MIN_KBLOCKS) segs = nkb / tg::SPLIT_MIN_KBLOCKS;
+            if (segs < 1) segs = 1;
+            pairs = p.tiles * segs;
+        }
+        p.grid = (int)(2 * pairs);
+        split_rule(p.tiles, pairs, nkb, p.split_max, sms / 2, &p.split_tiles, &p.split_segs);
+    } else {
+        int64_t grid = p.tiles < sms ? p.tiles : sms;
+        if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
+        p.grid = (int)(grid < 1 ? 1 : grid);
+    }
     p.vector_store = p.swap && ((uintptr_t)D % 16 == 0) && (ldc % 4 == 0);
     *plan = p;
     return TG_OK;
@@ -376,6 +480,17 @@ tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64
     p.ldb = ldbr;
     p.status = ds->status;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.split_max = 1;
+    p.l2_hint = (opts && opts->l2_hint == 2) ? 1 : 0;
+    if (la.pair && plan.split_segs > 1) {
+        Workspace w;
+        st = workspace_for(dev, stream, ds->sms / 2, &w);
+        if (st != TG_OK) return st;
+        p.split_max = plan.split_max;
+        p.ws_tiles = (int32_t)w.tiles;
+        p.ws = w.ws;
+        p.flags = w.flags;
+    }
     la.grid = plan.grid;
     la.device = dev;
     la.stream = stream;
@@ -428,6 +543,8 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     if (st != TG_OK) return st;
     out->block_m = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
     out->cta_pair = p.pair ? 1 : 0;
+    out->split_tiles = (int32_t)p.split_tiles;
+    out->split_segs = p.split_segs;
     out->block_n = p.block_n;
     out->block_k = in_dtype == TG_TF32 ? 32 : 64;
     out->stages = p.stages;
@@ -465,6 +582,7 @@ tg_status tg_check_device_status(void *stream, int32_t *where) {
         return TG_ERR_CUDA;
     if (word == 0) return TG_OK;
     if (cudaMemset(ds->status, 0, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
+    if (reset_workspace_flags(dev) != TG_OK) return TG_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
     if (where) *where = (int32_t)word;
     return TG_ERR_DEVICE_TIMEOUT;

@@ -71,6 +71,7 @@ enum WaitSite : uint32_t {
     SITE_CONVERTED = 5,
     SITE_DRAIN = 6,
     SITE_SELFTEST = 7,
+    SITE_PARTIAL = 8,
 };
 
 struct GemmParams {
@@ -89,6 +90,16 @@ struct GemmParams {
     int64_t lda, ldb;               // role-space leading strides (elements)
     uint32_t *status;               // per-device status word
     uint64_t wait_limit_ns;
+    // Split-K tail (CTA-pair kernel only): at most `split_max` K segments per
+    // tail tile (1 = off); partial tiles go to `ws` (room for `ws_tiles`
+    // 256 x 256 pair tiles), with one ready flag per partial half in `flags`.
+    int32_t split_max;
+    int32_t ws_tiles;
+    float *ws;
+    uint32_t *flags;
+    // L2 policy of the operand loads (CTA-pair kernel): 0 default; 1 A-role
+    // rows evict-last (they are reused by every wave of a raster group).
+    int32_t l2_hint;
 };
 
 constexpr int BLOCK_M = 128;
@@ -187,6 +198,31 @@ __device__ __forceinline__ float apply_epilogue(float x, float alpha, int relu) 
     float y = alpha * x;
     if (relu) y = (y > 0.0f || y != y) ? y : 0.0f;  // max(y, 0): NaN stays, -0 -> +0
     return y;
+}
+
+// Epilogue store of one 32-column chunk of a row (role space): y = epi(v),
+// bounded by the problem's columns.  D is written once and never read back
+// by the kernel, so the stores are marked streaming (evict-first) to keep
+// the operands' lines in L2.
+__device__ __forceinline__ void store_chunk(const GemmParams &p, float *drow, int32_t col0,
+                                            const uint32_t (&v)[32]) {
+    if (p.vector_store && col0 + 32 <= p.n) {
+        float4 *dst = reinterpret_cast<float4 *>(drow + col0);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            __stcs(dst + j / 4, make_float4(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
+                                            apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
+                                            apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
+                                            apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu)));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col0 + j < p.n)
+                __stcs(drow + (int64_t)(col0 + j) * p.d_col_stride,
+                       apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu));
+        }
+    }
 }
 
 // Narrow one FP32 bit pattern to TF32: round the magnitude to 10 fraction
@@ -390,28 +426,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
-                const int32_t col0 = nb * BN + c0;
-                if (row_ok) {
-                    if (p.vector_store && col0 + 32 <= p.n) {
-                        float4 *dst = reinterpret_cast<float4 *>(drow + col0);
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            dst[j / 4] = make_float4(
-                                apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < p.n) {
-                                drow[(int64_t)(col0 + j) * p.d_col_stride] =
-                                    apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu);
-                            }
-                        }
-                    }
-                }
+                if (row_ok) store_chunk(p, drow, nb * BN + c0, v);
             }
             tc_fence_before();
             mbar_arrive(bar(C::ACCE0 + acc));

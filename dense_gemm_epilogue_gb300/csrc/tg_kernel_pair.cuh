@@ -103,6 +103,63 @@ __device__ __forceinline__ void pair_pause_ns(uint64_t ns) {
     }
 }
 
+// Work units.  With P pairs and T tiles, the first T - R tiles (R = T mod P)
+// are whole units; when the split is on, each of the last R tiles is cut
+// into S contiguous K segments (S = min(P / R, split_max, K blocks / 8), so the
+// R * S tail units fit in one round of the P pairs).  Pair p takes units
+// p, p + P, ...; a tail tile's segments land on consecutive pairs of the
+// last round.  Segments 0 .. S-2 store their FP32 partial accumulators to
+// the workspace and raise a flag; segment S-1 (on the highest-numbered of
+// those pairs, so it only waits on pairs dispatched before it) adds the
+// partials in segment order, applies the epilogue and stores D, so the
+// summation order is fixed and the result is deterministic.
+// A K segment spans at least this many K blocks, so that a segment's MMA
+// work outweighs the finisher's read of one partial tile.
+constexpr int SPLIT_MIN_KBLOCKS = 8;
+
+struct UnitPlan {
+    int64_t tiles, whole, units;  // tiles, whole-tile units, total units
+    int32_t segs;                 // K segments per tail tile (1: no split)
+};
+
+__device__ __forceinline__ UnitPlan make_unit_plan(const GemmParams &p, int64_t pairs) {
+    UnitPlan u;
+    u.tiles = p.num_tiles;
+    u.segs = 1;
+    const int64_t rem = p.num_tiles % pairs;
+    if (p.split_max > 1 && rem > 0) {
+        int64_t s = pairs / rem;
+        if (s > p.split_max) s = p.split_max;
+        if (s > p.num_k_blocks / SPLIT_MIN_KBLOCKS) s = p.num_k_blocks / SPLIT_MIN_KBLOCKS;
+        if (s > 1 && rem * (s - 1) <= p.ws_tiles) u.segs = (int32_t)s;
+    }
+    u.whole = u.segs > 1 ? p.num_tiles - rem : p.num_tiles;
+    u.units = u.whole + (p.num_tiles - u.whole) * u.segs;
+    return u;
+}
+
+struct Unit {
+    int64_t tile;
+    int32_t k0, k1;  // K blocks [k0, k1)
+    int32_t seg;     // -1: whole tile; else segment index of a tail tile
+    int64_t tail;    // tail-tile index (seg >= 0)
+};
+
+__device__ __forceinline__ Unit decode_unit(const UnitPlan &up, int64_t u, int nkb) {
+    Unit r;
+    if (u < up.whole) {
+        r.tile = u; r.k0 = 0; r.k1 = nkb; r.seg = -1; r.tail = 0;
+    } else {
+        const int64_t j = u - up.whole;
+        r.tail = j / up.segs;
+        r.seg = (int32_t)(j % up.segs);
+        r.tile = up.whole + r.tail;
+        r.k0 = (int32_t)((int64_t)r.seg * nkb / up.segs);
+        r.k1 = (int32_t)((int64_t)(r.seg + 1) * nkb / up.segs);
+    }
+    return r;
+}
+
 template <Kind KD, int BN>
 __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -125,6 +182,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     auto b_stage = [&](int s) -> uint32_t { return sbase + C::B_OFF + s * C::B_BYTES; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    volatile int *fin_ready = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
     const PairWaitCtl ctl{abort_flag, map_shared_rank(smem_u32(smem + C::MISC_OFF + 4), rank ^ 1u),
                           p.status, p.wait_limit_ns};
 
@@ -152,25 +210,34 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
+    const UnitPlan up = make_unit_plan(p, num_pairs);
 
     if (warp == 0) {
         // ------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
+            const uint64_t pol_a = l2_policy_evict_last();
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs) {
+            for (int64_t u = pair; ok && u < up.units; u += num_pairs) {
+                const Unit un = decode_unit(up, u, nkb);
                 int mb, nb;
-                tile_coords(t, p, mb, nb);
+                tile_coords(un.tile, p, mb, nb);
                 const int32_t arow = mb * C::PAIR_M + (int32_t)rank * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)rank * C::B_ROWS;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = un.k0; kb < un.k1; ++kb) {
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * (C::A_BYTES + C::B_BYTES));
-                    tma_load_2d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow);
-                    tma_load_2d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow);
+                    if (p.l2_hint) {
+                        tma_load_2d_pair_hint(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow,
+                                              pol_a);
+                        tma_load_2d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow);
+                    } else {
+                        tma_load_2d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow);
+                        tma_load_2d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow);
+                    }
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
@@ -190,7 +257,8 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             uint32_t ph = 0;
             uint32_t tl = 0;
             bool ok = true;
-            for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs, ++tl) {
+            for (int64_t u = pair; ok && u < up.units; u += num_pairs, ++tl) {
+                const Unit un = decode_unit(up, u, nkb);
                 const uint32_t acc = tl & 1, use = tl >> 1;
                 if (!pair_wait(bar(C::ACCE0 + acc), (use & 1) ^ 1, ctl, SITE_ACC_EMPTY)) {
                     ok = false;
@@ -198,14 +266,15 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = un.k0; kb < un.k1; ++kb) {
                     if (!pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
 #pragma unroll
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
                         mma_f16_pair(d_tmem, smem_desc_sw128(a0 + kk * 32),
-                                     smem_desc_sw128(b0 + kk * 32), C::IDESC, (kb | kk) != 0);
+                                     smem_desc_sw128(b0 + kk * 32), C::IDESC,
+                                     (kb != un.k0) || (kk != 0));
                     }
                     mma_commit_pair_mcast(bar(C::EMPTY0 + s), (uint16_t)0x3);
                     if (++s == S) { s = 0; ph ^= 1; }
@@ -229,43 +298,88 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         // ------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
         const int row_in_half = q * 32 + lane;
+        const int etid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
         uint32_t tl = 0;
-        for (int64_t t = pair; t < p.num_tiles; t += num_pairs, ++tl) {
+        for (int64_t u = pair; u < up.units; u += num_pairs, ++tl) {
+            const Unit un = decode_unit(up, u, nkb);
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            tile_coords(un.tile, p, mb, nb);
             const uint32_t acc = tl & 1, use = tl >> 1;
             if (!pair_wait(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
             tc_fence_after();
-            const int32_t r = mb * C::PAIR_M + (int32_t)rank * BLOCK_M + row_in_half;
-            const bool row_ok = r < p.m;
-            float *drow = p.d + (int64_t)r * p.d_row_stride;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            // Partial tile `k` of this tail tile, this CTA's half: column-major
+            // 128 rows x BN columns of FP32.
+            auto part = [&](int32_t k) -> float * {
+                const int64_t pidx = un.tail * (up.segs - 1) + k;
+                return p.ws + ((pidx * 2 + rank) * BN) * (int64_t)BLOCK_M;
+            };
+            auto flag = [&](int32_t k) -> uint32_t * {
+                return p.flags + (un.tail * (up.segs - 1) + k) * 2 + rank;
+            };
+            if (un.seg >= 0 && un.seg < up.segs - 1) {
+                // Writer: raw FP32 partial sums to the workspace, then the flag.
+                float *dst = part(un.seg);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + c0, v);
-                tmem_ld_wait();
-                const int32_t col0 = nb * BN + c0;
-                if (row_ok) {
-                    if (p.vector_store && col0 + 32 <= p.n) {
-                        float4 *dst = reinterpret_cast<float4 *>(drow + col0);
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c0, v);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            dst[j / 4] = make_float4(
-                                apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
-                                apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < p.n) {
-                                drow[(int64_t)(col0 + j) * p.d_col_stride] =
-                                    apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu);
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(dst + (int64_t)(c0 + j) * BLOCK_M + row_in_half, __uint_as_float(v[j]));
+                }
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (etid == 0) st_release_gpu_u32(flag(un.seg), 1u);
+            } else {
+                const bool finisher = un.seg >= 0;  // last segment of a tail tile
+                bool ready = true;
+                if (finisher) {
+                    // Wait (bounded) for the earlier segments' partials.
+                    if (etid == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        for (int32_t k = 0; k < up.segs - 1 && ready; ++k) {
+                            while (ld_acquire_gpu_u32(flag(k)) == 0u) {
+                                if (*abort_flag || globaltimer_ns() - t0 > p.wait_limit_ns) {
+                                    if (!*abort_flag) pair_raise_abort(ctl, SITE_PARTIAL);
+                                    ready = false;
+                                    break;
+                                }
                             }
                         }
                     }
+                    if (etid == 0) *fin_ready = ready ? 1 : 0;
+                    named_bar_sync(1, 128);
+                    ready = *fin_ready != 0;
+                    if (ready) {
+                        for (int32_t k = 0; k < up.segs - 1; ++k) (void)ld_acquire_gpu_u32(flag(k));
+                    }
+                }
+                const int32_t r = mb * C::PAIR_M + (int32_t)rank * BLOCK_M + row_in_half;
+                const bool row_ok = r < p.m;
+                float *drow = p.d + (int64_t)r * p.d_row_stride;
+#pragma unroll 1
+                for (int c0 = 0; ready && c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (finisher) {
+                        for (int32_t k = 0; k < up.segs - 1; ++k) {
+                            const float *src = part(k) + (int64_t)c0 * BLOCK_M + row_in_half;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                                       __ldcg(src + (int64_t)j * BLOCK_M));
+                        }
+                    }
+                    if (row_ok) store_chunk(p, drow, nb * BN + c0, v);
+                }
+                if (finisher) {
+                    // Leave the flags at zero for the next launch.
+                    named_bar_sync(1, 128);
+                    if (etid == 0 && ready)
+                        for (int32_t k = 0; k < up.segs - 1; ++k) *flag(k) = 0u;
                 }
             }
             tc_fence_before();

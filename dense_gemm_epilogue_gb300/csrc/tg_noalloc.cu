@@ -167,7 +167,10 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
 
-    st = tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, nullptr, nd->sms, &info);
+    // No split-K tail here: it would need a workspace.
+    tg_options no_split = {};
+    no_split.split_k = 1;
+    st = tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, &no_split, nd->sms, &info);
     if (st != TG_OK) return st;
     const bool swap = info.swap_ab != 0;
     const int64_t mk = swap ? N : M, nk = swap ? M : N;
@@ -213,6 +216,7 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     p.ldb = ldbr;
     p.status = nd->scratch;
     p.wait_limit_ns = kNoAllocWaitLimitNs;
+    p.split_max = 1;  // no split-K tail: it would need a workspace
     la.grid = grid;
     la.device = dev;
     la.stream = stream;

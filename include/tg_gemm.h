@@ -27,9 +27,13 @@
  * Ownership: every buffer and the stream belong to the caller and are only
  * borrowed for the call ("Walk through GEMM", section 2: views never copy,
  * allocate or make data ready).  A, B and D are device pointers (or memory the
- * device can address); D must not overlap A or B.  The library keeps small
- * per-device state of its own (a status word, cached device attributes);
- * it allocates that state on the first call on a device.
+ * device can address); D must not overlap A or B.  The library keeps state of
+ * its own: per device a status word and cached attributes, allocated on the
+ * first call on the device; and per (device, stream) a workspace of about
+ * 20 MB (the partial sums of split tail tiles, plus their ready flags),
+ * allocated on the first call on that stream that splits a tile and kept
+ * until the process exits.  Calls on different streams never share a
+ * workspace.
  *
  * Asynchrony: tg_gemm enqueues its work on `stream` (a cudaStream_t passed as
  * void*, NULL for the legacy default stream) and returns without waiting;
@@ -106,7 +110,11 @@ typedef struct {
     int32_t raster_group; /* 0: planner; else number of M tiles per raster group (>= 1) */
     int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
     int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (BF16/FP16, TMA) */
-    int32_t reserved[2];  /* must be zero */
+    int32_t split_k;      /* 0: planner (pair tiles fewer than pairs: split them into up to 8
+                             K segments of >= 8 K blocks); 1: never split; n >= 2: split the
+                             last, partial wave into at most n segments */
+    int32_t l2_hint;      /* 0: planner (default policy); 1: default L2 policy for operand loads;
+                             2: A-role rows evict-last (CTA-pair tiles) */
 } tg_options;
 
 /* What the planner chose for one problem (host only; no CUDA call). */
@@ -125,6 +133,8 @@ typedef struct {
     int32_t tmem_cols;    /* tensor-memory columns per CTA */
     int32_t vector_store; /* 1 if the epilogue stores 16-byte vectors (swapped, aligned D) */
     int32_t cta_pair;     /* 1 if a pair of CTAs (a 2-CTA cluster) computes each tile */
+    int32_t split_tiles;  /* tiles of the last wave computed as K segments (0: none) */
+    int32_t split_segs;   /* K segments per such tile (1: none) */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides

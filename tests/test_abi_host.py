@@ -63,7 +63,8 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(A=FAKE + 1), dict(D=FAKE + 2),
     dict(dtype=3), dict(epi=2),
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
-    dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"reserved": [1, 0]}),
+    dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
+    dict(opts={"split_k": -1}), dict(opts={"split_k": 65}),
     dict(opts={"cta_pair": 3}), dict(opts={"cta_pair": 2, "block_n": 64}),
     dict(dtype=2, opts={"cta_pair": 2}),
 ])
@@ -102,6 +103,31 @@ def test_plan_headline_8192(tg):
     s = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"cta_pair": 1})
     assert (s["cta_pair"], s["block_m"], s["block_n"], s["tiles"]) == (0, 128, 256, 2048)
     assert s["stages"] == 4
+
+
+def test_plan_split_tail(tg):
+    """K segments for pair tiles: by default only when there are fewer tiles
+    than pairs; forced, the last partial wave (R = tiles mod pairs tiles) is
+    cut into S = min(pairs // R, split_k, K blocks // 8) segments."""
+    c4 = plan(tg, si.WORKLOADS["c4_bf16_8192"])        # 1024 tiles on 76 pairs
+    assert (c4["split_tiles"], c4["split_segs"]) == (0, 1)
+    forced = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"split_k": 8})
+    assert (forced["split_tiles"], forced["split_segs"]) == (1024 % 76, 2)
+    small = plan(tg, si.Workload("s", 500, 500, 2048, "bf16", 1.0, True, 0, "normal"),
+                 opts={"cta_pair": 2, "block_n": 256})
+    assert small["cta_pair"] == 1 and small["tiles"] == 4
+    assert (small["split_tiles"], small["split_segs"]) == (4, 4)   # 32 K blocks / 8
+    short_k = plan(tg, si.Workload("s", 500, 500, 512, "bf16", 1.0, True, 0, "normal"),
+                   opts={"cta_pair": 2})
+    assert short_k["split_segs"] == 1                            # 8 K blocks: no split
+    single = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"cta_pair": 1, "split_k": 8})
+    assert (single["split_tiles"], single["split_segs"]) == (0, 1)
+
+
+def test_plan_pair_needs_long_k(tg):
+    c5c = plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])      # 16 K blocks
+    assert c5c["cta_pair"] == 0
+    assert plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"], opts={"cta_pair": 2})["cta_pair"] == 1
 
 
 def test_plan_tma_illegal_strides_use_plain_loads(tg):
@@ -150,5 +176,6 @@ def test_plan_overrides(tg):
     assert p["raster_group"] == 32                     # clamped to the M tile count
     p = plan(tg, w, opts={"raster_group": 1000, "cta_pair": 2})
     assert p["raster_group"] == 16                     # 256-row tiles
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["raster_group"] == 8
     assert plan(tg, w, sms=7, opts={"cta_pair": 1})["grid"] == 7
     assert plan(tg, w, sms=7)["grid"] == 6             # pairs: 3 clusters of 2

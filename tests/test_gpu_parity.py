@@ -87,6 +87,30 @@ def test_cta_pair_persistent_and_swapped():
     check_full(ws, opts={"cta_pair": 2, "swap_ab": 2})
 
 
+@pytest.mark.parametrize("M,N,K,max_ctas,split_k,segs", [
+    (300, 600, 1024, 8, 8, 2),     # 6 pair tiles on 4 pairs: 2 tail tiles x 2 segments
+    (1100, 200, 2104, 8, 8, 4),    # 5 tiles on 4 pairs: 1 tail tile x 4 segments (ragged K)
+    (1100, 200, 2104, 8, 3, 3),    # at most 3 segments
+    (700, 300, 1000, 4, 8, 1),     # 6 tiles on 2 pairs: none left over -> whole tiles only
+    (1100, 260, 1024, 16, 8, 2),   # 16 K blocks allow at most 2 segments of >= 8 blocks
+    (1100, 200, 2104, 8, 1, 1),    # split off
+    (500, 500, 2048, 0, 0, 4),     # default split: 4 tiles on all pairs -> 4 segments of 8 blocks
+])
+def test_split_k_tail(M, N, K, max_ctas, split_k, segs):
+    """The last, partial wave of pair tiles is cut into K segments whose
+    partial sums are added by the last segment in a fixed order: within the
+    tolerance, deterministic over repeated calls, flags left clean."""
+    import dense_gemm_epilogue_gb300 as tg
+
+    w = si.Workload("split", M, N, K, "bf16", 1.25, True, 53 + M + K, "normal", ldc=M + 5)
+    opts = {"cta_pair": 2, "block_n": 256, "max_ctas": max_ctas, "split_k": split_k}
+    lda, ldb, ldc = w.strides
+    plan = tg.tg_plan(M, N, K, None, lda, None, ldb, None, ldc, "bf16", opts)
+    assert plan["split_segs"] == segs
+    assert (plan["split_tiles"] > 0) == (segs > 1)
+    check_full(w, opts=opts, repeats=3)
+
+
 @pytest.mark.parametrize("swap", [1, 2])
 @pytest.mark.parametrize("M,N", [(64, 1000), (200, 333), (5, 700)])
 def test_swap_roles(swap, M, N):

@@ -30,6 +30,8 @@ CASES = [
     # Roles swapped (short M), FP16, no epilogue.
     si.Workload("noalloc_swap", 40, 900, 200, "fp16", -0.5, False, 72, "normal", scale=0.1,
                 ldc=44),
+    # CTA-pair tiles (long K), which tg_gemm would also split along K.
+    si.Workload("noalloc_pair", 600, 900, 2048, "bf16", 1.0, True, 74, "normal", ldc=600),
     # TF32 narrowing warps.
     si.Workload("noalloc_tf32", 300, 200, 96, "tf32", 1.0, False, 73, "uniform", lo=0.0),
 ]
