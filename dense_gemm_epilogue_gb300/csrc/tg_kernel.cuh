@@ -132,7 +132,11 @@ struct Config {
     static constexpr int USED_BYTES = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = USED_BYTES + 1024;  // slack for 1024-byte alignment
     static constexpr int TMEM_COLS = 2 * BN;               // two FP32 accumulators
-    static constexpr int NUM_WARPS = TF32 ? 10 : 6;
+    // Warps: producer, MMA, then epilogue warps (8 for 16-bit kinds: two per
+    // tensor-memory lane quarter, each taking half the columns; 4 for TF32,
+    // whose warps 6-9 narrow the stages instead).
+    static constexpr int EPI_WARPS = TF32 ? 4 : 8;
+    static constexpr int NUM_WARPS = TF32 ? 10 : 2 + EPI_WARPS;
     static constexpr int NUM_THREADS = NUM_WARPS * 32;
     static constexpr int MMAS_PER_STAGE = BK / T::umma_k;
     // Instruction descriptor: D FP32 (bit 4), A/B formats (bits 7-9, 10-12),
@@ -195,25 +199,37 @@ __device__ __forceinline__ void tile_coords(int64_t t, const GemmParams &p, int 
 }
 
 __device__ __forceinline__ float apply_epilogue(float x, float alpha, int relu) {
-    float y = alpha * x;
-    if (relu) y = (y > 0.0f || y != y) ? y : 0.0f;  // max(y, 0): NaN stays, -0 -> +0
-    return y;
+    const float y = alpha * x;
+    // max(y, 0) when ReLU is on: NaN stays NaN, -0 and negatives give +0.
+    return (relu && !(y > 0.0f) && !(y != y)) ? 0.0f : y;
 }
 
 // Epilogue store of one 32-column chunk of a row (role space): y = epi(v),
 // bounded by the problem's columns.  D is written once and never read back
 // by the kernel, so the stores are marked streaming (evict-first) to keep
-// the operands' lines in L2.
+// the operands' lines in L2.  A chunk that lies wholly inside the problem
+// takes a branch-free path that steps a pointer by the column stride.
 __device__ __forceinline__ void store_chunk(const GemmParams &p, float *drow, int32_t col0,
                                             const uint32_t (&v)[32]) {
-    if (p.vector_store && col0 + 32 <= p.n) {
-        float4 *dst = reinterpret_cast<float4 *>(drow + col0);
+    if (col0 + 32 <= p.n) {
+        if (p.vector_store) {
+            float4 *dst = reinterpret_cast<float4 *>(drow + col0);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            __stcs(dst + j / 4, make_float4(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
-                                            apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
-                                            apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
-                                            apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu)));
+            for (int j = 0; j < 32; j += 4) {
+                __stcs(dst + j / 4,
+                       make_float4(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
+                                   apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
+                                   apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
+                                   apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu)));
+            }
+        } else {
+            const int64_t cs = p.d_col_stride;
+            float *q = drow + (int64_t)col0 * cs;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                __stcs(q, apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu));
+                q += cs;
+            }
         }
     } else {
 #pragma unroll
@@ -298,7 +314,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(C::ACCF0 + a), 1);
-            mbar_init(bar(C::ACCE0 + a), 128);
+            mbar_init(bar(C::ACCE0 + a), C::EPI_WARPS);
         }
         mbar_init(bar(C::DRAIN), 1);
         *abort_flag = 0;
@@ -406,10 +422,12 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 2 + C::EPI_WARPS) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int row_in_tile = q * 32 + lane;
+        constexpr int COLS = BN / (C::EPI_WARPS / 4);  // columns of this warp
+        const int cbase = ((warp - 2) / 4) * COLS;
         uint32_t tl = 0;
         for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
             int mb, nb;
@@ -422,14 +440,15 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
             float *drow = p.d + (int64_t)r * p.d_row_stride;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = cbase; c0 < cbase + COLS; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
                 if (row_ok) store_chunk(p, drow, nb * BN + c0, v);
             }
             tc_fence_before();
-            mbar_arrive(bar(C::ACCE0 + acc));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::ACCE0 + acc));
         }
     } else if (C::TF32) {
         // ------------------------------------------------------ TF32 narrowing

@@ -57,7 +57,8 @@ struct PairConfig {
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int NUM_WARPS = 6;
+    static constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quarter
+    static constexpr int NUM_WARPS = 2 + EPI_WARPS;
     static constexpr int NUM_THREADS = NUM_WARPS * 32;
     static constexpr int MMAS_PER_STAGE = BK / T::umma_k;
     // Instruction descriptor as in the single-CTA kernel with M = 256.
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(C::ACCF0 + a), 1);
-            mbar_init(bar(C::ACCE0 + a), 2 * 4);
+            mbar_init(bar(C::ACCE0 + a), 2 * C::EPI_WARPS);
         }
         mbar_init(bar(C::DRAIN), 1);
         *abort_flag = 0;
@@ -298,7 +299,10 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         // ------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
         const int row_in_half = q * 32 + lane;
-        const int etid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+        constexpr int EPI_THREADS = C::EPI_WARPS * 32;
+        const int etid = threadIdx.x - 64;  // 0 .. EPI_THREADS-1 over the epilogue warps
+        constexpr int COLS = BN / (C::EPI_WARPS / 4);  // columns of this warp
+        const int cbase = ((warp - 2) / 4) * COLS;
         uint32_t tl = 0;
         for (int64_t u = pair; u < up.units; u += num_pairs, ++tl) {
             const Unit un = decode_unit(up, u, nkb);
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 // Writer: raw FP32 partial sums to the workspace, then the flag.
                 float *dst = part(un.seg);
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = cbase; c0 < cbase + COLS; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + c0, v);
                     tmem_ld_wait();
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                         __stcg(dst + (int64_t)(c0 + j) * BLOCK_M + row_in_half, __uint_as_float(v[j]));
                 }
                 __threadfence();
-                named_bar_sync(1, 128);
+                named_bar_sync(1, EPI_THREADS);
                 if (etid == 0) st_release_gpu_u32(flag(un.seg), 1u);
             } else {
                 const bool finisher = un.seg >= 0;  // last segment of a tail tile
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                         }
                     }
                     if (etid == 0) *fin_ready = ready ? 1 : 0;
-                    named_bar_sync(1, 128);
+                    named_bar_sync(1, EPI_THREADS);
                     ready = *fin_ready != 0;
                     if (ready) {
                         for (int32_t k = 0; k < up.segs - 1; ++k) (void)ld_acquire_gpu_u32(flag(k));
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 const bool row_ok = r < p.m;
                 float *drow = p.d + (int64_t)r * p.d_row_stride;
 #pragma unroll 1
-                for (int c0 = 0; ready && c0 < BN; c0 += 32) {
+                for (int c0 = cbase; ready && c0 < cbase + COLS; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + c0, v);
                     tmem_ld_wait();
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 if (finisher) {
                     // Leave the flags at zero for the next launch.
-                    named_bar_sync(1, 128);
+                    named_bar_sync(1, EPI_THREADS);
                     if (etid == 0 && ready)
                         for (int32_t k = 0; k < up.segs - 1; ++k) *flag(k) = 0u;
                 }

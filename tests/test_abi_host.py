@@ -98,7 +98,7 @@ def test_plan_headline_8192(tg):
     assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 64)
     assert p["producer"] == 1 and p["swap_ab"] == 0
     assert p["tiles"] == 32 * 32 and p["grid"] == 152
-    assert p["stages"] == 7 and p["tmem_cols"] == 512 and p["threads"] == 192
+    assert p["stages"] == 7 and p["tmem_cols"] == 512 and p["threads"] == 320
     assert p["smem_bytes"] <= 232448
     s = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"cta_pair": 1})
     assert (s["cta_pair"], s["block_m"], s["block_n"], s["tiles"]) == (0, 128, 256, 2048)
