@@ -292,9 +292,8 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     // larger of the two.  Pair tiles need BF16/FP16 operands on TMA.
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
     if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
-    // Pair tiles pay off on long K loops; at short K (few K blocks per tile)
-    // the single-CTA kernel measured as fast or faster.
-    const bool pair_auto = pair_ok && ceil_div(K, 64) >= 24;
+    // Pair tiles need a few K blocks to fill their 7-stage ring.
+    const bool pair_auto = pair_ok && ceil_div(K, 64) >= 8;
     if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     struct Cand { bool pair; int bn; };
     Cand cands[5];

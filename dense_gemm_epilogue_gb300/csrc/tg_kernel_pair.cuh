@@ -21,7 +21,7 @@
 //   acc_full  lives in both CTAs; the leader's commit at the end of a tile
 //             arrives on both epilogues.
 //   acc_empty lives in the leader; one lane of each epilogue warp of both
-//             CTAs arrives (count 8) once its warp's rows have been read.
+//             CTAs arrives (count 16) once its warp's part has been read.
 // The producers make no remote arrivals: a cluster-scope release per K step
 // costs a memory barrier on the issuing thread and throttles the TMA issue.
 // No TMA multicast is used: each CTA loads only its own rows.
@@ -388,7 +388,13 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_shared_rank(bar(C::ACCE0 + acc), 0));
+            // Release the accumulator to the leader's MMA.  The leader's warps
+            // arrive locally; the peer's arrive remotely without a cluster-scope
+            // release, which would first wait for this warp's D stores to drain.
+            if (lane == 0) {
+                if (leader) mbar_arrive(bar(C::ACCE0 + acc));
+                else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE0 + acc), 0));
+            }
         }
     }
 

@@ -198,6 +198,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
+// Arrive on a peer CTA's barrier with no memory ordering (no fence): for
+// signals that only order tensor-memory reads already completed by
+// tcgen05.wait::ld, not memory writes.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                      bar_cluster),

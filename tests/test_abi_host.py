@@ -124,10 +124,12 @@ def test_plan_split_tail(tg):
     assert (single["split_tiles"], single["split_segs"]) == (0, 1)
 
 
-def test_plan_pair_needs_long_k(tg):
+def test_plan_pair_needs_some_k(tg):
     c5c = plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])      # 16 K blocks
-    assert c5c["cta_pair"] == 0
-    assert plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"], opts={"cta_pair": 2})["cta_pair"] == 1
+    assert c5c["cta_pair"] == 1
+    short = si.Workload("s", 4096, 4096, 256, "bf16", 1.0, True, 0, "normal")   # 4 K blocks
+    assert plan(tg, short)["cta_pair"] == 0
+    assert plan(tg, short, opts={"cta_pair": 2})["cta_pair"] == 1
 
 
 def test_plan_tma_illegal_strides_use_plain_loads(tg):
