@@ -64,6 +64,8 @@ class tg_options(ctypes.Structure):
         ("cta_pair", ctypes.c_int32),
         ("split_k", ctypes.c_int32),
         ("l2_hint", ctypes.c_int32),
+        ("prefetch_k", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 
@@ -170,7 +172,11 @@ def _options(opts):
         return ctypes.byref(opts)
     o = tg_options()
     for k, v in dict(opts).items():
-        setattr(o, k, int(v))
+        if k == "reserved":
+            for i, r in enumerate(v):
+                o.reserved[i] = int(r)
+        else:
+            setattr(o, k, int(v))
     return ctypes.byref(o)
 
 

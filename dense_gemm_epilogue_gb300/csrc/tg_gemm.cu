@@ -255,6 +255,8 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
         if (o->cta_pair < 0 || o->cta_pair > 2) return TG_ERR_INVALID_VALUE;
         if (o->split_k < 0 || o->split_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
+        if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
+        if (o->reserved[0] || o->reserved[1] || o->reserved[2]) return TG_ERR_INVALID_VALUE;
         // Overrides that cannot apply to this problem.
         const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
         if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
@@ -481,6 +483,7 @@ tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
     p.l2_hint = (opts && opts->l2_hint == 2) ? 1 : 0;
+    p.prefetch_k = (opts && opts->prefetch_k > 0) ? opts->prefetch_k : 0;
     if (la.pair && plan.split_segs > 1) {
         Workspace w;
         st = workspace_for(dev, stream, ds->sms / 2, &w);

@@ -100,6 +100,10 @@ struct GemmParams {
     // L2 policy of the operand loads (CTA-pair kernel): 0 default; 1 A-role
     // rows evict-last (they are reused by every wave of a raster group).
     int32_t l2_hint;
+    // Single-CTA TMA producer: every 4 K blocks, prefetch the A-role box of
+    // the 4 K blocks `prefetch_k` ahead into L2 in one burst (0 = off), so
+    // DRAM sees 512 contiguous bytes of each row at once.
+    int32_t prefetch_k;
 };
 
 constexpr int BLOCK_M = 128;
@@ -253,36 +257,54 @@ __device__ __forceinline__ uint32_t narrow_tf32(uint32_t u) {
 
 // Plain-load producer: one stage of `rows` x BK elements into the 128-byte
 // swizzled K-major layout (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
+// Each lane takes chunks lane, lane + 32, ...; it issues the loads of 8
+// chunks before storing any of them, so 64 (or 32) loads are in flight per
+// lane instead of one chunk's worth.
 template <int ELEM_BYTES, int ROWS>
 __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, int64_t ld,
                                                  int32_t row0, int32_t rows_total, int32_t k0,
                                                  int32_t k_total, int lane) {
     constexpr int EPC = 16 / ELEM_BYTES;  // elements per 16-byte chunk
     constexpr int CHUNKS = ROWS * 8;
-    for (int ch = lane; ch < CHUNKS; ch += 32) {
-        const int r = ch >> 3, c = ch & 7;
-        const int32_t gr = row0 + r;
-        uint32_t w[4];
-        if (ELEM_BYTES == 2) {
-            const uint16_t *s = static_cast<const uint16_t *>(src);
-            uint16_t h[8];
+    constexpr int PER_LANE = CHUNKS / 32;
+    constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
+    static_assert(PER_LANE % BATCH == 0, "chunks per lane");
+#pragma unroll 1
+    for (int b0 = 0; b0 < PER_LANE; b0 += BATCH) {
+        uint32_t w[BATCH][4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int32_t gk = k0 + c * EPC + e;
-                h[e] = (gr < rows_total && gk < k_total) ? s[(int64_t)gr * ld + gk] : (uint16_t)0;
-            }
+        for (int i = 0; i < BATCH; ++i) {
+            const int ch = lane + (b0 + i) * 32;
+            const int r = ch >> 3, c = ch & 7;
+            const int32_t gr = row0 + r;
+            const bool row_in = gr < rows_total;
+            if (ELEM_BYTES == 2) {
+                const uint16_t *s = static_cast<const uint16_t *>(src) + (int64_t)gr * ld;
+                uint16_t h[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = (uint32_t)h[2 * e] | ((uint32_t)h[2 * e + 1] << 16);
-        } else {
-            const uint32_t *s = static_cast<const uint32_t *>(src);
+                for (int e = 0; e < 8; ++e) {
+                    const int32_t gk = k0 + c * EPC + e;
+                    h[e] = (row_in && gk < k_total) ? s[gk] : (uint16_t)0;
+                }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int32_t gk = k0 + c * EPC + e;
-                w[e] = (gr < rows_total && gk < k_total) ? s[(int64_t)gr * ld + gk] : 0u;
+                for (int e = 0; e < 4; ++e)
+                    w[i][e] = (uint32_t)h[2 * e] | ((uint32_t)h[2 * e + 1] << 16);
+            } else {
+                const uint32_t *s = static_cast<const uint32_t *>(src) + (int64_t)gr * ld;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int32_t gk = k0 + c * EPC + e;
+                    w[i][e] = (row_in && gk < k_total) ? s[gk] : 0u;
+                }
             }
         }
-        uint4 *out = reinterpret_cast<uint4 *>(dst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
-        *out = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            const int ch = lane + (b0 + i) * 32;
+            const int r = ch >> 3, c = ch & 7;
+            uint4 *out = reinterpret_cast<uint4 *>(dst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
+            *out = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
+        }
     }
 }
 
@@ -364,7 +386,17 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
             for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
+                if (p.prefetch_k > 0) {
+                    for (int j = 0; j < p.prefetch_k && j < nkb; ++j)
+                        tma_prefetch_l2_2d(&tmap_a, j * C::BK, mb * BLOCK_M);
+                }
                 for (int kb = 0; kb < nkb; ++kb) {
+                    if (p.prefetch_k > 0 && (kb & 3) == 0) {
+                        for (int j = 0; j < 4; ++j) {
+                            const int kp = kb + p.prefetch_k + j;
+                            if (kp < nkb) tma_prefetch_l2_2d(&tmap_a, kp * C::BK, mb * BLOCK_M);
+                        }
+                    }
                     if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(C::FULL0 + s), C::A_BYTES + C::B_BYTES);
                     tma_load_2d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M);

@@ -115,6 +115,9 @@ typedef struct {
                              last, partial wave into at most n segments */
     int32_t l2_hint;      /* 0: planner (default policy); 1: default L2 policy for operand loads;
                              2: A-role rows evict-last (CTA-pair tiles) */
+    int32_t prefetch_k;   /* 0: planner; -1: off; n > 0: single-CTA TMA tiles prefetch the A-role
+                             rows n K blocks ahead into L2, 4 blocks per burst */
+    int32_t reserved[3];  /* must be zero */
 } tg_options;
 
 /* What the planner chose for one problem (host only; no CUDA call). */

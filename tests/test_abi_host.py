@@ -64,7 +64,8 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(dtype=3), dict(epi=2),
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
-    dict(opts={"split_k": -1}), dict(opts={"split_k": 65}),
+    dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
+    dict(opts={"reserved": [0, 1, 0]}),
     dict(opts={"cta_pair": 3}), dict(opts={"cta_pair": 2, "block_n": 64}),
     dict(dtype=2, opts={"cta_pair": 2}),
 ])

@@ -118,6 +118,14 @@ def test_swap_roles(swap, M, N):
     check_full(w, opts={"swap_ab": swap})
 
 
+@pytest.mark.parametrize("prefetch_k", [4, 8, 16])
+def test_l2_prefetch_option(prefetch_k):
+    """Single-CTA TMA tiles with the A-role L2 burst prefetch (skinny N)."""
+    w = si.Workload("prefetch", 2000, 64, 1500, "bf16", 1.0, True, 57, "uniform", lda=1512,
+                    ldb=1504, ldc=2008)
+    check_full(w, opts={"cta_pair": 1, "prefetch_k": prefetch_k})
+
+
 def test_swap_scalar_store_unaligned_ldc():
     w = si.Workload("swap_ldc", 33, 900, 77, "fp16", 1.0, False, 29, "uniform", ldc=35)
     check_full(w, opts={"swap_ab": 2})
