@@ -330,6 +330,7 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
         else pair_numbers<Kind::FP16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
     } else {
         config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+        if (p.producer == 2) p.threads += 4 * 32;  // plain-load producer warps
     }
     // Raster group: M tiles per group.  For 256-row pair tiles, 8 (a window
     // of about 8 x 9.5 tiles per wave of 76 pairs) measured the least DRAM

@@ -23,7 +23,7 @@ static cudaError_t launch_one(const LaunchArgs &a) {
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    kernel<<<a.grid, C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(a.map_a, a.map_b, a.p);
+    kernel<<<a.grid, C::threads(PLAIN), C::SMEM_BYTES, a.stream>>>(a.map_a, a.map_b, a.p);
     return cudaGetLastError();
 }
 

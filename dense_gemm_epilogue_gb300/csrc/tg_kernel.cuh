@@ -141,6 +141,9 @@ struct Config {
     // whose warps 6-9 narrow the stages instead).
     static constexpr int EPI_WARPS = TF32 ? 4 : 8;
     static constexpr int NUM_WARPS = TF32 ? 10 : 2 + EPI_WARPS;
+    // The plain-load producer runs on LOAD_WARPS extra warps after these.
+    static constexpr int LOAD_WARPS = 4;
+    static constexpr int threads(bool plain) { return (NUM_WARPS + (plain ? LOAD_WARPS : 0)) * 32; }
     static constexpr int NUM_THREADS = NUM_WARPS * 32;
     static constexpr int MMAS_PER_STAGE = BK / T::umma_k;
     // Instruction descriptor: D FP32 (bit 4), A/B formats (bits 7-9, 10-12),
@@ -257,16 +260,16 @@ __device__ __forceinline__ uint32_t narrow_tf32(uint32_t u) {
 
 // Plain-load producer: one stage of `rows` x BK elements into the 128-byte
 // swizzled K-major layout (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
-// Each lane takes chunks lane, lane + 32, ...; it issues the loads of 8
-// chunks before storing any of them, so 64 (or 32) loads are in flight per
-// lane instead of one chunk's worth.
-template <int ELEM_BYTES, int ROWS>
+// Thread t of the NT loader threads takes chunks t, t + NT, ...; it issues
+// the loads of up to 8 chunks before storing any of them, so many loads are
+// in flight per thread instead of one chunk's worth.
+template <int ELEM_BYTES, int ROWS, int NT>
 __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, int64_t ld,
                                                  int32_t row0, int32_t rows_total, int32_t k0,
                                                  int32_t k_total, int lane) {
     constexpr int EPC = 16 / ELEM_BYTES;  // elements per 16-byte chunk
     constexpr int CHUNKS = ROWS * 8;
-    constexpr int PER_LANE = CHUNKS / 32;
+    constexpr int PER_LANE = CHUNKS / NT;
     constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
     static_assert(PER_LANE % BATCH == 0, "chunks per lane");
 #pragma unroll 1
@@ -274,7 +277,7 @@ __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, 
         uint32_t w[BATCH][4];
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
-            const int ch = lane + (b0 + i) * 32;
+            const int ch = lane + (b0 + i) * NT;
             const int r = ch >> 3, c = ch & 7;
             const int32_t gr = row0 + r;
             const bool row_in = gr < rows_total;
@@ -300,7 +303,7 @@ __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, 
         }
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
-            const int ch = lane + (b0 + i) * 32;
+            const int ch = lane + (b0 + i) * NT;
             const int r = ch >> 3, c = ch & 7;
             uint4 *out = reinterpret_cast<uint4 *>(dst + r * ROW_BYTES + ((c ^ (r & 7)) << 4));
             *out = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
@@ -309,7 +312,7 @@ __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, 
 }
 
 template <Kind KD, int BN, bool PLAIN_LOADS>
-__global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
+__global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
     tg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
     using C = Config<KD, BN>;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar(C::FULL0 + s), PLAIN_LOADS ? 32 : 1);
+            mbar_init(bar(C::FULL0 + s), PLAIN_LOADS ? C::LOAD_WARPS * 32 : 1);
             mbar_init(bar(C::EMPTY0 + s), 1);
             mbar_init(bar(C::CONV0 + s), 128);
         }
@@ -356,28 +359,33 @@ __global__ void __launch_bounds__(Config<KD, BN>::NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        if (PLAIN_LOADS) {
-            int s = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int mb, nb;
-                tile_coords(t, p, mb, nb);
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
-                    load_stage_plain<C::T::elem_bytes, BLOCK_M>(smem + C::A_OFF + s * C::A_BYTES,
+    if (PLAIN_LOADS && warp >= C::NUM_WARPS) {
+        // ------------------------------------------------------ plain-load producer
+        constexpr int NT = C::LOAD_WARPS * 32;
+        const int ltid = threadIdx.x - C::NUM_WARPS * 32;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                load_stage_plain<C::T::elem_bytes, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES,
                                                                 p.a_ptr, p.lda, mb * BLOCK_M, p.m,
-                                                                kb * C::BK, p.k, lane);
-                    load_stage_plain<C::T::elem_bytes, BN>(smem + C::B_OFF + s * C::B_BYTES,
+                                                                kb * C::BK, p.k, ltid);
+                load_stage_plain<C::T::elem_bytes, BN, NT>(smem + C::B_OFF + s * C::B_BYTES,
                                                            p.b_ptr, p.ldb, nb * BN, p.n,
-                                                           kb * C::BK, p.k, lane);
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(C::FULL0 + s));
-                    if (++s == S) { s = 0; ph ^= 1; }
-                }
+                                                           kb * C::BK, p.k, ltid);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::FULL0 + s));
+                if (++s == S) { s = 0; ph ^= 1; }
             }
+        }
+    } else if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (PLAIN_LOADS) {
+            // (the plain-load producer runs on the loader warps)
         } else if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;

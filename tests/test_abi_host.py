@@ -136,6 +136,7 @@ def test_plan_pair_needs_some_k(tg):
 def test_plan_tma_illegal_strides_use_plain_loads(tg):
     p = plan(tg, si.WORKLOADS["c1_bf16_65x97x73"])   # 73 * 2 bytes is not a multiple of 16
     assert p["producer"] == 2 and p["swap_ab"] == 0
+    assert p["threads"] == 320 + 128                  # plus 4 loader warps
     with pytest.raises(tg.TgError):
         plan(tg, si.WORKLOADS["c1_bf16_65x97x73"], opts={"producer": 1})
     # A misaligned base also rules TMA out.
