@@ -138,9 +138,11 @@ struct Config {
     static constexpr int TMEM_COLS = 2 * BN;               // two FP32 accumulators
     // Warps: producer, MMA, then epilogue warps (8 for 16-bit kinds: two per
     // tensor-memory lane quarter, each taking half the columns; 4 for TF32,
-    // whose warps 6-9 narrow the stages instead).
+    // which adds 8 warps that narrow each landed stage in place).
     static constexpr int EPI_WARPS = TF32 ? 4 : 8;
-    static constexpr int NUM_WARPS = TF32 ? 10 : 2 + EPI_WARPS;
+    static constexpr int CONV_WARPS = TF32 ? 8 : 0;  // TF32: narrow each landed stage
+    static constexpr int CONV_THREADS = CONV_WARPS * 32;
+    static constexpr int NUM_WARPS = 2 + EPI_WARPS + CONV_WARPS;
     // The plain-load producer runs on LOAD_WARPS extra warps after these.
     static constexpr int LOAD_WARPS = 4;
     static constexpr int threads(bool plain) { return (NUM_WARPS + (plain ? LOAD_WARPS : 0)) * 32; }
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(C::FULL0 + s), PLAIN_LOADS ? C::LOAD_WARPS * 32 : 1);
             mbar_init(bar(C::EMPTY0 + s), 1);
-            mbar_init(bar(C::CONV0 + s), 128);
+            mbar_init(bar(C::CONV0 + s), C::CONV_THREADS > 0 ? C::CONV_THREADS : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(C::ACCF0 + a), 1);
@@ -490,27 +492,34 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::ACCE0 + acc));
         }
-    } else if (C::TF32) {
+    } else if constexpr (C::TF32) {
         // ------------------------------------------------------ TF32 narrowing
-        const int ct = threadIdx.x - 6 * 32;  // 0..127
+        constexpr int NT = C::CONV_THREADS;
+        constexpr int NA = C::A_BYTES / 16 / NT, NB = C::B_BYTES / 16 / NT;
+        static_assert(C::A_BYTES / 16 % NT == 0 && C::B_BYTES / 16 % NT == 0, "stage split");
+        const int ct = threadIdx.x - (2 + C::EPI_WARPS) * 32;  // 0 .. NT-1
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!wait_phase(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
-                uint4 *a4 = reinterpret_cast<uint4 *>(smem + C::A_OFF + s * C::A_BYTES);
-                for (int i = ct; i < C::A_BYTES / 16; i += 128) {
-                    uint4 x = a4[i];
-                    a4[i] = make_uint4(narrow_tf32(x.x), narrow_tf32(x.y), narrow_tf32(x.z),
-                                       narrow_tf32(x.w));
-                }
-                uint4 *b4 = reinterpret_cast<uint4 *>(smem + C::B_OFF + s * C::B_BYTES);
-                for (int i = ct; i < C::B_BYTES / 16; i += 128) {
-                    uint4 x = b4[i];
-                    b4[i] = make_uint4(narrow_tf32(x.x), narrow_tf32(x.y), narrow_tf32(x.z),
-                                       narrow_tf32(x.w));
-                }
+                uint4 *a4 = reinterpret_cast<uint4 *>(smem + C::A_OFF + s * C::A_BYTES) + ct;
+                uint4 *b4 = reinterpret_cast<uint4 *>(smem + C::B_OFF + s * C::B_BYTES) + ct;
+                // All loads of this thread's share first, then narrow and store.
+                uint4 xa[NA], xb[NB];
+#pragma unroll
+                for (int i = 0; i < NA; ++i) xa[i] = a4[i * NT];
+#pragma unroll
+                for (int i = 0; i < NB; ++i) xb[i] = b4[i * NT];
+#pragma unroll
+                for (int i = 0; i < NA; ++i)
+                    a4[i * NT] = make_uint4(narrow_tf32(xa[i].x), narrow_tf32(xa[i].y),
+                                            narrow_tf32(xa[i].z), narrow_tf32(xa[i].w));
+#pragma unroll
+                for (int i = 0; i < NB; ++i)
+                    b4[i * NT] = make_uint4(narrow_tf32(xb[i].x), narrow_tf32(xb[i].y),
+                                            narrow_tf32(xb[i].z), narrow_tf32(xb[i].w));
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::CONV0 + s));
                 if (++s == S) { s = 0; ph ^= 1; }

@@ -155,7 +155,7 @@ def test_plan_skinny_shapes(tg):
 
 def test_plan_tf32(tg):
     p = plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])
-    assert p["block_k"] == 32 and p["threads"] == 320 and p["cta_pair"] == 0
+    assert p["block_k"] == 32 and p["threads"] == 448 and p["cta_pair"] == 0
     with pytest.raises(tg.TgError):
         plan(tg, si.WORKLOADS["c2_tf32_256x128x512"], opts={"cta_pair": 2})
 
