@@ -21,4 +21,5 @@ from .oracle import (  # noqa: F401
     gemm_entries,
     host_threads,
     library_path,
+    round_output,
 )

@@ -18,6 +18,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
 
 _DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2}
+_OUT_CODE = {"f32": 0, "bf16": 1, "fp16": 2}
 GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread"]
 
 _lock = threading.Lock()
@@ -65,6 +66,8 @@ class Oracle:
         lib.orc_gemm_entries.restype = ip
         lib.orc_decode_array.argtypes = [vp, i64, ip, vp]
         lib.orc_decode_array.restype = None
+        lib.orc_round_output.argtypes = [vp, i64, ip]
+        lib.orc_round_output.restype = None
         lib.orc_num_host_threads.argtypes = []
         lib.orc_num_host_threads.restype = ip
         self.lib = lib
@@ -113,6 +116,12 @@ class Oracle:
             raise ValueError(f"orc_gemm_entries failed with {rc}")
         return out, scale
 
+    def round_output(self, y, out_dtype: str) -> np.ndarray:
+        """The output step: round float64 values to fp32 / bf16 / fp16 (RNE)."""
+        arr = np.array(y, dtype=np.float64, copy=True)
+        self.lib.orc_round_output(arr.ctypes.data, arr.size, _OUT_CODE[out_dtype])
+        return arr
+
     def decode(self, bits, dtype: str) -> np.ndarray:
         """The oracle's own decode of storage elements to float64."""
         x = _check_storage(bits, dtype, "bits")
@@ -143,3 +152,7 @@ def gemm_entries(*args, **kw):
 
 def decode(bits, dtype):
     return default().decode(bits, dtype)
+
+
+def round_output(y, out_dtype):
+    return default().round_output(y, out_dtype)

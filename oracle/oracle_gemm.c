@@ -18,6 +18,9 @@
  *   4. if ReLU: y = max(y, 0) with Julia's max semantics (... then the max
  *      with zero): NaN stays NaN, -0 becomes +0;
  *   5. D_ref[i + j*ldd] = y, as double.
+ *   6. (narrow outputs) orc_round_output rounds y to the output format.
+ * A batched GEMM is that definition applied to each batch entry on its own;
+ * the oracle's callers step the operand pointers.
  *
  * Storage ("Walk through GEMM", section 2 "Bind runtime global arrays"):
  *   A logical (M,K), K-contiguous:  a(i,k) = A[i*lda + k]
@@ -281,6 +284,47 @@ int orc_gemm_entries(int64_t M, int64_t N, int64_t K, double alpha,
     for (int t = started + 1; t < nthreads; ++t) entry_worker(&jobs[t]);
     free(jobs); free(tids);
     return 0;
+}
+
+/*
+ * Narrow output ("Matrix Multiplication", Step 4: keep the FP32 accumulator
+ * and convert on the way out).  Rounds a double to a binary format with
+ * `p` significand bits (implicit bit included), minimum normal exponent
+ * `emin` and maximum exponent `emax`, to nearest with ties to even; values
+ * beyond the largest finite number become infinity; NaN, infinities and
+ * signed zeros pass through.  Below 2^emin the quantum stays 2^(emin-p+1)
+ * (subnormals).
+ *   bf16: p = 8,  emin = -126, emax = 127
+ *   fp16: p = 11, emin = -14,  emax = 15
+ */
+static double round_format(double y, int p, int emin, int emax) {
+    if (isnan(y) || isinf(y) || y == 0.0) return y;
+    double a = fabs(y);
+    int e;
+    frexp(a, &e);         /* a in [2^(e-1), 2^e) */
+    int ee = e - 1;
+    if (ee < emin) ee = emin;
+    double quantum = ldexp(1.0, ee - (p - 1));
+    double q = a / quantum; /* exact: a power-of-two scaling */
+    double fq = floor(q);
+    double r = q - fq;
+    if (r > 0.5 || (r == 0.5 && fmod(fq, 2.0) == 1.0)) fq += 1.0;
+    double out = fq * quantum;
+    double maxf = ldexp(2.0 - ldexp(1.0, -(p - 1)), emax);
+    if (out > maxf) out = INFINITY;
+    return copysign(out, y);
+}
+
+/* Output formats: 0 = fp32, 1 = bf16, 2 = fp16.  In place on y[0..n). */
+void orc_round_output(double *y, int64_t n, int out_fmt) {
+    for (int64_t q = 0; q < n; ++q) {
+        switch (out_fmt) {
+        case 0: y[q] = round_format(y[q], 24, -126, 127); break;
+        case 1: y[q] = round_format(y[q], 8, -126, 127); break;
+        case 2: y[q] = round_format(y[q], 11, -14, 15); break;
+        default: break;
+        }
+    }
 }
 
 /* Decode a whole array of storage elements (for the decode pins). */

@@ -345,6 +345,63 @@ def check_degenerate(orc):
                     "bf16", True).shape == (3, 0)
 
 
+def rne_reference(x: float, p: int, emin: int, emax: int) -> float:
+    """Round to nearest even with exact rational arithmetic (a second
+    formulation of the output rounding, independent of the oracle's)."""
+    if math.isnan(x) or math.isinf(x) or x == 0.0:
+        return x
+    a = Fraction(abs(x))
+    e = 0
+    while a >= 2 ** (e + 1):
+        e += 1
+    while a < Fraction(2) ** e:
+        e -= 1
+    e = max(e, emin)
+    quantum = Fraction(2) ** (e - (p - 1))
+    q = a / quantum
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    out = fl * quantum
+    if out > (2 - Fraction(2) ** (1 - p)) * Fraction(2) ** emax:
+        return math.copysign(math.inf, x)
+    return math.copysign(float(out), x)
+
+
+def round_probe_values(seed=13, n=3000):
+    vals = [1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -11, 1.0 + 3 * 2 ** -11, 65504.0,
+            65519.99, 65520.0, 65536.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14,
+            (2 - 2 ** -8) * 2.0 ** 127, (2 - 2 ** -9) * 2.0 ** 127, 2.0 ** -133, 2.0 ** -134,
+            3 * 2.0 ** -135, 1e-40, 3.4e38, -0.0, 0.0, math.inf, -math.inf, -1.5]
+    u = si.raw_u64(seed, 0, 0, n)
+    mant = (u >> np.uint64(11)).astype(np.float64) * 2.0 ** -53 + 1.0
+    expo = (u % np.uint64(80)).astype(np.int64) - 40
+    sign = np.where((u >> np.uint64(7)) & np.uint64(1), -1.0, 1.0)
+    vals += list(sign * np.ldexp(mant, expo))
+    return np.array(vals, dtype=np.float64)
+
+
+def check_round_output(orc):
+    """Output rounding ("convert on the way out") against numpy's own float32 /
+    float16 conversions and an exact rational round-to-nearest-even."""
+    x = round_probe_values()
+    f32 = orc.round_output(x, "f32")
+    with np.errstate(over="ignore"):
+        assert np.array_equal(f32, x.astype(np.float32).astype(np.float64))
+        f16 = orc.round_output(x, "fp16")
+        want16 = x.astype(np.float16).astype(np.float64)
+    assert np.array_equal(f16, want16)
+    assert np.array_equal(np.signbit(f16), np.signbit(want16))
+    bf = orc.round_output(x, "bf16")
+    wantbf = np.array([rne_reference(float(v), 8, -126, 127) for v in x])
+    assert np.array_equal(bf, wantbf)
+    assert np.array_equal(np.signbit(bf), np.signbit(wantbf))
+    # Hand-worked: bf16 keeps 8 significant bits; ties go to the even neighbour.
+    hand = orc.round_output([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 255.5, 256.5, 257.0], "bf16")
+    assert list(hand) == [1.0, 1.0 + 2 ** -6, 256.0, 256.0, 256.0]
+
+
 ALL_CHECKS = [
     check_decode_tables,
     check_tf32_narrowing,
@@ -361,4 +418,5 @@ ALL_CHECKS = [
     check_entries_match_full,
     check_thread_independent,
     check_degenerate,
+    check_round_output,
 ]

@@ -33,6 +33,11 @@ MUTANTS = {
     "relu_before_alpha": ("double y = alpha * s;\n    return relu ? relu_max(y) : y;",
                           "return relu ? alpha * relu_max(s) : alpha * s;"),
     "alpha_dropped": ("double y = alpha * s;", "double y = s;"),
+    "round_ties_away": ("if (r > 0.5 || (r == 0.5 && fmod(fq, 2.0) == 1.0)) fq += 1.0;",
+                        "if (r >= 0.5) fq += 1.0;"),
+    "round_no_overflow": ("if (out > maxf) out = INFINITY;", "if (0) out = INFINITY;"),
+    "round_fp16_emin": ("case 2: y[q] = round_format(y[q], 11, -14, 15); break;",
+                        "case 2: y[q] = round_format(y[q], 11, -15, 15); break;"),
     "scale_signed_alpha": ("jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;",
                            "jb->scale[i + j * jb->ldd] = jb->alpha * t;"),
 }
