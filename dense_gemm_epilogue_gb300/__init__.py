@@ -33,6 +33,11 @@ DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32}
 TG_EPILOGUE_NONE = 0
 TG_EPILOGUE_RELU = 1
 
+TG_OUT_F32 = 0
+TG_OUT_BF16 = 1
+TG_OUT_F16 = 2
+OUT_CODES = {"f32": TG_OUT_F32, "bf16": TG_OUT_BF16, "fp16": TG_OUT_F16}
+
 # Every symbol include/tg_gemm.h declares.
 EXPORTED = (
     "tg_gemm",
@@ -44,6 +49,7 @@ EXPORTED = (
     "tg_selftest_wait_timeout",
     "tg_version",
     "tg_gemm_noalloc",
+    "tg_gemm_batched",
 )
 
 
@@ -126,6 +132,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_gemm_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, vp, i64,
                                         ctypes.c_int, ctypes.c_int, vp]
         lib.tg_gemm_noalloc.restype = ctypes.c_int
+        lib.tg_gemm_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, i64, vp, i64,
+                                        i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(tg_options), vp]
+        lib.tg_gemm_batched.restype = ctypes.c_int
         lib.tg_version.argtypes = []
         lib.tg_version.restype = i32
         if path is None:
@@ -199,6 +209,15 @@ def tg_gemm_noalloc(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue,
     allocates nothing in this call; see include/tg_gemm.h)."""
     return load().tg_gemm_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
                                   _dtype(in_dtype), _epi(epilogue), _stream(stream))
+
+
+def tg_gemm_batched(M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, D, ldc, stride_d, batch,
+                    in_dtype, out_dtype, epilogue, opts=None, stream=None) -> int:
+    """Strided batch of GEMMs with an output type (f32, bf16 or fp16)."""
+    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+    return load().tg_gemm_batched(M, N, K, alpha, _ptr(A), lda, stride_a, _ptr(B), ldb, stride_b,
+                                  _ptr(D), ldc, stride_d, batch, _dtype(in_dtype), out,
+                                  _epi(epilogue), _options(opts), _stream(stream))
 
 
 def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):

@@ -23,15 +23,20 @@
 
 namespace tg {
 
-// D = epi(alpha * 0) over the M x N output: the K == 0 case (empty sums).
-__global__ void tg_fill_empty_sum_kernel(float *d, int64_t m, int64_t n, int64_t ldc, float alpha,
+// D = epi(alpha * 0) over every M x N output of the batch: the K == 0 case
+// (empty sums), in the output format.
+__global__ void tg_fill_empty_sum_kernel(void *d, int64_t m, int64_t n, int64_t ldc,
+                                         int64_t stride_d, int64_t batch, int out_fmt, float alpha,
                                          int relu) {
     const float v = apply_epilogue(0.0f, alpha, relu);
-    const int64_t total = m * n;
+    const int64_t per = m * n, total = per * batch;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i % m, c = i / m;
-        d[r + c * ldc] = v;
+        const int64_t b = i / per, e = i - b * per;
+        const int64_t off = b * stride_d + (e % m) + (e / m) * ldc;
+        if (out_fmt == 0) static_cast<float *>(d)[off] = v;
+        else if (out_fmt == 1) static_cast<unsigned short *>(d)[off] = OutFormat<1>::cvt(v);
+        else static_cast<unsigned short *>(d)[off] = OutFormat<2>::cvt(v);
     }
 }
 
@@ -175,6 +180,24 @@ void split_rule(int64_t tiles, int64_t pairs, int64_t nkb, int split_max, int64_
     *segs_out = (int)segs;
 }
 
+// One call's problem: a batch of `batch` GEMMs of the same shape.
+struct Problem {
+    int64_t M, N, K;
+    float alpha;
+    const void *A;
+    int64_t lda, sa;  // leading stride, batch stride (elements of the input type)
+    const void *B;
+    int64_t ldb, sb;
+    void *D;
+    int64_t ldc, sd;  // elements of the output type
+    int64_t batch;
+    tg_dtype t;
+    int out_fmt;      // 0 FP32, 1 BF16, 2 FP16
+    int relu;
+};
+
+int out_bytes(int out_fmt) { return out_fmt == 0 ? 4 : 2; }
+
 struct Plan {
     bool pair = false;  // CTA-pair kernel (256-row tiles over a 2-CTA cluster)
     int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
@@ -186,7 +209,8 @@ struct Plan {
     int stages = 0;
     int group = 0;
     int grid = 0;
-    int64_t tiles = 0;
+    int64_t tiles = 0;            // all tiles of the batch
+    int64_t tiles_per_batch = 0;
     int threads = 0;
     int smem = 0;
     int tmem_cols = 0;
@@ -235,17 +259,33 @@ bool tma_legal(const void *p, int64_t ld, int esize) {
     return ((uintptr_t)p % 16) == 0 && stride % 16 == 0 && stride < (1ull << 40);
 }
 
-tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
-                   int64_t ldb, const float *D, int64_t ldc, tg_dtype t, const tg_options *o) {
+// A batch stride the TMA can address as a third tensor dimension (a zero
+// stride, one operand for every batch entry, needs no dimension at all).
+bool tma_batch_legal(int64_t stride, int esize, int64_t batch) {
+    if (batch <= 1 || stride == 0) return true;
+    const uint64_t bytes = (uint64_t)stride * (uint64_t)esize;
+    return bytes % 16 == 0 && bytes < (1ull << 40);
+}
+
+tg_status validate(const Problem &q, const tg_options *o) {
+    const tg_dtype t = q.t;
+    const int64_t M = q.M, N = q.N, K = q.K;
     if (t != TG_BF16 && t != TG_FP16 && t != TG_TF32) return TG_ERR_INVALID_VALUE;
-    if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_VALUE;
-    if (lda < (K > 1 ? K : 1) || ldb < (K > 1 ? K : 1) || ldc < (M > 1 ? M : 1))
+    if (q.out_fmt < 0 || q.out_fmt > 2) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || q.batch < 0) return TG_ERR_INVALID_VALUE;
+    if (q.lda < (K > 1 ? K : 1) || q.ldb < (K > 1 ? K : 1) || q.ldc < (M > 1 ? M : 1))
         return TG_ERR_INVALID_VALUE;
-    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TG_ERR_UNSUPPORTED;
-    const int e = elem_bytes(t);
-    if (M * K > 0 && (A == nullptr || (uintptr_t)A % e)) return TG_ERR_INVALID_VALUE;
-    if (K * N > 0 && (B == nullptr || (uintptr_t)B % e)) return TG_ERR_INVALID_VALUE;
-    if (M * N > 0 && (D == nullptr || (uintptr_t)D % 4)) return TG_ERR_INVALID_VALUE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || q.batch > INT32_MAX)
+        return TG_ERR_UNSUPPORTED;
+    if (q.batch > 1) {
+        // Operands may be shared by all batch entries (stride 0); outputs may not.
+        if (q.sa < 0 || q.sb < 0) return TG_ERR_INVALID_VALUE;
+        if (M * N > 0 && q.sd < q.ldc * N) return TG_ERR_INVALID_VALUE;
+    }
+    const int e = elem_bytes(t), eo = out_bytes(q.out_fmt);
+    if (M * K > 0 && (q.A == nullptr || (uintptr_t)q.A % e)) return TG_ERR_INVALID_VALUE;
+    if (K * N > 0 && (q.B == nullptr || (uintptr_t)q.B % e)) return TG_ERR_INVALID_VALUE;
+    if (M * N > 0 && (q.D == nullptr || (uintptr_t)q.D % eo)) return TG_ERR_INVALID_VALUE;
     if (o) {
         if (o->block_n != 0 && o->block_n != 64 && o->block_n != 128 && o->block_n != 256)
             return TG_ERR_INVALID_VALUE;
@@ -258,7 +298,8 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
         if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->reserved[0] || o->reserved[1] || o->reserved[2]) return TG_ERR_INVALID_VALUE;
         // Overrides that cannot apply to this problem.
-        const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
+        const bool legal = tma_legal(q.A, q.lda, e) && tma_legal(q.B, q.ldb, e) &&
+                           tma_batch_legal(q.sa, e, q.batch) && tma_batch_legal(q.sb, e, q.batch);
         if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
         if (o->cta_pair == 2 && (t == TG_TF32 || !legal || o->producer == 2 || o->block_n == 64))
             return TG_ERR_INVALID_VALUE;
@@ -266,12 +307,12 @@ tg_status validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
     return TG_OK;
 }
 
-// Plan a problem with M, N, K > 0 (arguments already validated).
-tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
-                    int64_t ldb, const float *D, int64_t ldc, tg_dtype t, const tg_options *o,
-                    int sms, Plan *plan) {
+// Plan a problem with M, N, K, batch > 0 (arguments already validated).
+tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) {
     static const tg_options kNone = {};
     if (!o) o = &kNone;
+    const int64_t M = q.M, N = q.N, K = q.K;
+    const tg_dtype t = q.t;
     Plan p;
     // Fill the 128-row MMA dimension: a short M with a long N runs with the
     // operand roles swapped (both are K-major, so nothing is transposed).
@@ -282,7 +323,8 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     p.nk = p.swap ? M : N;
 
     const int e = elem_bytes(t);
-    const bool legal = tma_legal(A, lda, e) && tma_legal(B, ldb, e);
+    const bool legal = tma_legal(q.A, q.lda, e) && tma_legal(q.B, q.ldb, e) &&
+                       tma_batch_legal(q.sa, e, q.batch) && tma_batch_legal(q.sb, e, q.batch);
     if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
     p.producer = o->producer ? o->producer : (legal ? 1 : 2);
 
@@ -294,9 +336,9 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     // larger of the two.  Pair tiles need BF16/FP16 operands on TMA.
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
     if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
+    if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     // Pair tiles need a few K blocks to fill their 7-stage ring.
     const bool pair_auto = pair_ok && ceil_div(K, 64) >= 8;
-    if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     struct Cand { bool pair; int bn; };
     Cand cands[5];
     int nc = 0;
@@ -311,7 +353,7 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     for (int i = 0; i < nc; ++i) {
         const Cand c = cands[i];
         const int rows = c.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
-        const int64_t tiles = ceil_div(p.mk, rows) * ceil_div(p.nk, c.bn);
+        const int64_t tiles = q.batch * ceil_div(p.mk, rows) * ceil_div(p.nk, c.bn);
         const int64_t slots = c.pair ? sms / 2 : sms;
         const int64_t mma = c.bn / 2;
         const int64_t smem = c.pair ? 64 + c.bn / 4 : 64 + c.bn / 2;
@@ -324,7 +366,8 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
     }
     const int rows = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
     const int64_t mblocks = ceil_div(p.mk, rows);
-    p.tiles = mblocks * ceil_div(p.nk, p.block_n);
+    p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
+    p.tiles = q.batch * p.tiles_per_batch;
     if (p.pair) {
         if (t == TG_BF16) pair_numbers<Kind::BF16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
         else pair_numbers<Kind::FP16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
@@ -364,7 +407,11 @@ tg_status make_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
         if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
         p.grid = (int)(grid < 1 ? 1 : grid);
     }
-    p.vector_store = p.swap && ((uintptr_t)D % 16 == 0) && (ldc % 4 == 0);
+    // Swapped roles store each thread's 32 consecutive columns as 16-byte
+    // vectors when every row of every batch entry starts 16-byte aligned.
+    const int eo = out_bytes(q.out_fmt);
+    p.vector_store = p.swap && ((uintptr_t)q.D % 16 == 0) && ((q.ldc * eo) % 16 == 0) &&
+                     (q.batch <= 1 || (q.sd * eo) % 16 == 0);
     *plan = p;
     return TG_OK;
 }
@@ -381,43 +428,42 @@ EncodeTiledFn encode_fn() {
     static std::once_flag once;
     std::call_once(once, [] {
         void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
+        cudaDriverEntryPointQueryResult qr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
 }
 
-// K-major operand with `rows` rows of `k` elements, leading stride `ld`;
-// box = 128-byte rows (block_k elements) x box_rows, 128-byte swizzle, zero
-// fill outside [0,k) x [0,rows).
+// K-major operand: `nb` batch entries (stride `sb` elements apart) of `rows`
+// rows of `k` elements, leading stride `ld`; box = 128-byte rows (block_k
+// elements) x box_rows x 1 entry, 128-byte swizzle, zero fill outside
+// [0,k) x [0,rows).
 bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows, int64_t k,
-                    int64_t ld, int box_rows) {
+                    int64_t ld, int64_t nb, int64_t sb, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int e = elem_bytes(t);
     CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                              : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * e)};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, (cuuint64_t)nb};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * e), (cuuint64_t)(nb > 1 ? sb * e : ld * e)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
-              const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype t, tg_epilogue epi,
-              const tg_options *opts, void *stream_ptr) {
+tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *stream_ptr) {
     if (epi != TG_EPILOGUE_NONE && epi != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
-    tg_status st = validate(M, N, K, A, lda, B, ldb, D, ldc, t, opts);
+    tg_status st = validate(q, opts);
     if (st != TG_OK) return st;
-    if (M == 0 || N == 0) return TG_OK;
+    if (q.M == 0 || q.N == 0 || q.batch == 0) return TG_OK;
     int dev = 0;
     DeviceState *ds = nullptr;
     st = device_state(&dev, &ds);
@@ -425,61 +471,74 @@ tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
 
-    if (K == 0) {
-        const int64_t total = M * N;
+    if (q.K == 0) {
+        const int64_t total = q.M * q.N * q.batch;
         int64_t blocks = ceil_div(total, 256);
         const int64_t cap = (int64_t)ds->sms * 8;
         if (blocks > cap) blocks = cap;
-        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(D, M, N, ldc, alpha,
-                                                                            relu);
+        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu);
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
 
     Plan plan;
-    st = make_plan(M, N, K, A, lda, B, ldb, D, ldc, t, opts, ds->sms, &plan);
+    st = make_plan(q, opts, ds->sms, &plan);
     if (st != TG_OK) return st;
 
     tg::LaunchArgs la;
     std::memset(&la, 0, sizeof(la));
-    const void *ar = plan.swap ? B : A;   // A-role operand
-    const void *br = plan.swap ? A : B;   // B-role operand
-    const int64_t ldar = plan.swap ? ldb : lda;
-    const int64_t ldbr = plan.swap ? lda : ldb;
+    const void *ar = plan.swap ? q.B : q.A;   // A-role operand
+    const void *br = plan.swap ? q.A : q.B;   // B-role operand
+    const int64_t ldar = plan.swap ? q.ldb : q.lda;
+    const int64_t ldbr = plan.swap ? q.lda : q.ldb;
+    const int64_t sar = plan.swap ? q.sb : q.sa;
+    const int64_t sbr = plan.swap ? q.sa : q.sb;
+    const int64_t nba = (q.batch > 1 && sar != 0) ? q.batch : 1;
+    const int64_t nbb = (q.batch > 1 && sbr != 0) ? q.batch : 1;
     la.block_n = plan.block_n;
     la.plain_loads = plan.producer == 2;
     la.pair = plan.pair;
     if (!la.plain_loads) {
         const int b_box = plan.pair ? plan.block_n / 2 : plan.block_n;
-        const bool ok = encode_operand(&la.map_a, t, ar, plan.mk, K, ldar, tg::BLOCK_M) &&
-                        encode_operand(&la.map_b, t, br, plan.nk, K, ldbr, b_box);
+        const bool ok = encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sar, tg::BLOCK_M) &&
+                        encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sbr, b_box);
         if (!ok) {
             if (opts && (opts->producer == 1 || opts->cta_pair == 2)) return TG_ERR_INVALID_VALUE;
             la.plain_loads = true;  // shapes the TMA unit cannot describe
             la.pair = false;
             plan.pair = false;
-            plan.tiles = ceil_div(plan.mk, tg::BLOCK_M) * ceil_div(plan.nk, plan.block_n);
+            plan.tiles_per_batch = ceil_div(plan.mk, tg::BLOCK_M) * ceil_div(plan.nk, plan.block_n);
+            plan.tiles = q.batch * plan.tiles_per_batch;
             plan.grid = (int)(plan.tiles < ds->sms ? plan.tiles : ds->sms);
         }
     }
     tg::GemmParams &p = la.p;
     p.m = (int32_t)plan.mk;
     p.n = (int32_t)plan.nk;
-    p.k = (int32_t)K;
+    p.k = (int32_t)q.K;
     p.num_m_blocks = (int32_t)ceil_div(plan.mk, plan.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
     p.num_n_blocks = (int32_t)ceil_div(plan.nk, plan.block_n);
-    p.num_k_blocks = (int32_t)ceil_div(K, t == TG_TF32 ? 32 : 64);
+    p.num_k_blocks = (int32_t)ceil_div(q.K, q.t == TG_TF32 ? 32 : 64);
     p.raster_group = plan.group;
     p.relu = relu;
     p.num_tiles = plan.tiles;
-    p.alpha = alpha;
+    p.tiles_per_batch = plan.tiles_per_batch;
+    p.batch = (int32_t)q.batch;
+    p.out_fmt = q.out_fmt;
+    p.alpha = q.alpha;
     p.vector_store = plan.vector_store ? 1 : 0;
-    p.d = D;
-    p.d_row_stride = plan.swap ? ldc : 1;
-    p.d_col_stride = plan.swap ? 1 : ldc;
+    p.d = q.D;
+    p.d_row_stride = plan.swap ? q.ldc : 1;
+    p.d_col_stride = plan.swap ? 1 : q.ldc;
+    p.stride_d = q.sd;
     p.a_ptr = ar;
     p.b_ptr = br;
     p.lda = ldar;
     p.ldb = ldbr;
+    p.stride_a = q.batch > 1 ? sar : 0;
+    p.stride_b = q.batch > 1 ? sbr : 0;
+    p.a_bmul = nba > 1 ? 1 : 0;
+    p.b_bmul = nbb > 1 ? 1 : 0;
     p.status = ds->status;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
@@ -499,10 +558,17 @@ tg_status run(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64
     la.stream = stream;
 
     cudaError_t e;
-    if (t == TG_BF16) e = tg::launch_bf16(la);
-    else if (t == TG_FP16) e = tg::launch_fp16(la);
+    if (q.t == TG_BF16) e = tg::launch_bf16(la);
+    else if (q.t == TG_FP16) e = tg::launch_fp16(la);
     else e = tg::launch_tf32(la);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+Problem single(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+               const void *B, int64_t ldb, void *D, int64_t ldc, tg_dtype t, int out_fmt,
+               tg_epilogue epi) {
+    return Problem{M, N, K, alpha, A, lda, 0, B, ldb, 0, D, ldc, 0, 1, t, out_fmt,
+                   epi == TG_EPILOGUE_RELU ? 1 : 0};
 }
 
 }  // namespace
@@ -512,13 +578,25 @@ extern "C" {
 tg_status tg_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                   const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype in_dtype,
                   tg_epilogue epilogue, void *stream) {
-    return run(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, nullptr, stream);
+    return run(single(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, 0, epilogue), epilogue,
+               nullptr, stream);
 }
 
 tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                      const void *B, int64_t ldb, float *D, int64_t ldc, tg_dtype in_dtype,
                      tg_epilogue epilogue, const tg_options *opts, void *stream) {
-    return run(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, epilogue, opts, stream);
+    return run(single(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, 0, epilogue), epilogue,
+               opts, stream);
+}
+
+tg_status tg_gemm_batched(int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                          int64_t lda, int64_t stride_a, const void *B, int64_t ldb,
+                          int64_t stride_b, void *D, int64_t ldc, int64_t stride_d, int64_t batch,
+                          tg_dtype in_dtype, tg_out_dtype out_dtype, tg_epilogue epilogue,
+                          const tg_options *opts, void *stream) {
+    Problem q{M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, D, ldc, stride_d, batch,
+              in_dtype, (int)out_dtype, epilogue == TG_EPILOGUE_RELU ? 1 : 0};
+    return run(q, epilogue, opts, stream);
 }
 
 tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -528,8 +606,9 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     // NULL operands are planned as 256-byte aligned.
     const void *a = A ? A : reinterpret_cast<const void *>(256);
     const void *b = B ? B : reinterpret_cast<const void *>(256);
-    const float *d = D ? D : reinterpret_cast<const float *>(256);
-    tg_status st = validate(M, N, K, a, lda, b, ldb, d, ldc, in_dtype, opts);
+    void *d = D ? const_cast<float *>(D) : reinterpret_cast<void *>(256);
+    const Problem q = single(M, N, K, 1.0f, a, lda, b, ldb, d, ldc, in_dtype, 0, TG_EPILOGUE_NONE);
+    tg_status st = validate(q, opts);
     if (st != TG_OK) return st;
     int sms = num_sms;
     if (sms <= 0) {
@@ -542,7 +621,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     std::memset(out, 0, sizeof(*out));
     if (M == 0 || N == 0 || K == 0) return TG_OK;  // nothing to tile
     Plan p;
-    st = make_plan(M, N, K, a, lda, b, ldb, d, ldc, in_dtype, opts, sms, &p);
+    st = make_plan(q, opts, sms, &p);
     if (st != TG_OK) return st;
     out->block_m = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
     out->cta_pair = p.pair ? 1 : 0;

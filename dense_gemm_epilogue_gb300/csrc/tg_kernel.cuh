@@ -38,6 +38,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include "tg_ptx.cuh"
 
 namespace tg {
@@ -82,7 +84,7 @@ struct GemmParams {
     int64_t num_tiles;
     float alpha;
     int32_t vector_store;           // 1: cols contiguous in D and 16-byte aligned
-    float *d;
+    void *d;                        // output, element type by out_fmt
     int64_t d_row_stride;           // D element stride between role-space rows
     int64_t d_col_stride;           // D element stride between role-space cols
     const void *a_ptr;              // plain-load producer only
@@ -104,6 +106,16 @@ struct GemmParams {
     // the 4 K blocks `prefetch_k` ahead into L2 in one burst (0 = off), so
     // DRAM sees 512 contiguous bytes of each row at once.
     int32_t prefetch_k;
+    // Batches: `batch` independent problems of the same shape.  Tile t is
+    // batch entry t / tiles_per_batch.  Operand batch strides are in
+    // role-space elements (plain loads); the TMA maps carry them as their
+    // third dimension, addressed as b * a_bmul (0: one operand for all).
+    int32_t batch;
+    int32_t out_fmt;                // 0 FP32, 1 BF16, 2 FP16 output
+    int64_t tiles_per_batch;
+    int64_t stride_a, stride_b;     // elements between batch entries (role space)
+    int64_t stride_d;               // output elements between batch entries
+    int32_t a_bmul, b_bmul;
 };
 
 constexpr int BLOCK_M = 128;
@@ -207,36 +219,85 @@ __device__ __forceinline__ void tile_coords(int64_t t, const GemmParams &p, int 
     nb = (int)(r / gsz);
 }
 
+// Tile t of the whole (batched) problem: batch entry b and its tile (mb, nb).
+__device__ __forceinline__ void batch_tile_coords(int64_t t, const GemmParams &p, int &b, int &mb,
+                                                  int &nb) {
+    b = (int)(t / p.tiles_per_batch);
+    tile_coords(t - (int64_t)b * p.tiles_per_batch, p, mb, nb);
+}
+
 __device__ __forceinline__ float apply_epilogue(float x, float alpha, int relu) {
     const float y = alpha * x;
     // max(y, 0) when ReLU is on: NaN stays NaN, -0 and negatives give +0.
     return (relu && !(y > 0.0f) && !(y != y)) ? 0.0f : y;
 }
 
+// Output formats of D ("Matrix Multiplication", Step 4: keep the FP32
+// accumulator and convert on the way out; round to nearest even).
+template <int FMT>
+struct OutFormat;
+template <>
+struct OutFormat<0> {
+    using T = float;
+    static constexpr int PER16 = 4;  // elements per 16-byte vector
+    __device__ static T cvt(float y) { return y; }
+    __device__ static uint4 pack(const float *y) {
+        return make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]),
+                          __float_as_uint(y[3]));
+    }
+};
+template <>
+struct OutFormat<1> {
+    using T = unsigned short;
+    static constexpr int PER16 = 8;
+    __device__ static T cvt(float y) { return __bfloat16_as_ushort(__float2bfloat16_rn(y)); }
+    __device__ static uint4 pack(const float *y) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = (uint32_t)cvt(y[2 * i]) | ((uint32_t)cvt(y[2 * i + 1]) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <>
+struct OutFormat<2> {
+    using T = unsigned short;
+    static constexpr int PER16 = 8;
+    __device__ static T cvt(float y) { return __half_as_ushort(__float2half_rn(y)); }
+    __device__ static uint4 pack(const float *y) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = (uint32_t)cvt(y[2 * i]) | ((uint32_t)cvt(y[2 * i + 1]) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
 // Epilogue store of one 32-column chunk of a row (role space): y = epi(v),
-// bounded by the problem's columns.  D is written once and never read back
-// by the kernel, so the stores are marked streaming (evict-first) to keep
-// the operands' lines in L2.  A chunk that lies wholly inside the problem
-// takes a branch-free path that steps a pointer by the column stride.
-__device__ __forceinline__ void store_chunk(const GemmParams &p, float *drow, int32_t col0,
-                                            const uint32_t (&v)[32]) {
+// converted to the output format, bounded by the problem's columns.  D is
+// written once and never read back by the kernel, so the stores are marked
+// streaming (evict-first) to keep the operands' lines in L2.  A chunk that
+// lies wholly inside the problem takes a branch-free path that steps a
+// pointer by the column stride.
+template <int FMT>
+__device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFormat<FMT>::T *drow,
+                                            int32_t col0, const uint32_t (&v)[32]) {
+    using F = OutFormat<FMT>;
     if (col0 + 32 <= p.n) {
         if (p.vector_store) {
-            float4 *dst = reinterpret_cast<float4 *>(drow + col0);
+            uint4 *dst = reinterpret_cast<uint4 *>(drow + col0);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                __stcs(dst + j / 4,
-                       make_float4(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu),
-                                   apply_epilogue(__uint_as_float(v[j + 1]), p.alpha, p.relu),
-                                   apply_epilogue(__uint_as_float(v[j + 2]), p.alpha, p.relu),
-                                   apply_epilogue(__uint_as_float(v[j + 3]), p.alpha, p.relu)));
+            for (int j = 0; j < 32; j += F::PER16) {
+                float y[F::PER16];
+#pragma unroll
+                for (int e = 0; e < F::PER16; ++e)
+                    y[e] = apply_epilogue(__uint_as_float(v[j + e]), p.alpha, p.relu);
+                __stcs(dst + j / F::PER16, F::pack(y));
             }
         } else {
             const int64_t cs = p.d_col_stride;
-            float *q = drow + (int64_t)col0 * cs;
+            typename F::T *q = drow + (int64_t)col0 * cs;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                __stcs(q, apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu));
+                __stcs(q, F::cvt(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu)));
                 q += cs;
             }
         }
@@ -245,9 +306,18 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, float *drow, in
         for (int j = 0; j < 32; ++j) {
             if (col0 + j < p.n)
                 __stcs(drow + (int64_t)(col0 + j) * p.d_col_stride,
-                       apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu));
+                       F::cvt(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu)));
         }
     }
+}
+
+// Row r (role space) of batch entry b: store one chunk in the output format.
+__device__ __forceinline__ void epilogue_store(const GemmParams &p, int b, int32_t r, int32_t col0,
+                                               const uint32_t (&v)[32]) {
+    const int64_t off = (int64_t)b * p.stride_d + (int64_t)r * p.d_row_stride;
+    if (p.out_fmt == 0) store_chunk<0>(p, static_cast<float *>(p.d) + off, col0, v);
+    else if (p.out_fmt == 1) store_chunk<1>(p, static_cast<unsigned short *>(p.d) + off, col0, v);
+    else store_chunk<2>(p, static_cast<unsigned short *>(p.d) + off, col0, v);
 }
 
 // Narrow one FP32 bit pattern to TF32: round the magnitude to 10 fraction
@@ -368,17 +438,18 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
+        constexpr int E = C::T::elem_bytes;
         for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            int mb, nb;
-            tile_coords(t, p, mb, nb);
+            int bt, mb, nb;
+            batch_tile_coords(t, p, bt, mb, nb);
+            const uint8_t *a_src = static_cast<const uint8_t *>(p.a_ptr) + (int64_t)bt * p.stride_a * E;
+            const uint8_t *b_src = static_cast<const uint8_t *>(p.b_ptr) + (int64_t)bt * p.stride_b * E;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
-                load_stage_plain<C::T::elem_bytes, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES,
-                                                                p.a_ptr, p.lda, mb * BLOCK_M, p.m,
-                                                                kb * C::BK, p.k, ltid);
-                load_stage_plain<C::T::elem_bytes, BN, NT>(smem + C::B_OFF + s * C::B_BYTES,
-                                                           p.b_ptr, p.ldb, nb * BN, p.n,
-                                                           kb * C::BK, p.k, ltid);
+                load_stage_plain<E, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES, a_src, p.lda,
+                                                 mb * BLOCK_M, p.m, kb * C::BK, p.k, ltid);
+                load_stage_plain<E, BN, NT>(smem + C::B_OFF + s * C::B_BYTES, b_src, p.ldb,
+                                            nb * BN, p.n, kb * C::BK, p.k, ltid);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::FULL0 + s));
                 if (++s == S) { s = 0; ph ^= 1; }
@@ -394,23 +465,24 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             int64_t issued = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int mb, nb;
-                tile_coords(t, p, mb, nb);
+                int bt, mb, nb;
+                batch_tile_coords(t, p, bt, mb, nb);
+                const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
                 if (p.prefetch_k > 0) {
                     for (int j = 0; j < p.prefetch_k && j < nkb; ++j)
-                        tma_prefetch_l2_2d(&tmap_a, j * C::BK, mb * BLOCK_M);
+                        tma_prefetch_l2_3d(&tmap_a, j * C::BK, mb * BLOCK_M, ab);
                 }
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (p.prefetch_k > 0 && (kb & 3) == 0) {
                         for (int j = 0; j < 4; ++j) {
                             const int kp = kb + p.prefetch_k + j;
-                            if (kp < nkb) tma_prefetch_l2_2d(&tmap_a, kp * C::BK, mb * BLOCK_M);
+                            if (kp < nkb) tma_prefetch_l2_3d(&tmap_a, kp * C::BK, mb * BLOCK_M, ab);
                         }
                     }
                     if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(C::FULL0 + s), C::A_BYTES + C::B_BYTES);
-                    tma_load_2d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M);
-                    tma_load_2d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kb * C::BK, nb * BN);
+                    tma_load_3d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M, ab);
+                    tma_load_3d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kb * C::BK, nb * BN, bb);
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
@@ -472,21 +544,20 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         const int cbase = ((warp - 2) / 4) * COLS;
         uint32_t tl = 0;
         for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
-            int mb, nb;
-            tile_coords(t, p, mb, nb);
+            int bt, mb, nb;
+            batch_tile_coords(t, p, bt, mb, nb);
             const uint32_t acc = tl & 1, use = tl >> 1;
             if (!wait_phase(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
             tc_fence_after();
             const int32_t r = mb * BLOCK_M + row_in_tile;
             const bool row_ok = r < p.m;
-            float *drow = p.d + (int64_t)r * p.d_row_stride;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int c0 = cbase; c0 < cbase + COLS; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
-                if (row_ok) store_chunk(p, drow, nb * BN + c0, v);
+                if (row_ok) epilogue_store(p, bt, r, nb * BN + c0, v);
             }
             tc_fence_before();
             __syncwarp();

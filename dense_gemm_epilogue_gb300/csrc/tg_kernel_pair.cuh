@@ -223,21 +223,22 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             bool ok = true;
             for (int64_t u = pair; ok && u < up.units; u += num_pairs) {
                 const Unit un = decode_unit(up, u, nkb);
-                int mb, nb;
-                tile_coords(un.tile, p, mb, nb);
+                int bt, mb, nb;
+                batch_tile_coords(un.tile, p, bt, mb, nb);
                 const int32_t arow = mb * C::PAIR_M + (int32_t)rank * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)rank * C::B_ROWS;
+                const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
                 for (int kb = un.k0; kb < un.k1; ++kb) {
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * (C::A_BYTES + C::B_BYTES));
                     if (p.l2_hint) {
-                        tma_load_2d_pair_hint(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow,
-                                              pol_a);
-                        tma_load_2d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow);
+                        tma_load_3d_pair_hint(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow,
+                                              ab, pol_a);
+                        tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
                     } else {
-                        tma_load_2d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow);
-                        tma_load_2d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow);
+                        tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow, ab);
+                        tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
                     }
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         uint32_t tl = 0;
         for (int64_t u = pair; u < up.units; u += num_pairs, ++tl) {
             const Unit un = decode_unit(up, u, nkb);
-            int mb, nb;
-            tile_coords(un.tile, p, mb, nb);
+            int bt, mb, nb;
+            batch_tile_coords(un.tile, p, bt, mb, nb);
             const uint32_t acc = tl & 1, use = tl >> 1;
             if (!pair_wait(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
             tc_fence_after();
@@ -362,7 +363,6 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 const int32_t r = mb * C::PAIR_M + (int32_t)rank * BLOCK_M + row_in_half;
                 const bool row_ok = r < p.m;
-                float *drow = p.d + (int64_t)r * p.d_row_stride;
 #pragma unroll 1
                 for (int c0 = cbase; ready && c0 < cbase + COLS; c0 += 32) {
                     uint32_t v[32];
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                                                        __ldcg(src + (int64_t)j * BLOCK_M));
                         }
                     }
-                    if (row_ok) store_chunk(p, drow, nb * BN + c0, v);
+                    if (row_ok) epilogue_store(p, bt, r, nb * BN + c0, v);
                 }
                 if (finisher) {
                     // Leave the flags at zero for the next launch.

@@ -122,11 +122,12 @@ bool noalloc_encode(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
     const CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                    : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * e)};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+    // Three dimensions (K, rows, one batch entry), as the kernels load.
+    cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * e), (cuuint64_t)(ld * e)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / e), (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -205,6 +206,9 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     p.raster_group = info.raster_group;
     p.relu = relu;
     p.num_tiles = tiles;
+    p.tiles_per_batch = tiles;
+    p.batch = 1;
+    p.out_fmt = 0;
     p.alpha = alpha;
     p.vector_store = info.vector_store;
     p.d = D;

@@ -71,6 +71,15 @@ typedef enum {
     TG_TF32 = 2   /* FP32 storage, narrowed to TF32 in the kernel */
 } tg_dtype;
 
+/* Output element type of tg_gemm_batched ("Matrix Multiplication", Step 4:
+ * the accumulator stays FP32 and the result is converted on the way out,
+ * rounding to nearest even). */
+typedef enum {
+    TG_OUT_F32 = 0,
+    TG_OUT_BF16 = 1,
+    TG_OUT_F16 = 2
+} tg_out_dtype;
+
 typedef enum {
     TG_EPILOGUE_NONE = 0,  /* D = alpha * A*B */
     TG_EPILOGUE_RELU = 1   /* D = max(alpha * A*B, 0); NaN stays NaN, -0 becomes +0 */
@@ -148,6 +157,27 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, float alpha,
                      float *D, int64_t ldc,
                      tg_dtype in_dtype, tg_epilogue epilogue,
                      const tg_options *opts, void *stream);
+
+/*
+ * A batch of independent GEMMs of one shape, with a choice of output type:
+ *   for b in [0, batch):  D_b = out(epi(alpha * A_b * B_b))
+ * with A_b = A + b*stride_a and B_b = B + b*stride_b (elements of in_dtype)
+ * and D_b = D + b*stride_d (elements of out_dtype), each laid out as for
+ * tg_gemm ("Matrix Multiplication", "Where to go from here": batched operands
+ * along a trailing batch dimension).  stride_a or stride_b may be 0 (one
+ * operand shared by every batch entry); outputs may not overlap:
+ * stride_d >= ldc*N when batch > 1.  out() rounds the FP32 result to
+ * out_dtype (round to nearest even; TG_OUT_F32 stores it as is).
+ * D must be aligned to its element size.  batch == 0 launches nothing.
+ * Strides that are not multiples of 16 bytes route to plain loads, as in
+ * tg_gemm.  Returns as tg_gemm_ex.
+ */
+tg_status tg_gemm_batched(int64_t M, int64_t N, int64_t K, float alpha,
+                          const void *A, int64_t lda, int64_t stride_a,
+                          const void *B, int64_t ldb, int64_t stride_b,
+                          void *D, int64_t ldc, int64_t stride_d, int64_t batch,
+                          tg_dtype in_dtype, tg_out_dtype out_dtype, tg_epilogue epilogue,
+                          const tg_options *opts, void *stream);
 
 /*
  * Run the planner only.  `num_sms` > 0 plans for that many SMs without

@@ -103,3 +103,92 @@ def check_full(w: si.Workload, opts=None, repeats: int = 1):
     for o in outs[1:]:
         assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)), "not deterministic"
     return rel
+
+
+# ----------------------------------------------------------------- batched / narrow output
+
+OUT_NP = {"f32": np.float32, "bf16": np.uint16, "fp16": np.uint16}
+# Output rounding adds at most one unit in the last place of the output type.
+OUT_ULP_REL = {"f32": 2.0 ** -23, "bf16": 2.0 ** -7, "fp16": 2.0 ** -10}
+OUT_ULP_ABS = {"f32": 2.0 ** -149, "bf16": 2.0 ** -133, "fp16": 2.0 ** -24}
+
+
+def decode_out(x: np.ndarray, out: str) -> np.ndarray:
+    if out == "f32":
+        return x.astype(np.float64)
+    if out == "fp16":
+        return x.view(np.float16).astype(np.float64)
+    return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def run_batched(w: si.Workload, batch: int, out: str, share_a=False, share_b=False,
+                pad_a=0, pad_b=0, pad_d=0, opts=None, repeats=1):
+    """tg_gemm_batched on `batch` entries drawn with seeds w.seed, w.seed+1, ...
+    Returns (A_list, B_list, D storage list per repeat, strides)."""
+    import torch
+    import dense_gemm_epilogue_gb300 as tg
+
+    lda, ldb, ldc = w.strides
+    entries = [si.make_operands(si.with_shape(w, seed=w.seed + b)) for b in range(batch)]
+    A_list = [entries[0][0]] * batch if share_a else [e[0] for e in entries]
+    B_list = [entries[0][1]] * batch if share_b else [e[1] for e in entries]
+    sa = 0 if share_a else w.M * lda + pad_a
+    sb = 0 if share_b else w.N * ldb + pad_b
+    sd = w.N * ldc + pad_d
+    ety = si.storage_numpy_dtype(w.dtype)
+    A = np.zeros(max(sa * (batch - 1), 0) + w.M * lda, dtype=ety)
+    B = np.zeros(max(sb * (batch - 1), 0) + w.N * ldb, dtype=ety)
+    for b in range(batch):
+        if not share_a or b == 0:
+            A[b * sa: b * sa + w.M * lda] = A_list[b].reshape(-1)
+        if not share_b or b == 0:
+            B[b * sb: b * sb + w.N * ldb] = B_list[b].reshape(-1)
+    sentinel = {"f32": np.uint32(0x7FC00002), "bf16": np.uint16(0x7FC3), "fp16": np.uint16(0x7E03)}
+    D0 = np.full(sd * max(batch - 1, 0) + w.N * ldc, sentinel[out],
+                 dtype=np.uint32 if out == "f32" else np.uint16)
+    dA, dB = torch_storage(A), torch_storage(B)
+    dD = torch.from_numpy(D0.view(np.int32 if out == "f32" else np.int16).copy()).cuda()
+    outs = []
+    for _ in range(repeats):
+        st = tg.tg_gemm_batched(w.M, w.N, w.K, w.alpha, dA, lda, sa, dB, ldb, sb, dD, ldc, sd, batch,
+                                w.dtype, out, w.relu, opts)
+        tg.check(st, "tg_gemm_batched")
+        st, where = tg.tg_check_device_status()
+        assert st == tg.TG_OK, f"device status {st} at wait site {where}"
+        outs.append(dD.cpu().numpy().view(np.uint32 if out == "f32" else np.uint16).copy())
+    return A_list, B_list, D0, outs, (sa, sb, sd)
+
+
+def check_batched(w: si.Workload, batch: int, out: str, repeats=1, **kw):
+    import oracle
+
+    lda, ldb, ldc = w.strides
+    A_list, B_list, D0, outs, (sa, sb, sd) = run_batched(w, batch, out, repeats=repeats, **kw)
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "not deterministic"
+    Dall = outs[0]
+    for b in range(batch):
+        ref, scale = oracle.gemm(w.M, w.N, w.K, w.alpha, A_list[b], lda, B_list[b], ldb, w.dtype,
+                                 w.relu, with_scale=True)
+        ref_out = oracle.round_output(ref, out)
+        store = Dall[b * sd: b * sd + w.N * ldc].reshape(w.N, ldc)
+        got = decode_out(store[:, : w.M].view(OUT_NP[out]).T, out)
+        # Stride padding of D (rows >= M, and the gap between batch entries) untouched.
+        assert np.array_equal(store[:, w.M:], D0[b * sd: b * sd + w.N * ldc].reshape(w.N, ldc)[:, w.M:])
+        if b + 1 < batch:
+            gap = slice(b * sd + w.N * ldc, (b + 1) * sd)
+            assert np.array_equal(Dall[gap], D0[gap])
+        inf = np.isinf(ref_out)
+        assert np.array_equal(got[inf], ref_out[inf]), f"{w.name}[{b}]: overflow differs"
+        fin = ~inf
+        tol = (TOL_REL[w.dtype] * scale + TOL_ABS + OUT_ULP_REL[out] * np.abs(ref) +
+               OUT_ULP_ABS[out])
+        nan_ref = np.isnan(ref_out)
+        assert np.array_equal(np.isnan(got) & nan_ref, nan_ref)
+        ok = fin & ~nan_ref
+        err = np.abs(got[ok] - ref_out[ok])
+        bad = ~(err <= tol[ok])
+        if bad.any():
+            i = np.flatnonzero(bad)[:6]
+            raise AssertionError(f"{w.name}[{b}] ({out}): {bad.sum()} elements off; err={err[i]} "
+                                 f"tol={tol[ok][i]} got={got[ok][i]} ref={ref_out[ok][i]}")

@@ -183,3 +183,23 @@ def test_plan_overrides(tg):
     assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["raster_group"] == 8
     assert plan(tg, w, sms=7, opts={"cta_pair": 1})["grid"] == 7
     assert plan(tg, w, sms=7)["grid"] == 6             # pairs: 3 clusters of 2
+
+
+@pytest.mark.parametrize("args", [
+    dict(sd=63), dict(sa=-1), dict(sb=-1), dict(batch=-1), dict(out=3), dict(D=FAKE + 1, out=1),
+    dict(D=FAKE + 2, out=0), dict(dtype=2, opts={"cta_pair": 2}),
+])
+def test_batched_invalid_arguments_rejected_before_cuda(tg, args):
+    a = dict(M=8, N=8, K=8, A=FAKE, lda=8, sa=64, B=FAKE, ldb=8, sb=64, D=FAKE, ldc=8, sd=64,
+             batch=2, dtype=0, out=0, opts=None)
+    a.update(args)
+    st = tg.tg_gemm_batched(a["M"], a["N"], a["K"], 1.0, a["A"], a["lda"], a["sa"], a["B"], a["ldb"],
+                            a["sb"], a["D"], a["ldc"], a["sd"], a["batch"], a["dtype"], a["out"], True,
+                            a["opts"])
+    assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def test_batched_empty_is_ok_without_cuda(tg):
+    assert tg.tg_gemm_batched(8, 8, 8, 1.0, FAKE, 8, 64, FAKE, 8, 64, FAKE, 8, 64, 0, "bf16", "bf16",
+                              True) == tg.TG_OK
+
