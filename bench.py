@@ -49,6 +49,14 @@ def parse():
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(si.WORKLOADS),
+                    help="problem to time (default: the 8192^3 BF16 + ReLU headline)")
+    ap.add_argument("--out", default="f32", choices=["f32", "bf16", "fp16"],
+                    help="output type of D (bf16/fp16 go through tg_gemm_batched)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="batch entries of the workload per step (tg_gemm_batched)")
+    ap.add_argument("--cpu-baseline", action="store_true",
+                    help="time the oracle also for a non-default workload")
     return ap.parse_args()
 
 
@@ -59,15 +67,28 @@ def dist_env():
     return rank, world, local
 
 
-def workload_config(w: si.Workload, world: int) -> dict:
+def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1) -> dict:
     lda, ldb, ldc = w.strides
-    return {
-        "workload": f"{w.name}: M=N=K={w.M} BF16 operands (seeded N(0,1) rounded to BF16), "
-                    f"alpha={w.alpha}, ReLU epilogue, FP32 accumulate, D FP32 column-major",
+    dist = ("N(0,1)" + (f"x{w.scale}" if w.scale != 1.0 else "") if w.dist == "normal"
+            else f"U[{w.lo},{w.hi})")
+    cfg = {
+        "workload": f"{w.name}: M={w.M} N={w.N} K={w.K} {w.dtype.upper()} operands (seeded "
+                    f"{dist}), alpha={w.alpha}, {'ReLU' if w.relu else 'no'} epilogue, FP32 "
+                    f"accumulate, D {out.upper()} column-major"
+                    + (f", batch of {batch} (entries share one seeded draw)" if batch > 1 else ""),
         "M": w.M, "N": w.N, "K": w.K, "lda": lda, "ldb": ldb, "ldc": ldc,
-        "l2": "inputs larger than L2 (A+B 268 MB and D 268 MB vs 129 MB L2); no flush",
         "parallelism": "replicas" if world > 1 else "single GPU",
     }
+    if batch > 1:
+        cfg["batch"] = batch
+    if out != "f32":
+        cfg["out"] = out
+    e = si.element_bytes(w.dtype)
+    ws = batch * ((w.M * w.K + w.K * w.N) * e + w.M * w.N * (4 if out == "f32" else 2))
+    cfg["l2"] = (f"working set {ws / 1e6:.0f} MB vs 129 MB L2" +
+                 ("; larger than L2, no flush" if ws > 129e6 else
+                  "; fits in L2: consecutive steps hit warm L2"))
+    return cfg
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -240,20 +261,31 @@ def run_gpu(args, rank, world, local):
 
     tg.build()
     tg.load()
-    w = si.WORKLOADS[WORKLOAD]
+    w = si.WORKLOADS[args.workload]
+    out, nbat = args.out, max(1, args.batch)
+    batched = nbat > 1 or out != "f32"
     lda, ldb, ldc = w.strides
     A, B = si.make_operands(w)
-    hA = torch.from_numpy(A.view(np.int16)).pin_memory()
-    hB = torch.from_numpy(B.view(np.int16)).pin_memory()
+    view = np.float32 if w.dtype == "tf32" else np.int16
+    hA = torch.from_numpy(np.tile(A.reshape(-1), nbat).view(view)).pin_memory()
+    hB = torch.from_numpy(np.tile(B.reshape(-1), nbat).view(view)).pin_memory()
     dA = hA.cuda()
     dB = hB.cuda()
-    dD = torch.empty((w.N, ldc), dtype=torch.float32, device="cuda")
-    hD = torch.empty((w.N, ldc), dtype=torch.float32).pin_memory()
+    odt = torch.float32 if out == "f32" else torch.int16
+    dD = torch.empty((nbat * w.N, ldc), dtype=odt, device="cuda")
+    hD = torch.empty((nbat * w.N, ldc), dtype=odt).pin_memory()
+    sa, sb, sd = w.M * lda, w.N * ldb, w.N * ldc
     stream = torch.cuda.Stream()
-    plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, dD, ldc, w.dtype)
+    plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, None, ldc, w.dtype)
+
+    def call(a_, b_, d_, st_):
+        if batched:
+            return tg.tg_gemm_batched(w.M, w.N, w.K, w.alpha, a_, lda, sa, b_, ldb, sb, d_, ldc, sd,
+                                      nbat, w.dtype, out, w.relu, None, st_)
+        return tg.tg_gemm(w.M, w.N, w.K, w.alpha, a_, lda, b_, ldb, d_, ldc, w.dtype, w.relu, st_)
 
     def step():
-        st = tg.tg_gemm(w.M, w.N, w.K, w.alpha, dA, lda, dB, ldb, dD, ldc, w.dtype, w.relu, stream)
+        st = call(dA, dB, dD, stream)
         if st != tg.TG_OK:
             raise tg.TgError(st, "tg_gemm")
 
@@ -316,8 +348,7 @@ def run_gpu(args, rank, world, local):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])         # step i-2's D has been read back
-        st_ = tg.tg_gemm(w.M, w.N, w.K, w.alpha, a_, lda, b_, ldb, d_, ldc, w.dtype, w.relu,
-                         stream)
+        st_ = call(a_, b_, d_, stream)
         if st_ != tg.TG_OK:
             raise tg.TgError(st_, "tg_gemm")
         ev_gemm[b].record(stream)
@@ -349,46 +380,70 @@ def run_gpu(args, rank, world, local):
         step_ms, e2e_ms = float(t[0]), float(t[1])
 
     if rank == 0:
-        flops = w.flops
+        flops = w.flops * nbat
+        e_in = si.element_bytes(w.dtype)
+        alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
         value = world * flops / (step_ms * 1e-3) / 1e12
         peaks, peak_src = load_peaks()
         launch_avg_ms = statistics.fmean(launch_ms)
-        achieved = flops / (launch_avg_ms * 1e-3) / 1e12
         # Back-to-back launches for more than ~50 ms run in the power-capped
         # regime the sustained peak was measured in; a short burst compares
-        # with the burst peak.  Both are reported.
+        # with the burst peak.  Both are reported.  TF32 takes the BF16 peak
+        # times the nominal TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s).
+        ratio = (1.1 / 2.25) if w.dtype == "tf32" else 1.0
         sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
-        peak = float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+        tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+        burst_tpeak = ratio * float(peaks["bf16_tflops"])
+        hbm = float(peaks["hbm_gbs"])
+        tensor_bound = flops / alg_bytes >= tpeak * 1e12 / (hbm * 1e9)
         first = launch_ms[: min(10, len(launch_ms))]
-        burst_ach = flops / (statistics.fmean(first) * 1e-3) / 1e12
-        burst_peak = float(peaks["bf16_tflops"])
         qs = sorted(launch_ms)
-        traffic = load_traffic(tg.source_hash())
+        if tensor_bound:
+            unit_r = UNIT
+            achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+            peak = tpeak
+            burst = {"achieved": flops / (statistics.fmean(first) * 1e-3) / 1e12,
+                     "peak": burst_tpeak}
+        else:
+            unit_r = "GB/s"
+            achieved = alg_bytes / (launch_avg_ms * 1e-3) / 1e9
+            peak = hbm
+            burst = {"achieved": alg_bytes / (statistics.fmean(first) * 1e-3) / 1e9, "peak": hbm}
+        burst["frac"] = burst["achieved"] / burst["peak"]
+        burst["launches"] = len(first)
+        dt = "bf16" if w.dtype == "bf16" else ("fp16" if w.dtype == "fp16" else "tf32")
+        kname = ("tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
+            f"<{dt.upper()}, {plan['block_m']}x{plan['block_n']}, " + \
+            f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>"
+        traffic = load_traffic(tg.source_hash()) if args.workload == WORKLOAD and not batched else None
+        default_run = args.workload == WORKLOAD and not batched
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": METRIC if default_run else
+                      f"{dt} GEMM{'+ReLU' if w.relu else ''} TFLOP/s at {w.M}x{w.N}x{w.K}"
+                      + (f" x{nbat}" if nbat > 1 else "") + (f", {out} out" if out != 'f32' else ""),
+            "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic", "config": workload_config(w, world),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+            "dtype": dt, "data": "synthetic", "config": workload_config(w, world, out, nbat),
+            "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
+                         "peak": peak, "unit": unit_r,
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": (f"bf16_tflops_sustained of {peak_src} (the timed region "
-                                         f"ran {region_ms:.0f} ms of back-to-back launches)"
-                                         if sustained else f"bf16_tflops (burst) of {peak_src}"),
-                         "burst": {"achieved": burst_ach, "peak": burst_peak,
-                                   "frac": burst_ach / burst_peak,
-                                   "launches": len(first),
-                                   "peak_source": f"bf16_tflops (burst) of {peak_src}"},
+                         "peak_source": (("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")
+                                         if tensor_bound else "hbm_gbs") + f" of {peak_src}" +
+                                        (" x 1.1/2.25 (TF32)" if tensor_bound and ratio != 1.0 else "") +
+                                        (f" (the timed region ran {region_ms:.0f} ms of back-to-back "
+                                         f"launches)" if tensor_bound and sustained else ""),
+                         "burst": burst,
                          "kernel_ms_p10_p50_p90": [qs[len(qs) // 10], qs[len(qs) // 2],
                                                    qs[(9 * len(qs)) // 10]],
-                         "kernel": ("tg_gemm_pair_kernel" if plan.get("cta_pair") else
-                                    "tg_gemm_kernel") +
-                                   f"<BF16, {plan['block_m']}x{plan['block_n']}, "
-                                   f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>",
+                         "kernel": kname,
                          "kernel_ms_avg": launch_avg_ms,
-                         "algorithmic_flops_per_launch": flops},
+                         "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": alg_bytes},
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                    "h2d_bytes_per_step": int(A.nbytes + B.nbytes),
-                    "d2h_bytes_per_step": int(w.N * ldc * 4),
+                    "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
+                                              hB.numel() * hB.element_size()),
+                    "d2h_bytes_per_step": int(hD.numel() * hD.element_size()),
                     "steps": e2e_steps, "wall_s": e2e_wall,
                     "pipelining": "2 buffer sets; H2D, compute and D2H on separate streams"},
             "gpu_launches": args.steps,
@@ -396,7 +451,7 @@ def run_gpu(args, rank, world, local):
             "plan": plan,
             "library_source_hash": tg.source_hash(),
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and (default_run or args.cpu_baseline):
             line["cpu_baseline"] = cpu_baseline(w, A, B)
         print(json.dumps(line), flush=True)
     if dist is not None:
