@@ -71,7 +71,8 @@ class tg_options(ctypes.Structure):
         ("split_k", ctypes.c_int32),
         ("l2_hint", ctypes.c_int32),
         ("prefetch_k", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("multicast", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -93,6 +94,7 @@ class tg_plan_info(ctypes.Structure):
         ("cta_pair", ctypes.c_int32),
         ("split_tiles", ctypes.c_int32),
         ("split_segs", ctypes.c_int32),
+        ("multicast", ctypes.c_int32),
     ]
 
 

@@ -200,6 +200,7 @@ int out_bytes(int out_fmt) { return out_fmt == 0 ? 4 : 2; }
 
 struct Plan {
     bool pair = false;  // CTA-pair kernel (256-row tiles over a 2-CTA cluster)
+    int mc = 1;         // pair kernel: pairs per cluster (2: A rows multicast)
     int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
     int64_t split_tiles = 0;
     int split_segs = 1;
@@ -296,7 +297,9 @@ tg_status validate(const Problem &q, const tg_options *o) {
         if (o->split_k < 0 || o->split_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
         if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
-        if (o->reserved[0] || o->reserved[1] || o->reserved[2]) return TG_ERR_INVALID_VALUE;
+        if (o->multicast < 0 || o->multicast > 2) return TG_ERR_INVALID_VALUE;
+        if (o->reserved[0] || o->reserved[1]) return TG_ERR_INVALID_VALUE;
+        if (o->multicast == 2 && o->cta_pair == 1) return TG_ERR_INVALID_VALUE;
         // Overrides that cannot apply to this problem.
         const bool legal = tma_legal(q.A, q.lda, e) && tma_legal(q.B, q.ldb, e) &&
                            tma_batch_legal(q.sa, e, q.batch) && tma_batch_legal(q.sb, e, q.batch);
@@ -366,7 +369,12 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     }
     const int rows = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
     const int64_t mblocks = ceil_div(p.mk, rows);
-    p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
+    const int64_t nblocks = ceil_div(p.nk, p.block_n);
+    // Two pairs per cluster share their A rows by multicast (a quarter less
+    // L2-to-SM traffic per CTA); a cluster then covers two N blocks.
+    if (p.pair) p.mc = (o->multicast == 2 && nblocks >= 2) ? 2 : 1;
+    if (o->multicast == 2 && p.pair && p.mc != 2) return TG_ERR_INVALID_VALUE;
+    p.tiles_per_batch = mblocks * ceil_div(nblocks, p.mc);
     p.tiles = q.batch * p.tiles_per_batch;
     if (p.pair) {
         if (t == TG_BF16) pair_numbers<Kind::BF16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
@@ -387,10 +395,12 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         // grid is sized for the tiles' K segments (so every segment gets a
         // pair); otherwise for all pairs, and only the last partial wave can
         // be split.  The kernel applies the same rule to its actual grid.
-        int64_t pairs_max = sms / 2;
-        if (o->max_ctas && pairs_max > o->max_ctas / 2) pairs_max = o->max_ctas / 2;
+        const int cl = 2 * p.mc;  // CTAs per cluster
+        int64_t pairs_max = sms / cl;
+        if (o->max_ctas && pairs_max > o->max_ctas / cl) pairs_max = o->max_ctas / cl;
         if (pairs_max < 1) pairs_max = 1;
         p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 1);
+        if (p.mc != 1) p.split_max = 1;  // K segments only with one pair per cluster
         const int64_t nkb = ceil_div(K, 64);
         int64_t pairs = pairs_max;
         if (p.tiles < pairs_max) {
@@ -400,7 +410,7 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
             if (segs < 1) segs = 1;
             pairs = p.tiles * segs;
         }
-        p.grid = (int)(2 * pairs);
+        p.grid = (int)(cl * pairs);
         split_rule(p.tiles, pairs, nkb, p.split_max, sms / 2, &p.split_tiles, &p.split_segs);
     } else {
         int64_t grid = p.tiles < sms ? p.tiles : sms;
@@ -498,15 +508,19 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     la.block_n = plan.block_n;
     la.plain_loads = plan.producer == 2;
     la.pair = plan.pair;
+    la.mc = plan.mc;
     if (!la.plain_loads) {
         const int b_box = plan.pair ? plan.block_n / 2 : plan.block_n;
-        const bool ok = encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sar, tg::BLOCK_M) &&
+        const int a_box = plan.pair && plan.mc == 2 ? tg::BLOCK_M / 2 : tg::BLOCK_M;
+        const bool ok = encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sar, a_box) &&
                         encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sbr, b_box);
         if (!ok) {
             if (opts && (opts->producer == 1 || opts->cta_pair == 2)) return TG_ERR_INVALID_VALUE;
             la.plain_loads = true;  // shapes the TMA unit cannot describe
             la.pair = false;
             plan.pair = false;
+            plan.mc = 1;
+            la.mc = 1;
             plan.tiles_per_batch = ceil_div(plan.mk, tg::BLOCK_M) * ceil_div(plan.nk, plan.block_n);
             plan.tiles = q.batch * plan.tiles_per_batch;
             plan.grid = (int)(plan.tiles < ds->sms ? plan.tiles : ds->sms);
@@ -517,7 +531,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.n = (int32_t)plan.nk;
     p.k = (int32_t)q.K;
     p.num_m_blocks = (int32_t)ceil_div(plan.mk, plan.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
-    p.num_n_blocks = (int32_t)ceil_div(plan.nk, plan.block_n);
+    p.num_n_blocks = (int32_t)ceil_div(ceil_div(plan.nk, plan.block_n), plan.mc);
     p.num_k_blocks = (int32_t)ceil_div(q.K, q.t == TG_TF32 ? 32 : 64);
     p.raster_group = plan.group;
     p.relu = relu;
@@ -627,6 +641,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->cta_pair = p.pair ? 1 : 0;
     out->split_tiles = (int32_t)p.split_tiles;
     out->split_segs = p.split_segs;
+    out->multicast = p.pair ? p.mc : 0;
     out->block_n = p.block_n;
     out->block_k = in_dtype == TG_TF32 ? 32 : 64;
     out->stages = p.stages;

@@ -29,17 +29,18 @@ static cudaError_t launch_one(const LaunchArgs &a) {
 
 // CTA-pair kernel: cluster of 2 along x; the grid is clamped to the number
 // of pairs the device can hold at once (queried once per device).
-template <Kind KD, int BN>
+template <Kind KD, int BN, int MC>
 static cudaError_t launch_pair(const LaunchArgs &a) {
     using C = PairConfig<KD, BN>;
-    auto kernel = tg_gemm_pair_kernel<KD, BN>;
+    constexpr int CL = 2 * MC;  // CTAs per cluster
+    auto kernel = tg_gemm_pair_kernel<KD, BN, MC>;
     static std::atomic<uint64_t> configured{0};
     static int max_clusters[64] = {0};
     const uint64_t bit = (a.device >= 0 && a.device < 64) ? (1ull << a.device) : 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
@@ -52,21 +53,21 @@ static cudaError_t launch_pair(const LaunchArgs &a) {
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int n = 0;
-        cfg.gridDim = dim3(2, 1, 1);
+        cfg.gridDim = dim3(CL, 1, 1);
         e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
         if (bit) max_clusters[a.device] = n;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    int grid = a.grid & ~1;
-    const int cap = bit ? 2 * max_clusters[a.device] : grid;
+    int grid = a.grid - a.grid % CL;
+    const int cap = bit ? CL * max_clusters[a.device] : grid;
     if (grid > cap) grid = cap;
-    if (grid < 2) grid = 2;
+    if (grid < CL) grid = CL;
     cfg.gridDim = dim3(grid, 1, 1);
     if (std::getenv("TG_LOG"))
-        std::fprintf(stderr, "tg_gemm: pair kernel BN=%d grid=%d (planned %d, %d co-resident pairs)\n",
-                     BN, grid, a.grid, bit ? max_clusters[a.device] : -1);
+        std::fprintf(stderr, "tg_gemm: pair kernel BN=%d MC=%d grid=%d (planned %d, %d co-resident clusters)\n",
+                     BN, MC, grid, a.grid, bit ? max_clusters[a.device] : -1);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a.map_a, a.map_b, a.p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -79,8 +80,13 @@ static cudaError_t launch_kind(const LaunchArgs &a) {
             return cudaErrorInvalidValue;
         } else {
             if (a.plain_loads) return cudaErrorInvalidValue;
-            if (a.block_n == 256) return launch_pair<KD, 256>(a);
-            if (a.block_n == 128) return launch_pair<KD, 128>(a);
+            if (a.mc == 2) {
+                if (a.block_n == 256) return launch_pair<KD, 256, 2>(a);
+                if (a.block_n == 128) return launch_pair<KD, 128, 2>(a);
+            } else {
+                if (a.block_n == 256) return launch_pair<KD, 256, 1>(a);
+                if (a.block_n == 128) return launch_pair<KD, 128, 1>(a);
+            }
             return cudaErrorInvalidValue;
         }
     }

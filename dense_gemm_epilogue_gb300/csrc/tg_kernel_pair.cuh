@@ -161,22 +161,35 @@ __device__ __forceinline__ Unit decode_unit(const UnitPlan &up, int64_t u, int n
     return r;
 }
 
-template <Kind KD, int BN>
+// MC = 1: a cluster is one CTA pair.  MC = 2: a cluster of four CTAs is two
+// pairs working on the same 256 A-role rows and neighbouring N blocks (pair
+// q of the cluster takes N block MC * nbc + q).  Then each CTA loads half of
+// its 128 A rows and multicasts them to itself and to the CTA holding the
+// same rows in the other pair, so each CTA moves 24 KB instead of 32 KB per
+// K step through L2; a stage is refilled only after both pairs' MMAs are
+// done with it (its empty barrier takes one arrival from each pair leader).
+template <Kind KD, int BN, int MC>
 __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
     using C = PairConfig<KD, BN>;
     constexpr int S = C::STAGES;
+    static_assert(MC == 1 || MC == 2, "one or two pairs per cluster");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int64_t pair = blockIdx.x >> 1;
-    const int64_t num_pairs = gridDim.x >> 1;
+    const uint32_t rank = cluster_ctarank();     // 0 .. 2*MC-1
+    const uint32_t half = rank & 1u;              // 0: pair leader, 1: pair peer
+    const uint32_t pic = rank >> 1;               // pair within the cluster
+    const uint32_t lead_rank = rank & ~1u;
+    const bool leader = half == 0;
+    const int64_t pair = blockIdx.x / (2 * MC);   // cluster index (work-unit stride)
+    const int64_t num_pairs = gridDim.x / (2 * MC);
+    constexpr uint16_t ALL_CTAS = (uint16_t)((1u << (2 * MC)) - 1u);
+    const uint16_t pair_ctas = (uint16_t)(0x3u << (2 * pic));
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
     auto a_stage = [&](int s) -> uint32_t { return sbase + C::A_OFF + s * C::A_BYTES; };
@@ -190,7 +203,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(C::FULL0 + s), 1);
-            mbar_init(bar(C::EMPTY0 + s), 1);
+            mbar_init(bar(C::EMPTY0 + s), MC);  // one arrival per pair leader
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(C::ACCF0 + a), 1);
@@ -223,16 +236,25 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             bool ok = true;
             for (int64_t u = pair; ok && u < up.units; u += num_pairs) {
                 const Unit un = decode_unit(up, u, nkb);
-                int bt, mb, nb;
-                batch_tile_coords(un.tile, p, bt, mb, nb);
-                const int32_t arow = mb * C::PAIR_M + (int32_t)rank * BLOCK_M;
-                const int32_t brow = nb * BN + (int32_t)rank * C::B_ROWS;
+                int bt, mb, nbc;
+                batch_tile_coords(un.tile, p, bt, mb, nbc);
+                const int nb = nbc * MC + (int)pic;
+                const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
+                const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
                 for (int kb = un.k0; kb < un.k1; ++kb) {
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
-                    const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
+                    const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), lead_rank);
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * (C::A_BYTES + C::B_BYTES));
-                    if (p.l2_hint) {
+                    if constexpr (MC == 2) {
+                        // Half of this CTA's A rows, to this CTA and its partner.
+                        constexpr int HALF_ROWS = BLOCK_M / 2;
+                        tma_load_3d_pair_mcast(a_stage(s) + pic * HALF_ROWS * ROW_BYTES, &tmap_a,
+                                               full_leader, kb * C::BK,
+                                               arow + (int32_t)pic * HALF_ROWS, ab,
+                                               (uint16_t)((1u << rank) | (1u << (rank ^ 2u))));
+                        tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
+                    } else if (p.l2_hint) {
                         tma_load_3d_pair_hint(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow,
                                               ab, pol_a);
                         tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
@@ -278,14 +300,15 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                                      smem_desc_sw128(b0 + kk * 32), C::IDESC,
                                      (kb != un.k0) || (kk != 0));
                     }
-                    mma_commit_pair_mcast(bar(C::EMPTY0 + s), (uint16_t)0x3);
+                    // Every CTA of the cluster may write this stage (multicast).
+                    mma_commit_pair_mcast(bar(C::EMPTY0 + s), ALL_CTAS);
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit_pair_mcast(bar(C::ACCF0 + acc), (uint16_t)0x3);
+                mma_commit_pair_mcast(bar(C::ACCF0 + acc), pair_ctas);
             }
             if (!ok) {
-                mma_commit_pair_mcast(bar(C::DRAIN), (uint16_t)0x1);
+                mma_commit_pair_mcast(bar(C::DRAIN), (uint16_t)(1u << rank));
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(bar(C::DRAIN), 0)) {
                     if (globaltimer_ns() - t0 > p.wait_limit_ns) {
@@ -307,8 +330,9 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         uint32_t tl = 0;
         for (int64_t u = pair; u < up.units; u += num_pairs, ++tl) {
             const Unit un = decode_unit(up, u, nkb);
-            int bt, mb, nb;
-            batch_tile_coords(un.tile, p, bt, mb, nb);
+            int bt, mb, nbc;
+            batch_tile_coords(un.tile, p, bt, mb, nbc);
+            const int nb = nbc * MC + (int)pic;
             const uint32_t acc = tl & 1, use = tl >> 1;
             if (!pair_wait(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
             tc_fence_after();
@@ -317,10 +341,10 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             // 128 rows x BN columns of FP32.
             auto part = [&](int32_t k) -> float * {
                 const int64_t pidx = un.tail * (up.segs - 1) + k;
-                return p.ws + ((pidx * 2 + rank) * BN) * (int64_t)BLOCK_M;
+                return p.ws + ((pidx * 2 + half) * BN) * (int64_t)BLOCK_M;
             };
             auto flag = [&](int32_t k) -> uint32_t * {
-                return p.flags + (un.tail * (up.segs - 1) + k) * 2 + rank;
+                return p.flags + (un.tail * (up.segs - 1) + k) * 2 + half;
             };
             if (un.seg >= 0 && un.seg < up.segs - 1) {
                 // Writer: raw FP32 partial sums to the workspace, then the flag.
@@ -361,7 +385,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                         for (int32_t k = 0; k < up.segs - 1; ++k) (void)ld_acquire_gpu_u32(flag(k));
                     }
                 }
-                const int32_t r = mb * C::PAIR_M + (int32_t)rank * BLOCK_M + row_in_half;
+                const int32_t r = mb * C::PAIR_M + (int32_t)half * BLOCK_M + row_in_half;
                 const bool row_ok = r < p.m;
 #pragma unroll 1
                 for (int c0 = cbase; ready && c0 < cbase + COLS; c0 += 32) {
@@ -393,7 +417,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             // release, which would first wait for this warp's D stores to drain.
             if (lane == 0) {
                 if (leader) mbar_arrive(bar(C::ACCE0 + acc));
-                else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE0 + acc), 0));
+                else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE0 + acc), lead_rank));
             }
         }
     }

@@ -15,7 +15,8 @@ struct LaunchArgs {
     CUtensorMap map_b;   // B-role operand
     int block_n;         // tile N: 64, 128 or 256 (single CTA); 128 or 256 (CTA pair)
     bool plain_loads;    // plain bounds-checked loads instead of TMA (single CTA only)
-    bool pair;           // CTA-pair kernel (cluster of 2, cta_group::2 MMA)
+    bool pair;           // CTA-pair kernel (cta_group::2 MMA)
+    int mc;              // pair kernel: pairs per cluster (1, or 2 with A multicast)
     int grid;            // persistent CTAs (even for the pair kernel)
     int device;          // current device ordinal (for the per-device attribute cache)
     cudaStream_t stream;

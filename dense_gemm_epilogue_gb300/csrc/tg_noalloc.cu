@@ -184,15 +184,18 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     la.block_n = info.block_n;
     la.plain_loads = info.producer == 2;
     la.pair = info.cta_pair != 0;
+    la.mc = info.multicast == 2 ? 2 : 1;
     int64_t tiles = info.tiles;
     int grid = info.grid;
     if (!la.plain_loads &&
-        !(noalloc_encode(&la.map_a, in_dtype, ar, mk, K, ldar, tg::BLOCK_M) &&
+        !(noalloc_encode(&la.map_a, in_dtype, ar, mk, K, ldar,
+                         la.pair && la.mc == 2 ? tg::BLOCK_M / 2 : tg::BLOCK_M) &&
           noalloc_encode(&la.map_b, in_dtype, br, nk, K, ldbr,
                          la.pair ? info.block_n / 2 : info.block_n))) {
         // Shapes the TMA unit cannot describe: single-CTA tiles, plain loads.
         la.plain_loads = true;
         la.pair = false;
+        la.mc = 1;
         tiles = cdiv(mk, tg::BLOCK_M) * cdiv(nk, info.block_n);
         grid = (int)(tiles < nd->sms ? tiles : nd->sms);
     }
@@ -201,7 +204,7 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     p.n = (int32_t)nk;
     p.k = (int32_t)K;
     p.num_m_blocks = (int32_t)cdiv(mk, la.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
-    p.num_n_blocks = (int32_t)cdiv(nk, info.block_n);
+    p.num_n_blocks = (int32_t)cdiv(cdiv(nk, info.block_n), la.mc);
     p.num_k_blocks = (int32_t)cdiv(K, info.block_k);
     p.raster_group = info.raster_group;
     p.relu = relu;

@@ -373,3 +373,22 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32
 }
 
 }  // namespace tg
+
+namespace tg {
+
+// 3-D CTA-pair load multicast to every CTA in `mask`: each destination gets
+// the box at offset `dst` of its own shared memory.  `bar` is a
+// shared::cluster barrier address in an even (leader) CTA: each
+// destination's bytes are signalled at that offset in the leader of the
+// destination's own pair.
+__device__ __forceinline__ void tma_load_3d_pair_mcast(uint32_t dst, const CUtensorMap *map,
+                                                       uint32_t bar, int32_t c0, int32_t c1,
+                                                       int32_t c2, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(mask)
+        : "memory");
+}
+
+}  // namespace tg

@@ -126,7 +126,9 @@ typedef struct {
                              2: A-role rows evict-last (CTA-pair tiles) */
     int32_t prefetch_k;   /* 0: planner; -1: off; n > 0: single-CTA TMA tiles prefetch the A-role
                              rows n K blocks ahead into L2, 4 blocks per burst */
-    int32_t reserved[3];  /* must be zero */
+    int32_t multicast;    /* 0: planner; 1: one CTA pair per cluster; 2: two pairs per cluster
+                             sharing their A-role rows by TMA multicast (CTA-pair tiles) */
+    int32_t reserved[2];  /* must be zero */
 } tg_options;
 
 /* What the planner chose for one problem (host only; no CUDA call). */
@@ -147,6 +149,7 @@ typedef struct {
     int32_t cta_pair;     /* 1 if a pair of CTAs (a 2-CTA cluster) computes each tile */
     int32_t split_tiles;  /* tiles of the last wave computed as K segments (0: none) */
     int32_t split_segs;   /* K segments per such tile (1: none) */
+    int32_t multicast;    /* CTA pairs per cluster sharing A rows (1 or 2; 0 for single-CTA) */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides

@@ -65,7 +65,8 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
     dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
-    dict(opts={"reserved": [0, 1, 0]}),
+    dict(opts={"reserved": [0, 1]}), dict(opts={"multicast": 3}),
+    dict(opts={"multicast": 2, "cta_pair": 1}),
     dict(opts={"cta_pair": 3}), dict(opts={"cta_pair": 2, "block_n": 64}),
     dict(dtype=2, opts={"cta_pair": 2}),
 ])
@@ -202,4 +203,20 @@ def test_batched_invalid_arguments_rejected_before_cuda(tg, args):
 def test_batched_empty_is_ok_without_cuda(tg):
     assert tg.tg_gemm_batched(8, 8, 8, 1.0, FAKE, 8, 64, FAKE, 8, 64, FAKE, 8, 64, 0, "bf16", "bf16",
                               True) == tg.TG_OK
+
+
+def test_plan_multicast_clusters(tg):
+    """Two CTA pairs per cluster share their A rows: a cluster covers two N
+    blocks, the grid is a multiple of four CTAs, and no K split is used."""
+    w = si.WORKLOADS["c4_bf16_8192"]
+    one = plan(tg, w, opts={"multicast": 1})
+    two = plan(tg, w, opts={"multicast": 2})
+    assert one["multicast"] == 1 and two["multicast"] == 2
+    assert two["tiles"] * 2 == one["tiles"] and two["grid"] % 4 == 0 and two["grid"] == 152
+    assert two["split_segs"] == 1
+    assert plan(tg, w, opts={"cta_pair": 1})["multicast"] == 0
+    # A single N block leaves nothing to share.
+    narrow = si.Workload("n", 4096, 200, 4096, "bf16", 1.0, True, 0, "normal")
+    with pytest.raises(tg.TgError):
+        plan(tg, narrow, opts={"multicast": 2, "cta_pair": 2, "block_n": 256})
 

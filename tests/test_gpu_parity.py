@@ -79,6 +79,30 @@ def test_cta_pair_configs(dtype, block_n, M, N, K):
     check_full(w, opts={"cta_pair": 2, "block_n": block_n})
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(600, 1100, 520), (257, 500, 64), (1000, 1800, 2048), (90, 700, 128)])
+def test_multicast_clusters(dtype, block_n, M, N, K):
+    """Two CTA pairs per cluster sharing their A rows by TMA multicast; odd
+    N-block counts give the second pair a tile wholly outside N."""
+    w = si.Workload("mc", M, N, K, dtype, 1.25, True, 91 + M + N, "uniform", ldc=M + 7)
+    check_full(w, opts={"cta_pair": 2, "multicast": 2, "block_n": block_n, "swap_ab": 1},
+               repeats=2)
+
+
+def test_multicast_persistent_swapped_and_batched():
+    from gemm_harness import check_batched
+
+    w = si.Workload("mc_p", 1300, 1500, 704, "bf16", 1.0, True, 92, "normal")
+    for g in (4, 8, 12):
+        check_full(w, opts={"cta_pair": 2, "multicast": 2, "max_ctas": g, "raster_group": 2})
+    # Swapped roles: role-space N is the original M (300 -> two N blocks).
+    ws = si.Workload("mc_s", 300, 2000, 512, "fp16", 1.0, False, 93, "uniform", ldc=304)
+    check_full(ws, opts={"cta_pair": 2, "multicast": 2, "swap_ab": 2})
+    wb = si.Workload("mc_b", 500, 700, 1024, "bf16", -1.0, True, 94, "uniform")
+    check_batched(wb, 3, "bf16", opts={"cta_pair": 2, "multicast": 2})
+
+
 def test_cta_pair_persistent_and_swapped():
     w = si.Workload("pair_persist", 1100, 900, 320, "bf16", 1.0, True, 37, "normal")
     for g in (2, 6):
