@@ -17,7 +17,9 @@ SOURCE = os.path.join(_HERE, "oracle_gemm.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
 
-_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2}
+_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4}
+_STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
+            "e5m2": np.uint8}
 _OUT_CODE = {"f32": 0, "bf16": 1, "fp16": 2}
 GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread"]
 
@@ -47,7 +49,7 @@ def build(force: bool = False) -> str:
 
 def _check_storage(x, dtype: str, name: str) -> np.ndarray:
     x = np.asarray(x)
-    want = np.float32 if dtype == "tf32" else np.uint16
+    want = _STORAGE[dtype]
     if x.dtype != want:
         raise TypeError(f"{name}: {dtype} storage must be {np.dtype(want).name}, got {x.dtype}")
     return np.ascontiguousarray(x)
@@ -81,7 +83,7 @@ class Oracle:
 
         ``A``/``B`` are flat or 2-D storage arrays: a(i,k) = A.flat[i*lda + k],
         b(k,j) = B.flat[k + j*ldb].  bf16/fp16 storage is uint16 bit patterns,
-        tf32 storage is float32.
+        e4m3/e5m2 storage uint8 bit patterns, tf32 storage float32.
         """
         A = _check_storage(A, dtype, "A")
         B = _check_storage(B, dtype, "B")

@@ -9,7 +9,7 @@
  *
  * What it computes (for every 0 <= i < M, 0 <= j < N):
  *   1. decode each operand element exactly from its storage format
- *      (bf16 / fp16 bit patterns, or fp32 narrowed to tf32);
+ *      (bf16 / fp16 / e4m3 / e5m2 bit patterns, or fp32 narrowed to tf32);
  *   2. s = sum_{k=0}^{K-1} a(i,k) * b(k,j), in double, k ascending
  *      ("Matrix Multiplication", Step 3 "Looping over K": C[i,j] is the sum
  *      over k of A[i,k]*B[k,j]; accumulate wider than the inputs);
@@ -44,7 +44,7 @@
 #include <unistd.h>
 
 /* Operand storage formats understood by the oracle. */
-enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_TF32 = 2 };
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_TF32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
 
 /* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
 double orc_decode_bf16(uint16_t h) {
@@ -107,10 +107,43 @@ double orc_decode_tf32(uint32_t u) {
     return s ? -v : v;
 }
 
+/*
+ * 8-bit floating point operands (the FP8 formats of the tensor core's
+ * f8f6f4 kind, the step before the block-scaled matmuls of "Matrix
+ * Multiplication", "Where to go from here").
+ * E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ *   infinities; exponent 15 with fraction 7 is NaN; largest finite 448.
+ * E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits; exponent
+ *   31 is infinity (fraction 0) or NaN; largest finite 57344.
+ */
+double orc_decode_e4m3(uint8_t h) {
+    int s = (h >> 7) & 1;
+    int e = (h >> 3) & 0xF;
+    int f = h & 0x7;
+    double v;
+    if (e == 0xF && f == 0x7) v = NAN;
+    else if (e == 0) v = ldexp((double)f, -6 - 3);
+    else v = ldexp((double)(8 + f), e - 7 - 3);
+    return s ? -v : v;
+}
+
+double orc_decode_e5m2(uint8_t h) {
+    int s = (h >> 7) & 1;
+    int e = (h >> 2) & 0x1F;
+    int f = h & 0x3;
+    double v;
+    if (e == 0x1F) v = (f == 0) ? INFINITY : NAN;
+    else if (e == 0) v = ldexp((double)f, -14 - 2);
+    else v = ldexp((double)(4 + f), e - 15 - 2);
+    return s ? -v : v;
+}
+
 static double decode_elem(const void *base, int64_t idx, int dtype) {
     switch (dtype) {
     case ORC_BF16: return orc_decode_bf16(((const uint16_t *)base)[idx]);
     case ORC_FP16: return orc_decode_fp16(((const uint16_t *)base)[idx]);
+    case ORC_E4M3: return orc_decode_e4m3(((const uint8_t *)base)[idx]);
+    case ORC_E5M2: return orc_decode_e5m2(((const uint8_t *)base)[idx]);
     default: {
         uint32_t u;
         memcpy(&u, (const unsigned char *)base + 4 * idx, 4);
@@ -182,7 +215,7 @@ int orc_gemm(int64_t M, int64_t N, int64_t K, double alpha,
              int dtype, int relu, double *D, int64_t ldd, double *scale,
              int nthreads) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldd < M) return -1;
-    if (dtype < ORC_BF16 || dtype > ORC_TF32) return -1;
+    if (dtype < ORC_BF16 || dtype > ORC_E5M2) return -1;
     if (M == 0 || N == 0) return 0;
     double *Ad = (double *)malloc(sizeof(double) * (size_t)(M * (K ? K : 1)));
     double *Bd = (double *)malloc(sizeof(double) * (size_t)(N * (K ? K : 1)));
@@ -257,7 +290,7 @@ int orc_gemm_entries(int64_t M, int64_t N, int64_t K, double alpha,
                      int dtype, int relu, const int64_t *I, const int64_t *J,
                      int64_t count, double *out, double *scale, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || count < 0) return -1;
-    if (dtype < ORC_BF16 || dtype > ORC_TF32) return -1;
+    if (dtype < ORC_BF16 || dtype > ORC_E5M2) return -1;
     for (int64_t q = 0; q < count; ++q)
         if (I[q] < 0 || I[q] >= M || J[q] < 0 || J[q] >= N) return -1;
     if (count == 0) return 0;

@@ -24,7 +24,8 @@ on every machine and every numpy version):
   ``sqrt(-2 ln(1 - u1)) * cos(2 pi u2)`` in float64, then float32.
 
 Operands are "rounded to BF16/FP16" from float32 by IEEE round to nearest,
-ties to even.  TF32 workloads keep float32 storage; the narrowing is the
+ties to even; FP8 (E4M3/E5M2) operands take the nearest code (ties to the
+even code, saturating at the largest finite value).  TF32 workloads keep float32 storage; the narrowing is the
 method's own step and happens inside the GEMM, not here.
 
 Storage follows the GEMM's conventions (Walk through GEMM, section 2 "Bind
@@ -125,15 +126,55 @@ def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
-DTYPES = ("bf16", "fp16", "tf32")
+def _fp8_table(ebits: int, mbits: int, bias: int, e4m3: bool) -> np.ndarray:
+    """Value of each non-negative finite FP8 code 0..127 (NaN/Inf codes as NaN)."""
+    vals = np.empty(128, dtype=np.float64)
+    for c in range(128):
+        e, f = c >> mbits, c & ((1 << mbits) - 1)
+        top = (1 << ebits) - 1
+        if (e4m3 and e == top and f == (1 << mbits) - 1) or (not e4m3 and e == top):
+            vals[c] = np.nan
+        elif e == 0:
+            vals[c] = f * 2.0 ** (1 - bias - mbits)
+        else:
+            vals[c] = (2 ** mbits + f) * 2.0 ** (e - bias - mbits)
+    return vals
+
+
+_FP8 = {"e4m3": _fp8_table(4, 3, 7, True), "e5m2": _fp8_table(5, 2, 15, False)}
+
+
+def f32_to_fp8_bits(x: np.ndarray, fmt: str) -> np.ndarray:
+    """Round float32 values to the nearest E4M3 / E5M2 code (ties to the even
+    code), saturating at the largest finite value; NaN -> the NaN code."""
+    table = _FP8[fmt]
+    fin = ~np.isnan(table)
+    vals = table[fin]
+    codes = np.arange(128)[fin]
+    a = np.abs(np.asarray(x, dtype=np.float64)).reshape(-1)
+    hi = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
+    lo = hi - 1
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    pick = np.where((dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0)), hi, lo)
+    pick = np.where(a >= vals[-1], len(vals) - 1, pick)
+    out = codes[pick].astype(np.uint8)
+    sign = np.signbit(np.asarray(x, dtype=np.float64).reshape(-1))
+    out = np.where(sign, out | 0x80, out).astype(np.uint8)
+    nan = np.isnan(np.asarray(x, dtype=np.float64).reshape(-1))
+    out[nan] = 0x7F
+    return out.reshape(np.shape(x))
+
+
+DTYPES = ("bf16", "fp16", "tf32", "e4m3", "e5m2")
 
 
 def element_bytes(dtype: str) -> int:
-    return {"bf16": 2, "fp16": 2, "tf32": 4}[dtype]
+    return {"bf16": 2, "fp16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1}[dtype]
 
 
 def storage_numpy_dtype(dtype: str):
-    return {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32}[dtype]
+    return {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
+            "e5m2": np.uint8}[dtype]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -201,6 +242,8 @@ def _to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
         return f32_to_bf16_bits(x32)
     if dtype == "fp16":
         return f32_to_fp16_bits(x32)
+    if dtype in ("e4m3", "e5m2"):
+        return f32_to_fp8_bits(x32, dtype)
     if dtype == "tf32":
         return np.ascontiguousarray(x32, dtype=np.float32)
     raise ValueError(dtype)
@@ -211,6 +254,8 @@ def pad_value(dtype: str):
         return np.uint16(PAD_BF16)
     if dtype == "fp16":
         return np.uint16(PAD_FP16)
+    if dtype in ("e4m3", "e5m2"):
+        return np.uint8(0x7F)      # NaN in both FP8 formats
     return np.array([PAD_F32_BITS], dtype=np.uint32).view(np.float32)[0]
 
 

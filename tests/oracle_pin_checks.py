@@ -42,11 +42,27 @@ def fp16_bits_exact(x) -> np.ndarray:
     return h.view(np.uint16)
 
 
+def fp8_bits_exact(x, dtype) -> np.ndarray:
+    """float -> FP8 code for values known to be exactly representable, using
+    the float16-based second decode as the table."""
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    table = (e5m2_by_fp16 if dtype == "e5m2" else e4m3_by_fp16)(codes)
+    f = np.asarray(x, dtype=np.float64)
+    out = np.zeros(f.shape, dtype=np.uint8)
+    for idx, v in np.ndenumerate(f):
+        hit = np.flatnonzero((table == v) & (np.signbit(table) == np.signbit(v)))
+        assert hit.size >= 1, f"{v} not exact in {dtype}"
+        out[idx] = hit[0]
+    return out
+
+
 def storage_of(x, dtype):
     if dtype == "bf16":
         return bf16_bits_exact(x)
     if dtype == "fp16":
         return fp16_bits_exact(x)
+    if dtype in ("e4m3", "e5m2"):
+        return fp8_bits_exact(x, dtype)
     return np.asarray(x, dtype=np.float32)
 
 
@@ -189,7 +205,7 @@ def check_rank1(orc):
     u, v, s, t = rank1_case()
     Alog, Blog = np.outer(u, s), np.outer(t, v)
     st = float(np.dot(s, t))
-    for dt in ("bf16", "fp16", "tf32"):
+    for dt in ("bf16", "fp16", "tf32", "e4m3", "e5m2"):
         for alpha, relu in ((1.0, False), (1.5, True), (-0.5, True)):
             D, S = run(orc, Alog, Blog, dt, alpha, relu, with_scale=True)
             want = alpha * st * np.outer(u, v)
@@ -245,7 +261,18 @@ def check_bruteforce_exact(orc):
         cb = si.raw_u64(seed, 1, 0, K * N) % np.uint64(129)
         Alog = (ca.astype(np.float64) - 64.0).reshape(M, K) / 64.0
         Blog = (cb.astype(np.float64) - 64.0).reshape(K, N) / 64.0
-        for dt in ("bf16", "fp16", "tf32"):
+        # FP8 holds 2-3 fraction bits: a coarser grid (c/8, |c| <= 8).
+        Alog8 = np.round(Alog * 8.0) / 8.0
+        Blog8 = np.round(Blog * 8.0) / 8.0
+        for dt in ("bf16", "fp16", "tf32", "e4m3", "e5m2"):
+            if dt in ("e4m3", "e5m2"):
+                for alpha, relu in ((1.0, False), (-1.5, True)):
+                    D = run(orc, Alog8, Blog8, dt, alpha, relu)
+                    E = exact_product(Alog8, Blog8, alpha, relu)
+                    for i in range(M):
+                        for j in range(N):
+                            assert Fraction(D[i, j]) == E[i][j], (dt, M, N, K, i, j)
+                continue
             for alpha, relu in ((1.0, False), (-1.5, True)):
                 D = run(orc, Alog, Blog, dt, alpha, relu)
                 E = exact_product(Alog, Blog, alpha, relu)
@@ -402,6 +429,60 @@ def check_round_output(orc):
     assert list(hand) == [1.0, 1.0 + 2 ** -6, 256.0, 256.0, 256.0]
 
 
+def e5m2_by_fp16(codes: np.ndarray) -> np.ndarray:
+    """E5M2 is the top byte of IEEE binary16 (same sign, 5-bit exponent with
+    bias 15, top 2 fraction bits): decode through numpy's float16."""
+    with np.errstate(invalid="ignore"):
+        return (codes.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+
+
+def e4m3_by_fp16(codes: np.ndarray) -> np.ndarray:
+    """E4M3 re-encoded as binary16 bits (exponent bias 7 -> 15, 3 fraction
+    bits -> the top of 10; subnormals shifted into normal fp16 numbers) and
+    decoded by numpy: a second path to the same values."""
+    out = np.empty(codes.shape, dtype=np.float64)
+    for idx, c in enumerate(codes.astype(np.int64)):
+        s, e, f = (c >> 7) & 1, (c >> 3) & 0xF, c & 7
+        if e == 15 and f == 7:
+            out[idx] = np.nan
+            continue
+        if e == 0:
+            if f == 0:
+                h = s << 15
+            else:                      # f * 2^-9 = (f << shift) / 8 * 2^(-6 - shift)
+                shift = 0
+                while not (f & 8):
+                    f <<= 1
+                    shift += 1
+                h = (s << 15) | ((-6 - shift + 15) << 10) | ((f & 7) << 7)
+        else:
+            h = (s << 15) | ((e - 7 + 15) << 10) | (f << 7)
+        out[idx] = np.array([h], dtype=np.uint16).view(np.float16).astype(np.float64)[0]
+    return out
+
+
+def check_fp8_decode(orc):
+    """All 256 E4M3 and E5M2 patterns against decodes through numpy's
+    float16, the format's landmark values, sign symmetry and monotonicity."""
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    for dt, second in (("e5m2", e5m2_by_fp16), ("e4m3", e4m3_by_fp16)):
+        got = orc.decode(codes, dt)
+        want = second(codes)
+        assert np.array_equal(np.isnan(got), np.isnan(want)), dt
+        ok = ~np.isnan(want)
+        assert np.array_equal(got[ok], want[ok]), dt
+        assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok])), dt
+        pos = got[:128]
+        fin = pos[~np.isnan(pos) & ~np.isinf(pos)]
+        assert np.all(np.diff(fin) > 0), dt                  # codes order the values
+        assert np.array_equal(got[128:][ok[:128]], -got[:128][ok[:128]]), dt
+    e4 = orc.decode(np.array([0x01, 0x08, 0x38, 0x7E, 0x7F, 0xFE], np.uint8), "e4m3")
+    assert list(e4[[0, 1, 2, 3, 5]]) == [2.0 ** -9, 2.0 ** -6, 1.0, 448.0, -448.0]
+    assert np.isnan(e4[4])
+    e5 = orc.decode(np.array([0x01, 0x04, 0x3C, 0x7B, 0x7C, 0x7D], np.uint8), "e5m2")
+    assert list(e5[:5]) == [2.0 ** -16, 2.0 ** -14, 1.0, 57344.0, math.inf] and np.isnan(e5[5])
+
+
 ALL_CHECKS = [
     check_decode_tables,
     check_tf32_narrowing,
@@ -419,4 +500,5 @@ ALL_CHECKS = [
     check_thread_independent,
     check_degenerate,
     check_round_output,
+    check_fp8_decode,
 ]

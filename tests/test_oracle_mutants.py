@@ -38,6 +38,11 @@ MUTANTS = {
     "round_no_overflow": ("if (out > maxf) out = INFINITY;", "if (0) out = INFINITY;"),
     "round_fp16_emin": ("case 2: y[q] = round_format(y[q], 11, -14, 15); break;",
                         "case 2: y[q] = round_format(y[q], 11, -15, 15); break;"),
+    "e4m3_bias": ("else v = ldexp((double)(8 + f), e - 7 - 3);", "else v = ldexp((double)(8 + f), e - 8 - 3);"),
+    "e4m3_subnormal": ("else if (e == 0) v = ldexp((double)f, -6 - 3);",
+                       "else if (e == 0) v = ldexp((double)f, -7 - 3);"),
+    "e4m3_no_nan": ("if (e == 0xF && f == 0x7) v = NAN;", "if (0) v = NAN;"),
+    "e5m2_inf_as_nan": ("if (e == 0x1F) v = (f == 0) ? INFINITY : NAN;", "if (e == 0x1F) v = NAN;"),
     "scale_signed_alpha": ("jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;",
                            "jb->scale[i + j * jb->ldd] = jb->alpha * t;"),
 }
