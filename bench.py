@@ -266,7 +266,7 @@ def run_gpu(args, rank, world, local):
     batched = nbat > 1 or out != "f32"
     lda, ldb, ldc = w.strides
     A, B = si.make_operands(w)
-    view = np.float32 if w.dtype == "tf32" else np.int16
+    view = {"tf32": np.float32, "e4m3": np.uint8, "e5m2": np.uint8}.get(w.dtype, np.int16)
     hA = torch.from_numpy(np.tile(A.reshape(-1), nbat).view(view)).pin_memory()
     hB = torch.from_numpy(np.tile(B.reshape(-1), nbat).view(view)).pin_memory()
     dA = hA.cuda()
@@ -388,9 +388,12 @@ def run_gpu(args, rank, world, local):
         launch_avg_ms = statistics.fmean(launch_ms)
         # Back-to-back launches for more than ~50 ms run in the power-capped
         # regime the sustained peak was measured in; a short burst compares
-        # with the burst peak.  Both are reported.  TF32 takes the BF16 peak
-        # times the nominal TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s).
-        ratio = (1.1 / 2.25) if w.dtype == "tf32" else 1.0
+        # with the burst peak.  Both are reported.  TF32 and the 8-bit floats
+        # take the BF16 peak times the nominal ratio to BF16 (1.1 / 2.25 and
+        # 4.5 / 2.25 PFLOP/s).
+        ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25}.get(w.dtype, 1.0)
+        ratio_note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
+                      "e5m2": " x 4.5/2.25 (FP8)"}.get(w.dtype, "")
         sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
         tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
         burst_tpeak = ratio * float(peaks["bf16_tflops"])
@@ -411,7 +414,7 @@ def run_gpu(args, rank, world, local):
             burst = {"achieved": alg_bytes / (statistics.fmean(first) * 1e-3) / 1e9, "peak": hbm}
         burst["frac"] = burst["achieved"] / burst["peak"]
         burst["launches"] = len(first)
-        dt = "bf16" if w.dtype == "bf16" else ("fp16" if w.dtype == "fp16" else "tf32")
+        dt = w.dtype
         kname = ("tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
             f"<{dt.upper()}, {plan['block_m']}x{plan['block_n']}, " + \
             f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>"
@@ -430,7 +433,7 @@ def run_gpu(args, rank, world, local):
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": (("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")
                                          if tensor_bound else "hbm_gbs") + f" of {peak_src}" +
-                                        (" x 1.1/2.25 (TF32)" if tensor_bound and ratio != 1.0 else "") +
+                                        (ratio_note if tensor_bound else "") +
                                         (f" (the timed region ran {region_ms:.0f} ms of back-to-back "
                                          f"launches)" if tensor_bound and sustained else ""),
                          "burst": burst,

@@ -28,7 +28,10 @@ TG_ERR_DEVICE_TIMEOUT = 4
 TG_BF16 = 0
 TG_FP16 = 1
 TG_TF32 = 2
-DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32}
+TG_E4M3 = 3
+TG_E5M2 = 4
+DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32, "e4m3": TG_E4M3,
+               "e5m2": TG_E5M2}
 
 TG_EPILOGUE_NONE = 0
 TG_EPILOGUE_RELU = 1

@@ -70,7 +70,16 @@ std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int elem_bytes(tg_dtype t) { return t == TG_TF32 ? 4 : 2; }
+int elem_bytes(tg_dtype t) {
+    return t == TG_TF32 ? 4 : (t == TG_E4M3 || t == TG_E5M2) ? 1 : 2;
+}
+
+// K elements per pipeline stage: one 128-byte swizzle row of the type.
+int block_k(tg_dtype t) { return 128 / elem_bytes(t); }
+
+bool known_dtype(tg_dtype t) {
+    return t == TG_BF16 || t == TG_FP16 || t == TG_TF32 || t == TG_E4M3 || t == TG_E5M2;
+}
 
 struct DeviceState {
     bool ready = false;
@@ -252,6 +261,8 @@ void pair_numbers(int bn, int *stages, int *smem, int *threads, int *tmem) {
 void config_numbers_for(tg_dtype t, int bn, int *stages, int *smem, int *threads, int *tmem) {
     if (t == TG_BF16) config_numbers<Kind::BF16>(bn, stages, smem, threads, tmem);
     else if (t == TG_FP16) config_numbers<Kind::FP16>(bn, stages, smem, threads, tmem);
+    else if (t == TG_E4M3) config_numbers<Kind::E4M3>(bn, stages, smem, threads, tmem);
+    else if (t == TG_E5M2) config_numbers<Kind::E5M2>(bn, stages, smem, threads, tmem);
     else config_numbers<Kind::TF32>(bn, stages, smem, threads, tmem);
 }
 
@@ -271,7 +282,7 @@ bool tma_batch_legal(int64_t stride, int esize, int64_t batch) {
 tg_status validate(const Problem &q, const tg_options *o) {
     const tg_dtype t = q.t;
     const int64_t M = q.M, N = q.N, K = q.K;
-    if (t != TG_BF16 && t != TG_FP16 && t != TG_TF32) return TG_ERR_INVALID_VALUE;
+    if (!known_dtype(t)) return TG_ERR_INVALID_VALUE;
     if (q.out_fmt < 0 || q.out_fmt > 2) return TG_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0 || q.batch < 0) return TG_ERR_INVALID_VALUE;
     if (q.lda < (K > 1 ? K : 1) || q.ldb < (K > 1 ? K : 1) || q.ldc < (M > 1 ? M : 1))
@@ -336,12 +347,14 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     // (128 rows each), and its shared memory moves the A and B bytes twice
     // (TMA write, tensor-core read) at about 128 B/cycle: 64 + BN/2 cycles for
     // a single-CTA tile, 64 + BN/4 when a CTA pair splits B.  A tile costs the
-    // larger of the two.  Pair tiles need BF16/FP16 operands on TMA.
+    // larger of the two.  Pair tiles need 16-bit or 8-bit operands on TMA.
+    // (8-bit kinds take 32 elements per 32-byte K step at twice the rate,
+    // so the same per-byte costs apply.)
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
     if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
     if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     // Pair tiles need a few K blocks to fill their 7-stage ring.
-    const bool pair_auto = pair_ok && ceil_div(K, 64) >= 8;
+    const bool pair_auto = pair_ok && ceil_div(K, block_k(t)) >= 8;
     struct Cand { bool pair; int bn; };
     Cand cands[5];
     int nc = 0;
@@ -378,7 +391,9 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     p.tiles = q.batch * p.tiles_per_batch;
     if (p.pair) {
         if (t == TG_BF16) pair_numbers<Kind::BF16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
-        else pair_numbers<Kind::FP16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+        else if (t == TG_FP16) pair_numbers<Kind::FP16>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+        else if (t == TG_E4M3) pair_numbers<Kind::E4M3>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+        else pair_numbers<Kind::E5M2>(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
     } else {
         config_numbers_for(t, p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
         if (p.producer == 2) p.threads += 4 * 32;  // plain-load producer warps
@@ -401,7 +416,7 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         if (pairs_max < 1) pairs_max = 1;
         p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 1);
         if (p.mc != 1) p.split_max = 1;  // K segments only with one pair per cluster
-        const int64_t nkb = ceil_div(K, 64);
+        const int64_t nkb = ceil_div(K, block_k(t));
         int64_t pairs = pairs_max;
         if (p.tiles < pairs_max) {
             int64_t segs = pairs_max / p.tiles;
@@ -458,6 +473,7 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
     const int e = elem_bytes(t);
     CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                              : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                             : e == 1       ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, (cuuint64_t)nb};
     cuuint64_t strides[2] = {(cuuint64_t)(ld * e), (cuuint64_t)(nb > 1 ? sb * e : ld * e)};
@@ -532,7 +548,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.k = (int32_t)q.K;
     p.num_m_blocks = (int32_t)ceil_div(plan.mk, plan.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M);
     p.num_n_blocks = (int32_t)ceil_div(ceil_div(plan.nk, plan.block_n), plan.mc);
-    p.num_k_blocks = (int32_t)ceil_div(q.K, q.t == TG_TF32 ? 32 : 64);
+    p.num_k_blocks = (int32_t)ceil_div(q.K, block_k(q.t));
     p.raster_group = plan.group;
     p.relu = relu;
     p.num_tiles = plan.tiles;
@@ -574,6 +590,8 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     cudaError_t e;
     if (q.t == TG_BF16) e = tg::launch_bf16(la);
     else if (q.t == TG_FP16) e = tg::launch_fp16(la);
+    else if (q.t == TG_E4M3) e = tg::launch_e4m3(la);
+    else if (q.t == TG_E5M2) e = tg::launch_e5m2(la);
     else e = tg::launch_tf32(la);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
@@ -643,7 +661,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->split_segs = p.split_segs;
     out->multicast = p.pair ? p.mc : 0;
     out->block_n = p.block_n;
-    out->block_k = in_dtype == TG_TF32 ? 32 : 64;
+    out->block_k = block_k(in_dtype);
     out->stages = p.stages;
     out->producer = p.producer;
     out->swap_ab = p.swap ? 1 : 0;

@@ -1,5 +1,5 @@
 // Kernel instantiation and launch for one operand kind; included once by each
-// tg_inst_<kind>.cu so the three kinds compile in parallel.
+// tg_inst_<kind>.cu so the operand kinds compile in parallel.
 #pragma once
 
 #include <atomic>

@@ -14,7 +14,8 @@
 //               K stage, consume, then release it; here the release is the
 //               tensor core's own completion signal).
 //   warp 1      tensor-memory allocator and MMA issuer: one thread issues
-//               tcgen05.mma (128 x BN x 16 for 16-bit kinds, x8 for TF32) into
+//               tcgen05.mma (128 x BN x 16 for 16-bit kinds, x8 for TF32, x32
+//               for 8-bit floats) into
 //               one of two TMEM accumulators, FP32 ("Matrix Multiplication"
 //               step 3: the accumulator is wider than the inputs).
 //   warps 2-5   epilogue: tcgen05.ld TMEM -> registers, y = alpha*x, then the
@@ -44,7 +45,10 @@
 
 namespace tg {
 
-enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2 };
+enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2, E4M3 = 3, E5M2 = 4 };
+
+// Tensor-core instruction family of a kind.
+enum class MmaKind : int { F16, TF32, F8 };
 
 template <Kind KD>
 struct KindTraits;
@@ -52,17 +56,52 @@ template <>
 struct KindTraits<Kind::BF16> {
     static constexpr int elem_bytes = 2, block_k = 64, umma_k = 16;
     static constexpr uint32_t fmt = 1;  // instruction-descriptor operand format: BF16
+    static constexpr MmaKind mma = MmaKind::F16;
 };
 template <>
 struct KindTraits<Kind::FP16> {
     static constexpr int elem_bytes = 2, block_k = 64, umma_k = 16;
     static constexpr uint32_t fmt = 0;  // F16
+    static constexpr MmaKind mma = MmaKind::F16;
 };
 template <>
 struct KindTraits<Kind::TF32> {
     static constexpr int elem_bytes = 4, block_k = 32, umma_k = 8;
     static constexpr uint32_t fmt = 2;  // TF32
+    static constexpr MmaKind mma = MmaKind::TF32;
 };
+// 8-bit floats: one 128-byte swizzle row holds 128 elements; one MMA takes
+// 32 of them (32 bytes of K, the same byte step as the 16-bit kinds).
+template <>
+struct KindTraits<Kind::E4M3> {
+    static constexpr int elem_bytes = 1, block_k = 128, umma_k = 32;
+    static constexpr uint32_t fmt = 0;  // E4M3 in the f8f6f4 format field
+    static constexpr MmaKind mma = MmaKind::F8;
+};
+template <>
+struct KindTraits<Kind::E5M2> {
+    static constexpr int elem_bytes = 1, block_k = 128, umma_k = 32;
+    static constexpr uint32_t fmt = 1;  // E5M2
+    static constexpr MmaKind mma = MmaKind::F8;
+};
+
+// One tcgen05.mma (single CTA) of the kind's family.
+template <Kind KD>
+__device__ __forceinline__ void mma_kind(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                         uint32_t accumulate) {
+    if constexpr (KindTraits<KD>::mma == MmaKind::TF32) mma_tf32(d_tmem, ad, bd, idesc, accumulate);
+    else if constexpr (KindTraits<KD>::mma == MmaKind::F8) mma_f8(d_tmem, ad, bd, idesc, accumulate);
+    else mma_f16(d_tmem, ad, bd, idesc, accumulate);
+}
+
+// One tcgen05.mma of a CTA pair (16-bit and 8-bit kinds).
+template <Kind KD>
+__device__ __forceinline__ void mma_kind_pair(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                              uint32_t idesc, uint32_t accumulate) {
+    static_assert(KindTraits<KD>::mma != MmaKind::TF32, "no TF32 pair tiles");
+    if constexpr (KindTraits<KD>::mma == MmaKind::F8) mma_f8_pair(d_tmem, ad, bd, idesc, accumulate);
+    else mma_f16_pair(d_tmem, ad, bd, idesc, accumulate);
+}
 
 // Codes written to the status word when a bounded wait runs out.
 enum WaitSite : uint32_t {
@@ -342,7 +381,8 @@ __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, 
     constexpr int EPC = 16 / ELEM_BYTES;  // elements per 16-byte chunk
     constexpr int CHUNKS = ROWS * 8;
     constexpr int PER_LANE = CHUNKS / NT;
-    constexpr int BATCH = PER_LANE < 8 ? PER_LANE : 8;
+    constexpr int BATCH_MAX = ELEM_BYTES == 1 ? 4 : 8;  // 16 byte loads per chunk: fewer
+    constexpr int BATCH = PER_LANE < BATCH_MAX ? PER_LANE : BATCH_MAX;
     static_assert(PER_LANE % BATCH == 0, "chunks per lane");
 #pragma unroll 1
     for (int b0 = 0; b0 < PER_LANE; b0 += BATCH) {
@@ -353,7 +393,19 @@ __device__ __forceinline__ void load_stage_plain(uint8_t *dst, const void *src, 
             const int r = ch >> 3, c = ch & 7;
             const int32_t gr = row0 + r;
             const bool row_in = gr < rows_total;
-            if (ELEM_BYTES == 2) {
+            if constexpr (ELEM_BYTES == 1) {
+                const uint8_t *s = static_cast<const uint8_t *>(src) + (int64_t)gr * ld;
+                uint8_t h[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int32_t gk = k0 + c * EPC + e;
+                    h[e] = (row_in && gk < k_total) ? s[gk] : (uint8_t)0;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[i][e] = (uint32_t)h[4 * e] | ((uint32_t)h[4 * e + 1] << 8) |
+                              ((uint32_t)h[4 * e + 2] << 16) | ((uint32_t)h[4 * e + 3] << 24);
+            } else if constexpr (ELEM_BYTES == 2) {
                 const uint16_t *s = static_cast<const uint16_t *>(src) + (int64_t)gr * ld;
                 uint16_t h[8];
 #pragma unroll
@@ -521,8 +573,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
                         const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
                         const uint32_t accumulate = (kb | kk) != 0;
-                        if (C::TF32) mma_tf32(d_tmem, ad, bd, C::IDESC, accumulate);
-                        else mma_f16(d_tmem, ad, bd, C::IDESC, accumulate);
+                        mma_kind<KD>(d_tmem, ad, bd, C::IDESC, accumulate);
                     }
                     mma_commit(bar(C::EMPTY0 + s));  // stage s is free once these MMAs finish
                     if (++s == S) { s = 0; ph ^= 1; }

@@ -65,7 +65,7 @@ struct PairConfig {
     static constexpr uint32_t IDESC = (1u << 4) | (T::fmt << 7) | (T::fmt << 10) |
                                       ((uint32_t)(BN >> 3) << 17) |
                                       ((uint32_t)(PAIR_M >> 4) << 24);
-    static_assert(KD != Kind::TF32, "the pair kernel covers the 16-bit kinds");
+    static_assert(KD != Kind::TF32, "the pair kernel covers the 16-bit and 8-bit kinds");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
 #pragma unroll
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
-                        mma_f16_pair(d_tmem, smem_desc_sw128(a0 + kk * 32),
+                        mma_kind_pair<KD>(d_tmem, smem_desc_sw128(a0 + kk * 32),
                                      smem_desc_sw128(b0 + kk * 32), C::IDESC,
                                      (kb != un.k0) || (kk != 0));
                     }

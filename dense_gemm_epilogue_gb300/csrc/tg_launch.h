@@ -25,5 +25,7 @@ struct LaunchArgs {
 cudaError_t launch_bf16(const LaunchArgs &a);
 cudaError_t launch_fp16(const LaunchArgs &a);
 cudaError_t launch_tf32(const LaunchArgs &a);
+cudaError_t launch_e4m3(const LaunchArgs &a);
+cudaError_t launch_e5m2(const LaunchArgs &a);
 
 }  // namespace tg

@@ -118,9 +118,11 @@ bool noalloc_encode(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
                     int64_t ld, int box_rows) {
     EncodeTiledFn fn = noalloc_encode_fn();
     if (!fn) return false;
-    const int e = t == TG_TF32 ? 4 : 2;
+    const bool fp8 = t == TG_E4M3 || t == TG_E5M2;
+    const int e = t == TG_TF32 ? 4 : fp8 ? 1 : 2;
     const CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                    : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : fp8          ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     // Three dimensions (K, rows, one batch entry), as the kernels load.
     cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, 1};
@@ -231,6 +233,8 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     cudaError_t e;
     if (in_dtype == TG_BF16) e = tg::launch_bf16(la);
     else if (in_dtype == TG_FP16) e = tg::launch_fp16(la);
+    else if (in_dtype == TG_E4M3) e = tg::launch_e4m3(la);
+    else if (in_dtype == TG_E5M2) e = tg::launch_e5m2(la);
     else e = tg::launch_tf32(la);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

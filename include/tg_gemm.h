@@ -20,7 +20,12 @@
  *   D: logical (M, N), M-contiguous:   D[i + j*ldc] (float),   ldc >= max(M,1)
  * Element types: TG_BF16 / TG_FP16 operands are 2-byte storage; TG_TF32
  * operands are FP32 storage narrowed in the kernel to TF32 (10 fraction bits,
- * round to nearest, ties away from zero).  Products accumulate in FP32; D is
+ * round to nearest, ties away from zero); TG_E4M3 / TG_E5M2 operands are
+ * 1-byte 8-bit floats (the OCP FP8 formats: E4M3 with bias 7, no infinities
+ * and NaN at S.1111.111; E5M2 with bias 15, IEEE-style infinities and NaNs),
+ * both operands of the same type, with alpha as the per-tensor scale
+ * ("Matrix Multiplication", "Where to go from here", names FP8 matmuls as the
+ * next step; these are its unscaled-block form).  Products accumulate in FP32; D is
  * FP32.  Only D[i + j*ldc] with i < M, j < N is written: stride padding of D
  * is left untouched, and stride padding of A and B is never read.
  *
@@ -68,7 +73,9 @@ typedef enum {
 typedef enum {
     TG_BF16 = 0,  /* bfloat16 operands */
     TG_FP16 = 1,  /* IEEE binary16 operands */
-    TG_TF32 = 2   /* FP32 storage, narrowed to TF32 in the kernel */
+    TG_TF32 = 2,  /* FP32 storage, narrowed to TF32 in the kernel */
+    TG_E4M3 = 3,  /* 8-bit float, 4 exponent / 3 fraction bits */
+    TG_E5M2 = 4   /* 8-bit float, 5 exponent / 2 fraction bits */
 } tg_dtype;
 
 /* Output element type of tg_gemm_batched ("Matrix Multiplication", Step 4:
@@ -118,7 +125,7 @@ typedef struct {
     int32_t swap_ab;      /* 0: planner; 1: never swap; 2: always swap the A/B roles */
     int32_t raster_group; /* 0: planner; else number of M tiles per raster group (>= 1) */
     int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
-    int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (BF16/FP16, TMA) */
+    int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (not TF32; TMA) */
     int32_t split_k;      /* 0: planner (pair tiles fewer than pairs: split them into up to 8
                              K segments of >= 8 K blocks); 1: never split; n >= 2: split the
                              last, partial wave into at most n segments */
@@ -135,7 +142,8 @@ typedef struct {
 typedef struct {
     int32_t block_m;      /* tile M: 128 (single CTA) or 256 (CTA pair) */
     int32_t block_n;      /* tile N */
-    int32_t block_k;      /* K elements per pipeline stage (64 for 2-byte types, 32 for TF32) */
+    int32_t block_k;      /* K elements per pipeline stage: 128 bytes of K (64 for 2-byte
+                             types, 32 for TF32, 128 for 8-bit floats) */
     int32_t stages;       /* shared-memory ring depth */
     int32_t producer;     /* 1 TMA, 2 plain loads */
     int32_t swap_ab;      /* 1 if the kernel computes D^T = B^T A^T with the roles swapped */

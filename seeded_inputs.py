@@ -126,43 +126,36 @@ def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
-def _fp8_table(ebits: int, mbits: int, bias: int, e4m3: bool) -> np.ndarray:
-    """Value of each non-negative finite FP8 code 0..127 (NaN/Inf codes as NaN)."""
-    vals = np.empty(128, dtype=np.float64)
-    for c in range(128):
-        e, f = c >> mbits, c & ((1 << mbits) - 1)
-        top = (1 << ebits) - 1
-        if (e4m3 and e == top and f == (1 << mbits) - 1) or (not e4m3 and e == top):
-            vals[c] = np.nan
-        elif e == 0:
-            vals[c] = f * 2.0 ** (1 - bias - mbits)
-        else:
-            vals[c] = (2 ** mbits + f) * 2.0 ** (e - bias - mbits)
-    return vals
-
-
-_FP8 = {"e4m3": _fp8_table(4, 3, 7, True), "e5m2": _fp8_table(5, 2, 15, False)}
+# (exponent bias, fraction bits, largest finite value) of the two OCP FP8 formats.
+_FP8 = {"e4m3": (7, 3, 448.0), "e5m2": (15, 2, 57344.0)}
 
 
 def f32_to_fp8_bits(x: np.ndarray, fmt: str) -> np.ndarray:
     """Round float32 values to the nearest E4M3 / E5M2 code (ties to the even
-    code), saturating at the largest finite value; NaN -> the NaN code."""
-    table = _FP8[fmt]
-    fin = ~np.isnan(table)
-    vals = table[fin]
-    codes = np.arange(128)[fin]
-    a = np.abs(np.asarray(x, dtype=np.float64)).reshape(-1)
-    hi = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
-    lo = hi - 1
-    dlo, dhi = a - vals[lo], vals[hi] - a
-    pick = np.where((dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0)), hi, lo)
-    pick = np.where(a >= vals[-1], len(vals) - 1, pick)
-    out = codes[pick].astype(np.uint8)
-    sign = np.signbit(np.asarray(x, dtype=np.float64).reshape(-1))
-    out = np.where(sign, out | 0x80, out).astype(np.uint8)
-    nan = np.isnan(np.asarray(x, dtype=np.float64).reshape(-1))
-    out[nan] = 0x7F
-    return out.reshape(np.shape(x))
+    code), saturating at the largest finite value; NaN -> code 0x7F (NaN in
+    both formats)."""
+    bias, mbits, top = _FP8[fmt]
+    x64 = np.asarray(x, dtype=np.float64).reshape(-1)
+    a = np.abs(x64)
+    nan = np.isnan(a)
+    a = np.where(nan, 0.0, a)
+    emin = 1 - bias
+    # Quantum of the binade holding |x| (the subnormal quantum below 2^emin).
+    _, ex = np.frexp(a)
+    e = np.maximum(ex - 1, emin)
+    q = np.ldexp(1.0, e - mbits)
+    r = np.minimum(np.round(a / q) * q, top)       # np.round: ties to even
+    # Encode: subnormal codes count quanta of 2^(emin - mbits); normal codes
+    # hold (biased exponent, fraction).
+    _, er = np.frexp(r)
+    er = er - 1
+    sub = r < 2.0 ** emin
+    code_sub = np.round(r / 2.0 ** (emin - mbits))
+    code_norm = ((er + bias) << mbits) + (np.ldexp(r, mbits - er) - (1 << mbits))
+    code = np.where(sub, code_sub, code_norm).astype(np.uint8)
+    code = np.where(np.signbit(x64), code | 0x80, code).astype(np.uint8)
+    code[nan] = 0x7F
+    return code.reshape(np.shape(x))
 
 
 DTYPES = ("bf16", "fp16", "tf32", "e4m3", "e5m2")
@@ -226,6 +219,10 @@ WORKLOADS = {
                                        lda=4104, ldb=4104, ldc=72),
     "c5c_bf16_8191x4097x1000": Workload("c5c_bf16_8191x4097x1000", 8191, 4097, 1000, "bf16", 1.0, True, 4, "uniform",
                                         lda=1008, ldb=1008, ldc=8199),
+    # 8-bit float operands at the headline size ("Matrix Multiplication",
+    # "Where to go from here": FP8 matmuls), N(0,1) entries rounded to the type.
+    "f8_e4m3_8192": Workload("f8_e4m3_8192", 8192, 8192, 8192, "e4m3", 1.0, True, 6, "normal"),
+    "f8_e5m2_8192": Workload("f8_e5m2_8192", 8192, 8192, 8192, "e5m2", 1.0, True, 7, "normal"),
 }
 
 
@@ -243,7 +240,11 @@ def _to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "fp16":
         return f32_to_fp16_bits(x32)
     if dtype in ("e4m3", "e5m2"):
-        return f32_to_fp8_bits(x32, dtype)
+        flat = np.asarray(x32).reshape(-1)
+        out = np.empty(flat.size, dtype=np.uint8)
+        for s0 in range(0, flat.size, CHUNK):
+            out[s0: s0 + CHUNK] = f32_to_fp8_bits(flat[s0: s0 + CHUNK], dtype)
+        return out.reshape(np.shape(x32))
     if dtype == "tf32":
         return np.ascontiguousarray(x32, dtype=np.float32)
     raise ValueError(dtype)

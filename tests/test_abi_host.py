@@ -61,7 +61,7 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(lda=9), dict(ldb=9), dict(ldc=9),
     dict(A=None), dict(B=None), dict(D=None),
     dict(A=FAKE + 1), dict(D=FAKE + 2),
-    dict(dtype=3), dict(epi=2),
+    dict(dtype=5), dict(dtype=-1), dict(epi=2),
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
     dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
@@ -159,6 +159,27 @@ def test_plan_tf32(tg):
     assert p["block_k"] == 32 and p["threads"] == 448 and p["cta_pair"] == 0
     with pytest.raises(tg.TgError):
         plan(tg, si.WORKLOADS["c2_tf32_256x128x512"], opts={"cta_pair": 2})
+
+
+def test_plan_fp8(tg):
+    """8-bit floats: 128 K elements per stage (one 128-byte row), pair tiles
+    from 8 K blocks on, TMA when strides are multiples of 16 bytes."""
+    for dt in ("e4m3", "e5m2"):
+        p = plan(tg, si.WORKLOADS[f"f8_{dt}_8192"])
+        assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 128)
+        assert p["cta_pair"] == 1 and p["producer"] == 1 and p["stages"] == 7
+        assert p["tiles"] == 1024 and p["threads"] == 320
+        assert plan(tg, si.Workload("s", 4096, 4096, 1024, dt, 1.0, True, 0, "normal"))["cta_pair"] == 1
+        assert plan(tg, si.Workload("s", 4096, 4096, 896, dt, 1.0, True, 0, "normal"))["cta_pair"] == 0
+        # lda = 1000 bytes: not a multiple of 16 -> plain loads; 1008 is.
+        w = si.Workload("s", 300, 300, 1000, dt, 1.0, True, 0, "normal")
+        assert plan(tg, w)["producer"] == 2
+        assert plan(tg, si.with_shape(w, lda=1008, ldb=1008))["producer"] == 1
+        # Any base address is element-aligned for 1-byte types.
+        assert plan(tg, si.with_shape(w, lda=1008, ldb=1008), A=FAKE + 1)["producer"] == 2
+        split = plan(tg, si.Workload("s", 500, 500, 8192, dt, 1.0, True, 0, "normal"),
+                     opts={"cta_pair": 2})
+        assert split["split_tiles"] == split["tiles"] and split["split_segs"] == 8  # 64 K blocks / 8
 
 
 def test_plan_pair_grid_is_even_and_capped(tg):
