@@ -16,9 +16,11 @@ from .oracle import (  # noqa: F401
     build,
     compile_source,
     decode,
+    decode_scale,
     default,
     gemm,
     gemm_entries,
+    gemm_mx,
     host_threads,
     library_path,
     round_output,

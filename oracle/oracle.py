@@ -70,6 +70,11 @@ class Oracle:
         lib.orc_decode_array.restype = None
         lib.orc_round_output.argtypes = [vp, i64, ip]
         lib.orc_round_output.restype = None
+        lib.orc_gemm_mx.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, vp, i64, vp, i64, ip, ip,
+                                    vp, i64, vp, ip]
+        lib.orc_gemm_mx.restype = ip
+        lib.orc_decode_e8m0_array.argtypes = [vp, i64, vp]
+        lib.orc_decode_e8m0_array.restype = None
         lib.orc_num_host_threads.argtypes = []
         lib.orc_num_host_threads.restype = ip
         self.lib = lib
@@ -99,6 +104,41 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"orc_gemm failed with {rc}")
         return (Dt.T, St.T) if with_scale else Dt.T
+
+    def gemm_mx(self, M, N, K, alpha, A, lda, SA, ldsa, B, ldb, SB, ldsb, dtype, relu,
+                with_scale=False, threads=0):
+        """Block-scaled D_ref (M, N) float64: FP8 operands as in ``gemm``, and
+        one 8-bit exponent scale per 32 k, Xa(i,kb) = SA.flat[i*ldsa + kb],
+        Xb(kb,j) = SB.flat[j*ldsb + kb] (uint8 codes)."""
+        A = _check_storage(A, dtype, "A")
+        B = _check_storage(B, dtype, "B")
+        SA = np.ascontiguousarray(SA, dtype=np.uint8)
+        SB = np.ascontiguousarray(SB, dtype=np.uint8)
+        kb = (K + 31) // 32
+        if M and K and A.size < (M - 1) * lda + K:
+            raise ValueError("A too small for (M, K, lda)")
+        if N and K and B.size < (N - 1) * ldb + K:
+            raise ValueError("B too small for (K, N, ldb)")
+        if M and kb and SA.size < (M - 1) * ldsa + kb:
+            raise ValueError("SA too small")
+        if N and kb and SB.size < (N - 1) * ldsb + kb:
+            raise ValueError("SB too small")
+        Dt = np.zeros((max(N, 0), max(M, 0)), dtype=np.float64)
+        St = np.zeros_like(Dt) if with_scale else None
+        rc = self.lib.orc_gemm_mx(M, N, K, float(alpha), A.ctypes.data, lda, SA.ctypes.data, ldsa,
+                                  B.ctypes.data, ldb, SB.ctypes.data, ldsb, _DTYPE_CODE[dtype],
+                                  int(bool(relu)), Dt.ctypes.data, max(M, 1),
+                                  St.ctypes.data if St is not None else None, int(threads))
+        if rc != 0:
+            raise ValueError(f"orc_gemm_mx failed with {rc}")
+        return (Dt.T, St.T) if with_scale else Dt.T
+
+    def decode_scale(self, codes) -> np.ndarray:
+        """The oracle's decode of 8-bit exponent scale codes to float64."""
+        x = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.zeros(x.shape, dtype=np.float64)
+        self.lib.orc_decode_e8m0_array(x.ctypes.data, x.size, out.ctypes.data)
+        return out
 
     def gemm_entries(self, M, N, K, alpha, A, lda, B, ldb, dtype, relu, I, J, threads=0):
         """D_ref and |alpha|*sum|a||b| at coordinates (I[q], J[q])."""
@@ -150,6 +190,14 @@ def gemm(*args, **kw):
 
 def gemm_entries(*args, **kw):
     return default().gemm_entries(*args, **kw)
+
+
+def gemm_mx(*args, **kw):
+    return default().gemm_mx(*args, **kw)
+
+
+def decode_scale(codes):
+    return default().decode_scale(codes)
 
 
 def decode(bits, dtype):

@@ -22,6 +22,17 @@
  * A batched GEMM is that definition applied to each batch entry on its own;
  * the oracle's callers step the operand pointers.
  *
+ * Block-scaled products (orc_gemm_mx; "Matrix Multiplication", "Where to go
+ * from here", names block-scaled FP8 and FP4 matmuls; the pages give no
+ * format, so the oracle takes the OCP Microscaling one): every run of 32
+ * consecutive k of a row of A, and of a column of B, shares one scale
+ * X = 2^(e-127) (an 8-bit exponent code e; e = 255 is NaN), and
+ *   s = sum over blocks kb of  Xa(i,kb) * Xb(kb,j) * (sum_{k in kb} a(i,k) b(k,j)),
+ * each block's inner sum taken first, blocks in ascending order; steps 3-5
+ * then apply as above.  Scales are stored one per row and block:
+ *   Xa(i,kb) from SA[i*ldsa + kb],  Xb(kb,j) from SB[j*ldsb + kb],
+ *   0 <= kb < ceil(K/32).
+ *
  * Storage ("Walk through GEMM", section 2 "Bind runtime global arrays"):
  *   A logical (M,K), K-contiguous:  a(i,k) = A[i*lda + k]
  *   B logical (K,N), K-contiguous:  b(k,j) = B[k + j*ldb]
@@ -358,6 +369,119 @@ void orc_round_output(double *y, int64_t n, int out_fmt) {
         default: break;
         }
     }
+}
+
+/* ---------------- block-scaled (microscaling) products ---------------- */
+
+#define ORC_MX_BLOCK 32
+
+/* 8-bit power-of-two scale: 2^(e-127); e = 255 is NaN. */
+double orc_decode_e8m0(uint8_t e) {
+    if (e == 0xFF) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+typedef struct {
+    int64_t M, K, KB;
+    double alpha;
+    int relu;
+    const double *Ad, *Bd;   /* decoded, unscaled: Ad[i*K + k], Bd[j*K + k] */
+    const double *Xa, *Xb;   /* decoded scales: Xa[i*KB + kb], Xb[j*KB + kb] */
+    double *D;
+    int64_t ldd;
+    double *scale;
+    int64_t j0, j1;
+} mx_job;
+
+static void *mx_worker(void *p) {
+    mx_job *jb = (mx_job *)p;
+    for (int64_t j = jb->j0; j < jb->j1; ++j) {
+        const double *bj = jb->Bd + j * jb->K;
+        const double *xb = jb->Xb + j * jb->KB;
+        for (int64_t i = 0; i < jb->M; ++i) {
+            const double *ai = jb->Ad + i * jb->K;
+            const double *xa = jb->Xa + i * jb->KB;
+            double s = 0.0, t = 0.0;
+            for (int64_t kb = 0; kb < jb->KB; ++kb) {
+                int64_t k0 = kb * ORC_MX_BLOCK;
+                int64_t k1 = k0 + ORC_MX_BLOCK < jb->K ? k0 + ORC_MX_BLOCK : jb->K;
+                double bs = 0.0, bt = 0.0;
+                for (int64_t k = k0; k < k1; ++k) {
+                    bs += ai[k] * bj[k];
+                    bt += fabs(ai[k]) * fabs(bj[k]);
+                }
+                double x = xa[kb] * xb[kb];
+                s += x * bs;
+                t += fabs(x) * bt;
+            }
+            jb->D[i + j * jb->ldd] = epilogue(jb->alpha, s, jb->relu);
+            if (jb->scale) jb->scale[i + j * jb->ldd] = t * fabs(jb->alpha);
+        }
+    }
+    return NULL;
+}
+
+/*
+ * Block-scaled D_ref for the whole M x N output (see the header comment):
+ * FP8 operands (E4M3 / E5M2) with one 8-bit exponent scale per 32 k.
+ * Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
+ */
+int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
+                const void *A, int64_t lda, const uint8_t *SA, int64_t ldsa,
+                const void *B, int64_t ldb, const uint8_t *SB, int64_t ldsb,
+                int dtype, int relu, double *D, int64_t ldd, double *scale, int nthreads) {
+    int64_t KB = (K + ORC_MX_BLOCK - 1) / ORC_MX_BLOCK;
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldd < M) return -1;
+    if (ldsa < KB || ldsb < KB) return -1;
+    if (dtype != ORC_E4M3 && dtype != ORC_E5M2) return -1;
+    if (M == 0 || N == 0) return 0;
+    size_t kk = (size_t)(K ? K : 1), kbb = (size_t)(KB ? KB : 1);
+    double *Ad = (double *)malloc(sizeof(double) * (size_t)M * kk);
+    double *Bd = (double *)malloc(sizeof(double) * (size_t)N * kk);
+    double *Xa = (double *)malloc(sizeof(double) * (size_t)M * kbb);
+    double *Xb = (double *)malloc(sizeof(double) * (size_t)N * kbb);
+    if (!Ad || !Bd || !Xa || !Xb) { free(Ad); free(Bd); free(Xa); free(Xb); return -2; }
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * lda;
+        for (int64_t k = 0; k < K; ++k) Ad[i * K + k] = decode_elem(A, row + k, dtype);
+        for (int64_t kb = 0; kb < KB; ++kb) Xa[i * KB + kb] = orc_decode_e8m0(SA[i * ldsa + kb]);
+    }
+    for (int64_t j = 0; j < N; ++j) {
+        const int64_t col = j * ldb;
+        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode_elem(B, col + k, dtype);
+        for (int64_t kb = 0; kb < KB; ++kb) Xb[j * KB + kb] = orc_decode_e8m0(SB[j * ldsb + kb]);
+    }
+    if (nthreads <= 0) nthreads = orc_num_host_threads();
+    if (nthreads > N) nthreads = (int)N;
+    mx_job *jobs = (mx_job *)calloc((size_t)nthreads, sizeof(mx_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(Ad); free(Bd); free(Xa); free(Xb); free(jobs); free(tids);
+        return -2;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        mx_job *jb = &jobs[t];
+        jb->M = M; jb->K = K; jb->KB = KB; jb->alpha = alpha; jb->relu = relu;
+        jb->Ad = Ad; jb->Bd = Bd; jb->Xa = Xa; jb->Xb = Xb;
+        jb->D = D; jb->ldd = ldd; jb->scale = scale;
+        jb->j0 = N * t / nthreads;
+        jb->j1 = N * (t + 1) / nthreads;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, mx_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    mx_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t) mx_worker(&jobs[t]);
+    free(jobs); free(tids); free(Ad); free(Bd); free(Xa); free(Xb);
+    return 0;
+}
+
+/* Decode an array of scale codes (for the decode pins). */
+void orc_decode_e8m0_array(const uint8_t *src, int64_t n, double *dst) {
+    for (int64_t q = 0; q < n; ++q) dst[q] = orc_decode_e8m0(src[q]);
 }
 
 /* Decode a whole array of storage elements (for the decode pins). */

@@ -483,6 +483,140 @@ def check_fp8_decode(orc):
     assert list(e5[:5]) == [2.0 ** -16, 2.0 ** -14, 1.0, 57344.0, math.inf] and np.isnan(e5[5])
 
 
+# ---------------------------------------------------------------- block-scaled (MX) products
+
+MX_GRID = np.arange(-8, 9) / 8.0     # exact in E4M3 and E5M2
+
+
+def mx_codes(vals, dtype):
+    return fp8_bits_exact(np.asarray(vals, dtype=np.float64), dtype)
+
+
+def run_mx(orc, Alog, Blog, SAc, SBc, dtype, alpha, relu, pad_s=5, **kw):
+    """Alog (M,K), Blog (K,N) exact FP8 values; SAc (M,KB), SBc (N,KB) scale
+    codes.  Scale rows are stored with `pad_s` extra codes of padding (255,
+    NaN) so a wrong block count or stride reads NaN into the result."""
+    M, K = Alog.shape
+    N = Blog.shape[1]
+    KB = SAc.shape[1]
+    A = mx_codes(Alog, dtype)
+    B = np.ascontiguousarray(mx_codes(Blog.T, dtype))
+    ldsa = ldsb = KB + pad_s
+    SA = np.full((M, ldsa), 255, dtype=np.uint8)
+    SB = np.full((N, ldsb), 255, dtype=np.uint8)
+    SA[:, :KB] = SAc
+    SB[:, :KB] = SBc
+    return orc.gemm_mx(M, N, K, alpha, A, K, SA, ldsa, B, K, SB, ldsb, dtype, relu, **kw)
+
+
+def check_mx_scale_decode(orc):
+    """8-bit exponent scales: 2^(e-127) at the landmarks, exact doubling from
+    code to code, NaN at 255."""
+    got = orc.decode_scale(np.arange(256, dtype=np.uint16).astype(np.uint8))
+    assert got[127] == 1.0 and got[128] == 2.0 and got[126] == 0.5
+    assert got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+    assert np.all(got[1:255] == 2.0 * got[0:254])
+    assert math.isnan(got[255])
+
+
+def check_mx_bruteforce_exact(orc):
+    """Tiny problems with ragged last blocks against exact rational
+    arithmetic of the microscaling definition."""
+    rng = np.random.default_rng(29)
+    for (M, N, K) in ((3, 4, 70), (2, 5, 32), (4, 3, 97), (1, 1, 1)):
+        KB = (K + 31) // 32
+        Alog = rng.choice(MX_GRID, size=(M, K))
+        Blog = rng.choice(MX_GRID, size=(K, N))
+        SAc = rng.integers(121, 134, size=(M, KB)).astype(np.uint8)
+        SBc = rng.integers(121, 134, size=(N, KB)).astype(np.uint8)
+        for dt in ("e4m3", "e5m2"):
+            for alpha, relu in ((1.0, False), (-1.5, True)):
+                D, S = run_mx(orc, Alog, Blog, SAc, SBc, dt, alpha, relu, with_scale=True)
+                assert np.all(np.isfinite(D)) and np.all(np.isfinite(S)), (dt, M, N, K)
+                for i in range(M):
+                    for j in range(N):
+                        s = Fraction(0)
+                        t = Fraction(0)
+                        for kb in range(KB):
+                            x = Fraction(2) ** (int(SAc[i, kb]) - 127) * \
+                                Fraction(2) ** (int(SBc[j, kb]) - 127)
+                            ks = range(32 * kb, min(32 * kb + 32, K))
+                            s += x * sum((Fraction(Alog[i, k]) * Fraction(Blog[k, j]) for k in ks),
+                                         Fraction(0))
+                            t += x * sum((abs(Fraction(Alog[i, k]) * Fraction(Blog[k, j])) for k in ks),
+                                         Fraction(0))
+                        y = Fraction(alpha) * s
+                        if relu and y < 0:
+                            y = Fraction(0)
+                        assert Fraction(D[i, j]) == y, (dt, M, N, K, i, j)
+                        assert Fraction(S[i, j]) == abs(Fraction(alpha)) * t
+
+
+def check_mx_block_boundaries(orc):
+    """A single one in row i at column k: D(i,j) = Xa(i, k // 32) * Xb(k // 32, j)
+    exactly, at every block edge; pins the block size, the block offset and
+    which scale row belongs to which operand row or column."""
+    M, N, K = 2, 3, 100
+    KB = 4
+    SAc = np.array([[127 + kb + 4 * i for kb in range(KB)] for i in range(M)], dtype=np.uint8)
+    SBc = np.array([[120 - 2 * kb - 9 * j for kb in range(KB)] for j in range(N)], dtype=np.uint8)
+    Blog = np.ones((K, N))
+    for k in (0, 15, 16, 31, 32, 33, 63, 64, 95, 96, 99):
+        Alog = np.zeros((M, K))
+        Alog[0, k] = 1.0
+        Alog[1, K - 1 - k] = -1.0
+        D = run_mx(orc, Alog, Blog, SAc, SBc, "e4m3", 1.0, False)
+        for j in range(N):
+            kb0, kb1 = k // 32, (K - 1 - k) // 32
+            want0 = 2.0 ** (int(SAc[0, kb0]) - 127 + int(SBc[j, kb0]) - 127)
+            want1 = -(2.0 ** (int(SAc[1, kb1]) - 127 + int(SBc[j, kb1]) - 127))
+            assert D[0, j] == want0 and D[1, j] == want1, (k, j)
+
+
+def check_mx_scale_invariances(orc):
+    """One code step on every scale of row i of A doubles row i exactly; on
+    every scale of column j of B doubles column j; nothing else moves."""
+    rng = np.random.default_rng(31)
+    M, N, K = 5, 6, 130
+    KB = 5
+    Alog = rng.choice(MX_GRID, size=(M, K))
+    Blog = rng.choice(MX_GRID, size=(K, N))
+    SAc = rng.integers(122, 132, size=(M, KB)).astype(np.uint8)
+    SBc = rng.integers(122, 132, size=(N, KB)).astype(np.uint8)
+    D = run_mx(orc, Alog, Blog, SAc, SBc, "e5m2", 0.75, False)
+    SA2 = SAc.copy()
+    SA2[3] += 1
+    D2 = run_mx(orc, Alog, Blog, SA2, SBc, "e5m2", 0.75, False)
+    assert np.array_equal(D2[3], 2 * D[3]) and np.array_equal(np.delete(D2, 3, 0), np.delete(D, 3, 0))
+    SB2 = SBc.copy()
+    SB2[4] -= 1
+    D3 = run_mx(orc, Alog, Blog, SAc, SB2, "e5m2", 0.75, False)
+    assert np.array_equal(D3[:, 4], D[:, 4] / 2)
+    assert np.array_equal(np.delete(D3, 4, 1), np.delete(D, 4, 1))
+    # All scales one: the unscaled product of the same codes.
+    ones = run_mx(orc, Alog, Blog, np.full((M, KB), 127, np.uint8), np.full((N, KB), 127, np.uint8),
+                  "e5m2", 0.75, False)
+    A = mx_codes(Alog, "e5m2")
+    B = np.ascontiguousarray(mx_codes(Blog.T, "e5m2"))
+    assert np.array_equal(ones, orc.gemm(M, N, K, 0.75, A, K, B, K, "e5m2", False))
+
+
+def check_mx_nan_scale(orc):
+    """A NaN scale makes its whole row (or column) NaN, even where the block's
+    elements are zero."""
+    M, N, K = 3, 4, 64
+    Alog = np.ones((M, K)) / 2
+    Alog[1, 32:] = 0.0
+    Blog = np.ones((K, N))
+    SAc = np.full((M, 2), 127, np.uint8)
+    SBc = np.full((N, 2), 127, np.uint8)
+    SAc[1, 1] = 255
+    SBc[2, 0] = 255
+    D = run_mx(orc, Alog, Blog, SAc, SBc, "e4m3", 1.0, True)
+    assert np.all(np.isnan(D[1])) and np.all(np.isnan(D[:, 2]))
+    assert np.all(D[[0, 2]][:, [0, 1, 3]] == 32.0)
+
+
 ALL_CHECKS = [
     check_decode_tables,
     check_tf32_narrowing,
@@ -501,4 +635,9 @@ ALL_CHECKS = [
     check_degenerate,
     check_round_output,
     check_fp8_decode,
+    check_mx_scale_decode,
+    check_mx_bruteforce_exact,
+    check_mx_block_boundaries,
+    check_mx_scale_invariances,
+    check_mx_nan_scale,
 ]

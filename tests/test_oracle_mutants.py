@@ -43,6 +43,16 @@ MUTANTS = {
                        "else if (e == 0) v = ldexp((double)f, -7 - 3);"),
     "e4m3_no_nan": ("if (e == 0xF && f == 0x7) v = NAN;", "if (0) v = NAN;"),
     "e5m2_inf_as_nan": ("if (e == 0x1F) v = (f == 0) ? INFINITY : NAN;", "if (e == 0x1F) v = NAN;"),
+    "mx_block_16": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 16"),
+    "mx_block_64": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 64"),
+    "mx_scale_bias": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 128);"),
+    "mx_scale_no_nan": ("if (e == 0xFF) return NAN;", "if (0) return NAN;"),
+    "mx_only_a_scale": ("double x = xa[kb] * xb[kb];", "double x = xa[kb];"),
+    "mx_block_shift": ("double x = xa[kb] * xb[kb];",
+                       "double x = xa[kb] * xb[kb > 0 ? kb - 1 : 0];"),
+    "mx_wrong_row_scale": ("Xa[i * KB + kb] = orc_decode_e8m0(SA[i * ldsa + kb]);",
+                           "Xa[i * KB + kb] = orc_decode_e8m0(SA[(M - 1 - i) * ldsa + kb]);"),
+    "mx_scale_abs_dropped": ("t += fabs(x) * bt;", "t += bt;"),
     "scale_signed_alpha": ("jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;",
                            "jb->scale[i + j * jb->ldd] = jb->alpha * t;"),
 }
