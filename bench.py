@@ -69,11 +69,16 @@ def dist_env():
 
 def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1) -> dict:
     lda, ldb, ldc = w.strides
+    scales = ""
+    if w.block_scaled:
+        lo, hi = si.MX_BENCH_SCALES
+        scales = (f", one 8-bit exponent scale per 32 K (seeded codes {lo}..{hi}: "
+                  f"2^{lo - 127}..2^{hi - 127})")
     dist = ("N(0,1)" + (f"x{w.scale}" if w.scale != 1.0 else "") if w.dist == "normal"
             else f"U[{w.lo},{w.hi})")
     cfg = {
         "workload": f"{w.name}: M={w.M} N={w.N} K={w.K} {w.dtype.upper()} operands (seeded "
-                    f"{dist}), alpha={w.alpha}, {'ReLU' if w.relu else 'no'} epilogue, FP32 "
+                    f"{dist}){scales}, alpha={w.alpha}, {'ReLU' if w.relu else 'no'} epilogue, FP32 "
                     f"accumulate, D {out.upper()} column-major"
                     + (f", batch of {batch} (entries share one seeded draw)" if batch > 1 else ""),
         "M": w.M, "N": w.N, "K": w.K, "lda": lda, "ldb": ldb, "ldc": ldc,
@@ -102,6 +107,13 @@ def oracle_sample_time(w: si.Workload, A, B, rows: int, cols: int, threads: int 
     lda, ldb, _ = w.strides
     As = np.ascontiguousarray(A[:rows])
     Bs = np.ascontiguousarray(B[:cols])
+    if w.block_scaled:
+        SA, SB = si.make_mx_scales(si.with_shape(w, M=rows, N=cols), *si.MX_BENCH_SCALES)
+        kb = SA.shape[1]
+        t0 = time.perf_counter()
+        oracle.gemm_mx(rows, cols, w.K, w.alpha, As, lda, SA, kb, Bs, ldb, SB, kb, w.dtype, w.relu,
+                       threads=threads)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
     oracle.gemm(rows, cols, w.K, w.alpha, As, lda, Bs, ldb, w.dtype, w.relu, threads=threads)
     return time.perf_counter() - t0
@@ -276,9 +288,31 @@ def run_gpu(args, rank, world, local):
     hD = torch.empty((nbat * w.N, ldc), dtype=odt).pin_memory()
     sa, sb, sd = w.M * lda, w.N * ldb, w.N * ldc
     stream = torch.cuda.Stream()
-    plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, None, ldc, w.dtype)
+    mx = w.block_scaled
+    if mx:
+        if batched:
+            raise SystemExit("block-scaled workloads run unbatched with FP32 output")
+        # Scale atoms, packed on the device by the library from the seeded
+        # row-major scales; they are inputs like A and B (uploaded in e2e).
+        SA, SB = si.make_mx_scales(w, *si.MX_BENCH_SCALES)
+        dSA = torch.empty(tg.tg_mx_scale_bytes(w.M, w.K), dtype=torch.uint8, device="cuda")
+        dSB = torch.empty(tg.tg_mx_scale_bytes(w.N, w.K), dtype=torch.uint8, device="cuda")
+        tg.check(tg.tg_mx_pack_scales(w.M, w.K, torch.from_numpy(SA).cuda(), SA.shape[1], dSA),
+                 "tg_mx_pack_scales")
+        tg.check(tg.tg_mx_pack_scales(w.N, w.K, torch.from_numpy(SB).cuda(), SB.shape[1], dSB),
+                 "tg_mx_pack_scales")
+        torch.cuda.synchronize()
+        hSA, hSB = dSA.cpu().pin_memory(), dSB.cpu().pin_memory()
+        plan = tg.tg_plan_mx(w.M, w.N, w.K, lda, ldb, ldc, w.dtype)
+    else:
+        plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, None, ldc, w.dtype)
+    scale_inputs = {}
 
     def call(a_, b_, d_, st_):
+        if mx:
+            sfa, sfb = scale_inputs.get(a_.data_ptr(), (dSA, dSB))
+            return tg.tg_gemm_mx(w.M, w.N, w.K, w.alpha, a_, lda, sfa, b_, ldb, sfb, d_, ldc,
+                                 w.dtype, "f32", w.relu, None, st_)
         if batched:
             return tg.tg_gemm_batched(w.M, w.N, w.K, w.alpha, a_, lda, sa, b_, ldb, sb, d_, ldc, sd,
                                       nbat, w.dtype, out, w.relu, None, st_)
@@ -330,6 +364,10 @@ def run_gpu(args, rank, world, local):
     e2e_steps = max(2, args.e2e_steps)
     bufs = [(dA, dB, dD)]
     bufs.append((torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dD)))
+    if mx:
+        scale_bufs = [(dSA, dSB), (torch.empty_like(dSA), torch.empty_like(dSB))]
+        for (a_, _, _), sc in zip(bufs, scale_bufs):
+            scale_inputs[a_.data_ptr()] = sc
     hDs = [hD, torch.empty_like(hD).pin_memory()]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -344,6 +382,10 @@ def run_gpu(args, rank, world, local):
         with torch.cuda.stream(s_in):
             a_.copy_(hA, non_blocking=True)
             b_.copy_(hB, non_blocking=True)
+            if mx:
+                sfa_, sfb_ = scale_bufs[b]
+                sfa_.copy_(hSA, non_blocking=True)
+                sfb_.copy_(hSB, non_blocking=True)
             ev_in[b].record(s_in)
         stream.wait_event(ev_in[b])
         if i >= 2:
@@ -383,6 +425,8 @@ def run_gpu(args, rank, world, local):
         flops = w.flops * nbat
         e_in = si.element_bytes(w.dtype)
         alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
+        if mx:
+            alg_bytes += (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
         value = world * flops / (step_ms * 1e-3) / 1e12
         peaks, peak_src = load_peaks()
         launch_avg_ms = statistics.fmean(launch_ms)
@@ -415,13 +459,15 @@ def run_gpu(args, rank, world, local):
         burst["frac"] = burst["achieved"] / burst["peak"]
         burst["launches"] = len(first)
         dt = w.dtype
-        kname = ("tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
+        kname = ("tg_gemm_mx_kernel" if mx else
+                 "tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
             f"<{dt.upper()}, {plan['block_m']}x{plan['block_n']}, " + \
             f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>"
         traffic = load_traffic(tg.source_hash()) if args.workload == WORKLOAD and not batched else None
         default_run = args.workload == WORKLOAD and not batched
         line = {
             "metric": METRIC if default_run else
+                      f"{'block-scaled (32-element blocks) ' if mx else ''}"
                       f"{dt} GEMM{'+ReLU' if w.relu else ''} TFLOP/s at {w.M}x{w.N}x{w.K}"
                       + (f" x{nbat}" if nbat > 1 else "") + (f", {out} out" if out != 'f32' else ""),
             "value": value, "unit": UNIT, "n_gpus": world,
@@ -445,7 +491,8 @@ def run_gpu(args, rank, world, local):
                          "algorithmic_bytes_per_launch": alg_bytes},
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
-                                              hB.numel() * hB.element_size()),
+                                              hB.numel() * hB.element_size() +
+                                              (hSA.numel() + hSB.numel() if mx else 0)),
                     "d2h_bytes_per_step": int(hD.numel() * hD.element_size()),
                     "steps": e2e_steps, "wall_s": e2e_wall,
                     "pipelining": "2 buffer sets; H2D, compute and D2H on separate streams"},

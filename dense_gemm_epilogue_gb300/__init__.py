@@ -53,6 +53,10 @@ EXPORTED = (
     "tg_version",
     "tg_gemm_noalloc",
     "tg_gemm_batched",
+    "tg_gemm_mx",
+    "tg_plan_mx",
+    "tg_mx_scale_bytes",
+    "tg_mx_pack_scales",
 )
 
 
@@ -141,6 +145,17 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                         i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(tg_options), vp]
         lib.tg_gemm_batched.restype = ctypes.c_int
+        lib.tg_gemm_mx.argtypes = [i64, i64, i64, f32, vp, i64, vp, vp, i64, vp, vp, i64,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.POINTER(tg_options), vp]
+        lib.tg_gemm_mx.restype = ctypes.c_int
+        lib.tg_plan_mx.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                                   ctypes.POINTER(tg_options), i32, ctypes.POINTER(tg_plan_info)]
+        lib.tg_plan_mx.restype = ctypes.c_int
+        lib.tg_mx_scale_bytes.argtypes = [i64, i64]
+        lib.tg_mx_scale_bytes.restype = i64
+        lib.tg_mx_pack_scales.argtypes = [i64, i64, vp, i64, vp, vp]
+        lib.tg_mx_pack_scales.restype = ctypes.c_int
         lib.tg_version.argtypes = []
         lib.tg_version.restype = i32
         if path is None:
@@ -233,6 +248,35 @@ def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):
     if st != TG_OK:
         raise TgError(st, "tg_plan")
     return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
+
+
+def tg_gemm_mx(M, N, K, alpha, A, lda, SFA, B, ldb, SFB, D, ldc, in_dtype, out_dtype, epilogue,
+               opts=None, stream=None) -> int:
+    """Block-scaled FP8 GEMM; SFA / SFB are scale-atom buffers (see
+    include/tg_gemm.h, tg_gemm_mx)."""
+    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+    return load().tg_gemm_mx(M, N, K, alpha, _ptr(A), lda, _ptr(SFA), _ptr(B), ldb, _ptr(SFB),
+                             _ptr(D), ldc, _dtype(in_dtype), out, _epi(epilogue), _options(opts),
+                             _stream(stream))
+
+
+def tg_plan_mx(M, N, K, lda, ldb, ldc, in_dtype, opts=None, num_sms=0):
+    """The block-scaled planner's choice as a dict; raises TgError on invalid arguments."""
+    info = tg_plan_info()
+    st = load().tg_plan_mx(M, N, K, lda, ldb, ldc, _dtype(in_dtype), _options(opts), num_sms,
+                           ctypes.byref(info))
+    if st != TG_OK:
+        raise TgError(st, "tg_plan_mx")
+    return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
+
+
+def tg_mx_scale_bytes(rows, K) -> int:
+    return int(load().tg_mx_scale_bytes(rows, K))
+
+
+def tg_mx_pack_scales(rows, K, src, ld_src, dst, stream=None) -> int:
+    """Row-major scale codes (device) -> scale atoms (device)."""
+    return load().tg_mx_pack_scales(rows, K, _ptr(src), ld_src, _ptr(dst), _stream(stream))
 
 
 def tg_status_string(status: int) -> str:

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libtg_gemm.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 SOURCES = ["tg_gemm.cu", "tg_inst_bf16.cu", "tg_inst_fp16.cu", "tg_inst_tf32.cu",
-           "tg_inst_e4m3.cu", "tg_inst_e5m2.cu", "tg_noalloc.cu"]
+           "tg_inst_e4m3.cu", "tg_inst_e5m2.cu", "tg_inst_mx.cu", "tg_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

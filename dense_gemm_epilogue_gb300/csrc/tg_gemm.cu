@@ -55,6 +55,22 @@ __global__ void tg_selftest_wait_kernel(uint32_t *status, uint64_t limit_ns) {
     }
 }
 
+// Scale atoms from row-major scales: dst byte o of atom (rb, kg) holds the
+// scale of row rb*128 + ((o % 512) % 16) / 4 * 32 + (o % 512) / 16 and block
+// kg*4 + o % 4 (zero outside the rows x blocks given).
+__global__ void tg_mx_pack_scales_kernel(const uint8_t *src, int64_t rows, int64_t kblocks,
+                                         int64_t ld_src, int64_t kgroups, int64_t total,
+                                         uint8_t *dst) {
+    for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < total;
+         o += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t atom = o >> 9, w = o & 511;
+        const int64_t rb = atom / kgroups, kg = atom - rb * kgroups;
+        const int64_t r = rb * 128 + ((w & 15) >> 2) * 32 + (w >> 4);
+        const int64_t kb = kg * 4 + (w & 3);
+        dst[o] = (r < rows && kb < kblocks) ? src[r * ld_src + kb] : (uint8_t)0;
+    }
+}
+
 }  // namespace tg
 
 namespace {
@@ -596,6 +612,165 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ block-scaled products
+
+int64_t mx_scale_bytes(int64_t rows, int64_t K) {
+    return ceil_div(rows, tg::BLOCK_M) * ceil_div(K, 128) * 512;
+}
+
+// Options the block-scaled path honours: tile N (128 or 256), role swap,
+// raster group and grid cap; everything else must stay at its default.
+bool mx_options_ok(const tg_options *o) {
+    if (!o) return true;
+    if (o->block_n != 0 && o->block_n != 128 && o->block_n != 256) return false;
+    if (o->swap_ab < 0 || o->swap_ab > 2 || o->raster_group < 0 || o->max_ctas < 0) return false;
+    if (o->producer < 0 || o->producer > 1) return false;
+    if (o->cta_pair < 0 || o->cta_pair == 1 || o->cta_pair > 2) return false;
+    if (o->split_k < 0 || o->split_k > 1) return false;
+    if (o->l2_hint || o->prefetch_k < -1 || o->prefetch_k > 0) return false;
+    if (o->multicast < 0 || o->multicast > 1) return false;
+    return !o->reserved[0] && !o->reserved[1];
+}
+
+tg_status validate_mx(const Problem &q, const void *sfa, const void *sfb, const tg_options *o) {
+    if (q.t != TG_E4M3 && q.t != TG_E5M2) return TG_ERR_INVALID_VALUE;
+    tg_status st = validate(q, nullptr);
+    if (st != TG_OK) return st;
+    if (!mx_options_ok(o)) return TG_ERR_INVALID_VALUE;
+    if (q.M > 0 && q.N > 0 && q.K > 0) {
+        if (!tma_legal(q.A, q.lda, 1) || !tma_legal(q.B, q.ldb, 1)) return TG_ERR_INVALID_VALUE;
+        if (!sfa || !sfb || (uintptr_t)sfa % 16 || (uintptr_t)sfb % 16) return TG_ERR_INVALID_VALUE;
+    }
+    return TG_OK;
+}
+
+// CTA-pair tiles of 256 x 128 or 256 x 256: the candidate with the smaller
+// (waves x cycles per K step), with the same per-step costs as make_plan.
+tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) {
+    static const tg_options kNone = {};
+    if (!o) o = &kNone;
+    Plan p;
+    p.pair = true;
+    p.mc = 1;
+    p.producer = 1;
+    if (o->swap_ab == 1) p.swap = false;
+    else if (o->swap_ab == 2) p.swap = true;
+    else p.swap = (q.M < tg::BLOCK_M) && (q.N >= tg::BLOCK_M) && (q.N >= 2 * q.M);
+    p.mk = p.swap ? q.N : q.M;
+    p.nk = p.swap ? q.M : q.N;
+    int64_t pairs = sms / 2;
+    if (o->max_ctas && pairs > o->max_ctas / 2) pairs = o->max_ctas / 2;
+    if (pairs < 1) pairs = 1;
+    int64_t best = -1;
+    for (int bn : {256, 128}) {
+        if (o->block_n && o->block_n != bn) continue;
+        const int64_t tiles = ceil_div(p.mk, 2 * tg::BLOCK_M) * ceil_div(p.nk, bn);
+        const int64_t mma = bn / 2, smem = 64 + bn / 4;
+        const int64_t est = ceil_div(tiles, pairs) * (mma > smem ? mma : smem);
+        if (best < 0 || est < best) {
+            best = est;
+            p.block_n = bn;
+        }
+    }
+    const int64_t mblocks = ceil_div(p.mk, 2 * tg::BLOCK_M);
+    p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
+    p.tiles = p.tiles_per_batch;
+    tg::mx_config_numbers(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    int64_t g = o->raster_group ? o->raster_group : 8;
+    if (g > mblocks) g = mblocks;
+    p.group = (int)g;
+    p.grid = (int)(2 * (p.tiles < pairs ? p.tiles : pairs));
+    const int eo = out_bytes(q.out_fmt);
+    p.vector_store = p.swap && ((uintptr_t)q.D % 16 == 0) && ((q.ldc * eo) % 16 == 0);
+    *plan = p;
+    return TG_OK;
+}
+
+// Scale atoms of an operand with `rows` rows as a 3-D tensor of 32-bit words:
+// (128 words = one 512-byte atom, atoms, 1); one atom per box.
+bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int64_t atoms = ceil_div(rows, tg::BLOCK_M) * ceil_div(K, 128);
+    cuuint64_t dims[3] = {128, (cuuint64_t)atoms, 1};
+    cuuint64_t strides[2] = {512, (cuuint64_t)(atoms * 512)};
+    cuuint32_t box[3] = {128, 1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue epi,
+                 const tg_options *opts, void *stream_ptr) {
+    if (epi != TG_EPILOGUE_NONE && epi != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
+    tg_status st = validate_mx(q, sfa, sfb, opts);
+    if (st != TG_OK) return st;
+    if (q.M == 0 || q.N == 0) return TG_OK;
+    int dev = 0;
+    DeviceState *ds = nullptr;
+    st = device_state(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
+    if (q.K == 0) {
+        int64_t blocks = ceil_div(q.M * q.N, 256);
+        const int64_t cap = (int64_t)ds->sms * 8;
+        if (blocks > cap) blocks = cap;
+        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+            q.D, q.M, q.N, q.ldc, 0, 1, q.out_fmt, q.alpha, relu);
+        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
+    Plan plan;
+    st = make_mx_plan(q, opts, ds->sms, &plan);
+    if (st != TG_OK) return st;
+
+    tg::LaunchArgs la;
+    std::memset(&la, 0, sizeof(la));
+    const void *ar = plan.swap ? q.B : q.A, *br = plan.swap ? q.A : q.B;
+    const void *sar = plan.swap ? sfb : sfa, *sbr = plan.swap ? sfa : sfb;
+    const int64_t ldar = plan.swap ? q.ldb : q.lda, ldbr = plan.swap ? q.lda : q.ldb;
+    if (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, 1, 0, tg::BLOCK_M) ||
+        !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, 1, 0, plan.block_n / 2) ||
+        !encode_scales(&la.map_sfa, sar, plan.mk, q.K) ||
+        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K))
+        return TG_ERR_INVALID_VALUE;
+    la.block_n = plan.block_n;
+    la.pair = true;
+    la.mc = 1;
+    tg::GemmParams &p = la.p;
+    p.m = (int32_t)plan.mk;
+    p.n = (int32_t)plan.nk;
+    p.k = (int32_t)q.K;
+    p.num_m_blocks = (int32_t)ceil_div(plan.mk, 2 * tg::BLOCK_M);
+    p.num_n_blocks = (int32_t)ceil_div(plan.nk, plan.block_n);
+    p.num_k_blocks = (int32_t)ceil_div(q.K, block_k(q.t));
+    p.raster_group = plan.group;
+    p.relu = relu;
+    p.num_tiles = plan.tiles;
+    p.tiles_per_batch = plan.tiles_per_batch;
+    p.batch = 1;
+    p.out_fmt = q.out_fmt;
+    p.alpha = q.alpha;
+    p.vector_store = plan.vector_store ? 1 : 0;
+    p.d = q.D;
+    p.d_row_stride = plan.swap ? q.ldc : 1;
+    p.d_col_stride = plan.swap ? 1 : q.ldc;
+    p.a_ptr = ar;
+    p.b_ptr = br;
+    p.lda = ldar;
+    p.ldb = ldbr;
+    p.status = ds->status;
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.split_max = 1;
+    la.grid = plan.grid;
+    la.device = dev;
+    la.stream = stream;
+    const cudaError_t e = tg::launch_mx(la, q.t == TG_E4M3 ? Kind::E4M3 : Kind::E5M2);
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
 Problem single(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                const void *B, int64_t ldb, void *D, int64_t ldc, tg_dtype t, int out_fmt,
                tg_epilogue epi) {
@@ -673,6 +848,80 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->tmem_cols = p.tmem_cols;
     out->vector_store = p.vector_store ? 1 : 0;
     return TG_OK;
+}
+
+tg_status tg_gemm_mx(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                     const void *SFA, const void *B, int64_t ldb, const void *SFB, void *D,
+                     int64_t ldc, tg_dtype in_dtype, tg_out_dtype out_dtype, tg_epilogue epilogue,
+                     const tg_options *opts, void *stream) {
+    const Problem q = single(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, (int)out_dtype,
+                             epilogue);
+    return run_mx(q, SFA, SFB, epilogue, opts, stream);
+}
+
+tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                     tg_dtype in_dtype, const tg_options *opts, int32_t num_sms,
+                     tg_plan_info *out) {
+    if (!out) return TG_ERR_INVALID_VALUE;
+    const void *fake = reinterpret_cast<const void *>(256);
+    const Problem q = single(M, N, K, 1.0f, fake, lda, fake, ldb, const_cast<void *>(fake), ldc,
+                             in_dtype, 0, TG_EPILOGUE_NONE);
+    tg_status st = validate_mx(q, fake, fake, opts);
+    if (st != TG_OK) return st;
+    int sms = num_sms;
+    if (sms <= 0) {
+        int dev = 0;
+        DeviceState *ds = nullptr;
+        st = device_state(&dev, &ds);
+        if (st != TG_OK) return st;
+        sms = ds->sms;
+    }
+    std::memset(out, 0, sizeof(*out));
+    if (M == 0 || N == 0 || K == 0) return TG_OK;
+    Plan p;
+    st = make_mx_plan(q, opts, sms, &p);
+    if (st != TG_OK) return st;
+    out->block_m = 2 * tg::BLOCK_M;
+    out->block_n = p.block_n;
+    out->block_k = block_k(in_dtype);
+    out->stages = p.stages;
+    out->producer = 1;
+    out->swap_ab = p.swap ? 1 : 0;
+    out->raster_group = p.group;
+    out->grid = p.grid;
+    out->tiles = p.tiles;
+    out->threads = p.threads;
+    out->smem_bytes = p.smem;
+    out->tmem_cols = p.tmem_cols;
+    out->vector_store = p.vector_store ? 1 : 0;
+    out->cta_pair = 1;
+    out->split_segs = 1;
+    out->multicast = 1;
+    return TG_OK;
+}
+
+int64_t tg_mx_scale_bytes(int64_t rows, int64_t K) {
+    if (rows < 0 || K < 0) return -1;
+    return mx_scale_bytes(rows, K);
+}
+
+tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t ld_src,
+                            uint8_t *dst, void *stream) {
+    const int64_t kblocks = ceil_div(K, 32);
+    if (rows < 0 || K < 0 || ld_src < (kblocks > 1 ? kblocks : 1)) return TG_ERR_INVALID_VALUE;
+    const int64_t total = mx_scale_bytes(rows, K);
+    if (total == 0) return TG_OK;
+    if (!src || !dst) return TG_ERR_INVALID_VALUE;
+    int dev = 0;
+    DeviceState *ds = nullptr;
+    tg_status st = device_state(&dev, &ds);
+    if (st != TG_OK) return st;
+    int64_t blocks = ceil_div(total, 256);
+    const int64_t cap = (int64_t)ds->sms * 8;
+    if (blocks > cap) blocks = cap;
+    tg::tg_mx_pack_scales_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        src, rows, kblocks, ld_src, ceil_div(K, 128), total, dst);
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
 const char *tg_status_string(tg_status s) {

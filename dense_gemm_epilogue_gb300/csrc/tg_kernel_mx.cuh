@@ -1,0 +1,277 @@
+// Block-scaled (microscaling) FP8 GEMM on CTA pairs.
+//
+//   D = epi(alpha * sum_kb Xa(i,kb) Xb(kb,j) sum_{k in kb} a(i,k) b(k,j))
+//
+// with E4M3 / E5M2 operands and one 8-bit power-of-two scale (2^(e-127)) per
+// 32 consecutive K elements of each A row and each B column ("Matrix
+// Multiplication", "Where to go from here": block-scaled FP8 matmuls; the
+// scale format is the OCP Microscaling one).  The tensor core applies the
+// scales itself: tcgen05.mma.kind::mxf8f6f4.block_scale reads them from
+// tensor memory next to the accumulator.
+//
+// Scale storage ("scale atoms"): for an operand with R rows (A: M, B: N) and
+// KB = ceil(K/32) scale blocks, the scales are grouped in atoms of 128 rows x
+// 4 blocks = 512 contiguous bytes; atom (rb, kg) starts at byte
+// (rb * ceil(KB/4) + kg) * 512, and inside it the scale of row r, block kb
+// sits at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4.  That is the
+// order in which one 32-lane x 16-byte tcgen05.cp, repeated over the four
+// lane quarters, puts row r's four scales in tensor-memory column r / 32,
+// bytes 0-3 (lane r % 32 of every quarter) -- where the block-scaled MMA
+// reads them, one byte per 32-wide MMA chosen by the descriptor's scale ID.
+//
+// One 128-byte K stage holds 128 FP8 elements = 4 scale blocks = one atom
+// column, so a stage carries exactly one A atom per CTA and BN/128 B atoms.
+//
+// Differences from the CTA-pair kernel of tg_kernel_pair.cuh:
+//   - each stage also lands its scale atoms (TMA, 512 bytes each); each CTA
+//     loads the A atom of its own 128 rows and all BN/128 B atoms (every
+//     CTA's tensor core scales all BN columns);
+//   - the MMA thread copies a stage's atoms into that stage's tensor-memory
+//     slot (tcgen05.cp) right before the stage's four MMAs; a slot is reused
+//     only after the producer has refilled the stage, which waits for those
+//     MMAs to finish, so no copy can overwrite scales still being read;
+//   - one accumulator (the scale slots take the rest of tensor memory): the
+//     epilogue warps load their whole share of the tile into registers,
+//     release the accumulator at once, and store from registers while the
+//     next tile's MMAs run;
+//   - no split-K tail, no multicast clusters.
+// Every wait is bounded as in the other kernels.
+#pragma once
+
+#include <cstdint>
+#include "tg_kernel_pair.cuh"
+
+namespace tg {
+
+template <Kind KD, int BN>
+struct MxConfig {
+    using T = KindTraits<KD>;
+    static_assert(T::mma == MmaKind::F8, "block scaling covers the 8-bit float kinds");
+    static_assert(BN == 128 || BN == 256, "tile N: whole 128-row scale atoms");
+    static constexpr int BK = T::block_k;                // 128 K elements per stage
+    static constexpr int PAIR_M = 2 * BLOCK_M;
+    static constexpr int B_ROWS = BN / 2;
+    static constexpr int SFB_ATOMS = BN / 128;
+    static constexpr int ATOM_BYTES = 512;
+    static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
+    static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
+    static constexpr int SFA_BYTES = ATOM_BYTES;
+    static constexpr int SFB_BYTES = SFB_ATOMS * ATOM_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int FIT = (SMEM_LIMIT - 2048) / STAGE_BYTES;
+    static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = STAGES * A_BYTES;
+    static constexpr int SFA_OFF = B_OFF + STAGES * B_BYTES;
+    static constexpr int SFB_OFF = SFA_OFF + STAGES * SFA_BYTES;
+    static constexpr int BAR_OFF = SFB_OFF + STAGES * SFB_BYTES;
+    static constexpr int FULL0 = 0, EMPTY0 = STAGES;
+    static constexpr int ACCF = 2 * STAGES, ACCE = 2 * STAGES + 1, DRAIN = 2 * STAGES + 2;
+    static constexpr int NUM_BARS = 2 * STAGES + 3;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+    // Tensor memory: the accumulator in columns [0, BN); then one 16-column
+    // scale slot per stage (A atom at +0..3, B atoms at +8..+8+4*SFB_ATOMS).
+    static constexpr int SLOT_COLS = 16;
+    static constexpr int SF_COL0 = BN;
+    static constexpr int USED_COLS = BN + STAGES * SLOT_COLS;
+    static constexpr int TMEM_COLS = USED_COLS <= 256 ? 256 : 512;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int NUM_WARPS = 2 + EPI_WARPS;
+    static constexpr int NUM_THREADS = NUM_WARPS * 32;
+    static constexpr int MMAS_PER_STAGE = BK / T::umma_k;  // 4: one per scale block
+    static constexpr int COLS = BN / 2;                      // columns per epilogue warp
+    // Block-scaled instruction descriptor: B scale ID (bits 4-5, per MMA),
+    // A/B formats (7-9, 10-12), K-major operands (15, 16 zero), N >> 3
+    // (17-22), scale type 8-bit exponent (bit 23), M >> 4 (24-28), A scale ID
+    // (29-30, per MMA).
+    static constexpr uint32_t IDESC = (T::fmt << 7) | (T::fmt << 10) |
+                                      ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                                      ((uint32_t)(PAIR_M >> 4) << 24);
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+    static_assert(STAGES >= 4, "pipeline depth");
+    static_assert(USED_COLS <= 512, "tensor memory");
+    static_assert(SFB_ATOMS * 4 <= 8, "B atoms fit the slot");
+};
+
+__device__ __forceinline__ uint32_t mx_idesc(uint32_t base, int kk) {
+    return base | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+}
+
+template <Kind KD, int BN>
+__global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
+    tg_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_sfa,
+                      const __grid_constant__ CUtensorMap tmap_sfb, const GemmParams p) {
+    using C = MxConfig<KD, BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
+    const uint32_t half = rank & 1u;
+    const bool leader = half == 0;
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t num_pairs = gridDim.x / 2;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8 * i; };
+    auto a_stage = [&](int s) -> uint32_t { return sbase + C::A_OFF + s * C::A_BYTES; };
+    auto b_stage = [&](int s) -> uint32_t { return sbase + C::B_OFF + s * C::B_BYTES; };
+    auto sfa_stage = [&](int s) -> uint32_t { return sbase + C::SFA_OFF + s * C::SFA_BYTES; };
+    auto sfb_stage = [&](int s) -> uint32_t { return sbase + C::SFB_OFF + s * C::SFB_BYTES; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    const PairWaitCtl ctl{abort_flag, map_shared_rank(smem_u32(smem + C::MISC_OFF + 4), rank ^ 1u),
+                          p.status, p.wait_limit_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(C::FULL0 + s), 1);
+            mbar_init(bar(C::EMPTY0 + s), 1);
+        }
+        mbar_init(bar(C::ACCF), 1);
+        mbar_init(bar(C::ACCE), 2 * C::EPI_WARPS);
+        mbar_init(bar(C::DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_sfa);
+        prefetch_tensormap(&tmap_sfb);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nkb = p.num_k_blocks;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs) {
+                int bt, mb, nb;
+                batch_tile_coords(t, p, bt, mb, nb);
+                const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
+                const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
+                const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
+                // Scale atoms: this CTA's 128 A rows; all BN B rows.
+                const int32_t sfa_rb = mb * 2 + (int32_t)half;
+                const int32_t sfb_rb = nb * C::SFB_ATOMS;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                    const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
+                    if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * C::STAGE_BYTES);
+                    tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow, ab);
+                    tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
+                    tma_load_3d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, sfa_rb * nkb + kb, ab);
+#pragma unroll
+                    for (int a = 0; a < C::SFB_ATOMS; ++a)
+                        tma_load_3d_pair(sfb_stage(s) + a * C::ATOM_BYTES, &tmap_sfb, full_leader, 0,
+                                         (sfb_rb + a) * nkb + kb, bb);
+                    ++issued;
+                    if (++s == S) { s = 0; ph ^= 1; }
+                }
+            }
+            if (!ok && issued) pair_pause_ns(200000);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer (leader)
+        if (leader && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t tl = 0;
+            bool ok = true;
+            for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs, ++tl) {
+                if (!pair_wait(bar(C::ACCE), (tl & 1) ^ 1, ctl, SITE_ACC_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t slot = tmem_base + C::SF_COL0 + s * C::SLOT_COLS;
+                    tmem_cp_32x128b_x4_pair(slot, smem_desc_rows16(sfa_stage(s)));
+#pragma unroll
+                    for (int a = 0; a < C::SFB_ATOMS; ++a)
+                        tmem_cp_32x128b_x4_pair(slot + 8 + 4 * a,
+                                                smem_desc_rows16(sfb_stage(s) + a * C::ATOM_BYTES));
+                    const uint32_t a0 = a_stage(s), b0 = b_stage(s);
+#pragma unroll
+                    for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
+                        mma_mx_pair(tmem_base, smem_desc_sw128(a0 + kk * 32),
+                                    smem_desc_sw128(b0 + kk * 32), mx_idesc(C::IDESC, kk), slot,
+                                    slot + 8, (kb | kk) != 0);
+                    }
+                    mma_commit_pair_mcast(bar(C::EMPTY0 + s), 0x3);
+                    if (++s == S) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit_pair_mcast(bar(C::ACCF), 0x3);
+            }
+            if (!ok) {
+                mma_commit_pair_mcast(bar(C::DRAIN), (uint16_t)(1u << rank));
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar(C::DRAIN), 0)) {
+                    if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+                        atomicCAS(p.status, 0u, (uint32_t)SITE_DRAIN);
+                        break;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row_in_half = q * 32 + lane;
+        const int cbase = ((warp - 2) / 4) * C::COLS;
+        uint32_t tl = 0;
+        for (int64_t t = pair; t < p.num_tiles; t += num_pairs, ++tl) {
+            int bt, mb, nb;
+            batch_tile_coords(t, p, bt, mb, nb);
+            if (!pair_wait(bar(C::ACCF), tl & 1, ctl, SITE_ACC_FULL)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + cbase;
+            uint32_t v[C::COLS / 32][32];
+#pragma unroll
+            for (int c = 0; c < C::COLS / 32; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+            tmem_ld_wait();
+            // The accumulator is in registers: hand it back to the MMA.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(bar(C::ACCE));
+                else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE), 0));
+            }
+            const int32_t r = mb * C::PAIR_M + (int32_t)half * BLOCK_M + row_in_half;
+            if (r < p.m) {
+#pragma unroll
+                for (int c = 0; c < C::COLS / 32; ++c)
+                    epilogue_store(p, bt, r, nb * BN + cbase + c * 32, v[c]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tg

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include "tg_kernel.cuh"
 #include "tg_kernel_pair.cuh"
+#include "tg_kernel_mx.cuh"
 
 namespace tg {
 
@@ -13,6 +14,8 @@ struct LaunchArgs {
     GemmParams p;
     CUtensorMap map_a;   // A-role operand (unused by the plain-load producer)
     CUtensorMap map_b;   // B-role operand
+    CUtensorMap map_sfa; // block-scaled kernel: A-role scale atoms
+    CUtensorMap map_sfb; // block-scaled kernel: B-role scale atoms
     int block_n;         // tile N: 64, 128 or 256 (single CTA); 128 or 256 (CTA pair)
     bool plain_loads;    // plain bounds-checked loads instead of TMA (single CTA only)
     bool pair;           // CTA-pair kernel (cta_group::2 MMA)
@@ -27,5 +30,10 @@ cudaError_t launch_fp16(const LaunchArgs &a);
 cudaError_t launch_tf32(const LaunchArgs &a);
 cudaError_t launch_e4m3(const LaunchArgs &a);
 cudaError_t launch_e5m2(const LaunchArgs &a);
+// Block-scaled 8-bit float kernel (CTA pairs, block_n 128 or 256).
+cudaError_t launch_mx(const LaunchArgs &a, Kind kind);
+// Threads, shared memory, stages and tensor-memory columns of a block-scaled
+// configuration (0 when the configuration does not exist).
+void mx_config_numbers(int block_n, int *stages, int *smem, int *threads, int *tmem);
 
 }  // namespace tg

@@ -188,6 +188,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor without swizzle: rows of 16 bytes, 8-row
+// groups 128 bytes apart (a dense row-major block of 16-byte rows).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;   // leading byte offset (unused: one 16-byte column)
+    d |= (uint64_t)(128u >> 4) << 32;   // stride byte offset: next 8 rows
+    d |= (uint64_t)1 << 46;             // descriptor version
+    return d;                            // layout type 0: no swizzle
+}
+
 }  // namespace tg
 
 // ------------------------------------------------------------------ clusters / CTA pairs
@@ -285,6 +296,31 @@ __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, ui
         "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// CTA-pair MMA with block-scaled 8-bit float operands (microscaling: one
+// 8-bit exponent scale per 32 K elements, one scale per MMA), scales read
+// from tensor memory at `sfa_tmem` / `sfb_tmem`; the instruction
+// descriptor's scale-ID fields pick the byte of each 32-bit scale word.
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (described by `desc`) into
+// tensor-memory columns taddr .. taddr+3 of lanes 0-31, repeated in each of
+// the four 32-lane quarters; issued for the CTA pair (each CTA's own shared
+// memory into its own tensor memory).
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
 }
 
 // One arrival on the barrier at the same offset in every CTA of `mask` once

@@ -202,6 +202,56 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
                   const float *D, int64_t ldc, tg_dtype in_dtype,
                   const tg_options *opts, int32_t num_sms, tg_plan_info *out);
 
+/*
+ * Block-scaled (microscaling) FP8 GEMM ("Matrix Multiplication", "Where to
+ * go from here": block-scaled FP8 matmuls; the pages fix no format, this is
+ * the OCP Microscaling one):
+ *   D = out(epi(alpha * s)),  s(i,j) = sum over kb of Xa(i,kb) * Xb(kb,j) *
+ *                                      sum_{k in block kb} a(i,k) * b(k,j)
+ * where block kb covers k in [32*kb, 32*kb + 32) and each scale is a power of
+ * two 2^(e-127) given by an 8-bit code e (e = 255 is NaN).  in_dtype is
+ * TG_E4M3 or TG_E5M2 (both operands); A, B and D are laid out as for tg_gemm
+ * (D of type out_dtype).  A and B must start 16-byte aligned and lda, ldb must
+ * be multiples of 16 (no plain-load fallback here).
+ *
+ * Scales (SFA for the M rows of A, SFB for the N columns of B) are stored as
+ * "scale atoms": with R rows and KB = ceil(K/32) blocks, atom (rb, kg), for
+ * rows [128*rb, 128*rb + 128) and blocks [4*kg, 4*kg + 4), is 512 contiguous
+ * bytes at byte offset (rb * ceil(KB/4) + kg) * 512, and the scale of row r,
+ * block kb is at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + (kb % 4) of its
+ * atom.  The buffer holds tg_mx_scale_bytes(R, K) bytes, 16-byte aligned;
+ * entries for rows >= R or blocks >= KB are padding and must not be 255
+ * (zero is the usual fill).  tg_mx_pack_scales writes this layout from
+ * row-major scales.
+ *
+ * opts may set block_n (128 or 256), swap_ab, raster_group and max_ctas; any
+ * other field must be 0 (or the value that forces what this path does:
+ * producer 1, cta_pair 2, split_k 1, multicast 1, prefetch_k -1).  Returns as
+ * tg_gemm_ex.
+ */
+tg_status tg_gemm_mx(int64_t M, int64_t N, int64_t K, float alpha,
+                     const void *A, int64_t lda, const void *SFA,
+                     const void *B, int64_t ldb, const void *SFB,
+                     void *D, int64_t ldc,
+                     tg_dtype in_dtype, tg_out_dtype out_dtype, tg_epilogue epilogue,
+                     const tg_options *opts, void *stream);
+
+/* The tg_gemm_mx planner without launching (num_sms as for tg_plan). */
+tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                     tg_dtype in_dtype, const tg_options *opts, int32_t num_sms,
+                     tg_plan_info *out);
+
+/* Bytes of the scale-atom buffer for `rows` rows and K (-1 on negative input). */
+int64_t tg_mx_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * Rewrite row-major scales (row r, block kb at src[r*ld_src + kb], ld_src >=
+ * ceil(K/32)) as scale atoms into dst (tg_mx_scale_bytes(rows, K) bytes),
+ * padding with zeros, on `stream`.  Both are device buffers.
+ */
+tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t ld_src,
+                            uint8_t *dst, void *stream);
+
 /* Static text for a status code ("TG_OK", ...); never NULL. */
 const char *tg_status_string(tg_status status);
 

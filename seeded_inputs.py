@@ -52,6 +52,8 @@ PAD_F32_BITS = 0x7FC00001
 
 STREAM_A = 0
 STREAM_B = 1
+STREAM_SA = 2   # block scales of A (microscaling workloads)
+STREAM_SB = 3   # block scales of B
 
 
 def splitmix64(x: np.ndarray) -> np.ndarray:
@@ -190,6 +192,7 @@ class Workload:
     lda: int | None = None
     ldb: int | None = None
     ldc: int | None = None
+    block_scaled: bool = False  # microscaling: one 8-bit exponent scale per 32 K
 
     @property
     def strides(self):
@@ -202,7 +205,8 @@ class Workload:
     @property
     def algorithmic_bytes(self) -> float:
         e = element_bytes(self.dtype)
-        return float((self.M * self.K + self.K * self.N) * e + 4 * self.M * self.N)
+        scales = (self.M + self.N) * ((self.K + 31) // 32) if self.block_scaled else 0
+        return float((self.M * self.K + self.K * self.N) * e + scales + 4 * self.M * self.N)
 
 
 # The problems the pages and their configurations fix.
@@ -223,6 +227,10 @@ WORKLOADS = {
     # "Where to go from here": FP8 matmuls), N(0,1) entries rounded to the type.
     "f8_e4m3_8192": Workload("f8_e4m3_8192", 8192, 8192, 8192, "e4m3", 1.0, True, 6, "normal"),
     "f8_e5m2_8192": Workload("f8_e5m2_8192", 8192, 8192, 8192, "e5m2", 1.0, True, 7, "normal"),
+    # Block-scaled (microscaling) E4M3 at the headline size: N(0,1) entries
+    # rounded to E4M3, one scale 2^e, e in [-7, 7], per 32 K elements.
+    "mx_e4m3_8192": Workload("mx_e4m3_8192", 8192, 8192, 8192, "e4m3", 1.0, True, 8, "normal",
+                             block_scaled=True),
 }
 
 
@@ -283,6 +291,29 @@ def make_output(w: Workload, fill_bits: int = 0x7FC00002) -> np.ndarray:
     rows i >= M of each column (stride padding) can be checked untouched."""
     _, _, ldc = w.strides
     return np.full((w.N, ldc), fill_bits, dtype=np.uint32).view(np.float32)
+
+
+def scale_codes(seed: int, stream: int, rows: int, kblocks: int, lo: int, hi: int) -> np.ndarray:
+    """(rows, kblocks) uint8 scale exponent codes drawn uniformly from
+    [lo, hi], row-major from draw 0 of the stream."""
+    n = rows * kblocks
+    out = np.empty(n, dtype=np.uint8)
+    span = np.uint64(hi - lo + 1)
+    for s0 in range(0, n, CHUNK):
+        c = min(CHUNK, n - s0)
+        out[s0: s0 + c] = (raw_u64(seed, stream, s0, c) % span + np.uint64(lo)).astype(np.uint8)
+    return out.reshape(rows, kblocks)
+
+
+MX_BENCH_SCALES = (120, 134)   # codes of the benchmark's block scales: 2^-7 .. 2^7
+
+
+def make_mx_scales(w: Workload, lo: int = 120, hi: int = 134):
+    """Row-major block scales (one per 32 K elements) for A's M rows and B's
+    N columns of workload ``w``: codes e in [lo, hi], value 2^(e-127)."""
+    kb = (w.K + 31) // 32
+    return (scale_codes(w.seed, STREAM_SA, w.M, kb, lo, hi),
+            scale_codes(w.seed, STREAM_SB, w.N, kb, lo, hi))
 
 
 def with_shape(w: Workload, **kw) -> Workload:

@@ -197,3 +197,95 @@ def check_batched(w: si.Workload, batch: int, out: str, repeats=1, **kw):
             i = np.flatnonzero(bad)[:6]
             raise AssertionError(f"{w.name}[{b}] ({out}): {bad.sum()} elements off; err={err[i]} "
                                  f"tol={tol[ok][i]} got={got[ok][i]} ref={ref_out[ok][i]}")
+
+
+# ----------------------------------------------------------------- block-scaled (microscaling)
+
+def to_atoms(S: np.ndarray, K: int) -> np.ndarray:
+    """Row-major scale codes (R, >= ceil(K/32)) -> the scale-atom byte layout
+    of tg_gemm_mx: atom (rb, kg) at (rb * KG + kg) * 512, byte
+    (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4 inside it; zero padding."""
+    R = S.shape[0]
+    KB = (K + 31) // 32
+    RB, KG = -(-R // 128), -(-KB // 4)
+    full = np.zeros((RB * 128, KG * 4), dtype=np.uint8)
+    full[:R, :KB] = S[:, :KB]
+    # (rb, q, l, kg, j) with r = rb*128 + q*32 + l and kb = kg*4 + j
+    t = full.reshape(RB, 4, 32, KG, 4)
+    # atom (rb, kg), bytes in order (l, q, j)
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
+def mx_padded(w: si.Workload):
+    """The workload with lda, ldb rounded up to multiples of 16 (TMA-legal)."""
+    r16 = lambda x: -(-max(x, 1) // 16) * 16
+    return si.with_shape(w, lda=w.lda or r16(w.K), ldb=w.ldb or r16(w.K))
+
+
+def run_mx(w: si.Workload, A, B, SA, SB, out="f32", opts=None, repeats=1, D0=None):
+    """tg_gemm_mx on the given storage (A (M, lda), B (N, ldb) FP8 codes,
+    SA (M, KB), SB (N, KB) row-major scale codes).  Returns D storage (N, ldc)
+    per repeat."""
+    import torch
+    import dense_gemm_epilogue_gb300 as tg
+
+    lda, ldb, ldc = w.strides
+    dA, dB = torch_storage(A), torch_storage(B)
+    dSA = torch_storage(to_atoms(SA, w.K))
+    dSB = torch_storage(to_atoms(SB, w.K))
+    assert dSA.numel() == tg.tg_mx_scale_bytes(w.M, w.K)
+    assert dSB.numel() == tg.tg_mx_scale_bytes(w.N, w.K)
+    onp = {"f32": np.uint32, "bf16": np.uint16, "fp16": np.uint16}[out]
+    if D0 is None:
+        D0 = np.full((w.N, ldc), 0x7FC00002 if out == "f32" else 0x7FC3, dtype=onp)
+    tdt = torch.int32 if out == "f32" else torch.int16
+    dD = torch.from_numpy(D0.view(np.int32 if out == "f32" else np.int16).copy()).cuda()
+    outs = []
+    for _ in range(repeats):
+        st = tg.tg_gemm_mx(w.M, w.N, w.K, w.alpha, dA, lda, dSA, dB, ldb, dSB, dD, ldc, w.dtype,
+                           out, w.relu, opts)
+        tg.check(st, "tg_gemm_mx")
+        st, where = tg.tg_check_device_status()
+        assert st == tg.TG_OK, f"device status {st} at wait site {where}"
+        outs.append(dD.cpu().numpy().view(onp).copy())
+    assert tdt is not None
+    return D0, outs
+
+
+def check_mx(w: si.Workload, out="f32", opts=None, repeats=1, scale_range=(120, 134)):
+    """Whole-output parity of tg_gemm_mx against the oracle's block-scaled
+    product: |D - D_ref| <= 2^-7 * |alpha| * sum_kb |Xa Xb| sum |a||b| + 1e-6
+    (plus one output ulp for narrow outputs); padding untouched; repeats
+    bitwise identical.  Returns the largest error relative to that scale."""
+    import oracle
+
+    w = mx_padded(w)
+    lda, ldb, ldc = w.strides
+    A, B = si.make_operands(w)
+    SA, SB = si.make_mx_scales(w, *scale_range)
+    D0, outs = run_mx(w, A, B, SA, SB, out=out, opts=opts, repeats=repeats)
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "not deterministic"
+    KB = (w.K + 31) // 32
+    ref, scale = oracle.gemm_mx(w.M, w.N, w.K, w.alpha, A, lda, SA, max(KB, 1), B, ldb, SB,
+                                max(KB, 1), w.dtype, w.relu, with_scale=True)
+    store = outs[0]
+    assert np.array_equal(store[:, w.M:], D0[:, w.M:]), "D stride padding was written"
+    got = decode_out(store[:, : w.M].view(OUT_NP[out]).T, out)
+    ref_out = oracle.round_output(ref, out)
+    nan_ref = np.isnan(ref_out)
+    assert np.array_equal(np.isnan(got) & nan_ref, nan_ref), f"{w.name}: NaN positions differ"
+    inf = np.isinf(ref_out)
+    assert np.array_equal(got[inf], ref_out[inf]), f"{w.name}: overflow differs"
+    ok = ~nan_ref & ~inf
+    err = np.abs(got[ok] - ref_out[ok])
+    tol = TOL_REL[w.dtype] * scale[ok] + TOL_ABS
+    if out != "f32":
+        tol = tol + OUT_ULP_REL[out] * np.abs(ref[ok]) + OUT_ULP_ABS[out]
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.flatnonzero(bad)[:8]
+        raise AssertionError(f"{w.name}: {bad.sum()} of {bad.size} elements off; err={err[idx]} "
+                             f"tol={tol[idx]} got={got[ok][idx]} ref={ref_out[ok][idx]}")
+    rel = err / np.maximum(scale[ok], 1e-30)
+    return float(rel.max()) if rel.size else 0.0

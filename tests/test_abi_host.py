@@ -241,3 +241,50 @@ def test_plan_multicast_clusters(tg):
     with pytest.raises(tg.TgError):
         plan(tg, narrow, opts={"multicast": 2, "cta_pair": 2, "block_n": 256})
 
+
+
+# ----------------------------------------------------------------- block-scaled path (host only)
+
+def test_mx_scale_bytes(tg):
+    assert tg.tg_mx_scale_bytes(0, 100) == 0 and tg.tg_mx_scale_bytes(100, 0) == 0
+    assert tg.tg_mx_scale_bytes(1, 1) == 512
+    assert tg.tg_mx_scale_bytes(128, 128) == 512
+    assert tg.tg_mx_scale_bytes(129, 129) == 4 * 512
+    assert tg.tg_mx_scale_bytes(8192, 8192) == 64 * 64 * 512
+    assert tg.tg_mx_scale_bytes(-1, 5) == -1
+
+
+@pytest.mark.parametrize("args", [
+    dict(dtype="bf16"), dict(dtype="tf32"), dict(lda=1000), dict(ldb=1000), dict(A=FAKE + 8),
+    dict(SFA=None), dict(SFB=FAKE + 4), dict(epi=2), dict(out=3), dict(ldc=9),
+    dict(opts={"block_n": 64}), dict(opts={"cta_pair": 1}), dict(opts={"split_k": 2}),
+    dict(opts={"multicast": 2}), dict(opts={"producer": 2}), dict(opts={"l2_hint": 1}),
+])
+def test_mx_invalid_arguments_rejected_before_cuda(tg, args):
+    a = dict(M=10, N=10, K=1024, A=FAKE, lda=1024, SFA=FAKE, B=FAKE, ldb=1024, SFB=FAKE, D=FAKE,
+             ldc=10, dtype="e4m3", out="f32", epi=1, opts=None)
+    a.update(args)
+    st = tg.tg_gemm_mx(a["M"], a["N"], a["K"], 1.0, a["A"], a["lda"], a["SFA"], a["B"], a["ldb"],
+                       a["SFB"], a["D"], a["ldc"], a["dtype"], a["out"], a["epi"], a["opts"])
+    assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def test_mx_empty_output_is_ok_without_cuda(tg):
+    assert tg.tg_gemm_mx(0, 10, 64, 1.0, None, 64, None, FAKE, 64, FAKE, None, 1, "e4m3", "f32",
+                         True) == tg.TG_OK
+
+
+def test_plan_mx(tg):
+    p = tg.tg_plan_mx(8192, 8192, 8192, 8192, 8192, 8192, "e4m3", None, 152)
+    assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 128)
+    assert p["cta_pair"] == 1 and p["tiles"] == 1024 and p["grid"] == 152
+    assert p["stages"] == 6 and p["tmem_cols"] == 512 and p["threads"] == 320
+    assert p["smem_bytes"] <= 232448
+    q = tg.tg_plan_mx(8192, 8192, 8192, 8192, 8192, 8192, "e5m2", {"block_n": 128}, 152)
+    assert q["block_n"] == 128 and q["stages"] == 8 and q["tmem_cols"] == 256
+    s = tg.tg_plan_mx(64, 4096, 1024, 1024, 1024, 64, "e4m3", None, 152)
+    assert s["swap_ab"] == 1
+    small = tg.tg_plan_mx(300, 300, 256, 256, 256, 300, "e4m3", None, 152)
+    assert small["grid"] == 2 * small["tiles"]
+    with pytest.raises(tg.TgError):
+        tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", None, 152)   # lda not 16-byte multiple

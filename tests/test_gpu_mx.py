@@ -1,0 +1,103 @@
+"""Block-scaled (microscaling) FP8 GEMM, tg_gemm_mx, against the oracle's
+block-scaled product, element by element, through the C ABI; and the
+scale-packing call against the layout's definition."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+from gemm_harness import (check_mx, decode_out, logical, mx_padded, run_mx, to_atoms,
+                          torch_storage)
+
+pytestmark = pytest.mark.gpu
+FP8 = ["e4m3", "e5m2"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_gemm_epilogue_gb300 as tg
+
+    tg.build()
+    tg.load()
+
+
+@pytest.mark.parametrize("rows,K,ld", [(1, 1, 1), (200, 283, 9), (128, 128, 4), (513, 4100, 140)])
+def test_pack_scales_matches_layout(rows, K, ld):
+    import dense_gemm_epilogue_gb300 as tg
+
+    kb = (K + 31) // 32
+    S = si.scale_codes(5, 2, rows, ld, 0, 254)
+    dst = torch_storage(np.full(tg.tg_mx_scale_bytes(rows, K), 0xAB, dtype=np.uint8))
+    tg.check(tg.tg_mx_pack_scales(rows, K, torch_storage(S), ld, dst), "tg_mx_pack_scales")
+    got = dst.cpu().numpy()
+    assert np.array_equal(got, to_atoms(S[:, :kb], K))
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (1, 1, 1), (129, 65, 33), (300, 520, 1040),
+                                   (257, 255, 129), (513, 1000, 2048), (64, 1000, 512)])
+def test_mx_shapes(dtype, M, N, K):
+    w = si.Workload(f"mx_{dtype}", M, N, K, dtype, 1.5, True, 400 + M + N + K, "normal",
+                    ldc=M + 3)
+    check_mx(w, repeats=2)
+
+
+@pytest.mark.parametrize("dtype", FP8)
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("swap", [1, 2])
+def test_mx_tile_configs(dtype, block_n, swap):
+    w = si.Workload("mx_cfg", 600, 700, 1000, dtype, -0.75, False, 91, "normal")
+    check_mx(w, opts={"block_n": block_n, "swap_ab": swap})
+
+
+@pytest.mark.parametrize("out", ["bf16", "fp16"])
+def test_mx_narrow_outputs(out):
+    """Narrow outputs; the wide scale range overflows FP16 in places (those
+    elements must be the same infinities as the oracle's rounding)."""
+    w = si.Workload("mx_out", 520, 600, 768, "e4m3", 0.5, True, 92, "normal")
+    check_mx(w, out=out)
+    check_mx(si.with_shape(w, seed=96, relu=False), out=out, scale_range=(122, 130))
+
+
+def test_mx_persistent_and_wide_scale_range():
+    """Few pairs (several tiles each, the single accumulator reused), and
+    scales spanning 2^-40 .. 2^40."""
+    w = si.Workload("mx_persist", 1100, 1300, 640, "e5m2", 1.0, True, 93, "normal")
+    for g in (2, 6):
+        check_mx(w, opts={"max_ctas": g, "raster_group": 2})
+    check_mx(si.with_shape(w, seed=94), scale_range=(87, 167))
+
+
+def test_mx_nan_scale_and_k_zero():
+    import dense_gemm_epilogue_gb300 as tg
+    import oracle
+
+    w = mx_padded(si.Workload("mx_nan", 300, 200, 256, "e4m3", 1.0, True, 95, "normal"))
+    A, B = si.make_operands(w)
+    SA, SB = si.make_mx_scales(w)
+    SA[17, 3] = 255
+    SB[33, 0] = 255
+    _, outs = run_mx(w, A, B, SA, SB)
+    got = decode_out(outs[0][:, : w.M].view(np.float32).T, "f32")
+    assert np.all(np.isnan(got[17])) and np.all(np.isnan(got[:, 33]))
+    rest = np.delete(np.delete(got, 17, 0), 33, 1)
+    assert not np.any(np.isnan(rest))
+    lda, ldb, _ = w.strides
+    ref = oracle.gemm_mx(w.M, w.N, w.K, w.alpha, A, lda, SA, 8, B, ldb, SB, 8, "e4m3", True)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    # K = 0: the epilogue of an empty sum, nothing read.
+    import torch
+    D = torch.full((20, 30), 7.0, device="cuda")
+    st = tg.tg_gemm_mx(30, 20, 0, 2.0, None, 16, None, None, 16, None, D, 30, "e4m3", "f32",
+                       False)
+    assert st == tg.TG_OK
+    assert float(D.abs().max()) == 0.0
+
+
+def test_mx_8192_full():
+    check_mx(si.WORKLOADS["mx_e4m3_8192"])
