@@ -17,9 +17,11 @@ SOURCE = os.path.join(_HERE, "oracle_gemm.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
 
-_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4}
+_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 _STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
-            "e5m2": np.uint8}
+            "e5m2": np.uint8, "e2m1": np.uint8}
+# Elements per storage unit (E2M1: two per byte, low nibble first).
+_PER_UNIT = {"e2m1": 2}
 _OUT_CODE = {"f32": 0, "bf16": 1, "fp16": 2}
 GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread"]
 
@@ -109,15 +111,17 @@ class Oracle:
                 with_scale=False, threads=0):
         """Block-scaled D_ref (M, N) float64: FP8 operands as in ``gemm``, and
         one 8-bit exponent scale per 32 k, Xa(i,kb) = SA.flat[i*ldsa + kb],
-        Xb(kb,j) = SB.flat[j*ldsb + kb] (uint8 codes)."""
+        Xb(kb,j) = SB.flat[j*ldsb + kb] (uint8 codes).  For e2m1, A and B are
+        packed bytes and lda, ldb count elements (even)."""
         A = _check_storage(A, dtype, "A")
         B = _check_storage(B, dtype, "B")
+        per = _PER_UNIT.get(dtype, 1)
         SA = np.ascontiguousarray(SA, dtype=np.uint8)
         SB = np.ascontiguousarray(SB, dtype=np.uint8)
         kb = (K + 31) // 32
-        if M and K and A.size < (M - 1) * lda + K:
+        if M and K and A.size * per < (M - 1) * lda + K:
             raise ValueError("A too small for (M, K, lda)")
-        if N and K and B.size < (N - 1) * ldb + K:
+        if N and K and B.size * per < (N - 1) * ldb + K:
             raise ValueError("B too small for (K, N, ldb)")
         if M and kb and SA.size < (M - 1) * ldsa + kb:
             raise ValueError("SA too small")
@@ -165,10 +169,14 @@ class Oracle:
         return arr
 
     def decode(self, bits, dtype: str) -> np.ndarray:
-        """The oracle's own decode of storage elements to float64."""
+        """The oracle's own decode of storage elements to float64 (e2m1: each
+        byte gives two elements, low nibble first; the result has twice the
+        last dimension)."""
         x = _check_storage(bits, dtype, "bits")
-        out = np.zeros(x.shape, dtype=np.float64)
-        self.lib.orc_decode_array(x.ctypes.data, x.size, _DTYPE_CODE[dtype], out.ctypes.data)
+        per = _PER_UNIT.get(dtype, 1)
+        shape = x.shape[:-1] + (x.shape[-1] * per,) if x.ndim else (per,)
+        out = np.zeros(shape, dtype=np.float64)
+        self.lib.orc_decode_array(x.ctypes.data, x.size * per, _DTYPE_CODE[dtype], out.ctypes.data)
         return out
 
 

@@ -9,7 +9,8 @@
  *
  * What it computes (for every 0 <= i < M, 0 <= j < N):
  *   1. decode each operand element exactly from its storage format
- *      (bf16 / fp16 / e4m3 / e5m2 bit patterns, or fp32 narrowed to tf32);
+ *      (bf16 / fp16 / e4m3 / e5m2 / e2m1 bit patterns, or fp32 narrowed to
+ *      tf32);
  *   2. s = sum_{k=0}^{K-1} a(i,k) * b(k,j), in double, k ascending
  *      ("Matrix Multiplication", Step 3 "Looping over K": C[i,j] is the sum
  *      over k of A[i,k]*B[k,j]; accumulate wider than the inputs);
@@ -55,7 +56,7 @@
 #include <unistd.h>
 
 /* Operand storage formats understood by the oracle. */
-enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_TF32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_TF32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E2M1 = 5 };
 
 /* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
 double orc_decode_bf16(uint16_t h) {
@@ -149,8 +150,26 @@ double orc_decode_e5m2(uint8_t h) {
     return s ? -v : v;
 }
 
+/*
+ * 4-bit floating point (E2M1, the FP4 of the block-scaled matmuls): 1 sign
+ * bit, 2 exponent bits (bias 1), 1 fraction bit; no infinities or NaN.
+ * Magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6.  Stored two per byte:
+ * element 2t in the low nibble of byte t, element 2t + 1 in the high nibble.
+ */
+double orc_decode_e2m1(uint8_t nibble) {
+    int s = (nibble >> 3) & 1;
+    int e = (nibble >> 1) & 0x3;
+    int f = nibble & 0x1;
+    double v = (e == 0) ? ldexp((double)f, -1) : ldexp((double)(2 + f), e - 1 - 1);
+    return s ? -v : v;
+}
+
 static double decode_elem(const void *base, int64_t idx, int dtype) {
     switch (dtype) {
+    case ORC_E2M1: {
+        uint8_t byte = ((const uint8_t *)base)[idx >> 1];
+        return orc_decode_e2m1((idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF));
+    }
     case ORC_BF16: return orc_decode_bf16(((const uint16_t *)base)[idx]);
     case ORC_FP16: return orc_decode_fp16(((const uint16_t *)base)[idx]);
     case ORC_E4M3: return orc_decode_e4m3(((const uint8_t *)base)[idx]);
@@ -423,7 +442,8 @@ static void *mx_worker(void *p) {
 
 /*
  * Block-scaled D_ref for the whole M x N output (see the header comment):
- * FP8 operands (E4M3 / E5M2) with one 8-bit exponent scale per 32 k.
+ * FP8 (E4M3 / E5M2) or FP4 (E2M1, packed) operands with one 8-bit exponent
+ * scale per 32 k.  For E2M1, lda and ldb count elements and must be even.
  * Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
  */
 int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
@@ -433,7 +453,8 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
     int64_t KB = (K + ORC_MX_BLOCK - 1) / ORC_MX_BLOCK;
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldd < M) return -1;
     if (ldsa < KB || ldsb < KB) return -1;
-    if (dtype != ORC_E4M3 && dtype != ORC_E5M2) return -1;
+    if (dtype != ORC_E4M3 && dtype != ORC_E5M2 && dtype != ORC_E2M1) return -1;
+    if (dtype == ORC_E2M1 && ((lda | ldb) & 1)) return -1;  /* rows start on whole bytes */
     if (M == 0 || N == 0) return 0;
     size_t kk = (size_t)(K ? K : 1), kbb = (size_t)(KB ? KB : 1);
     double *Ad = (double *)malloc(sizeof(double) * (size_t)M * kk);

@@ -163,13 +163,39 @@ def f32_to_fp8_bits(x: np.ndarray, fmt: str) -> np.ndarray:
 DTYPES = ("bf16", "fp16", "tf32", "e4m3", "e5m2")
 
 
-def element_bytes(dtype: str) -> int:
-    return {"bf16": 2, "fp16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1}[dtype]
+# E2M1 (FP4): magnitudes of codes 0..7; no infinities or NaN.
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+PAD_E2M1 = 0x7  # +6: stride padding of packed FP4 rows (never read)
+
+
+def f32_to_e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 code (ties to the even code), saturating at
+    6; 4-bit codes in uint8 (sign in bit 3).  NaN is not representable and
+    maps to +6."""
+    x64 = np.asarray(x, dtype=np.float64).reshape(-1)
+    a = np.abs(np.where(np.isnan(x64), 6.0, x64))
+    hi = np.clip(np.searchsorted(E2M1_VALUES, a), 1, 7)
+    lo = hi - 1
+    dlo, dhi = a - E2M1_VALUES[lo], E2M1_VALUES[hi] - a
+    pick = np.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo)
+    pick = np.where(a >= 6.0, 7, pick).astype(np.uint8)
+    sign = np.signbit(x64) & ~np.isnan(x64)
+    return np.where(sign, pick | 0x8, pick).astype(np.uint8).reshape(np.shape(x))
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """(..., 2n) 4-bit codes -> (..., n) bytes, element 2t in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def element_bytes(dtype: str) -> float:
+    return {"bf16": 2, "fp16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e2m1": 0.5}[dtype]
 
 
 def storage_numpy_dtype(dtype: str):
     return {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
-            "e5m2": np.uint8}[dtype]
+            "e5m2": np.uint8, "e2m1": np.uint8}[dtype]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -273,10 +299,25 @@ def make_operands(w: Workload):
 
     A has shape (M, lda): row i holds A[i, 0:K] then NaN padding.
     B has shape (N, ldb): row j holds B[0:K, j] then NaN padding.
+    (E2M1: packed, shapes (M, lda/2) and (N, ldb/2) bytes; padding +6.)
     A's logical entries use stream 0 in row-major (i, k) order, B's use
     stream 1 in (j, k) order.
     """
     lda, ldb, _ = w.strides
+    if w.dtype == "e2m1":
+        # Packed FP4: rows of lda / 2 bytes (lda even), padding code +6.
+        assert lda % 2 == 0 and ldb % 2 == 0, "E2M1 rows must hold an even number of elements"
+        out = []
+        for rows, ld, stream in ((w.M, lda, STREAM_A), (w.N, ldb, STREAM_B)):
+            codes = np.full((rows, ld), PAD_E2M1, dtype=np.uint8)
+            if rows * w.K:
+                flat = _draw(w, stream, rows * w.K)
+                q = np.empty(flat.size, dtype=np.uint8)
+                for s0 in range(0, flat.size, CHUNK):
+                    q[s0: s0 + CHUNK] = f32_to_e2m1_codes(flat[s0: s0 + CHUNK])
+                codes[:, : w.K] = q.reshape(rows, w.K)
+            out.append(pack_e2m1(codes))
+        return out[0], out[1]
     A = np.full((w.M, lda), pad_value(w.dtype), dtype=storage_numpy_dtype(w.dtype))
     B = np.full((w.N, ldb), pad_value(w.dtype), dtype=storage_numpy_dtype(w.dtype))
     if w.M * w.K:

@@ -488,7 +488,32 @@ def check_fp8_decode(orc):
 MX_GRID = np.arange(-8, 9) / 8.0     # exact in E4M3 and E5M2
 
 
+# E2M1 values of codes 0..15 as the OCP format lists them (sign in bit 3).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+FP4_GRID = np.array([-6, -4, -3, -2, -1.5, -1, -0.5, 0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float64)
+
+
+def e2m1_codes_exact(vals) -> np.ndarray:
+    v = np.asarray(vals, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.uint8)
+    for idx, x in np.ndenumerate(v):
+        hits = [c for c, t in enumerate(E2M1_TABLE)
+                if t == x and math.copysign(1.0, t) == math.copysign(1.0, x)]
+        assert hits, f"{x} not exact in e2m1"
+        out[idx] = hits[0]
+    return out
+
+
 def mx_codes(vals, dtype):
+    """Exact values (rows, K) -> storage rows: FP8 codes, or packed E2M1 with
+    the row length rounded up to an even count (padding code +6)."""
+    if dtype == "e2m1":
+        v = np.asarray(vals, dtype=np.float64)
+        rows, K = v.shape
+        codes = np.full((rows, K + (K & 1)), 7, dtype=np.uint8)
+        codes[:, :K] = e2m1_codes_exact(v)
+        return np.ascontiguousarray((codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4))
     return fp8_bits_exact(np.asarray(vals, dtype=np.float64), dtype)
 
 
@@ -501,12 +526,13 @@ def run_mx(orc, Alog, Blog, SAc, SBc, dtype, alpha, relu, pad_s=5, **kw):
     KB = SAc.shape[1]
     A = mx_codes(Alog, dtype)
     B = np.ascontiguousarray(mx_codes(Blog.T, dtype))
+    ld = K + (K & 1) if dtype == "e2m1" else K
     ldsa = ldsb = KB + pad_s
     SA = np.full((M, ldsa), 255, dtype=np.uint8)
     SB = np.full((N, ldsb), 255, dtype=np.uint8)
     SA[:, :KB] = SAc
     SB[:, :KB] = SBc
-    return orc.gemm_mx(M, N, K, alpha, A, K, SA, ldsa, B, K, SB, ldsb, dtype, relu, **kw)
+    return orc.gemm_mx(M, N, K, alpha, A, ld, SA, ldsa, B, ld, SB, ldsb, dtype, relu, **kw)
 
 
 def check_mx_scale_decode(orc):
@@ -519,17 +545,28 @@ def check_mx_scale_decode(orc):
     assert math.isnan(got[255])
 
 
+def check_e2m1_decode(orc):
+    """Every byte decodes to (low nibble, high nibble) per the E2M1 table."""
+    got = orc.decode(np.arange(256, dtype=np.uint16).astype(np.uint8), "e2m1").reshape(256, 2)
+    for b in range(256):
+        for half, code in ((0, b & 0xF), (1, b >> 4)):
+            want = E2M1_TABLE[code]
+            assert got[b, half] == want and math.copysign(1.0, got[b, half]) == \
+                math.copysign(1.0, want), (b, half)
+
+
 def check_mx_bruteforce_exact(orc):
     """Tiny problems with ragged last blocks against exact rational
     arithmetic of the microscaling definition."""
     rng = np.random.default_rng(29)
     for (M, N, K) in ((3, 4, 70), (2, 5, 32), (4, 3, 97), (1, 1, 1)):
         KB = (K + 31) // 32
-        Alog = rng.choice(MX_GRID, size=(M, K))
-        Blog = rng.choice(MX_GRID, size=(K, N))
         SAc = rng.integers(121, 134, size=(M, KB)).astype(np.uint8)
         SBc = rng.integers(121, 134, size=(N, KB)).astype(np.uint8)
-        for dt in ("e4m3", "e5m2"):
+        for dt in ("e4m3", "e5m2", "e2m1"):
+            grid = FP4_GRID if dt == "e2m1" else MX_GRID
+            Alog = rng.choice(grid, size=(M, K))
+            Blog = rng.choice(grid, size=(K, N))
             for alpha, relu in ((1.0, False), (-1.5, True)):
                 D, S = run_mx(orc, Alog, Blog, SAc, SBc, dt, alpha, relu, with_scale=True)
                 assert np.all(np.isfinite(D)) and np.all(np.isfinite(S)), (dt, M, N, K)
@@ -561,16 +598,20 @@ def check_mx_block_boundaries(orc):
     SAc = np.array([[127 + kb + 4 * i for kb in range(KB)] for i in range(M)], dtype=np.uint8)
     SBc = np.array([[120 - 2 * kb - 9 * j for kb in range(KB)] for j in range(N)], dtype=np.uint8)
     Blog = np.ones((K, N))
-    for k in (0, 15, 16, 31, 32, 33, 63, 64, 95, 96, 99):
-        Alog = np.zeros((M, K))
-        Alog[0, k] = 1.0
-        Alog[1, K - 1 - k] = -1.0
-        D = run_mx(orc, Alog, Blog, SAc, SBc, "e4m3", 1.0, False)
-        for j in range(N):
-            kb0, kb1 = k // 32, (K - 1 - k) // 32
-            want0 = 2.0 ** (int(SAc[0, kb0]) - 127 + int(SBc[j, kb0]) - 127)
-            want1 = -(2.0 ** (int(SAc[1, kb1]) - 127 + int(SBc[j, kb1]) - 127))
-            assert D[0, j] == want0 and D[1, j] == want1, (k, j)
+    for dt in ("e4m3", "e2m1"):
+        for k in (0, 1, 15, 16, 30, 31, 32, 33, 63, 64, 95, 96, 98, 99):
+            Alog = np.zeros((M, K))
+            Alog[0, k] = 1.0
+            Alog[1, K - 1 - k] = -1.0
+            Bk = Blog.copy()
+            Bk[k, :] = 4.0       # the row meeting A's nonzero (pins E2M1 nibble order)
+            Bk[K - 1 - k, :] = 2.0 if K - 1 - k != k else 4.0
+            D = run_mx(orc, Alog, Bk, SAc, SBc, dt, 1.0, False)
+            for j in range(N):
+                kb0, kb1 = k // 32, (K - 1 - k) // 32
+                want0 = Bk[k, j] * 2.0 ** (int(SAc[0, kb0]) - 127 + int(SBc[j, kb0]) - 127)
+                want1 = -Bk[K - 1 - k, j] * 2.0 ** (int(SAc[1, kb1]) - 127 + int(SBc[j, kb1]) - 127)
+                assert D[0, j] == want0 and D[1, j] == want1, (dt, k, j)
 
 
 def check_mx_scale_invariances(orc):
@@ -636,6 +677,7 @@ ALL_CHECKS = [
     check_round_output,
     check_fp8_decode,
     check_mx_scale_decode,
+    check_e2m1_decode,
     check_mx_bruteforce_exact,
     check_mx_block_boundaries,
     check_mx_scale_invariances,

@@ -49,3 +49,23 @@ def test_fp8_nan_and_signed_zero():
         c = si.f32_to_fp8_bits(np.float32([np.nan, -0.0, 0.0]), fmt)
         assert np.isnan(DECODE[fmt](c[:1]))[0]
         assert c[1] == 0x80 and c[2] == 0x00
+
+
+def test_e2m1_nearest_by_brute_force_and_packing():
+    from oracle_pin_checks import E2M1_TABLE
+
+    table = np.array(E2M1_TABLE)
+    x = np.concatenate([si.normal_f32(11, 0, 3000, 2.5),
+                        np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 100.0, -0.25, -5.0])])
+    codes = si.f32_to_e2m1_codes(x)
+    for v, c in zip(x.astype(np.float64), codes):
+        cv = min(max(v, -6.0), 6.0)
+        d = np.abs(table - cv)
+        best = np.flatnonzero(d == d.min())
+        if v != 0:
+            best = best[np.signbit(table[best]) == np.signbit(v)]
+        if best.size > 1:
+            best = best[best % 2 == 0]
+        assert c in best, (v, c, best)
+    packed = si.pack_e2m1(np.arange(16, dtype=np.uint8))
+    assert list(packed) == [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]

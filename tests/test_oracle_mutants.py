@@ -43,6 +43,10 @@ MUTANTS = {
                        "else if (e == 0) v = ldexp((double)f, -7 - 3);"),
     "e4m3_no_nan": ("if (e == 0xF && f == 0x7) v = NAN;", "if (0) v = NAN;"),
     "e5m2_inf_as_nan": ("if (e == 0x1F) v = (f == 0) ? INFINITY : NAN;", "if (e == 0x1F) v = NAN;"),
+    "e2m1_nibble_swap": ("return orc_decode_e2m1((idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF));",
+                         "return orc_decode_e2m1((idx & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4));"),
+    "e2m1_subnormal": ("double v = (e == 0) ? ldexp((double)f, -1)", "double v = (e == 0) ? ldexp((double)f, -2)"),
+    "e2m1_bias": ("ldexp((double)(2 + f), e - 1 - 1);", "ldexp((double)(2 + f), e - 2 - 1);"),
     "mx_block_16": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 16"),
     "mx_block_64": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 64"),
     "mx_scale_bias": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 128);"),
