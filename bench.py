@@ -278,7 +278,8 @@ def run_gpu(args, rank, world, local):
     batched = nbat > 1 or out != "f32"
     lda, ldb, ldc = w.strides
     A, B = si.make_operands(w)
-    view = {"tf32": np.float32, "e4m3": np.uint8, "e5m2": np.uint8}.get(w.dtype, np.int16)
+    view = {"tf32": np.float32, "e4m3": np.uint8, "e5m2": np.uint8,
+            "e2m1": np.uint8}.get(w.dtype, np.int16)
     hA = torch.from_numpy(np.tile(A.reshape(-1), nbat).view(view)).pin_memory()
     hB = torch.from_numpy(np.tile(B.reshape(-1), nbat).view(view)).pin_memory()
     dA = hA.cuda()
@@ -286,7 +287,7 @@ def run_gpu(args, rank, world, local):
     odt = torch.float32 if out == "f32" else torch.int16
     dD = torch.empty((nbat * w.N, ldc), dtype=odt, device="cuda")
     hD = torch.empty((nbat * w.N, ldc), dtype=odt).pin_memory()
-    sa, sb, sd = w.M * lda, w.N * ldb, w.N * ldc
+    sa, sb, sd = w.M * lda, w.N * ldb, w.N * ldc   # elements (unused for block-scaled FP4)
     stream = torch.cuda.Stream()
     mx = w.block_scaled
     if mx:
@@ -432,12 +433,13 @@ def run_gpu(args, rank, world, local):
         launch_avg_ms = statistics.fmean(launch_ms)
         # Back-to-back launches for more than ~50 ms run in the power-capped
         # regime the sustained peak was measured in; a short burst compares
-        # with the burst peak.  Both are reported.  TF32 and the 8-bit floats
-        # take the BF16 peak times the nominal ratio to BF16 (1.1 / 2.25 and
-        # 4.5 / 2.25 PFLOP/s).
-        ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25}.get(w.dtype, 1.0)
+        # with the burst peak.  Both are reported.  TF32, the 8-bit and the
+        # 4-bit floats take the BF16 peak times the nominal ratio to BF16
+        # (1.1, 4.5 and 13.5 over 2.25 PFLOP/s).
+        ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
+                 "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
         ratio_note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
-                      "e5m2": " x 4.5/2.25 (FP8)"}.get(w.dtype, "")
+                      "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
         sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
         tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
         burst_tpeak = ratio * float(peaks["bf16_tflops"])

@@ -30,8 +30,9 @@ TG_FP16 = 1
 TG_TF32 = 2
 TG_E4M3 = 3
 TG_E5M2 = 4
+TG_E2M1 = 5
 DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32, "e4m3": TG_E4M3,
-               "e5m2": TG_E5M2}
+               "e5m2": TG_E5M2, "e2m1": TG_E2M1}
 
 TG_EPILOGUE_NONE = 0
 TG_EPILOGUE_RELU = 1

@@ -90,8 +90,9 @@ int elem_bytes(tg_dtype t) {
     return t == TG_TF32 ? 4 : (t == TG_E4M3 || t == TG_E5M2) ? 1 : 2;
 }
 
-// K elements per pipeline stage: one 128-byte swizzle row of the type.
-int block_k(tg_dtype t) { return 128 / elem_bytes(t); }
+// K elements per pipeline stage: one 128-byte swizzle row of the type
+// (packed FP4: 256).
+int block_k(tg_dtype t) { return t == TG_E2M1 ? 256 : 128 / elem_bytes(t); }
 
 bool known_dtype(tg_dtype t) {
     return t == TG_BF16 || t == TG_FP16 || t == TG_TF32 || t == TG_E4M3 || t == TG_E5M2;
@@ -486,6 +487,12 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
                     int64_t ld, int64_t nb, int64_t sb, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    if (t == TG_E2M1) {  // packed FP4: described as bytes, two elements each
+        k = (k + 1) / 2;
+        ld /= 2;
+        sb /= 2;
+        t = TG_E4M3;
+    }
     const int e = elem_bytes(t);
     CUtensorMapDataType dt = t == TG_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                              : t == TG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -633,12 +640,18 @@ bool mx_options_ok(const tg_options *o) {
 }
 
 tg_status validate_mx(const Problem &q, const void *sfa, const void *sfb, const tg_options *o) {
-    if (q.t != TG_E4M3 && q.t != TG_E5M2) return TG_ERR_INVALID_VALUE;
-    tg_status st = validate(q, nullptr);
+    if (q.t != TG_E4M3 && q.t != TG_E5M2 && q.t != TG_E2M1) return TG_ERR_INVALID_VALUE;
+    const bool fp4 = q.t == TG_E2M1;
+    Problem qq = q;
+    if (fp4) qq.t = TG_E4M3;  // the generic checks, on 1-byte storage
+    tg_status st = validate(qq, nullptr);
     if (st != TG_OK) return st;
     if (!mx_options_ok(o)) return TG_ERR_INVALID_VALUE;
+    // Packed FP4: rows and the reduction hold whole bytes.
+    if (fp4 && ((q.lda | q.ldb | q.K) & 1)) return TG_ERR_INVALID_VALUE;
     if (q.M > 0 && q.N > 0 && q.K > 0) {
-        if (!tma_legal(q.A, q.lda, 1) || !tma_legal(q.B, q.ldb, 1)) return TG_ERR_INVALID_VALUE;
+        const int64_t lda_b = fp4 ? q.lda / 2 : q.lda, ldb_b = fp4 ? q.ldb / 2 : q.ldb;
+        if (!tma_legal(q.A, lda_b, 1) || !tma_legal(q.B, ldb_b, 1)) return TG_ERR_INVALID_VALUE;
         if (!sfa || !sfb || (uintptr_t)sfa % 16 || (uintptr_t)sfb % 16) return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
@@ -675,7 +688,8 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     const int64_t mblocks = ceil_div(p.mk, 2 * tg::BLOCK_M);
     p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
     p.tiles = p.tiles_per_batch;
-    tg::mx_config_numbers(p.block_n, &p.stages, &p.smem, &p.threads, &p.tmem_cols);
+    tg::mx_config_numbers(q.t == TG_E2M1 ? Kind::E2M1 : Kind::E4M3, p.block_n, &p.stages, &p.smem,
+                          &p.threads, &p.tmem_cols);
     int64_t g = o->raster_group ? o->raster_group : 8;
     if (g > mblocks) g = mblocks;
     p.group = (int)g;
@@ -687,13 +701,14 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
 }
 
 // Scale atoms of an operand with `rows` rows as a 3-D tensor of 32-bit words:
-// (128 words = one 512-byte atom, atoms, 1); one atom per box.
+// (128 words = one 512-byte atom, atom column kg, row block rb); one atom per
+// box, so a column or row block past the end reads as zeros.
 bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const int64_t atoms = ceil_div(rows, tg::BLOCK_M) * ceil_div(K, 128);
-    cuuint64_t dims[3] = {128, (cuuint64_t)atoms, 1};
-    cuuint64_t strides[2] = {512, (cuuint64_t)(atoms * 512)};
+    const int64_t kg = ceil_div(K, 128), rb = ceil_div(rows, tg::BLOCK_M);
+    cuuint64_t dims[3] = {128, (cuuint64_t)kg, (cuuint64_t)rb};
+    cuuint64_t strides[2] = {512, (cuuint64_t)(kg * 512)};
     cuuint32_t box[3] = {128, 1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
@@ -767,7 +782,9 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     la.grid = plan.grid;
     la.device = dev;
     la.stream = stream;
-    const cudaError_t e = tg::launch_mx(la, q.t == TG_E4M3 ? Kind::E4M3 : Kind::E5M2);
+    const cudaError_t e = tg::launch_mx(la, q.t == TG_E4M3   ? Kind::E4M3
+                                            : q.t == TG_E5M2 ? Kind::E5M2
+                                                             : Kind::E2M1);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

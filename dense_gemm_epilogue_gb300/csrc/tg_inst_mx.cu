@@ -1,4 +1,4 @@
-// Block-scaled 8-bit float kernel instantiations and their launch (CTA-pair
+// Block-scaled 8-bit / packed 4-bit float kernel instantiations and their launch (CTA-pair
 // clusters, grid clamped to the pairs the device holds at once).
 #include <atomic>
 #include <cstdio>
@@ -60,19 +60,26 @@ static cudaError_t launch_mx_kind(const LaunchArgs &a) {
 cudaError_t launch_mx(const LaunchArgs &a, Kind kind) {
     if (kind == Kind::E4M3) return launch_mx_kind<Kind::E4M3>(a);
     if (kind == Kind::E5M2) return launch_mx_kind<Kind::E5M2>(a);
+    if (kind == Kind::E2M1) return launch_mx_kind<Kind::E2M1>(a);
     return cudaErrorInvalidValue;
 }
 
-void mx_config_numbers(int block_n, int *stages, int *smem, int *threads, int *tmem) {
+template <Kind KD>
+static void mx_numbers(int block_n, int *stages, int *smem, int *threads, int *tmem) {
     if (block_n == 256) {
-        using C = MxConfig<Kind::E4M3, 256>;
+        using C = MxConfig<KD, 256>;
         *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
     } else if (block_n == 128) {
-        using C = MxConfig<Kind::E4M3, 128>;
+        using C = MxConfig<KD, 128>;
         *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
     } else {
         *stages = *smem = *threads = *tmem = 0;
     }
+}
+
+void mx_config_numbers(Kind kind, int block_n, int *stages, int *smem, int *threads, int *tmem) {
+    if (kind == Kind::E2M1) mx_numbers<Kind::E2M1>(block_n, stages, smem, threads, tmem);
+    else mx_numbers<Kind::E4M3>(block_n, stages, smem, threads, tmem);
 }
 
 }  // namespace tg

@@ -45,10 +45,10 @@
 
 namespace tg {
 
-enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2, E4M3 = 3, E5M2 = 4 };
+enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2, E4M3 = 3, E5M2 = 4, E2M1 = 5 };
 
 // Tensor-core instruction family of a kind.
-enum class MmaKind : int { F16, TF32, F8 };
+enum class MmaKind : int { F16, TF32, F8, F4 };
 
 template <Kind KD>
 struct KindTraits;
@@ -83,6 +83,15 @@ struct KindTraits<Kind::E5M2> {
     static constexpr int elem_bytes = 1, block_k = 128, umma_k = 32;
     static constexpr uint32_t fmt = 1;  // E5M2
     static constexpr MmaKind mma = MmaKind::F8;
+};
+// Packed 4-bit floats (block-scaled kernel only): two per byte, so one
+// 128-byte row holds 256 elements and one MMA (kind::mxf4) takes 64 -- again
+// 32 bytes of K.  elem_bytes is not defined for this kind.
+template <>
+struct KindTraits<Kind::E2M1> {
+    static constexpr int block_k = 256, umma_k = 64;
+    static constexpr uint32_t fmt = 1;  // E2M1 in the mxf4 format field
+    static constexpr MmaKind mma = MmaKind::F4;
 };
 
 // One tcgen05.mma (single CTA) of the kind's family.

@@ -20,7 +20,9 @@
 // reads them, one byte per 32-wide MMA chosen by the descriptor's scale ID.
 //
 // One 128-byte K stage holds 128 FP8 elements = 4 scale blocks = one atom
-// column, so a stage carries exactly one A atom per CTA and BN/128 B atoms.
+// column, so a stage carries one A atom per CTA and BN/128 B atoms; with
+// packed FP4 (E2M1) a stage holds 256 elements = two atom columns, and each
+// 64-wide MMA (kind::mxf4, two scales per row) reads bytes (0, 1) or (2, 3).
 //
 // Differences from the CTA-pair kernel of tg_kernel_pair.cuh:
 //   - each stage also lands its scale atoms (TMA, 512 bytes each); each CTA
@@ -46,17 +48,20 @@ namespace tg {
 template <Kind KD, int BN>
 struct MxConfig {
     using T = KindTraits<KD>;
-    static_assert(T::mma == MmaKind::F8, "block scaling covers the 8-bit float kinds");
+    static constexpr bool FP4 = T::mma == MmaKind::F4;
+    static_assert(T::mma == MmaKind::F8 || FP4, "block scaling covers the 8- and 4-bit floats");
     static_assert(BN == 128 || BN == 256, "tile N: whole 128-row scale atoms");
-    static constexpr int BK = T::block_k;                // 128 K elements per stage
+    static constexpr int BK = T::block_k;                // K elements per stage (128 / 256)
+    static constexpr int BK_UNITS = ROW_BYTES;           // the same in tensor-map units (bytes)
     static constexpr int PAIR_M = 2 * BLOCK_M;
     static constexpr int B_ROWS = BN / 2;
-    static constexpr int SFB_ATOMS = BN / 128;
+    static constexpr int SFB_ATOMS = BN / 128;           // B atoms per atom column
+    static constexpr int KGS = BK / 128;                 // atom columns per stage (4 blocks each)
     static constexpr int ATOM_BYTES = 512;
     static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
-    static constexpr int SFA_BYTES = ATOM_BYTES;
-    static constexpr int SFB_BYTES = SFB_ATOMS * ATOM_BYTES;
+    static constexpr int SFA_BYTES = KGS * ATOM_BYTES;   // [kg][atom]
+    static constexpr int SFB_BYTES = KGS * SFB_ATOMS * ATOM_BYTES;  // [kg][row block][atom]
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int FIT = (SMEM_LIMIT - 2048) / STAGE_BYTES;
     static constexpr int STAGES = FIT > 8 ? 8 : FIT;
@@ -70,9 +75,12 @@ struct MxConfig {
     static constexpr int NUM_BARS = 2 * STAGES + 3;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
-    // Tensor memory: the accumulator in columns [0, BN); then one 16-column
-    // scale slot per stage (A atom at +0..3, B atoms at +8..+8+4*SFB_ATOMS).
-    static constexpr int SLOT_COLS = 16;
+    // Tensor memory: the accumulator in columns [0, BN); then one scale slot
+    // per stage: A atoms at +4*kg .. +4*kg+3, B atoms from +8, atom column kg
+    // at +8 + 4*SFB_ATOMS*kg (+4 per row block).
+    static constexpr int SFB_COL = 8;
+    static constexpr int SFB_COLS = 4 * SFB_ATOMS * KGS;
+    static constexpr int SLOT_COLS = (SFB_COL + SFB_COLS + 15) / 16 * 16;
     static constexpr int SF_COL0 = BN;
     static constexpr int USED_COLS = BN + STAGES * SLOT_COLS;
     static constexpr int TMEM_COLS = USED_COLS <= 256 ? 256 : 512;
@@ -91,11 +99,15 @@ struct MxConfig {
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
     static_assert(STAGES >= 4, "pipeline depth");
     static_assert(USED_COLS <= 512, "tensor memory");
-    static_assert(SFB_ATOMS * 4 <= 8, "B atoms fit the slot");
+    static_assert(4 * KGS <= SFB_COL, "A atoms fit below the B atoms");
 };
 
+// Per-MMA descriptor: scale ID kk (one scale per 32 K; FP8) or 2*(kk % 2)
+// (two per 64 K; FP4) for both operands.
+template <bool FP4>
 __device__ __forceinline__ uint32_t mx_idesc(uint32_t base, int kk) {
-    return base | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+    const uint32_t id = FP4 ? (uint32_t)((kk & 1) * 2) : (uint32_t)kk;
+    return base | (id << 4) | (id << 29);
 }
 
 template <Kind KD, int BN>
@@ -166,20 +178,28 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                 const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
-                // Scale atoms: this CTA's 128 A rows; all BN B rows.
+                // Scale atoms: this CTA's 128 A rows; all BN B rows.  An atom
+                // column past the last one (FP4 with an odd count) reads as zeros.
                 const int32_t sfa_rb = mb * 2 + (int32_t)half;
                 const int32_t sfb_rb = nb * C::SFB_ATOMS;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * C::STAGE_BYTES);
-                    tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK, arow, ab);
-                    tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK, brow, bb);
-                    tma_load_3d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, sfa_rb * nkb + kb, ab);
+                    tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK_UNITS, arow, ab);
+                    tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK_UNITS, brow, bb);
 #pragma unroll
-                    for (int a = 0; a < C::SFB_ATOMS; ++a)
-                        tma_load_3d_pair(sfb_stage(s) + a * C::ATOM_BYTES, &tmap_sfb, full_leader, 0,
-                                         (sfb_rb + a) * nkb + kb, bb);
+                    for (int g = 0; g < C::KGS; ++g) {
+                        const int32_t kg = kb * C::KGS + g;
+                        tma_load_3d_pair(sfa_stage(s) + g * C::ATOM_BYTES, &tmap_sfa, full_leader, 0,
+                                         kg, sfa_rb);
+#pragma unroll
+                        for (int a = 0; a < C::SFB_ATOMS; ++a)
+                            tma_load_3d_pair(sfb_stage(s) + (g * C::SFB_ATOMS + a) * C::ATOM_BYTES,
+                                             &tmap_sfb, full_leader, 0, kg, sfb_rb + a);
+                    }
+                    (void)ab;
+                    (void)bb;
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
@@ -204,17 +224,28 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                     if (!pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t slot = tmem_base + C::SF_COL0 + s * C::SLOT_COLS;
-                    tmem_cp_32x128b_x4_pair(slot, smem_desc_rows16(sfa_stage(s)));
 #pragma unroll
-                    for (int a = 0; a < C::SFB_ATOMS; ++a)
-                        tmem_cp_32x128b_x4_pair(slot + 8 + 4 * a,
-                                                smem_desc_rows16(sfb_stage(s) + a * C::ATOM_BYTES));
+                    for (int g = 0; g < C::KGS; ++g) {
+                        tmem_cp_32x128b_x4_pair(slot + 4 * g,
+                                                smem_desc_rows16(sfa_stage(s) + g * C::ATOM_BYTES));
+#pragma unroll
+                        for (int a = 0; a < C::SFB_ATOMS; ++a)
+                            tmem_cp_32x128b_x4_pair(
+                                slot + C::SFB_COL + 4 * (g * C::SFB_ATOMS + a),
+                                smem_desc_rows16(sfb_stage(s) + (g * C::SFB_ATOMS + a) * C::ATOM_BYTES));
+                    }
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
 #pragma unroll
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
-                        mma_mx_pair(tmem_base, smem_desc_sw128(a0 + kk * 32),
-                                    smem_desc_sw128(b0 + kk * 32), mx_idesc(C::IDESC, kk), slot,
-                                    slot + 8, (kb | kk) != 0);
+                        // Atom column of this MMA's scale blocks within the stage.
+                        const int g = C::FP4 ? kk >> 1 : 0;
+                        const uint32_t sfa = slot + 4 * g;
+                        const uint32_t sfb = slot + C::SFB_COL + 4 * C::SFB_ATOMS * g;
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
+                        const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
+                        const uint32_t id = mx_idesc<C::FP4>(C::IDESC, kk);
+                        if constexpr (C::FP4) mma_mxf4_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
+                        else mma_mx_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
                     }
                     mma_commit_pair_mcast(bar(C::EMPTY0 + s), 0x3);
                     if (++s == S) { s = 0; ph ^= 1; }

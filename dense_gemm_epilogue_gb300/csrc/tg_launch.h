@@ -30,10 +30,10 @@ cudaError_t launch_fp16(const LaunchArgs &a);
 cudaError_t launch_tf32(const LaunchArgs &a);
 cudaError_t launch_e4m3(const LaunchArgs &a);
 cudaError_t launch_e5m2(const LaunchArgs &a);
-// Block-scaled 8-bit float kernel (CTA pairs, block_n 128 or 256).
+// Block-scaled 8-bit / packed 4-bit float kernel (CTA pairs, block_n 128 or 256).
 cudaError_t launch_mx(const LaunchArgs &a, Kind kind);
 // Threads, shared memory, stages and tensor-memory columns of a block-scaled
 // configuration (0 when the configuration does not exist).
-void mx_config_numbers(int block_n, int *stages, int *smem, int *threads, int *tmem);
+void mx_config_numbers(Kind kind, int block_n, int *stages, int *smem, int *threads, int *tmem);
 
 }  // namespace tg

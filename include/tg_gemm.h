@@ -75,7 +75,8 @@ typedef enum {
     TG_FP16 = 1,  /* IEEE binary16 operands */
     TG_TF32 = 2,  /* FP32 storage, narrowed to TF32 in the kernel */
     TG_E4M3 = 3,  /* 8-bit float, 4 exponent / 3 fraction bits */
-    TG_E5M2 = 4   /* 8-bit float, 5 exponent / 2 fraction bits */
+    TG_E5M2 = 4,  /* 8-bit float, 5 exponent / 2 fraction bits */
+    TG_E2M1 = 5   /* 4-bit float (2 exponent / 1 fraction bits), two per byte; tg_gemm_mx only */
 } tg_dtype;
 
 /* Output element type of tg_gemm_batched ("Matrix Multiplication", Step 4:
@@ -210,9 +211,13 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
  *                                      sum_{k in block kb} a(i,k) * b(k,j)
  * where block kb covers k in [32*kb, 32*kb + 32) and each scale is a power of
  * two 2^(e-127) given by an 8-bit code e (e = 255 is NaN).  in_dtype is
- * TG_E4M3 or TG_E5M2 (both operands); A, B and D are laid out as for tg_gemm
- * (D of type out_dtype).  A and B must start 16-byte aligned and lda, ldb must
- * be multiples of 16 (no plain-load fallback here).
+ * TG_E4M3, TG_E5M2 or TG_E2M1 (both operands); A, B and D are laid out as for
+ * tg_gemm (D of type out_dtype).  A and B must start 16-byte aligned and their
+ * row strides (lda, ldb bytes) must be multiples of 16 (no plain-load
+ * fallback here).  TG_E2M1 (FP4: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) is
+ * packed two per byte, element 2t in the low nibble of byte t of its row;
+ * lda, ldb and K count elements and must be even (so lda, ldb are multiples
+ * of 32).
  *
  * Scales (SFA for the M rows of A, SFB for the N columns of B) are stored as
  * "scale atoms": with R rows and KB = ceil(K/32) blocks, atom (rb, kg), for

@@ -257,6 +257,9 @@ WORKLOADS = {
     # rounded to E4M3, one scale 2^e, e in [-7, 7], per 32 K elements.
     "mx_e4m3_8192": Workload("mx_e4m3_8192", 8192, 8192, 8192, "e4m3", 1.0, True, 8, "normal",
                              block_scaled=True),
+    # The same with packed E2M1 (FP4) operands: N(0,1) rounded to E2M1.
+    "mx_e2m1_8192": Workload("mx_e2m1_8192", 8192, 8192, 8192, "e2m1", 1.0, True, 9, "normal",
+                             block_scaled=True),
 }
 
 

@@ -19,7 +19,7 @@ import numpy as np
 import seeded_inputs as si
 
 TOL_REL = {"bf16": 2.0 ** -7, "fp16": 2.0 ** -7, "tf32": 2.0 ** -9, "e4m3": 2.0 ** -7,
-           "e5m2": 2.0 ** -7}
+           "e5m2": 2.0 ** -7, "e2m1": 2.0 ** -7}
 TOL_ABS = 1e-6
 
 
@@ -217,9 +217,11 @@ def to_atoms(S: np.ndarray, K: int) -> np.ndarray:
 
 
 def mx_padded(w: si.Workload):
-    """The workload with lda, ldb rounded up to multiples of 16 (TMA-legal)."""
-    r16 = lambda x: -(-max(x, 1) // 16) * 16
-    return si.with_shape(w, lda=w.lda or r16(w.K), ldb=w.ldb or r16(w.K))
+    """The workload with lda, ldb rounded up to TMA-legal strides: multiples
+    of 16 bytes (16 FP8 or 32 packed FP4 elements)."""
+    q = 32 if w.dtype == "e2m1" else 16
+    rq = lambda x: -(-max(x, 1) // q) * q
+    return si.with_shape(w, lda=w.lda or rq(w.K), ldb=w.ldb or rq(w.K))
 
 
 def run_mx(w: si.Workload, A, B, SA, SB, out="f32", opts=None, repeats=1, D0=None):

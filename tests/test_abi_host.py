@@ -269,6 +269,23 @@ def test_mx_invalid_arguments_rejected_before_cuda(tg, args):
     assert st == tg.TG_ERR_INVALID_VALUE
 
 
+@pytest.mark.parametrize("args", [
+    dict(lda=1025, ldb=1025), dict(K=1023, lda=1024, ldb=1024), dict(lda=1040), dict(ldb=1040),
+])
+def test_mx_fp4_layout_rules(tg, args):
+    """Packed FP4: even lda, ldb and K; row strides of 16-byte multiples."""
+    a = dict(M=10, N=10, K=1024, lda=1024, ldb=1024)
+    a.update(args)
+    st = tg.tg_gemm_mx(a["M"], a["N"], a["K"], 1.0, FAKE, a["lda"], FAKE, FAKE, a["ldb"], FAKE,
+                       FAKE, 10, "e2m1", "f32", 1)
+    assert st == tg.TG_ERR_INVALID_VALUE
+    # Only the block-scaled path takes FP4.
+    assert tg.tg_gemm(10, 10, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 10, "e2m1", True) == \
+        tg.TG_ERR_INVALID_VALUE
+    p = tg.tg_plan_mx(8192, 8192, 8192, 8192, 8192, 8192, "e2m1", None, 152)
+    assert (p["block_k"], p["stages"], p["tmem_cols"]) == (256, 6, 512)
+
+
 def test_mx_empty_output_is_ok_without_cuda(tg):
     assert tg.tg_gemm_mx(0, 10, 64, 1.0, None, 64, None, FAKE, 64, FAKE, None, 1, "e4m3", "f32",
                          True) == tg.TG_OK

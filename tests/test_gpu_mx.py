@@ -99,5 +99,39 @@ def test_mx_nan_scale_and_k_zero():
     assert float(D.abs().max()) == 0.0
 
 
-def test_mx_8192_full():
-    check_mx(si.WORKLOADS["mx_e4m3_8192"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1, 1, 2), (129, 65, 34), (300, 520, 1040),
+                                   (257, 255, 130), (513, 1000, 2048), (64, 1000, 512),
+                                   (300, 200, 384), (130, 260, 130), (200, 300, 4000)])
+def test_fp4_shapes(M, N, K):
+    """Packed E2M1 with block scales: ragged edges; K = 384 and 130 leave an
+    odd number of scale-atom columns (the last stage's second one is past
+    the end and reads as zeros)."""
+    w = si.Workload("mx_fp4", M, N, K, "e2m1", 1.5, True, 500 + M + N + K, "normal", ldc=M + 3)
+    check_mx(w, repeats=2)
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("swap", [1, 2])
+def test_fp4_tile_configs(block_n, swap):
+    w = si.Workload("mx_fp4_cfg", 600, 700, 1024, "e2m1", -0.75, False, 97, "normal")
+    check_mx(w, opts={"block_n": block_n, "swap_ab": swap})
+
+
+def test_fp4_narrow_outputs_and_nan_scale():
+    w = si.Workload("mx_fp4_out", 520, 600, 768, "e2m1", 0.5, True, 98, "normal")
+    check_mx(w, out="bf16")
+    check_mx(si.with_shape(w, seed=99, relu=False), out="fp16", scale_range=(122, 130))
+    w = mx_padded(si.Workload("mx_fp4_nan", 300, 200, 256, "e2m1", 1.0, True, 95, "normal"))
+    A, B = si.make_operands(w)
+    SA, SB = si.make_mx_scales(w)
+    SA[17, 3] = 255
+    SB[33, 0] = 255
+    _, outs = run_mx(w, A, B, SA, SB)
+    got = decode_out(outs[0][:, : w.M].view(np.float32).T, "f32")
+    assert np.all(np.isnan(got[17])) and np.all(np.isnan(got[:, 33]))
+    assert not np.any(np.isnan(np.delete(np.delete(got, 17, 0), 33, 1)))
+
+
+@pytest.mark.parametrize("name", ["mx_e4m3_8192", "mx_e2m1_8192"])
+def test_mx_8192_full(name):
+    check_mx(si.WORKLOADS[name])
