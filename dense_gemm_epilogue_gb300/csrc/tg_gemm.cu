@@ -701,15 +701,17 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
 }
 
 // Scale atoms of an operand with `rows` rows as a 3-D tensor of 32-bit words:
-// (128 words = one 512-byte atom, atom column kg, row block rb); one atom per
-// box, so a column or row block past the end reads as zeros.
-bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
+// (128 words = one 512-byte atom, atom column kg, row block rb); a box holds
+// `box_kg` x `box_rb` atoms (one K stage of one tile side), and columns or
+// row blocks past the end read as zeros.
+bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_kg,
+                   int box_rb) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int64_t kg = ceil_div(K, 128), rb = ceil_div(rows, tg::BLOCK_M);
     cuuint64_t dims[3] = {128, (cuuint64_t)kg, (cuuint64_t)rb};
     cuuint64_t strides[2] = {512, (cuuint64_t)(kg * 512)};
-    cuuint32_t box[3] = {128, 1, 1};
+    cuuint32_t box[3] = {128, (cuuint32_t)box_kg, (cuuint32_t)box_rb};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -746,10 +748,11 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     const void *ar = plan.swap ? q.B : q.A, *br = plan.swap ? q.A : q.B;
     const void *sar = plan.swap ? sfb : sfa, *sbr = plan.swap ? sfa : sfb;
     const int64_t ldar = plan.swap ? q.ldb : q.lda, ldbr = plan.swap ? q.lda : q.ldb;
+    const int kgs = block_k(q.t) / 128;  // scale-atom columns per K stage
     if (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, 1, 0, tg::BLOCK_M) ||
         !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, 1, 0, plan.block_n / 2) ||
-        !encode_scales(&la.map_sfa, sar, plan.mk, q.K) ||
-        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K))
+        !encode_scales(&la.map_sfa, sar, plan.mk, q.K, kgs, 1) ||
+        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, kgs, plan.block_n / tg::BLOCK_M))
         return TG_ERR_INVALID_VALUE;
     la.block_n = plan.block_n;
     la.pair = true;

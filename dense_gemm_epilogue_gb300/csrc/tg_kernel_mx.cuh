@@ -61,7 +61,7 @@ struct MxConfig {
     static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
     static constexpr int SFA_BYTES = KGS * ATOM_BYTES;   // [kg][atom]
-    static constexpr int SFB_BYTES = KGS * SFB_ATOMS * ATOM_BYTES;  // [kg][row block][atom]
+    static constexpr int SFB_BYTES = KGS * SFB_ATOMS * ATOM_BYTES;  // [row block][kg][atom]
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int FIT = (SMEM_LIMIT - 2048) / STAGE_BYTES;
     static constexpr int STAGES = FIT > 8 ? 8 : FIT;
@@ -188,16 +188,10 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * C::STAGE_BYTES);
                     tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK_UNITS, arow, ab);
                     tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK_UNITS, brow, bb);
-#pragma unroll
-                    for (int g = 0; g < C::KGS; ++g) {
-                        const int32_t kg = kb * C::KGS + g;
-                        tma_load_3d_pair(sfa_stage(s) + g * C::ATOM_BYTES, &tmap_sfa, full_leader, 0,
-                                         kg, sfa_rb);
-#pragma unroll
-                        for (int a = 0; a < C::SFB_ATOMS; ++a)
-                            tma_load_3d_pair(sfb_stage(s) + (g * C::SFB_ATOMS + a) * C::ATOM_BYTES,
-                                             &tmap_sfb, full_leader, 0, kg, sfb_rb + a);
-                    }
+                    // One box per operand: the stage's KGS atom columns of the
+                    // CTA's A row block, and of the tile's SFB_ATOMS B row blocks.
+                    tma_load_3d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, kb * C::KGS, sfa_rb);
+                    tma_load_3d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, kb * C::KGS, sfb_rb);
                     (void)ab;
                     (void)bb;
                     ++issued;
@@ -232,7 +226,7 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                         for (int a = 0; a < C::SFB_ATOMS; ++a)
                             tmem_cp_32x128b_x4_pair(
                                 slot + C::SFB_COL + 4 * (g * C::SFB_ATOMS + a),
-                                smem_desc_rows16(sfb_stage(s) + (g * C::SFB_ATOMS + a) * C::ATOM_BYTES));
+                                smem_desc_rows16(sfb_stage(s) + (a * C::KGS + g) * C::ATOM_BYTES));
                     }
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
 #pragma unroll
