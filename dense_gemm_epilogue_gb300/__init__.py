@@ -80,7 +80,8 @@ class tg_options(ctypes.Structure):
         ("l2_hint", ctypes.c_int32),
         ("prefetch_k", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("schedule", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
 

@@ -228,6 +228,7 @@ struct Plan {
     bool pair = false;  // CTA-pair kernel (256-row tiles over a 2-CTA cluster)
     int mc = 1;         // pair kernel: pairs per cluster (2: A rows multicast)
     int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
+    bool dynamic = false;  // pair kernel: one cluster per tile, launch-control stealing
     int64_t split_tiles = 0;
     int split_segs = 1;
     bool swap = false;
@@ -326,8 +327,11 @@ tg_status validate(const Problem &q, const tg_options *o) {
         if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
         if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->multicast < 0 || o->multicast > 2) return TG_ERR_INVALID_VALUE;
-        if (o->reserved[0] || o->reserved[1]) return TG_ERR_INVALID_VALUE;
+        if (o->schedule < 0 || o->schedule > 2 || o->reserved[0]) return TG_ERR_INVALID_VALUE;
         if (o->multicast == 2 && o->cta_pair == 1) return TG_ERR_INVALID_VALUE;
+        // The dynamic schedule runs CTA-pair tiles, one pair per cluster, whole tiles.
+        if (o->schedule == 2 && (o->cta_pair == 1 || o->multicast == 2 || o->split_k > 1))
+            return TG_ERR_INVALID_VALUE;
         // Overrides that cannot apply to this problem.
         const bool legal = tma_legal(q.A, q.lda, e) && tma_legal(q.B, q.ldb, e) &&
                            tma_batch_legal(q.sa, e, q.batch) && tma_batch_legal(q.sb, e, q.batch);
@@ -368,8 +372,10 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     // (8-bit kinds take 32 elements per 32-byte K step at twice the rate,
     // so the same per-byte costs apply.)
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
-    if (o->cta_pair == 2 && !pair_ok) return TG_ERR_INVALID_VALUE;
-    if (o->cta_pair == 2 && o->block_n == 64) return TG_ERR_INVALID_VALUE;
+    // The dynamic schedule runs CTA-pair tiles only.
+    const bool force_pair = o->cta_pair == 2 || o->schedule == 2;
+    if (force_pair && !pair_ok) return TG_ERR_INVALID_VALUE;
+    if (force_pair && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     // Pair tiles need a few K blocks to fill their 7-stage ring.
     const bool pair_auto = pair_ok && ceil_div(K, block_k(t)) >= 8;
     struct Cand { bool pair; int bn; };
@@ -377,10 +383,10 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     int nc = 0;
     // Ties go to single-CTA tiles, then to the wider tile.
     for (int bn : {256, 128, 64})
-        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 2) cands[nc++] = {false, bn};
+        if ((!o->block_n || o->block_n == bn) && !force_pair) cands[nc++] = {false, bn};
     for (int bn : {256, 128})
         if ((!o->block_n || o->block_n == bn) && o->cta_pair != 1 &&
-            (o->cta_pair == 2 ? pair_ok : pair_auto))
+            (force_pair ? pair_ok : pair_auto))
             cands[nc++] = {true, bn};
     int64_t best = -1;
     for (int i = 0; i < nc; ++i) {
@@ -444,7 +450,18 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         }
         p.grid = (int)(cl * pairs);
         split_rule(p.tiles, pairs, nkb, p.split_max, sms / 2, &p.split_tiles, &p.split_segs);
+        if (o->schedule == 2) {
+            // Dynamic: one cluster launched per tile; the hardware starts as
+            // many as fit and the running ones take over the rest.
+            if (p.mc != 1 || p.tiles > INT32_MAX / 2) return TG_ERR_INVALID_VALUE;
+            p.dynamic = true;
+            p.split_max = 1;
+            p.split_tiles = 0;
+            p.split_segs = 1;
+            p.grid = (int)(2 * p.tiles);
+        }
     } else {
+        if (o->schedule == 2) return TG_ERR_INVALID_VALUE;  // needs CTA-pair tiles
         int64_t grid = p.tiles < sms ? p.tiles : sms;
         if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
         p.grid = (int)(grid < 1 ? 1 : grid);
@@ -554,7 +571,8 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
         const bool ok = encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sar, a_box) &&
                         encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sbr, b_box);
         if (!ok) {
-            if (opts && (opts->producer == 1 || opts->cta_pair == 2)) return TG_ERR_INVALID_VALUE;
+            if (opts && (opts->producer == 1 || opts->cta_pair == 2 || opts->schedule == 2))
+                return TG_ERR_INVALID_VALUE;
             la.plain_loads = true;  // shapes the TMA unit cannot describe
             la.pair = false;
             plan.pair = false;
@@ -596,6 +614,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
     p.l2_hint = (opts && opts->l2_hint == 2) ? 1 : 0;
+    p.dynamic = la.pair && plan.dynamic ? 1 : 0;
     p.prefetch_k = (opts && opts->prefetch_k > 0) ? opts->prefetch_k : 0;
     if (la.pair && plan.split_segs > 1) {
         Workspace w;
@@ -636,7 +655,7 @@ bool mx_options_ok(const tg_options *o) {
     if (o->split_k < 0 || o->split_k > 1) return false;
     if (o->l2_hint || o->prefetch_k < -1 || o->prefetch_k > 0) return false;
     if (o->multicast < 0 || o->multicast > 1) return false;
-    return !o->reserved[0] && !o->reserved[1];
+    return o->schedule >= 0 && o->schedule <= 1 && !o->reserved[0];
 }
 
 tg_status validate_mx(const Problem &q, const void *sfa, const void *sfb, const tg_options *o) {

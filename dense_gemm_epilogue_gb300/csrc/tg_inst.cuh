@@ -61,7 +61,9 @@ static cudaError_t launch_pair(const LaunchArgs &a) {
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     int grid = a.grid - a.grid % CL;
-    const int cap = bit ? CL * max_clusters[a.device] : grid;
+    // A dynamic schedule launches one cluster per tile (not capped: clusters
+    // that do not fit wait, and running clusters may take over their tiles).
+    const int cap = bit && !a.p.dynamic ? CL * max_clusters[a.device] : grid;
     if (grid > cap) grid = cap;
     if (grid < CL) grid = CL;
     cfg.gridDim = dim3(grid, 1, 1);

@@ -121,6 +121,7 @@ enum WaitSite : uint32_t {
     SITE_CONVERTED = 5,
     SITE_DRAIN = 6,
     SITE_SELFTEST = 7,
+    SITE_SCHED = 10,
     SITE_PARTIAL = 8,
 };
 
@@ -164,6 +165,9 @@ struct GemmParams {
     int64_t stride_a, stride_b;     // elements between batch entries (role space)
     int64_t stride_d;               // output elements between batch entries
     int32_t a_bmul, b_bmul;
+    // CTA-pair kernel: 1 = dynamic schedule (one cluster launched per tile;
+    // running clusters take over clusters not yet started).
+    int32_t dynamic;
 };
 
 constexpr int BLOCK_M = 128;

@@ -53,14 +53,23 @@ struct PairConfig {
     static constexpr int BAR_OFF = B_OFF + STAGES * B_BYTES;
     static constexpr int FULL0 = 0, EMPTY0 = STAGES;
     static constexpr int ACCF0 = 2 * STAGES, ACCE0 = 2 * STAGES + 2, DRAIN = 2 * STAGES + 4;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    // Dynamic schedule: a ring of CLC_SLOTS launch-control answers, each with
+    // a full barrier (answer landed, in both CTAs) and an empty barrier (in
+    // the leader: every reader of both CTAs is done with it).
+    static constexpr int CLC_SLOTS = 4;
+    static constexpr int CLCF0 = 2 * STAGES + 5, CLCE0 = CLCF0 + CLC_SLOTS;
+    static constexpr int NUM_BARS = CLCE0 + CLC_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+    static constexpr int CLC_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
+    static constexpr int SMEM_BYTES = CLC_OFF + 16 * CLC_SLOTS + 1024;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quarter
     static constexpr int NUM_WARPS = 2 + EPI_WARPS;
     static constexpr int NUM_THREADS = NUM_WARPS * 32;
     static constexpr int MMAS_PER_STAGE = BK / T::umma_k;
+    // Readers of each answer: producer, MMA thread and epilogue warps of the
+    // leader; producer and epilogue warps of the peer.
+    static constexpr int CLC_READERS = 2 * (1 + EPI_WARPS) + 1;
     // Instruction descriptor as in the single-CTA kernel with M = 256.
     static constexpr uint32_t IDESC = (1u << 4) | (T::fmt << 7) | (T::fmt << 10) |
                                       ((uint32_t)(BN >> 3) << 17) |
@@ -210,6 +219,10 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             mbar_init(bar(C::ACCE0 + a), 2 * C::EPI_WARPS);
         }
         mbar_init(bar(C::DRAIN), 1);
+        for (int c = 0; c < C::CLC_SLOTS; ++c) {
+            mbar_init(bar(C::CLCF0 + c), 1);
+            mbar_init(bar(C::CLCE0 + c), C::CLC_READERS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmap_a);
@@ -225,6 +238,33 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
     const UnitPlan up = make_unit_plan(p, num_pairs);
+    // Work sequence.  Static: units pair, pair + P, ...  Dynamic (MC == 1,
+    // no split): this cluster's own tile, then the tile of each cluster that
+    // launch control cancelled for it, until an answer says none was left.
+    const bool dyn = MC == 1 && p.dynamic != 0;
+    const int64_t first_unit = dyn ? (int64_t)(blockIdx.x / 2) : pair;
+    // Read answer `step` (waiting for it), release its slot, return the next
+    // unit (-1: no more work; -2: the wait gave up).  One thread per reader.
+    auto clc_read = [&](int64_t step) -> int64_t {
+        const int slot = (int)(step % C::CLC_SLOTS);
+        int64_t next = -2;
+        if (pair_wait(bar(C::CLCF0 + slot), (uint32_t)((step / C::CLC_SLOTS) & 1), ctl,
+                      SITE_SCHED)) {
+            const volatile uint64_t *r =
+                reinterpret_cast<const volatile uint64_t *>(smem + C::CLC_OFF + 16 * slot);
+            const int32_t x = clc_cancelled_x(r[0], r[1]);
+            next = x >= 0 ? (int64_t)(x / 2) : -1;
+        }
+        if (leader) mbar_arrive(bar(C::CLCE0 + slot));
+        else mbar_arrive_cluster(map_shared_rank(bar(C::CLCE0 + slot), lead_rank));
+        return next;
+    };
+    // The same for a whole warp: lane 0 reads, every lane gets the result.
+    auto clc_read_warp = [&](int64_t step) -> int64_t {
+        int64_t next = 0;
+        if (lane == 0) next = clc_read(step);
+        return __shfl_sync(0xffffffffu, next, 0);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ producer (both CTAs)
@@ -234,7 +274,23 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t u = pair; ok && u < up.units; u += num_pairs) {
+            int64_t step = 0;
+            for (int64_t u = first_unit; ok && u >= 0 && u < up.units;) {
+                if (dyn) {
+                    // Ask for the unit after this one (answer `step`), into a
+                    // slot all readers have released.
+                    const int slot = (int)(step % C::CLC_SLOTS);
+                    mbar_arrive_expect_tx(bar(C::CLCF0 + slot), 16);
+                    if (leader) {
+                        if (step >= C::CLC_SLOTS &&
+                            !pair_wait(bar(C::CLCE0 + slot),
+                                       (uint32_t)(((step / C::CLC_SLOTS) - 1) & 1), ctl, SITE_SCHED)) {
+                            ok = false;
+                            break;
+                        }
+                        clc_try_cancel_all(sbase + C::CLC_OFF + 16 * slot, bar(C::CLCF0 + slot));
+                    }
+                }
                 const Unit un = decode_unit(up, u, nkb);
                 int bt, mb, nbc;
                 batch_tile_coords(un.tile, p, bt, mb, nbc);
@@ -265,6 +321,8 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
+                if (!ok) break;
+                u = dyn ? clc_read(step++) : u + num_pairs;
             }
             if (!ok && issued) {
                 // Copies already issued land within microseconds; let them
@@ -281,7 +339,8 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             uint32_t ph = 0;
             uint32_t tl = 0;
             bool ok = true;
-            for (int64_t u = pair; ok && u < up.units; u += num_pairs, ++tl) {
+            int64_t step = 0;
+            for (int64_t u = first_unit; ok && u >= 0 && u < up.units; ++tl) {
                 const Unit un = decode_unit(up, u, nkb);
                 const uint32_t acc = tl & 1, use = tl >> 1;
                 if (!pair_wait(bar(C::ACCE0 + acc), (use & 1) ^ 1, ctl, SITE_ACC_EMPTY)) {
@@ -306,6 +365,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit_pair_mcast(bar(C::ACCF0 + acc), pair_ctas);
+                u = dyn ? clc_read(step++) : u + num_pairs;
             }
             if (!ok) {
                 mma_commit_pair_mcast(bar(C::DRAIN), (uint16_t)(1u << rank));
@@ -328,7 +388,8 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         constexpr int COLS = BN / (C::EPI_WARPS / 4);  // columns of this warp
         const int cbase = ((warp - 2) / 4) * COLS;
         uint32_t tl = 0;
-        for (int64_t u = pair; u < up.units; u += num_pairs, ++tl) {
+        int64_t step = 0;
+        for (int64_t u = first_unit; u >= 0 && u < up.units; ++tl) {
             const Unit un = decode_unit(up, u, nkb);
             int bt, mb, nbc;
             batch_tile_coords(un.tile, p, bt, mb, nbc);
@@ -419,6 +480,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 if (leader) mbar_arrive(bar(C::ACCE0 + acc));
                 else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE0 + acc), lead_rank));
             }
+            u = dyn ? clc_read_warp(step++) : u + num_pairs;
         }
     }
 

@@ -337,6 +337,34 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t
                  : "memory");
 }
 
+// Cluster launch control: ask the hardware to cancel the launch of one
+// cluster of this grid that has not started yet; the 16-byte answer lands at
+// `resp` (same offset in every CTA of this cluster), completing 16
+// transaction bytes on the barrier at `bar` (same offset in every CTA).
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+        ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// Decode an answer: the x index of the first CTA of the cancelled cluster,
+// or -1 if nothing was cancelled (no cluster left to take).
+__device__ __forceinline__ int32_t clc_cancelled_x(uint64_t lo, uint64_t hi) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "mov.b128 r, {%2, %3};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "l"(lo), "l"(hi)
+        : "memory");
+    return ok ? (int32_t)x : -1;
+}
+
 // One arrival on the barrier at the same offset in every CTA of `mask` once
 // the pair's previously issued tcgen05 operations complete.
 __device__ __forceinline__ void mma_commit_pair_mcast(uint32_t bar, uint16_t mask) {

@@ -136,7 +136,11 @@ typedef struct {
                              rows n K blocks ahead into L2, 4 blocks per burst */
     int32_t multicast;    /* 0: planner; 1: one CTA pair per cluster; 2: two pairs per cluster
                              sharing their A-role rows by TMA multicast (CTA-pair tiles) */
-    int32_t reserved[2];  /* must be zero */
+    int32_t schedule;     /* 0: planner (static); 1: static persistent tiles; 2: dynamic: one
+                             2-CTA cluster per tile, running clusters take over clusters not
+                             yet started (cluster launch control); CTA-pair tiles, no split-K,
+                             no multicast */
+    int32_t reserved[1];  /* must be zero */
 } tg_options;
 
 /* What the planner chose for one problem (host only; no CUDA call). */

@@ -65,7 +65,9 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
     dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
-    dict(opts={"reserved": [0, 1]}), dict(opts={"multicast": 3}),
+    dict(opts={"reserved": [1]}), dict(opts={"multicast": 3}), dict(opts={"schedule": 3}),
+    dict(opts={"schedule": 2, "cta_pair": 1}), dict(opts={"schedule": 2, "multicast": 2}),
+    dict(opts={"schedule": 2, "split_k": 2}),
     dict(opts={"multicast": 2, "cta_pair": 1}),
     dict(opts={"cta_pair": 3}), dict(opts={"cta_pair": 2, "block_n": 64}),
     dict(dtype=2, opts={"cta_pair": 2}),
@@ -305,3 +307,18 @@ def test_plan_mx(tg):
     assert small["grid"] == 2 * small["tiles"]
     with pytest.raises(tg.TgError):
         tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", None, 152)   # lda not 16-byte multiple
+
+
+def test_plan_dynamic_schedule(tg):
+    """schedule = 2: CTA-pair tiles, one 2-CTA cluster launched per tile."""
+    c4 = si.WORKLOADS["c4_bf16_8192"]
+    p = plan(tg, c4, opts={"schedule": 2})
+    assert p["cta_pair"] == 1 and p["grid"] == 2 * p["tiles"] == 2048
+    assert (p["split_segs"], p["multicast"]) == (1, 1)
+    small = plan(tg, si.Workload("s", 500, 500, 2048, "bf16", 1.0, True, 0, "normal"),
+                 opts={"schedule": 2, "cta_pair": 2})
+    assert small["split_segs"] == 1 and small["grid"] == 2 * small["tiles"]
+    with pytest.raises(tg.TgError):      # plain loads: no pair tiles
+        plan(tg, si.WORKLOADS["c1_bf16_65x97x73"], opts={"schedule": 2})
+    with pytest.raises(tg.TgError):      # TF32 has no pair tiles
+        plan(tg, si.WORKLOADS["c2_tf32_256x128x512"], opts={"schedule": 2})

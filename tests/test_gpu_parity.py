@@ -237,3 +237,24 @@ def test_large_configs_full(name):
 def test_headline_8192_full():
     """The 8192^3 BF16 + ReLU workload, every element against the oracle."""
     check_full(si.WORKLOADS["c4_bf16_8192"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "e4m3"])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 1024), (1100, 1300, 640), (257, 4000, 512),
+                                   (1, 17, 64), (2000, 2000, 2048)])
+def test_dynamic_schedule(dtype, M, N, K):
+    """One 2-CTA cluster per tile; running clusters take over the tiles of
+    clusters not yet started (cluster launch control).  Every tile exactly
+    once: full parity, bitwise repeatable."""
+    w = si.Workload("dyn", M, N, K, dtype, 1.25, True, 61 + M + N, "normal", ldc=M + 5)
+    check_full(w, opts={"schedule": 2}, repeats=3)
+
+
+def test_dynamic_schedule_swapped_batched_narrow():
+    from gemm_harness import check_batched
+
+    ws = si.Workload("dyn_s", 100, 3000, 512, "bf16", 1.0, False, 62, "uniform", ldc=104)
+    check_full(ws, opts={"schedule": 2, "swap_ab": 2})
+    wb = si.Workload("dyn_b", 600, 700, 1024, "fp16", -1.0, True, 63, "normal")
+    check_batched(wb, 3, "bf16", opts={"schedule": 2})
+    check_batched(wb, 2, "f32", share_a=True, opts={"schedule": 2, "block_n": 128})
