@@ -238,6 +238,12 @@ def test_plan_multicast_clusters(tg):
     assert two["tiles"] * 2 == one["tiles"] and two["grid"] % 4 == 0 and two["grid"] == 152
     assert two["split_segs"] == 1
     assert plan(tg, w, opts={"cta_pair": 1})["multicast"] == 0
+    # The planner's own choice: short K loops over several waves share A rows.
+    c5c = plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])
+    assert c5c["cta_pair"] == 1 and c5c["multicast"] == 2 and c5c["grid"] % 4 == 0
+    assert plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"], opts={"multicast": 1})["multicast"] == 1
+    assert plan(tg, w)["multicast"] == 1                                   # 128 K blocks
+    assert plan(tg, si.WORKLOADS["c3_fp16_4096"])["multicast"] == 1        # 64 K blocks
     # A single N block leaves nothing to share.
     narrow = si.Workload("n", 4096, 200, 4096, "bf16", 1.0, True, 0, "normal")
     with pytest.raises(tg.TgError):
