@@ -12,6 +12,7 @@ rational brute force, hand-worked examples under ``tests/golden/``), and
 """
 
 from .oracle import (  # noqa: F401
+    EPI_KINDS,
     Oracle,
     build,
     compile_source,
@@ -20,6 +21,7 @@ from .oracle import (  # noqa: F401
     default,
     gemm,
     gemm_entries,
+    gemm_epi,
     gemm_mx,
     host_threads,
     library_path,

@@ -23,6 +23,8 @@ _STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np
 # Elements per storage unit (E2M1: two per byte, low nibble first).
 _PER_UNIT = {"e2m1": 2}
 _OUT_CODE = {"f32": 0, "bf16": 1, "fp16": 2}
+EPI_KINDS = {"scale": 0, "add": 1, "relu": 2, "leaky_relu": 3, "clamp": 4, "sigmoid": 5,
+             "silu": 6, "gelu_tanh": 7, "bias_row": 8, "bias_col": 9}
 GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread"]
 
 _lock = threading.Lock()
@@ -77,6 +79,9 @@ class Oracle:
         lib.orc_gemm_mx.restype = ip
         lib.orc_decode_e8m0_array.argtypes = [vp, i64, vp]
         lib.orc_decode_e8m0_array.restype = None
+        lib.orc_gemm_epi.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, ip, vp, vp, vp, vp, ip,
+                                     vp, i64, vp, ip]
+        lib.orc_gemm_epi.restype = ip
         lib.orc_num_host_threads.argtypes = []
         lib.orc_num_host_threads.restype = ip
         self.lib = lib
@@ -144,6 +149,31 @@ class Oracle:
         self.lib.orc_decode_e8m0_array(x.ctypes.data, x.size, out.ctypes.data)
         return out
 
+    def gemm_epi(self, M, N, K, alpha, A, lda, B, ldb, dtype, ops, with_scale=False, threads=0):
+        """D_ref with a composed pointwise epilogue: y = alpha * s, then each
+        op of ``ops`` in order; an op is (kind, a, b, bias) with kind a name
+        of EPI_KINDS and bias a float32 array (or None)."""
+        A = _check_storage(A, dtype, "A")
+        B = _check_storage(B, dtype, "B")
+        n = len(ops)
+        kinds = np.array([EPI_KINDS[o[0]] for o in ops] or [0], dtype=np.int32)
+        av = np.array([float(o[1]) for o in ops] or [0.0], dtype=np.float64)
+        bv = np.array([float(o[2]) for o in ops] or [0.0], dtype=np.float64)
+        keep = [np.ascontiguousarray(o[3], dtype=np.float32) if o[3] is not None else None
+                for o in ops]
+        ptrs = (ctypes.c_void_p * max(n, 1))(*[k.ctypes.data if k is not None else None
+                                               for k in keep] or [None])
+        Dt = np.zeros((max(N, 0), max(M, 0)), dtype=np.float64)
+        St = np.zeros_like(Dt) if with_scale else None
+        rc = self.lib.orc_gemm_epi(M, N, K, float(alpha), A.ctypes.data, lda, B.ctypes.data, ldb,
+                                   _DTYPE_CODE[dtype], kinds.ctypes.data, av.ctypes.data,
+                                   bv.ctypes.data, ctypes.cast(ptrs, ctypes.c_void_p), n,
+                                   Dt.ctypes.data, max(M, 1),
+                                   St.ctypes.data if St is not None else None, int(threads))
+        if rc != 0:
+            raise ValueError(f"orc_gemm_epi failed with {rc}")
+        return (Dt.T, St.T) if with_scale else Dt.T
+
     def gemm_entries(self, M, N, K, alpha, A, lda, B, ldb, dtype, relu, I, J, threads=0):
         """D_ref and |alpha|*sum|a||b| at coordinates (I[q], J[q])."""
         A = _check_storage(A, dtype, "A")
@@ -202,6 +232,10 @@ def gemm_entries(*args, **kw):
 
 def gemm_mx(*args, **kw):
     return default().gemm_mx(*args, **kw)
+
+
+def gemm_epi(*args, **kw):
+    return default().gemm_epi(*args, **kw)
 
 
 def decode_scale(codes):

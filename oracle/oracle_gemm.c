@@ -500,6 +500,75 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
     return 0;
 }
 
+/* ---------------- composed pointwise epilogues ---------------- */
+
+/*
+ * "Walk through GEMM", section 5 applies the epilogue as a pointwise map of
+ * the accumulator, and "Tylo README" lists composed epilogues among its
+ * worked consumers: elementwise functions keep each value where it is, so a
+ * chain of them runs where the accumulator is.  orc_gemm_epi computes
+ *   y = alpha * s  (s as in orc_gemm), then y = op_n(... op_1(y)),
+ * every op in double, and reports y.  Ops (kind, a, b, bias):
+ *   0 SCALE      y = a * y
+ *   1 ADD        y = y + a
+ *   2 RELU       y = max(y, 0)  (Julia's max: NaN stays, -0 becomes +0)
+ *   3 LEAKY      y > 0 ? y : a * y   (NaN stays)
+ *   4 CLAMP      min(max(y, a), b)   (NaN stays)
+ *   5 SIGMOID    1 / (1 + exp(-y))
+ *   6 SILU       y / (1 + exp(-y))
+ *   7 GELU_TANH  y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 y^3)))
+ *                (the tanh form of the Gaussian error linear unit,
+ *                Hendrycks and Gimpel)
+ *   8 BIAS_ROW   y = y + bias[i]   (one value per output row)
+ *   9 BIAS_COL   y = y + bias[j]   (one value per output column)
+ * The scale output is |alpha| * sum_k |a||b| as in orc_gemm (the bound of
+ * the product before the ops).
+ */
+enum { ORC_EPI_SCALE = 0, ORC_EPI_ADD, ORC_EPI_RELU, ORC_EPI_LEAKY, ORC_EPI_CLAMP, ORC_EPI_SIGMOID,
+       ORC_EPI_SILU, ORC_EPI_GELU_TANH, ORC_EPI_BIAS_ROW, ORC_EPI_BIAS_COL, ORC_EPI_KINDS };
+
+static double apply_op(int kind, double a, double b, const float *bias, int64_t i, int64_t j,
+                       double y) {
+    switch (kind) {
+    case ORC_EPI_SCALE: return a * y;
+    case ORC_EPI_ADD: return y + a;
+    case ORC_EPI_RELU: return relu_max(y);
+    case ORC_EPI_LEAKY: return (isnan(y) || y > 0.0) ? y : a * y;
+    case ORC_EPI_CLAMP:  /* both comparisons are false for NaN, which stays */
+        if (y < a) y = a;
+        if (y > b) y = b;
+        return y;
+    case ORC_EPI_SIGMOID: return 1.0 / (1.0 + exp(-y));
+    case ORC_EPI_SILU: return y / (1.0 + exp(-y));
+    case ORC_EPI_GELU_TANH:
+        return 0.5 * y * (1.0 + tanh(sqrt(2.0 / M_PI) * (y + 0.044715 * y * y * y)));
+    case ORC_EPI_BIAS_ROW: return y + (double)bias[i];
+    case ORC_EPI_BIAS_COL: return y + (double)bias[j];
+    default: return NAN;
+    }
+}
+
+int orc_gemm_epi(int64_t M, int64_t N, int64_t K, double alpha,
+                 const void *A, int64_t lda, const void *B, int64_t ldb, int dtype,
+                 const int *kinds, const double *as, const double *bs, const float *const *biases,
+                 int n_ops, double *D, int64_t ldd, double *scale, int nthreads) {
+    if (n_ops < 0) return -1;
+    for (int q = 0; q < n_ops; ++q) {
+        if (kinds[q] < 0 || kinds[q] >= ORC_EPI_KINDS) return -1;
+        if ((kinds[q] == ORC_EPI_BIAS_ROW || kinds[q] == ORC_EPI_BIAS_COL) && !biases[q]) return -1;
+    }
+    /* The product alpha * s first (no ReLU), then the chain. */
+    int rc = orc_gemm(M, N, K, alpha, A, lda, B, ldb, dtype, 0, D, ldd, scale, nthreads);
+    if (rc != 0) return rc;
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t i = 0; i < M; ++i) {
+            double y = D[i + j * ldd];
+            for (int q = 0; q < n_ops; ++q) y = apply_op(kinds[q], as[q], bs[q], biases[q], i, j, y);
+            D[i + j * ldd] = y;
+        }
+    return 0;
+}
+
 /* Decode an array of scale codes (for the decode pins). */
 void orc_decode_e8m0_array(const uint8_t *src, int64_t n, double *dst) {
     for (int64_t q = 0; q < n; ++q) dst[q] = orc_decode_e8m0(src[q]);

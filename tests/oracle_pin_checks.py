@@ -658,6 +658,76 @@ def check_mx_nan_scale(orc):
     assert np.all(D[[0, 2]][:, [0, 1, 3]] == 32.0)
 
 
+# ---------------------------------------------------------------- composed pointwise epilogues
+
+def _epi_identity_case(vals):
+    """A = I (M = K), B holding `vals` (K x N, exact BF16): s(i,j) = vals[i, j]."""
+    M, N = vals.shape
+    A = bf16_bits_exact(np.eye(M)).reshape(M, M)
+    B = np.ascontiguousarray(bf16_bits_exact(vals.T))   # column j of B as row j
+    return M, N, A, B
+
+
+def run_epi(orc, vals, ops, alpha=1.0):
+    M, N, A, B = _epi_identity_case(vals)
+    return orc.gemm_epi(M, N, M, alpha, A, M, B, M, "bf16", ops)
+
+
+def check_epi_pointwise_forms(orc):
+    """Each op against its closed form at landmark points and its invariants."""
+    ys = np.array([[-8.0, -2.0, -0.5, 0.0], [0.25, 1.0, 3.0, 10.0]])
+    neg = -ys
+    assert np.array_equal(run_epi(orc, ys, [("scale", -1.5, 0, None)]), -1.5 * ys)
+    assert np.array_equal(run_epi(orc, ys, [("add", 0.75, 0, None)]), ys + 0.75)
+    r = run_epi(orc, ys, [("relu", 0, 0, None)])
+    assert np.array_equal(r, np.maximum(ys, 0.0)) and not np.any(np.signbit(r))
+    assert np.array_equal(run_epi(orc, ys, [("leaky_relu", 0.125, 0, None)]),
+                          np.where(ys > 0, ys, 0.125 * ys))
+    assert np.array_equal(run_epi(orc, ys, [("clamp", -1.0, 2.0, None)]), np.clip(ys, -1.0, 2.0))
+    sg, sgn = run_epi(orc, ys, [("sigmoid", 0, 0, None)]), run_epi(orc, neg, [("sigmoid", 0, 0, None)])
+    assert sg[0, 3] == 0.5 and np.allclose(sg + sgn, 1.0, rtol=0, atol=1e-15)
+    assert np.all((sg > 0) & (sg < 1)) and np.all(np.diff(sg[1]) > 0)
+    si_ = run_epi(orc, ys, [("silu", 0, 0, None)])
+    assert si_[0, 3] == 0.0 and np.allclose(si_, ys * sg, rtol=1e-15, atol=0)    # silu = y sigmoid(y)
+    ge, gen = run_epi(orc, ys, [("gelu_tanh", 0, 0, None)]), run_epi(orc, neg, [("gelu_tanh", 0, 0, None)])
+    assert ge[0, 3] == 0.0 and np.allclose(ge - gen, ys, rtol=0, atol=1e-14)      # odd tanh
+    assert abs(ge[1, 3] - 10.0) < 1e-12 and abs(ge[0, 0]) < 1e-12                  # tails
+    # Slope at 0 is 1/2; the cubic term bends it by 0.044715 * sqrt(2/pi) at small y.
+    small = np.array([[1.0 / 1024, 1.0 / 256, 1.0 / 64, 1.0 / 16]])
+    g = run_epi(orc, small, [("gelu_tanh", 0, 0, None)])
+    k = math.sqrt(2.0 / math.pi)
+    for y, gy in zip(small[0], g[0]):
+        series = 0.5 * y + 0.5 * k * y * y + 0.5 * k * 0.044715 * y ** 4 - k ** 3 * y ** 4 / 6
+        assert abs(gy - series) < 1e-6 * y ** 2, (y, gy, series)
+
+
+def check_epi_composition_and_bias(orc):
+    """Ops apply in list order after alpha; row biases follow i, column biases j."""
+    rng = np.random.default_rng(37)
+    vals = rng.integers(-8, 9, size=(5, 7)) / 8.0
+    a1 = run_epi(orc, vals, [("scale", 2.0, 0, None), ("add", 1.0, 0, None)])
+    a2 = run_epi(orc, vals, [("add", 1.0, 0, None), ("scale", 2.0, 0, None)])
+    assert np.array_equal(a1, 2 * vals + 1) and np.array_equal(a2, 2 * vals + 2)
+    al = run_epi(orc, vals, [("relu", 0, 0, None)], alpha=-1.0)
+    assert np.array_equal(al, np.maximum(-vals, 0.0))
+    br = np.arange(5, dtype=np.float32) * 0.5
+    bc = np.arange(7, dtype=np.float32) * -0.25
+    d = run_epi(orc, vals, [("bias_row", 0, 0, br), ("bias_col", 0, 0, bc)])
+    assert np.array_equal(d, vals + br[:, None] + bc[None, :])
+    assert np.array_equal(run_epi(orc, vals, []), vals)
+
+
+def check_epi_nan(orc):
+    """NaN passes the max-style ops (ReLU, leaky, clamp) as in the ReLU epilogue."""
+    M, N = 3, 2
+    A = bf16_bits_exact(np.eye(M)).reshape(M, M)
+    B = np.ascontiguousarray(bf16_bits_exact(np.ones((N, M))))
+    A[1, 1] = np.uint16(0x7FC0)
+    for op in (("relu", 0, 0, None), ("leaky_relu", 0.5, 0, None), ("clamp", -1.0, 1.0, None)):
+        d = orc.gemm_epi(M, N, M, 1.0, A, M, B, M, "bf16", [op])
+        assert np.all(np.isnan(d[1])) and not np.any(np.isnan(d[[0, 2]])), op
+
+
 ALL_CHECKS = [
     check_decode_tables,
     check_tf32_narrowing,
@@ -682,4 +752,7 @@ ALL_CHECKS = [
     check_mx_block_boundaries,
     check_mx_scale_invariances,
     check_mx_nan_scale,
+    check_epi_pointwise_forms,
+    check_epi_composition_and_bias,
+    check_epi_nan,
 ]

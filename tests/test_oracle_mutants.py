@@ -47,6 +47,19 @@ MUTANTS = {
                          "return orc_decode_e2m1((idx & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4));"),
     "e2m1_subnormal": ("double v = (e == 0) ? ldexp((double)f, -1)", "double v = (e == 0) ? ldexp((double)f, -2)"),
     "e2m1_bias": ("ldexp((double)(2 + f), e - 1 - 1);", "ldexp((double)(2 + f), e - 2 - 1);"),
+    "epi_bias_row_by_column": ("case ORC_EPI_BIAS_ROW: return y + (double)bias[i];",
+                               "case ORC_EPI_BIAS_ROW: return y + (double)bias[j];"),
+    "epi_gelu_constant": ("(y + 0.044715 * y * y * y)", "(y + 0.04 * y * y * y)"),
+    "epi_silu_as_sigmoid": ("case ORC_EPI_SILU: return y / (1.0 + exp(-y));",
+                            "case ORC_EPI_SILU: return 1.0 / (1.0 + exp(-y));"),
+    "epi_reverse_order": ("for (int q = 0; q < n_ops; ++q) y = apply_op(kinds[q], as[q], bs[q], biases[q], i, j, y);",
+                          "for (int q = n_ops - 1; q >= 0; --q) y = apply_op(kinds[q], as[q], bs[q], biases[q], i, j, y);"),
+    "epi_leaky_scales_positive": ("case ORC_EPI_LEAKY: return (isnan(y) || y > 0.0) ? y : a * y;",
+                                  "case ORC_EPI_LEAKY: return a * y;"),
+    "epi_clamp_bounds_swapped": ("        if (y < a) y = a;\n        if (y > b) y = b;",
+                                 "        if (y < b) y = b;\n        if (y > a) y = a;"),
+    "epi_alpha_after": ("int rc = orc_gemm(M, N, K, alpha, A, lda, B, ldb, dtype, 0, D, ldd, scale, nthreads);",
+                        "int rc = orc_gemm(M, N, K, 1.0, A, lda, B, ldb, dtype, 0, D, ldd, scale, nthreads);"),
     "mx_block_16": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 16"),
     "mx_block_64": ("#define ORC_MX_BLOCK 32", "#define ORC_MX_BLOCK 64"),
     "mx_scale_bias": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 128);"),
