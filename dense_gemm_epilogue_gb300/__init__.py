@@ -54,6 +54,7 @@ EXPORTED = (
     "tg_version",
     "tg_gemm_noalloc",
     "tg_gemm_batched",
+    "tg_gemm_epilogue",
     "tg_gemm_mx",
     "tg_plan_mx",
     "tg_mx_scale_bytes",
@@ -82,6 +83,19 @@ class tg_options(ctypes.Structure):
         ("multicast", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
         ("reserved", ctypes.c_int32 * 1),
+    ]
+
+
+EPI_KINDS = {"scale": 0, "add": 1, "relu": 2, "leaky_relu": 3, "clamp": 4, "sigmoid": 5,
+             "silu": 6, "gelu_tanh": 7, "bias_row": 8, "bias_col": 9}
+
+
+class tg_epi_op(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("a", ctypes.c_float),
+        ("b", ctypes.c_float),
+        ("bias", ctypes.c_void_p),
     ]
 
 
@@ -147,6 +161,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                         i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(tg_options), vp]
         lib.tg_gemm_batched.restype = ctypes.c_int
+        lib.tg_gemm_epilogue.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, vp, i64,
+                                         ctypes.c_int, ctypes.c_int, ctypes.POINTER(tg_epi_op),
+                                         i32, ctypes.POINTER(tg_options), vp]
+        lib.tg_gemm_epilogue.restype = ctypes.c_int
         lib.tg_gemm_mx.argtypes = [i64, i64, i64, f32, vp, i64, vp, vp, i64, vp, vp, i64,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(tg_options), vp]
@@ -250,6 +268,22 @@ def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):
     if st != TG_OK:
         raise TgError(st, "tg_plan")
     return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
+
+
+def tg_gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, out_dtype, ops,
+                     opts=None, stream=None) -> int:
+    """D = out(op_n(... op_1(alpha * A B))); ops: sequence of (kind, a, b, bias)
+    with kind a name of EPI_KINDS (or its code) and bias a device tensor or None."""
+    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+    arr = (tg_epi_op * max(len(ops), 1))()
+    for q, (kind, a, b, bias) in enumerate(ops):
+        arr[q].kind = EPI_KINDS[kind] if isinstance(kind, str) else int(kind)
+        arr[q].a = float(a)
+        arr[q].b = float(b)
+        arr[q].bias = _ptr(bias)
+    return load().tg_gemm_epilogue(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
+                                   _dtype(in_dtype), out, arr, len(ops), _options(opts),
+                                   _stream(stream))
 
 
 def tg_gemm_mx(M, N, K, alpha, A, lda, SFA, B, ldb, SFB, D, ldc, in_dtype, out_dtype, epilogue,

@@ -27,13 +27,15 @@ namespace tg {
 // (empty sums), in the output format.
 __global__ void tg_fill_empty_sum_kernel(void *d, int64_t m, int64_t n, int64_t ldc,
                                          int64_t stride_d, int64_t batch, int out_fmt, float alpha,
-                                         int relu) {
-    const float v = apply_epilogue(0.0f, alpha, relu);
+                                         int relu, const EpiProgram prog) {
+    const float v0 = apply_epilogue(0.0f, alpha, relu);
     const int64_t per = m * n, total = per * batch;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t b = i / per, e = i - b * per;
         const int64_t off = b * stride_d + (e % m) + (e / m) * ldc;
+        float v = v0;
+        for (int q = 0; q < prog.n; ++q) v = epi_op(prog.op[q], v, e % m, e / m);
         if (out_fmt == 0) static_cast<float *>(d)[off] = v;
         else if (out_fmt == 1) static_cast<unsigned short *>(d)[off] = OutFormat<1>::cvt(v);
         else static_cast<unsigned short *>(d)[off] = OutFormat<2>::cvt(v);
@@ -530,7 +532,29 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
     return r == CUDA_SUCCESS;
 }
 
-tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *stream_ptr) {
+// A composed epilogue from the caller's op list (checked: count, kinds,
+// bias pointers present and float-aligned).
+tg_status make_program(const tg_epi_op *ops, int32_t n_ops, tg::EpiProgram *prog) {
+    std::memset(prog, 0, sizeof(*prog));
+    if (n_ops < 0 || n_ops > tg::EPI_MAX_OPS || (n_ops > 0 && !ops)) return TG_ERR_INVALID_VALUE;
+    for (int q = 0; q < n_ops; ++q) {
+        const tg_epi_op &o = ops[q];
+        if (o.kind < 0 || o.kind >= tg::EPI_KINDS) return TG_ERR_INVALID_VALUE;
+        const bool bias = o.kind == TG_EPI_BIAS_ROW || o.kind == TG_EPI_BIAS_COL;
+        if (bias && (!o.bias || (uintptr_t)o.bias % 4)) return TG_ERR_INVALID_VALUE;
+        prog->op[q].kind = o.kind;
+        prog->op[q].a = o.a;
+        prog->op[q].b = o.b;
+        prog->op[q].bias = bias ? o.bias : nullptr;
+    }
+    prog->n = n_ops;
+    return TG_OK;
+}
+
+tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *stream_ptr,
+              const tg::EpiProgram *prog = nullptr) {
+    static const tg::EpiProgram kNoOps = {};
+    if (!prog) prog = &kNoOps;
     if (epi != TG_EPILOGUE_NONE && epi != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
     tg_status st = validate(q, opts);
     if (st != TG_OK) return st;
@@ -548,7 +572,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
         const int64_t cap = (int64_t)ds->sms * 8;
         if (blocks > cap) blocks = cap;
         tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu);
+            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu, *prog);
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
 
@@ -620,6 +644,8 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.split_max = 1;
     p.l2_hint = (opts && opts->l2_hint == 2) ? 1 : 0;
     p.dynamic = la.pair && plan.dynamic ? 1 : 0;
+    p.swap = plan.swap ? 1 : 0;
+    p.epi = *prog;
     p.prefetch_k = (opts && opts->prefetch_k > 0) ? opts->prefetch_k : 0;
     if (la.pair && plan.split_segs > 1) {
         Workspace w;
@@ -760,7 +786,7 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
         const int64_t cap = (int64_t)ds->sms * 8;
         if (blocks > cap) blocks = cap;
         tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-            q.D, q.M, q.N, q.ldc, 0, 1, q.out_fmt, q.alpha, relu);
+            q.D, q.M, q.N, q.ldc, 0, 1, q.out_fmt, q.alpha, relu, tg::EpiProgram{});
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
     Plan plan;
@@ -803,6 +829,7 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     p.b_ptr = br;
     p.lda = ldar;
     p.ldb = ldbr;
+    p.swap = plan.swap ? 1 : 0;
     p.status = ds->status;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
@@ -892,6 +919,18 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->tmem_cols = p.tmem_cols;
     out->vector_store = p.vector_store ? 1 : 0;
     return TG_OK;
+}
+
+tg_status tg_gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                           int64_t lda, const void *B, int64_t ldb, void *D, int64_t ldc,
+                           tg_dtype in_dtype, tg_out_dtype out_dtype, const tg_epi_op *ops,
+                           int32_t n_ops, const tg_options *opts, void *stream) {
+    tg::EpiProgram prog;
+    const tg_status st = make_program(ops, n_ops, &prog);
+    if (st != TG_OK) return st;
+    const Problem q = single(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, (int)out_dtype,
+                             TG_EPILOGUE_NONE);
+    return run(q, TG_EPILOGUE_NONE, opts, stream, &prog);
 }
 
 tg_status tg_gemm_mx(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,

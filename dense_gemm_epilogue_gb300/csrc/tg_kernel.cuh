@@ -125,6 +125,32 @@ enum WaitSite : uint32_t {
     SITE_PARTIAL = 8,
 };
 
+// Composed pointwise epilogue: after y = alpha * acc (and the ReLU flag),
+// ops[0..n) apply in order to each output value, on the thread that owns it.
+enum EpiKind : int32_t {
+    EPI_SCALE = 0,      // y = a * y
+    EPI_ADD = 1,        // y = y + a
+    EPI_RELU = 2,       // y = max(y, 0): NaN stays, -0 becomes +0
+    EPI_LEAKY = 3,      // y > 0 ? y : a * y (NaN stays)
+    EPI_CLAMP = 4,      // min(max(y, a), b) (NaN stays)
+    EPI_SIGMOID = 5,    // 1 / (1 + exp(-y))
+    EPI_SILU = 6,       // y / (1 + exp(-y))
+    EPI_GELU_TANH = 7,  // y/2 (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3)))
+    EPI_BIAS_ROW = 8,   // y + bias[i]
+    EPI_BIAS_COL = 9,   // y + bias[j]
+    EPI_KINDS = 10,
+};
+constexpr int EPI_MAX_OPS = 8;
+struct EpiOp {
+    int32_t kind;
+    float a, b;
+    const float *bias;  // BIAS_ROW: M values, BIAS_COL: N values (logical rows / columns)
+};
+struct EpiProgram {
+    int32_t n;
+    EpiOp op[EPI_MAX_OPS];
+};
+
 struct GemmParams {
     int32_t m, n, k;                // role-space problem: rows, cols, reduction
     int32_t num_m_blocks, num_n_blocks, num_k_blocks;
@@ -168,6 +194,8 @@ struct GemmParams {
     // CTA-pair kernel: 1 = dynamic schedule (one cluster launched per tile;
     // running clusters take over clusters not yet started).
     int32_t dynamic;
+    int32_t swap;                   // 1: role-space rows are D's columns (operands swapped)
+    EpiProgram epi;                 // composed epilogue (n = 0: alpha and ReLU only)
 };
 
 constexpr int BLOCK_M = 128;
@@ -323,15 +351,49 @@ struct OutFormat<2> {
     }
 };
 
-// Epilogue store of one 32-column chunk of a row (role space): y = epi(v),
-// converted to the output format, bounded by the problem's columns.  D is
-// written once and never read back by the kernel, so the stores are marked
-// streaming (evict-first) to keep the operands' lines in L2.  A chunk that
-// lies wholly inside the problem takes a branch-free path that steps a
-// pointer by the column stride.
-template <int FMT>
-__device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFormat<FMT>::T *drow,
-                                            int32_t col0, const uint32_t (&v)[32]) {
+// One op of a composed epilogue on a value at logical output (i, j).
+__device__ __forceinline__ float epi_op(const EpiOp &o, float y, int64_t i, int64_t j) {
+    switch (o.kind) {
+    case EPI_SCALE: return o.a * y;
+    case EPI_ADD: return y + o.a;
+    case EPI_RELU: return (!(y > 0.0f) && !(y != y)) ? 0.0f : y;
+    case EPI_LEAKY: return (y > 0.0f || y != y) ? y : o.a * y;
+    case EPI_CLAMP: return y < o.a ? o.a : (y > o.b ? o.b : y);
+    case EPI_SIGMOID: return 1.0f / (1.0f + expf(-y));
+    case EPI_SILU: return y / (1.0f + expf(-y));
+    case EPI_GELU_TANH: return 0.5f * y * (1.0f + tanhf(0.7978845608f * (y + 0.044715f * y * y * y)));
+    case EPI_BIAS_ROW: return y + o.bias[i];
+    case EPI_BIAS_COL: return y + o.bias[j];
+    default: return y;
+    }
+}
+
+// The composed ops on one 32-column chunk of role-space row r: op by op
+// (the branch is uniform across the warp), columns col0 .. col0 + 31 of which
+// only those below p.n are real.  Kept out of line so that the kernels'
+// register budget is set by their main loops, not by this path.
+static __device__ __noinline__ void epi_program(const GemmParams &p, int32_t r, int32_t col0,
+                                                float *y) {
+    for (int q = 0; q < p.epi.n; ++q) {
+        const EpiOp o = p.epi.op[q];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int32_t c = col0 + j < p.n ? col0 + j : p.n - 1;  // bias reads stay in range
+            const int64_t i = p.swap ? c : r, jj = p.swap ? r : c;
+            y[j] = epi_op(o, y[j], i, jj);
+        }
+    }
+}
+
+// Stores of one 32-column chunk: value(j) gives the epilogue's result for
+// column col0 + j, converted to the output format, bounded by the problem's
+// columns.  D is written once and never read back by the kernel, so the
+// stores are marked streaming (evict-first) to keep the operands' lines in
+// L2.  A chunk that lies wholly inside the problem takes a branch-free path
+// that steps a pointer by the column stride.
+template <int FMT, class Value>
+__device__ __forceinline__ void store_values(const GemmParams &p, typename OutFormat<FMT>::T *drow,
+                                             int32_t col0, Value value) {
     using F = OutFormat<FMT>;
     if (col0 + 32 <= p.n) {
         if (p.vector_store) {
@@ -340,8 +402,7 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFor
             for (int j = 0; j < 32; j += F::PER16) {
                 float y[F::PER16];
 #pragma unroll
-                for (int e = 0; e < F::PER16; ++e)
-                    y[e] = apply_epilogue(__uint_as_float(v[j + e]), p.alpha, p.relu);
+                for (int e = 0; e < F::PER16; ++e) y[e] = value(j + e);
                 __stcs(dst + j / F::PER16, F::pack(y));
             }
         } else {
@@ -349,17 +410,33 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFor
             typename F::T *q = drow + (int64_t)col0 * cs;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                __stcs(q, F::cvt(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu)));
+                __stcs(q, F::cvt(value(j)));
                 q += cs;
             }
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            if (col0 + j < p.n)
-                __stcs(drow + (int64_t)(col0 + j) * p.d_col_stride,
-                       F::cvt(apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu)));
+            if (col0 + j < p.n) __stcs(drow + (int64_t)(col0 + j) * p.d_col_stride, F::cvt(value(j)));
         }
+    }
+}
+
+// Epilogue store of one 32-column chunk of role-space row r: alpha and the
+// ReLU flag inline; a composed epilogue stages the chunk's values first.
+template <int FMT>
+__device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFormat<FMT>::T *drow,
+                                            int32_t r, int32_t col0, const uint32_t (&v)[32]) {
+    if (p.epi.n == 0) {
+        store_values<FMT>(p, drow, col0, [&](int j) {
+            return apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu);
+        });
+    } else {
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = apply_epilogue(__uint_as_float(v[j]), p.alpha, p.relu);
+        epi_program(p, r, col0, y);
+        store_values<FMT>(p, drow, col0, [&](int j) { return y[j]; });
     }
 }
 
@@ -367,9 +444,9 @@ __device__ __forceinline__ void store_chunk(const GemmParams &p, typename OutFor
 __device__ __forceinline__ void epilogue_store(const GemmParams &p, int b, int32_t r, int32_t col0,
                                                const uint32_t (&v)[32]) {
     const int64_t off = (int64_t)b * p.stride_d + (int64_t)r * p.d_row_stride;
-    if (p.out_fmt == 0) store_chunk<0>(p, static_cast<float *>(p.d) + off, col0, v);
-    else if (p.out_fmt == 1) store_chunk<1>(p, static_cast<unsigned short *>(p.d) + off, col0, v);
-    else store_chunk<2>(p, static_cast<unsigned short *>(p.d) + off, col0, v);
+    if (p.out_fmt == 0) store_chunk<0>(p, static_cast<float *>(p.d) + off, r, col0, v);
+    else if (p.out_fmt == 1) store_chunk<1>(p, static_cast<unsigned short *>(p.d) + off, r, col0, v);
+    else store_chunk<2>(p, static_cast<unsigned short *>(p.d) + off, r, col0, v);
 }
 
 // Narrow one FP32 bit pattern to TF32: round the magnitude to 10 fraction

@@ -261,6 +261,44 @@ int64_t tg_mx_scale_bytes(int64_t rows, int64_t K);
 tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t ld_src,
                             uint8_t *dst, void *stream);
 
+/*
+ * Composed pointwise epilogue ("Walk through GEMM", section 5: the epilogue
+ * is a pointwise map of the accumulator, applied by the thread that owns each
+ * value; "Tylo README", worked consumers: composed epilogues):
+ *   y = alpha * sum_k a(i,k) b(k,j),  then  y = op_n(... op_1(y)),
+ *   D[i + j*ldc] = out(y)
+ * with each op one of the kinds below (a, b its float arguments; bias a device
+ * array of floats).  Everything else is as tg_gemm_batched with batch = 1
+ * (any output type).  At most TG_EPI_MAX_OPS ops; n_ops = 0 gives alpha * AB.
+ * Returns TG_ERR_INVALID_VALUE for an unknown kind, a missing or misaligned
+ * bias pointer, or n_ops out of range, besides tg_gemm_ex's errors.
+ */
+#define TG_EPI_MAX_OPS 8
+typedef enum {
+    TG_EPI_SCALE = 0,      /* y = a * y */
+    TG_EPI_ADD = 1,        /* y = y + a */
+    TG_EPI_RELU = 2,       /* y = max(y, 0) (NaN stays NaN, -0 becomes +0) */
+    TG_EPI_LEAKY_RELU = 3, /* y = y > 0 ? y : a * y (NaN stays) */
+    TG_EPI_CLAMP = 4,      /* y = min(max(y, a), b) (NaN stays) */
+    TG_EPI_SIGMOID = 5,    /* y = 1 / (1 + exp(-y)) */
+    TG_EPI_SILU = 6,       /* y = y / (1 + exp(-y)) */
+    TG_EPI_GELU_TANH = 7,  /* y = y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 y^3))) */
+    TG_EPI_BIAS_ROW = 8,   /* y = y + bias[i], bias: M floats */
+    TG_EPI_BIAS_COL = 9    /* y = y + bias[j], bias: N floats */
+} tg_epi_kind;
+
+typedef struct {
+    int32_t kind;        /* tg_epi_kind */
+    float a, b;          /* arguments (unused ones ignored) */
+    const float *bias;   /* TG_EPI_BIAS_ROW / TG_EPI_BIAS_COL only; borrowed, device memory */
+} tg_epi_op;
+
+tg_status tg_gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                           const void *A, int64_t lda, const void *B, int64_t ldb,
+                           void *D, int64_t ldc, tg_dtype in_dtype, tg_out_dtype out_dtype,
+                           const tg_epi_op *ops, int32_t n_ops,
+                           const tg_options *opts, void *stream);
+
 /* Static text for a status code ("TG_OK", ...); never NULL. */
 const char *tg_status_string(tg_status status);
 

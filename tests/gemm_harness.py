@@ -291,3 +291,81 @@ def check_mx(w: si.Workload, out="f32", opts=None, repeats=1, scale_range=(120, 
                              f"tol={tol[idx]} got={got[ok][idx]} ref={ref_out[ok][idx]}")
     rel = err / np.maximum(scale[ok], 1e-30)
     return float(rel.max()) if rel.size else 0.0
+
+
+# ----------------------------------------------------------------- composed pointwise epilogues
+
+# Largest slope of each op (how much it can grow an error in its input).
+EPI_LIPSCHITZ = {"scale": None, "add": 1.0, "relu": 1.0, "leaky_relu": None, "clamp": 1.0,
+                 "sigmoid": 0.25, "silu": 1.1, "gelu_tanh": 1.13, "bias_row": 1.0, "bias_col": 1.0}
+
+
+def epi_lipschitz(ops) -> float:
+    lip = 1.0
+    for kind, a, _b, _bias in ops:
+        if kind == "scale":
+            lip *= abs(a)
+        elif kind == "leaky_relu":
+            lip *= max(1.0, abs(a))
+        else:
+            lip *= EPI_LIPSCHITZ[kind]
+    return lip
+
+
+def check_epi(w: si.Workload, ops, out="f32", opts=None, repeats=1, bias_seed=5):
+    """tg_gemm_epilogue against the oracle's composed epilogue, every element:
+    |D - D_ref| <= TOL_REL * |alpha| sum|a||b| * L + 2^-18 (1 + |D_ref|) + 1e-6
+    (+ one output ulp), L the product of the ops' largest slopes (the GEMM
+    bound carried through the chain) and the 2^-18 term the FP32 evaluation of
+    the ops.  `ops` use names; a bias entry of "rows" / "cols" is replaced by
+    a seeded float32 vector of M / N values.  D's stride padding must be
+    untouched; repeats bitwise identical."""
+    import torch
+    import oracle
+    import dense_gemm_epilogue_gb300 as tg
+
+    lda, ldb, ldc = w.strides
+    A, B = si.make_operands(w)
+    host_ops, dev_ops, keep = [], [], []
+    for q, (kind, a, b, bias) in enumerate(ops):
+        vec = None
+        if bias in ("rows", "cols"):
+            n = w.M if bias == "rows" else w.N
+            vec = si.uniform_f32(bias_seed, 10 + q, n, -1.0, 1.0).astype(np.float32)
+            t = torch.from_numpy(vec).cuda()
+            keep.append(t)
+        host_ops.append((kind, a, b, vec))
+        dev_ops.append((kind, a, b, keep[-1] if vec is not None else None))
+    onp = {"f32": np.uint32, "bf16": np.uint16, "fp16": np.uint16}[out]
+    D0 = np.full((w.N, ldc), 0x7FC00002 if out == "f32" else 0x7FC3, dtype=onp)
+    dA, dB = torch_storage(A), torch_storage(B)
+    dD = torch.from_numpy(D0.view(np.int32 if out == "f32" else np.int16).copy()).cuda()
+    outs = []
+    for _ in range(repeats):
+        st = tg.tg_gemm_epilogue(w.M, w.N, w.K, w.alpha, dA, lda, dB, ldb, dD, ldc, w.dtype, out,
+                                 dev_ops, opts)
+        tg.check(st, "tg_gemm_epilogue")
+        st, where = tg.tg_check_device_status()
+        assert st == tg.TG_OK, f"device status {st} at wait site {where}"
+        outs.append(dD.cpu().numpy().view(onp).copy())
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "not deterministic"
+    ref, scale = oracle.gemm_epi(w.M, w.N, w.K, w.alpha, A, lda, B, ldb, w.dtype, host_ops,
+                                 with_scale=True)
+    store = outs[0]
+    assert np.array_equal(store[:, w.M:], D0[:, w.M:]), "D stride padding was written"
+    got = decode_out(store[:, : w.M].view(OUT_NP[out]).T, out)
+    ref_out = oracle.round_output(ref, out)
+    nan_ref = np.isnan(ref_out)
+    assert np.array_equal(np.isnan(got) & nan_ref, nan_ref), f"{w.name}: NaN positions differ"
+    ok = ~nan_ref
+    err = np.abs(got[ok] - ref_out[ok])
+    tol = (TOL_REL[w.dtype] * scale[ok] * epi_lipschitz(ops) + 2.0 ** -18 * (1 + np.abs(ref[ok]))
+           + TOL_ABS)
+    if out != "f32":
+        tol = tol + OUT_ULP_REL[out] * np.abs(ref[ok]) + OUT_ULP_ABS[out]
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.flatnonzero(bad)[:8]
+        raise AssertionError(f"{w.name} {ops}: {bad.sum()} of {bad.size} off; err={err[idx]} "
+                             f"tol={tol[idx]} got={got[ok][idx]} ref={ref_out[ok][idx]}")

@@ -328,3 +328,12 @@ def test_plan_dynamic_schedule(tg):
         plan(tg, si.WORKLOADS["c1_bf16_65x97x73"], opts={"schedule": 2})
     with pytest.raises(tg.TgError):      # TF32 has no pair tiles
         plan(tg, si.WORKLOADS["c2_tf32_256x128x512"], opts={"schedule": 2})
+
+
+@pytest.mark.parametrize("ops", [
+    [(10, 0, 0, None)], [(-1, 0, 0, None)], [("bias_row", 0, 0, None)],
+    [("bias_col", 0, 0, FAKE + 2)], [("relu", 0, 0, None)] * 9,
+])
+def test_epilogue_invalid_ops_rejected_before_cuda(tg, ops):
+    st = tg.tg_gemm_epilogue(10, 10, 10, 1.0, FAKE, 10, FAKE, 10, FAKE, 10, "bf16", "f32", ops)
+    assert st == tg.TG_ERR_INVALID_VALUE
