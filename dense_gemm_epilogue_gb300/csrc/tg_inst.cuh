@@ -23,7 +23,18 @@ static cudaError_t launch_one(const LaunchArgs &a) {
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    kernel<<<a.grid, C::threads(PLAIN), C::SMEM_BYTES, a.stream>>>(a.map_a, a.map_b, a.p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(a.grid, 1, 1);
+    cfg.blockDim = dim3(C::threads(PLAIN), 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e2 = cudaLaunchKernelEx(&cfg, kernel, a.map_a, a.map_b, a.p);
+    if (e2 != cudaSuccess) return e2;
     return cudaGetLastError();
 }
 
@@ -38,11 +49,13 @@ static cudaError_t launch_pair(const LaunchArgs &a) {
     static int max_clusters[64] = {0};
     const uint64_t bit = (a.device >= 0 && a.device < 64) ? (1ull << a.device) : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = a.stream;
@@ -70,6 +83,7 @@ static cudaError_t launch_pair(const LaunchArgs &a) {
     if (std::getenv("TG_LOG"))
         std::fprintf(stderr, "tg_gemm: pair kernel BN=%d MC=%d grid=%d (planned %d, %d co-resident clusters)\n",
                      BN, MC, grid, a.grid, bit ? max_clusters[a.device] : -1);
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a.map_a, a.map_b, a.p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

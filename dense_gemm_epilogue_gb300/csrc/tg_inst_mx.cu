@@ -15,7 +15,9 @@ static cudaError_t launch_mx_one(const LaunchArgs &a) {
     static int max_clusters[64] = {0};
     const uint64_t bit = (a.device >= 0 && a.device < 64) ? (1ull << a.device) : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -45,6 +47,7 @@ static cudaError_t launch_mx_one(const LaunchArgs &a) {
     if (std::getenv("TG_LOG"))
         std::fprintf(stderr, "tg_gemm_mx: BN=%d stages=%d grid=%d (planned %d)\n", BN, C::STAGES,
                      grid, a.grid);
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a.map_a, a.map_b, a.map_sfa, a.map_sfb, a.p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

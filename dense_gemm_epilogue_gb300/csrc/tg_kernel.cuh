@@ -570,6 +570,8 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();
+    griddep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
 

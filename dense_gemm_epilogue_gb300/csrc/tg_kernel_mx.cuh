@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
     tc_fence_before();
     cluster_sync_all();
     tc_fence_after();
+    griddep_wait();
+    griddep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
 

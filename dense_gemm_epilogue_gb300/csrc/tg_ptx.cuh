@@ -13,6 +13,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  The kernels are launched so that the next
+// kernel of the stream may start while this one finishes; each kernel waits
+// (griddep_wait) for the preceding grid to complete, with its memory
+// visible, before its first global-memory access, and lets the next grid
+// start launching (griddep_launch) right after that wait.  Only the prologue
+// (barrier set-up, tensor-memory allocation) overlaps the previous kernel.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
