@@ -254,6 +254,24 @@ def load_traffic(kernel_hash: str):
     return e.get("dram_bytes_per_launch")
 
 
+def slowest_rank(dist, times_ms, device):
+    """Replicas: every rank times the same work on its own GPU; the job's time
+    is the slowest rank's (max over ranks of each entry).  No data moves
+    between ranks: this is the only collective, and only for timing."""
+    if dist is None:
+        return [float(x) for x in times_ms]
+    import torch
+
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def replica_throughput(flops_per_rank: float, world: int, slowest_ms: float) -> float:
+    """TFLOP/s of the whole job: the FLOPs every rank did over the slowest time."""
+    return world * flops_per_rank / (slowest_ms * 1e-3) / 1e12
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -416,11 +434,7 @@ def run_gpu(args, rank, world, local):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    step_ms = region_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+    step_ms, e2e_ms = slowest_rank(dist, [region_ms / args.steps, e2e_ms], "cuda")
 
     if rank == 0:
         flops = w.flops * nbat
@@ -428,7 +442,7 @@ def run_gpu(args, rank, world, local):
         alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
         if mx:
             alg_bytes += (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
-        value = world * flops / (step_ms * 1e-3) / 1e12
+        value = replica_throughput(flops, world, step_ms)
         peaks, peak_src = load_peaks()
         launch_avg_ms = statistics.fmean(launch_ms)
         # Back-to-back launches for more than ~50 ms run in the power-capped
