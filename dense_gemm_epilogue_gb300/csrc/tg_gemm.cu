@@ -24,21 +24,36 @@
 namespace tg {
 
 // D = epi(alpha * 0) over every M x N output of the batch: the K == 0 case
-// (empty sums), in the output format.
+// (empty sums), in the output format.  Each block covers 1024 rows (M is
+// contiguous in D; four rows per thread) of one column, then steps over the
+// batch's columns by the grid's y size; the column and batch indices advance
+// without a division per element.
 __global__ void tg_fill_empty_sum_kernel(void *d, int64_t m, int64_t n, int64_t ldc,
                                          int64_t stride_d, int64_t batch, int out_fmt, float alpha,
                                          int relu, const EpiProgram prog) {
     const float v0 = apply_epilogue(0.0f, alpha, relu);
-    const int64_t per = m * n, total = per * batch;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t b = i / per, e = i - b * per;
-        const int64_t off = b * stride_d + (e % m) + (e / m) * ldc;
-        float v = v0;
-        for (int q = 0; q < prog.n; ++q) v = epi_op(prog.op[q], v, e % m, e / m);
-        if (out_fmt == 0) static_cast<float *>(d)[off] = v;
-        else if (out_fmt == 1) static_cast<unsigned short *>(d)[off] = OutFormat<1>::cvt(v);
-        else static_cast<unsigned short *>(d)[off] = OutFormat<2>::cvt(v);
+    const int64_t i0 = blockIdx.x * 1024 + threadIdx.x;
+    int64_t b = blockIdx.y / n, j = blockIdx.y - (blockIdx.y / n) * n;
+    const int64_t bstep = gridDim.y / n, jstep = gridDim.y - bstep * n;
+    for (; b < batch;) {
+        const int64_t base = b * stride_d + j * ldc;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t i = i0 + 256 * r;
+            if (i < m) {
+                float v = v0;
+                for (int q = 0; q < prog.n; ++q) v = epi_op(prog.op[q], v, i, j);
+                if (out_fmt == 0) static_cast<float *>(d)[base + i] = v;
+                else if (out_fmt == 1) static_cast<unsigned short *>(d)[base + i] = OutFormat<1>::cvt(v);
+                else static_cast<unsigned short *>(d)[base + i] = OutFormat<2>::cvt(v);
+            }
+        }
+        b += bstep;
+        j += jstep;
+        if (j >= n) {
+            j -= n;
+            ++b;
+        }
     }
 }
 
@@ -532,6 +547,16 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
     return r == CUDA_SUCCESS;
 }
 
+// Grid of the K == 0 fill: 1024 rows per block in x; in y, enough column
+// steps for about 16 blocks per SM (each block then loops over columns).
+dim3 fill_grid(int64_t m, int64_t cols, int sms) {
+    const int64_t gx = ceil_div(m, 1024);
+    int64_t gy = ceil_div((int64_t)sms * 16, gx);
+    if (gy > cols) gy = cols;
+    if (gy > 65535) gy = 65535;
+    return dim3((unsigned)gx, (unsigned)(gy > 0 ? gy : 1), 1);
+}
+
 // A composed epilogue from the caller's op list (checked: count, kinds,
 // bias pointers present and float-aligned).
 tg_status make_program(const tg_epi_op *ops, int32_t n_ops, tg::EpiProgram *prog) {
@@ -567,11 +592,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
 
     if (q.K == 0) {
-        const int64_t total = q.M * q.N * q.batch;
-        int64_t blocks = ceil_div(total, 256);
-        const int64_t cap = (int64_t)ds->sms * 8;
-        if (blocks > cap) blocks = cap;
-        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N * q.batch, ds->sms), 256, 0, stream>>>(
             q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu, *prog);
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
@@ -782,10 +803,7 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
     if (q.K == 0) {
-        int64_t blocks = ceil_div(q.M * q.N, 256);
-        const int64_t cap = (int64_t)ds->sms * 8;
-        if (blocks > cap) blocks = cap;
-        tg::tg_fill_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N, ds->sms), 256, 0, stream>>>(
             q.D, q.M, q.N, q.ldc, 0, 1, q.out_fmt, q.alpha, relu, tg::EpiProgram{});
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
