@@ -258,3 +258,33 @@ def test_dynamic_schedule_swapped_batched_narrow():
     wb = si.Workload("dyn_b", 600, 700, 1024, "fp16", -1.0, True, 63, "normal")
     check_batched(wb, 3, "bf16", opts={"schedule": 2})
     check_batched(wb, 2, "f32", share_a=True, opts={"schedule": 2, "block_n": 128})
+
+
+@pytest.mark.parametrize("dtype,opts", [("bf16", {"cta_pair": 1}), ("bf16", None), ("e4m3", None),
+                                        ("tf32", None)])
+def test_long_k_accumulation(dtype, opts):
+    """K = 131072 (2048 BF16 K blocks; 1024 for FP8, 4096 for TF32): every
+    stage barrier wraps its phase hundreds of times within one tile."""
+    w = si.Workload("longk", 256, 384, 131072, dtype, 0.25, True, 81, "uniform", ldc=259)
+    check_full(w, opts=opts)
+
+
+def test_many_ragged_tiles_sampled():
+    """A 24577 x 24575 output (9312 CTA-pair tiles, 123 waves, ragged in both
+    dimensions) against the oracle on sampled entries: every edge row and
+    column plus 20000 random elements; D's padding untouched."""
+    import oracle
+    from gemm_harness import assert_within
+
+    w = si.Workload("many", 24577, 24575, 512, "bf16", 1.0, True, 82, "normal", ldc=24580)
+    lda, ldb, ldc = w.strides
+    A, B = si.make_operands(w)
+    D0 = si.make_output(w)
+    out = run_tg(w, A, B, D0)
+    rng = np.random.default_rng(83)
+    I = np.concatenate([rng.integers(0, w.M, 20000), np.full(w.N, w.M - 1), np.arange(w.M) % w.M])
+    J = np.concatenate([rng.integers(0, w.N, 20000), np.arange(w.N), np.full(w.M, w.N - 1)])
+    ref, scale = oracle.gemm_entries(w.M, w.N, w.K, w.alpha, A, lda, B, ldb, w.dtype, w.relu, I, J)
+    got = out[J, I]
+    assert_within(got, ref, scale, w.dtype, w.name)
+    assert np.array_equal(out[:, w.M:].view(np.uint32), D0[:, w.M:].view(np.uint32))
