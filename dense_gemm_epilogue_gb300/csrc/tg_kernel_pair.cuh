@@ -24,7 +24,10 @@
 //             CTAs arrives (count 16) once its warp's part has been read.
 // The producers make no remote arrivals: a cluster-scope release per K step
 // costs a memory barrier on the issuing thread and throttles the TMA issue.
-// No TMA multicast is used: each CTA loads only its own rows.
+// With one pair per cluster (MC = 1) each CTA loads only its own rows; with
+// two (MC = 2, below) the pairs share their A rows by TMA multicast.  Work
+// is a static persistent sequence of units, or (MC = 1, p.dynamic) one
+// cluster per tile with tiles taken over through cluster launch control.
 #pragma once
 
 #include <cstdint>
