@@ -82,6 +82,8 @@ class Oracle:
         lib.orc_gemm_epi.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, ip, vp, vp, vp, vp, ip,
                                      vp, i64, vp, ip]
         lib.orc_gemm_epi.restype = ip
+        lib.orc_apply_epi.argtypes = [i64, i64, vp, vp, vp, vp, ip, vp, i64]
+        lib.orc_apply_epi.restype = ip
         lib.orc_num_host_threads.argtypes = []
         lib.orc_num_host_threads.restype = ip
         self.lib = lib
@@ -149,12 +151,8 @@ class Oracle:
         self.lib.orc_decode_e8m0_array(x.ctypes.data, x.size, out.ctypes.data)
         return out
 
-    def gemm_epi(self, M, N, K, alpha, A, lda, B, ldb, dtype, ops, with_scale=False, threads=0):
-        """D_ref with a composed pointwise epilogue: y = alpha * s, then each
-        op of ``ops`` in order; an op is (kind, a, b, bias) with kind a name
-        of EPI_KINDS and bias a float32 array (or None)."""
-        A = _check_storage(A, dtype, "A")
-        B = _check_storage(B, dtype, "B")
+    @staticmethod
+    def _ops(ops):
         n = len(ops)
         kinds = np.array([EPI_KINDS[o[0]] for o in ops] or [0], dtype=np.int32)
         av = np.array([float(o[1]) for o in ops] or [0.0], dtype=np.float64)
@@ -163,6 +161,28 @@ class Oracle:
                 for o in ops]
         ptrs = (ctypes.c_void_p * max(n, 1))(*[k.ctypes.data if k is not None else None
                                                for k in keep] or [None])
+        return n, kinds, av, bv, keep, ptrs
+
+    def apply_epi(self, y, ops) -> np.ndarray:
+        """The op chain of ``gemm_epi`` alone, on an (M, N) array of products
+        y = alpha * s; returns a new float64 array."""
+        Dt = np.array(np.asarray(y, dtype=np.float64).T, dtype=np.float64, order="C", copy=True)
+        N, M = Dt.shape
+        n, kinds, av, bv, keep, ptrs = self._ops(ops)
+        rc = self.lib.orc_apply_epi(M, N, kinds.ctypes.data, av.ctypes.data, bv.ctypes.data,
+                                    ctypes.cast(ptrs, ctypes.c_void_p), n, Dt.ctypes.data,
+                                    max(M, 1))
+        if rc != 0:
+            raise ValueError(f"orc_apply_epi failed with {rc}")
+        return Dt.T
+
+    def gemm_epi(self, M, N, K, alpha, A, lda, B, ldb, dtype, ops, with_scale=False, threads=0):
+        """D_ref with a composed pointwise epilogue: y = alpha * s, then each
+        op of ``ops`` in order; an op is (kind, a, b, bias) with kind a name
+        of EPI_KINDS and bias a float32 array (or None)."""
+        A = _check_storage(A, dtype, "A")
+        B = _check_storage(B, dtype, "B")
+        n, kinds, av, bv, keep, ptrs = self._ops(ops)
         Dt = np.zeros((max(N, 0), max(M, 0)), dtype=np.float64)
         St = np.zeros_like(Dt) if with_scale else None
         rc = self.lib.orc_gemm_epi(M, N, K, float(alpha), A.ctypes.data, lda, B.ctypes.data, ldb,
@@ -232,6 +252,10 @@ def gemm_entries(*args, **kw):
 
 def gemm_mx(*args, **kw):
     return default().gemm_mx(*args, **kw)
+
+
+def apply_epi(*args, **kw):
+    return default().apply_epi(*args, **kw)
 
 
 def gemm_epi(*args, **kw):

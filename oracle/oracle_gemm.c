@@ -548,18 +548,20 @@ static double apply_op(int kind, double a, double b, const float *bias, int64_t 
     }
 }
 
-int orc_gemm_epi(int64_t M, int64_t N, int64_t K, double alpha,
-                 const void *A, int64_t lda, const void *B, int64_t ldb, int dtype,
-                 const int *kinds, const double *as, const double *bs, const float *const *biases,
-                 int n_ops, double *D, int64_t ldd, double *scale, int nthreads) {
+static int check_ops(const int *kinds, const float *const *biases, int n_ops) {
     if (n_ops < 0) return -1;
     for (int q = 0; q < n_ops; ++q) {
         if (kinds[q] < 0 || kinds[q] >= ORC_EPI_KINDS) return -1;
         if ((kinds[q] == ORC_EPI_BIAS_ROW || kinds[q] == ORC_EPI_BIAS_COL) && !biases[q]) return -1;
     }
-    /* The product alpha * s first (no ReLU), then the chain. */
-    int rc = orc_gemm(M, N, K, alpha, A, lda, B, ldb, dtype, 0, D, ldd, scale, nthreads);
-    if (rc != 0) return rc;
+    return 0;
+}
+
+/* The chain alone, in place on an M x N column-major array of products. */
+int orc_apply_epi(int64_t M, int64_t N, const int *kinds, const double *as, const double *bs,
+                  const float *const *biases, int n_ops, double *D, int64_t ldd) {
+    if (check_ops(kinds, biases, n_ops) != 0 || M < 0 || N < 0 || ldd < (M > 1 ? M : 1))
+        return -1;
     for (int64_t j = 0; j < N; ++j)
         for (int64_t i = 0; i < M; ++i) {
             double y = D[i + j * ldd];
@@ -567,6 +569,17 @@ int orc_gemm_epi(int64_t M, int64_t N, int64_t K, double alpha,
             D[i + j * ldd] = y;
         }
     return 0;
+}
+
+int orc_gemm_epi(int64_t M, int64_t N, int64_t K, double alpha,
+                 const void *A, int64_t lda, const void *B, int64_t ldb, int dtype,
+                 const int *kinds, const double *as, const double *bs, const float *const *biases,
+                 int n_ops, double *D, int64_t ldd, double *scale, int nthreads) {
+    if (check_ops(kinds, biases, n_ops) != 0) return -1;
+    /* The product alpha * s first (no ReLU), then the chain. */
+    int rc = orc_gemm(M, N, K, alpha, A, lda, B, ldb, dtype, 0, D, ldd, scale, nthreads);
+    if (rc != 0) return rc;
+    return orc_apply_epi(M, N, kinds, as, bs, biases, n_ops, D, ldd);
 }
 
 /* Decode an array of scale codes (for the decode pins). */

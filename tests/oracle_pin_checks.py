@@ -728,6 +728,23 @@ def check_epi_nan(orc):
         assert np.all(np.isnan(d[1])) and not np.any(np.isnan(d[[0, 2]])), op
 
 
+def check_apply_epi_alone(orc):
+    """The chain on given products (no GEMM): closed forms on a 5 x 7 array,
+    row biases along i and column biases along j, the input left as it was."""
+    rng = np.random.default_rng(41)
+    y = rng.integers(-16, 17, size=(5, 7)) / 4.0
+    keep = y.copy()
+    br = (np.arange(5, dtype=np.float32) - 2) * 0.5
+    bc = np.arange(7, dtype=np.float32) * 0.125
+    d = orc.apply_epi(y, [("bias_row", 0, 0, br), ("clamp", -1.0, 1.5, None),
+                          ("bias_col", 0, 0, bc), ("scale", 2.0, 0, None)])
+    assert d.shape == (5, 7) and np.array_equal(y, keep)
+    assert np.array_equal(d, 2.0 * (np.clip(y + br[:, None], -1.0, 1.5) + bc[None, :]))
+    assert np.array_equal(orc.apply_epi(y, []), y)
+    z = orc.apply_epi(np.zeros((3, 2)), [("add", 0.25, 0, None), ("sigmoid", 0, 0, None)])
+    assert np.allclose(z, 1.0 / (1.0 + math.exp(-0.25)), rtol=1e-15, atol=0)
+
+
 ALL_CHECKS = [
     check_decode_tables,
     check_tf32_narrowing,
@@ -755,4 +772,5 @@ ALL_CHECKS = [
     check_epi_pointwise_forms,
     check_epi_composition_and_bias,
     check_epi_nan,
+    check_apply_epi_alone,
 ]
