@@ -56,6 +56,7 @@ EXPORTED = (
     "tg_gemm_batched",
     "tg_gemm_epilogue",
     "tg_gemm_mx",
+    "tg_gemm_mx_batched",
     "tg_plan_mx",
     "tg_mx_scale_bytes",
     "tg_mx_pack_scales",
@@ -169,6 +170,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(tg_options), vp]
         lib.tg_gemm_mx.restype = ctypes.c_int
+        lib.tg_gemm_mx_batched.argtypes = [i64, i64, i64, f32, vp, i64, i64, vp, i64, vp, i64,
+                                           i64, vp, i64, vp, i64, i64, i64, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(tg_epi_op), i32,
+                                           ctypes.POINTER(tg_options), vp]
+        lib.tg_gemm_mx_batched.restype = ctypes.c_int
         lib.tg_plan_mx.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_int,
                                    ctypes.POINTER(tg_options), i32, ctypes.POINTER(tg_plan_info)]
         lib.tg_plan_mx.restype = ctypes.c_int
@@ -270,17 +276,22 @@ def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):
     return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
 
 
-def tg_gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, out_dtype, ops,
-                     opts=None, stream=None) -> int:
-    """D = out(op_n(... op_1(alpha * A B))); ops: sequence of (kind, a, b, bias)
-    with kind a name of EPI_KINDS (or its code) and bias a device tensor or None."""
-    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+def _epi_ops(ops):
     arr = (tg_epi_op * max(len(ops), 1))()
     for q, (kind, a, b, bias) in enumerate(ops):
         arr[q].kind = EPI_KINDS[kind] if isinstance(kind, str) else int(kind)
         arr[q].a = float(a)
         arr[q].b = float(b)
         arr[q].bias = _ptr(bias)
+    return arr
+
+
+def tg_gemm_epilogue(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, out_dtype, ops,
+                     opts=None, stream=None) -> int:
+    """D = out(op_n(... op_1(alpha * A B))); ops: sequence of (kind, a, b, bias)
+    with kind a name of EPI_KINDS (or its code) and bias a device tensor or None."""
+    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+    arr = _epi_ops(ops)
     return load().tg_gemm_epilogue(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, _ptr(D), ldc,
                                    _dtype(in_dtype), out, arr, len(ops), _options(opts),
                                    _stream(stream))
@@ -294,6 +305,19 @@ def tg_gemm_mx(M, N, K, alpha, A, lda, SFA, B, ldb, SFB, D, ldc, in_dtype, out_d
     return load().tg_gemm_mx(M, N, K, alpha, _ptr(A), lda, _ptr(SFA), _ptr(B), ldb, _ptr(SFB),
                              _ptr(D), ldc, _dtype(in_dtype), out, _epi(epilogue), _options(opts),
                              _stream(stream))
+
+
+def tg_gemm_mx_batched(M, N, K, alpha, A, lda, stride_a, SFA, stride_sfa, B, ldb, stride_b, SFB,
+                       stride_sfb, D, ldc, stride_d, batch, in_dtype, out_dtype, ops=(),
+                       opts=None, stream=None) -> int:
+    """Strided batch of block-scaled GEMMs with a composed epilogue (see
+    include/tg_gemm.h, tg_gemm_mx_batched); scale strides in bytes."""
+    out = OUT_CODES[out_dtype] if isinstance(out_dtype, str) else int(out_dtype)
+    arr = _epi_ops(ops)
+    return load().tg_gemm_mx_batched(M, N, K, alpha, _ptr(A), lda, stride_a, _ptr(SFA),
+                                     stride_sfa, _ptr(B), ldb, stride_b, _ptr(SFB), stride_sfb,
+                                     _ptr(D), ldc, stride_d, batch, _dtype(in_dtype), out, arr,
+                                     len(ops), _options(opts), _stream(stream))
 
 
 def tg_plan_mx(M, N, K, lda, ldb, ldc, in_dtype, opts=None, num_sms=0):

@@ -710,7 +710,16 @@ bool mx_options_ok(const tg_options *o) {
     return o->schedule >= 0 && o->schedule <= 1 && !o->reserved[0];
 }
 
-tg_status validate_mx(const Problem &q, const void *sfa, const void *sfb, const tg_options *o) {
+// Scale-atom batch strides (bytes): 0 (one scale set for every entry), or a
+// multiple of 16 no smaller than one entry's atoms.
+bool mx_scale_stride_ok(int64_t stride, int64_t rows, int64_t K, int64_t batch) {
+    if (batch <= 1 || stride == 0) return true;
+    return stride > 0 && stride % 16 == 0 && stride >= mx_scale_bytes(rows, K) &&
+           stride < (int64_t)(1ull << 40);
+}
+
+tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sfb,
+                      int64_t ssfb, const tg_options *o) {
     if (q.t != TG_E4M3 && q.t != TG_E5M2 && q.t != TG_E2M1) return TG_ERR_INVALID_VALUE;
     const bool fp4 = q.t == TG_E2M1;
     Problem qq = q;
@@ -718,11 +727,17 @@ tg_status validate_mx(const Problem &q, const void *sfa, const void *sfb, const 
     tg_status st = validate(qq, nullptr);
     if (st != TG_OK) return st;
     if (!mx_options_ok(o)) return TG_ERR_INVALID_VALUE;
-    // Packed FP4: rows and the reduction hold whole bytes.
+    // Packed FP4: rows, batch entries and the reduction hold whole bytes.
     if (fp4 && ((q.lda | q.ldb | q.K) & 1)) return TG_ERR_INVALID_VALUE;
-    if (q.M > 0 && q.N > 0 && q.K > 0) {
+    if (fp4 && q.batch > 1 && ((q.sa | q.sb) & 1)) return TG_ERR_INVALID_VALUE;
+    if (!mx_scale_stride_ok(ssfa, q.M, q.K, q.batch) || !mx_scale_stride_ok(ssfb, q.N, q.K, q.batch))
+        return TG_ERR_INVALID_VALUE;
+    if (q.M > 0 && q.N > 0 && q.K > 0 && q.batch > 0) {
         const int64_t lda_b = fp4 ? q.lda / 2 : q.lda, ldb_b = fp4 ? q.ldb / 2 : q.ldb;
+        const int64_t sa_b = fp4 ? q.sa / 2 : q.sa, sb_b = fp4 ? q.sb / 2 : q.sb;
         if (!tma_legal(q.A, lda_b, 1) || !tma_legal(q.B, ldb_b, 1)) return TG_ERR_INVALID_VALUE;
+        if (!tma_batch_legal(sa_b, 1, q.batch) || !tma_batch_legal(sb_b, 1, q.batch))
+            return TG_ERR_INVALID_VALUE;
         if (!sfa || !sfb || (uintptr_t)sfa % 16 || (uintptr_t)sfb % 16) return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
@@ -748,7 +763,8 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     int64_t best = -1;
     for (int bn : {256, 128}) {
         if (o->block_n && o->block_n != bn) continue;
-        const int64_t tiles = ceil_div(p.mk, 2 * tg::BLOCK_M) * ceil_div(p.nk, bn);
+        const int64_t tiles =
+            (q.batch > 1 ? q.batch : 1) * ceil_div(p.mk, 2 * tg::BLOCK_M) * ceil_div(p.nk, bn);
         const int64_t mma = bn / 2, smem = 64 + bn / 4;
         const int64_t est = ceil_div(tiles, pairs) * (mma > smem ? mma : smem);
         if (best < 0 || est < best) {
@@ -758,7 +774,7 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     }
     const int64_t mblocks = ceil_div(p.mk, 2 * tg::BLOCK_M);
     p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
-    p.tiles = p.tiles_per_batch;
+    p.tiles = (q.batch > 1 ? q.batch : 1) * p.tiles_per_batch;
     tg::mx_config_numbers(q.t == TG_E2M1 ? Kind::E2M1 : Kind::E4M3, p.block_n, &p.stages, &p.smem,
                           &p.threads, &p.tmem_cols);
     int64_t g = o->raster_group ? o->raster_group : 8;
@@ -771,40 +787,42 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     return TG_OK;
 }
 
-// Scale atoms of an operand with `rows` rows as a 3-D tensor of 32-bit words:
-// (128 words = one 512-byte atom, atom column kg, row block rb); a box holds
-// `box_kg` x `box_rb` atoms (one K stage of one tile side), and columns or
+// Scale atoms of an operand with `rows` rows as a 4-D tensor of 32-bit words:
+// (128 words = one 512-byte atom, atom column kg, row block rb, batch entry),
+// entries `stride` bytes apart (nb == 1: one entry); a box holds `box_kg` x
+// `box_rb` atoms of one entry (one K stage of one tile side), and columns or
 // row blocks past the end read as zeros.
-bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_kg,
-                   int box_rb) {
+bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int64_t nb,
+                   int64_t stride, int box_kg, int box_rb) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int64_t kg = ceil_div(K, 128), rb = ceil_div(rows, tg::BLOCK_M);
-    cuuint64_t dims[3] = {128, (cuuint64_t)kg, (cuuint64_t)rb};
-    cuuint64_t strides[2] = {512, (cuuint64_t)(kg * 512)};
-    cuuint32_t box[3] = {128, (cuuint32_t)box_kg, (cuuint32_t)box_rb};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
+    cuuint64_t dims[4] = {128, (cuuint64_t)kg, (cuuint64_t)rb, (cuuint64_t)nb};
+    cuuint64_t strides[3] = {512, (cuuint64_t)(kg * 512),
+                             (cuuint64_t)(nb > 1 ? stride : rb * kg * 512)};
+    cuuint32_t box[4] = {128, (cuuint32_t)box_kg, (cuuint32_t)box_rb, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue epi,
-                 const tg_options *opts, void *stream_ptr) {
-    if (epi != TG_EPILOGUE_NONE && epi != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
-    tg_status st = validate_mx(q, sfa, sfb, opts);
+// Block-scaled GEMM over `q.batch` entries: scale sets `ssfa` / `ssfb` bytes
+// apart (0: shared), then the composed program `prog` (or ReLU alone).
+tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sfb, int64_t ssfb,
+                 int relu, const tg::EpiProgram &prog, const tg_options *opts, void *stream_ptr) {
+    tg_status st = validate_mx(q, sfa, ssfa, sfb, ssfb, opts);
     if (st != TG_OK) return st;
-    if (q.M == 0 || q.N == 0) return TG_OK;
+    if (q.M == 0 || q.N == 0 || q.batch == 0) return TG_OK;
     int dev = 0;
     DeviceState *ds = nullptr;
     st = device_state(&dev, &ds);
     if (st != TG_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-    const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
     if (q.K == 0) {
-        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N, ds->sms), 256, 0, stream>>>(
-            q.D, q.M, q.N, q.ldc, 0, 1, q.out_fmt, q.alpha, relu, tg::EpiProgram{});
+        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N * q.batch, ds->sms), 256, 0, stream>>>(
+            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu, prog);
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
     Plan plan;
@@ -816,11 +834,16 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     const void *ar = plan.swap ? q.B : q.A, *br = plan.swap ? q.A : q.B;
     const void *sar = plan.swap ? sfb : sfa, *sbr = plan.swap ? sfa : sfb;
     const int64_t ldar = plan.swap ? q.ldb : q.lda, ldbr = plan.swap ? q.lda : q.ldb;
+    const int64_t sa = plan.swap ? q.sb : q.sa, sb = plan.swap ? q.sa : q.sb;
+    const int64_t ssa = plan.swap ? ssfb : ssfa, ssb = plan.swap ? ssfa : ssfb;
+    const bool many = q.batch > 1;
+    const int64_t nba = many && sa ? q.batch : 1, nbb = many && sb ? q.batch : 1;
+    const int64_t nsa = many && ssa ? q.batch : 1, nsb = many && ssb ? q.batch : 1;
     const int kgs = block_k(q.t) / 128;  // scale-atom columns per K stage
-    if (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, 1, 0, tg::BLOCK_M) ||
-        !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, 1, 0, plan.block_n / 2) ||
-        !encode_scales(&la.map_sfa, sar, plan.mk, q.K, kgs, 1) ||
-        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, kgs, plan.block_n / tg::BLOCK_M))
+    if (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sa, tg::BLOCK_M) ||
+        !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sb, plan.block_n / 2) ||
+        !encode_scales(&la.map_sfa, sar, plan.mk, q.K, nsa, ssa, kgs, 1) ||
+        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, nsb, ssb, kgs, plan.block_n / tg::BLOCK_M))
         return TG_ERR_INVALID_VALUE;
     la.block_n = plan.block_n;
     la.pair = true;
@@ -836,18 +859,24 @@ tg_status run_mx(const Problem &q, const void *sfa, const void *sfb, tg_epilogue
     p.relu = relu;
     p.num_tiles = plan.tiles;
     p.tiles_per_batch = plan.tiles_per_batch;
-    p.batch = 1;
+    p.batch = (int32_t)(many ? q.batch : 1);
     p.out_fmt = q.out_fmt;
     p.alpha = q.alpha;
     p.vector_store = plan.vector_store ? 1 : 0;
     p.d = q.D;
     p.d_row_stride = plan.swap ? q.ldc : 1;
     p.d_col_stride = plan.swap ? 1 : q.ldc;
+    p.stride_d = many ? q.sd : 0;
     p.a_ptr = ar;
     p.b_ptr = br;
     p.lda = ldar;
     p.ldb = ldbr;
+    p.a_bmul = nba > 1 ? 1 : 0;
+    p.b_bmul = nbb > 1 ? 1 : 0;
+    p.sfa_bmul = nsa > 1 ? 1 : 0;
+    p.sfb_bmul = nsb > 1 ? 1 : 0;
     p.swap = plan.swap ? 1 : 0;
+    p.epi = prog;
     p.status = ds->status;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
@@ -955,9 +984,26 @@ tg_status tg_gemm_mx(int64_t M, int64_t N, int64_t K, float alpha, const void *A
                      const void *SFA, const void *B, int64_t ldb, const void *SFB, void *D,
                      int64_t ldc, tg_dtype in_dtype, tg_out_dtype out_dtype, tg_epilogue epilogue,
                      const tg_options *opts, void *stream) {
+    if (epilogue != TG_EPILOGUE_NONE && epilogue != TG_EPILOGUE_RELU) return TG_ERR_INVALID_VALUE;
     const Problem q = single(M, N, K, alpha, A, lda, B, ldb, D, ldc, in_dtype, (int)out_dtype,
                              epilogue);
-    return run_mx(q, SFA, SFB, epilogue, opts, stream);
+    return run_mx(q, SFA, 0, SFB, 0, epilogue == TG_EPILOGUE_RELU ? 1 : 0, tg::EpiProgram{}, opts,
+                  stream);
+}
+
+tg_status tg_gemm_mx_batched(int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                             int64_t lda, int64_t stride_a, const void *SFA, int64_t stride_sfa,
+                             const void *B, int64_t ldb, int64_t stride_b, const void *SFB,
+                             int64_t stride_sfb, void *D, int64_t ldc, int64_t stride_d,
+                             int64_t batch, tg_dtype in_dtype, tg_out_dtype out_dtype,
+                             const tg_epi_op *ops, int32_t n_ops, const tg_options *opts,
+                             void *stream) {
+    tg::EpiProgram prog;
+    const tg_status st = make_program(ops, n_ops, &prog);
+    if (st != TG_OK) return st;
+    const Problem q{M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, D, ldc, stride_d, batch,
+                    in_dtype, (int)out_dtype, 0};
+    return run_mx(q, SFA, stride_sfa, SFB, stride_sfb, 0, prog, opts, stream);
 }
 
 tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -967,7 +1013,7 @@ tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, 
     const void *fake = reinterpret_cast<const void *>(256);
     const Problem q = single(M, N, K, 1.0f, fake, lda, fake, ldb, const_cast<void *>(fake), ldc,
                              in_dtype, 0, TG_EPILOGUE_NONE);
-    tg_status st = validate_mx(q, fake, fake, opts);
+    tg_status st = validate_mx(q, fake, 0, fake, 0, opts);
     if (st != TG_OK) return st;
     int sms = num_sms;
     if (sms <= 0) {

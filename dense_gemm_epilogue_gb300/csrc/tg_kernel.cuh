@@ -191,6 +191,7 @@ struct GemmParams {
     int64_t stride_a, stride_b;     // elements between batch entries (role space)
     int64_t stride_d;               // output elements between batch entries
     int32_t a_bmul, b_bmul;
+    int32_t sfa_bmul, sfb_bmul;     // block-scaled kernel: scale-atom batch multipliers
     // CTA-pair kernel: 1 = dynamic schedule (one cluster launched per tile;
     // running clusters take over clusters not yet started).
     int32_t dynamic;

@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                 // column past the last one (FP4 with an odd count) reads as zeros.
                 const int32_t sfa_rb = mb * 2 + (int32_t)half;
                 const int32_t sfb_rb = nb * C::SFB_ATOMS;
+                const int32_t sfa_b = bt * p.sfa_bmul, sfb_b = bt * p.sfb_bmul;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), 0);
@@ -192,10 +193,10 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                     tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK_UNITS, brow, bb);
                     // One box per operand: the stage's KGS atom columns of the
                     // CTA's A row block, and of the tile's SFB_ATOMS B row blocks.
-                    tma_load_3d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, kb * C::KGS, sfa_rb);
-                    tma_load_3d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, kb * C::KGS, sfb_rb);
-                    (void)ab;
-                    (void)bb;
+                    tma_load_4d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, kb * C::KGS, sfa_rb,
+                                     sfa_b);
+                    tma_load_4d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, kb * C::KGS, sfb_rb,
+                                     sfb_b);
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }

@@ -464,6 +464,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 4-D CTA-pair load: coordinates (c0, c1, c2, c3), innermost first.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap *map,
                                                       uint32_t bar_cluster, int32_t c0, int32_t c1,
                                                       int32_t c2, uint64_t policy) {

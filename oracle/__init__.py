@@ -13,6 +13,7 @@ rational brute force, hand-worked examples under ``tests/golden/``), and
 
 from .oracle import (  # noqa: F401
     EPI_KINDS,
+    apply_epi,
     Oracle,
     build,
     compile_source,

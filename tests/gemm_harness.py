@@ -369,3 +369,119 @@ def check_epi(w: si.Workload, ops, out="f32", opts=None, repeats=1, bias_seed=5)
         idx = np.flatnonzero(bad)[:8]
         raise AssertionError(f"{w.name} {ops}: {bad.sum()} of {bad.size} off; err={err[idx]} "
                              f"tol={tol[idx]} got={got[ok][idx]} ref={ref_out[ok][idx]}")
+
+
+# ----------------------------------------------------------------- batched block-scaled
+
+def _bias_vectors(w: si.Workload, ops, bias_seed: int):
+    """Ops with "rows" / "cols" bias entries replaced by seeded float32
+    vectors of M / N values: (host ops, device ops, device tensors kept)."""
+    import torch
+
+    host_ops, dev_ops, keep = [], [], []
+    for q, (kind, a, b, bias) in enumerate(ops):
+        vec = None
+        if bias in ("rows", "cols"):
+            n = w.M if bias == "rows" else w.N
+            vec = si.uniform_f32(bias_seed, 10 + q, n, -1.0, 1.0).astype(np.float32)
+            keep.append(torch.from_numpy(vec).cuda())
+        host_ops.append((kind, a, b, vec))
+        dev_ops.append((kind, a, b, keep[-1] if vec is not None else None))
+    return host_ops, dev_ops, keep
+
+
+def check_mx_batched(w: si.Workload, batch: int, out="f32", ops=(), share_a=False, share_b=False,
+                     share_sfa=False, share_sfb=False, pad_a=0, pad_b=0, pad_sf=0, pad_d=0,
+                     opts=None, repeats=1, scale_range=(120, 134), bias_seed=7):
+    """tg_gemm_mx_batched on `batch` entries drawn with seeds w.seed, w.seed+1,
+    ... (operands and scales each either per entry or shared), against the
+    oracle's block-scaled product of each entry followed by its op chain,
+    every element, with check_epi's bound.  Operand paddings count elements
+    (multiples of 16 bytes); pad_sf counts bytes.  D's padding and the gaps
+    between entries must be untouched; repeats bitwise identical."""
+    import torch
+    import oracle
+    import dense_gemm_epilogue_gb300 as tg
+
+    w = mx_padded(w)
+    lda, ldb, ldc = w.strides
+    per = 2 if w.dtype == "e2m1" else 1  # elements per storage byte
+    KB = (w.K + 31) // 32
+    ents = [si.with_shape(w, seed=w.seed + b) for b in range(batch)]
+    ops_ = [si.make_operands(e) for e in ents]
+    scs = [si.make_mx_scales(e, *scale_range) for e in ents]
+    pick = lambda lst, shared: [lst[0]] * batch if shared else lst
+    A_list = pick([o[0] for o in ops_], share_a)
+    B_list = pick([o[1] for o in ops_], share_b)
+    SA_list = pick([s[0] for s in scs], share_sfa)
+    SB_list = pick([s[1] for s in scs], share_sfb)
+    sa = 0 if share_a else w.M * lda + pad_a
+    sb = 0 if share_b else w.N * ldb + pad_b
+    fa, fb = tg.tg_mx_scale_bytes(w.M, w.K), tg.tg_mx_scale_bytes(w.N, w.K)
+    ssa = 0 if share_sfa else fa + pad_sf
+    ssb = 0 if share_sfb else fb + pad_sf
+    sd = w.N * ldc + pad_d
+
+    def pack(lst, stride_bytes, one_bytes, dtype):
+        buf = np.zeros(max(stride_bytes * (batch - 1), 0) + one_bytes, dtype=dtype)
+        for b in range(batch if stride_bytes else 1):
+            buf[b * stride_bytes: b * stride_bytes + one_bytes] = lst[b].reshape(-1)
+        return buf
+
+    ety = A_list[0].dtype
+    A = pack(A_list, sa // per, A_list[0].size, ety)
+    B = pack(B_list, sb // per, B_list[0].size, ety)
+    SA = pack([to_atoms(s, w.K) for s in SA_list], ssa, fa, np.uint8)
+    SB = pack([to_atoms(s, w.K) for s in SB_list], ssb, fb, np.uint8)
+    host_ops, dev_ops, keep = _bias_vectors(w, ops, bias_seed)
+    sentinel = {"f32": np.uint32(0x7FC00002), "bf16": np.uint16(0x7FC3), "fp16": np.uint16(0x7E03)}
+    onp = np.uint32 if out == "f32" else np.uint16
+    D0 = np.full(sd * max(batch - 1, 0) + w.N * ldc, sentinel[out], dtype=onp)
+    dev = lambda x: torch_storage(x) if x.size else None
+    dA, dB, dSA, dSB = dev(A), dev(B), dev(SA), dev(SB)
+    dD = torch.from_numpy(D0.view(np.int32 if out == "f32" else np.int16).copy()).cuda()
+    outs = []
+    for _ in range(repeats):
+        st = tg.tg_gemm_mx_batched(w.M, w.N, w.K, w.alpha, dA, lda, sa, dSA, ssa, dB, ldb, sb,
+                                   dSB, ssb, dD, ldc, sd, batch, w.dtype, out, dev_ops, opts)
+        tg.check(st, "tg_gemm_mx_batched")
+        st, where = tg.tg_check_device_status()
+        assert st == tg.TG_OK, f"device status {st} at wait site {where}"
+        outs.append(dD.cpu().numpy().view(onp).copy())
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "not deterministic"
+    Dall = outs[0]
+    lip = epi_lipschitz(ops)
+    worst = 0.0
+    for b in range(batch):
+        prod, scale = oracle.gemm_mx(w.M, w.N, w.K, w.alpha, A_list[b], lda, SA_list[b],
+                                     max(KB, 1), B_list[b], ldb, SB_list[b], max(KB, 1), w.dtype,
+                                     False, with_scale=True)
+        ref = oracle.apply_epi(prod, host_ops)
+        ref_out = oracle.round_output(ref, out)
+        store = Dall[b * sd: b * sd + w.N * ldc].reshape(w.N, ldc)
+        pad0 = D0[b * sd: b * sd + w.N * ldc].reshape(w.N, ldc)
+        assert np.array_equal(store[:, w.M:], pad0[:, w.M:]), "D stride padding was written"
+        if b + 1 < batch:
+            gap = slice(b * sd + w.N * ldc, (b + 1) * sd)
+            assert np.array_equal(Dall[gap], D0[gap]), "gap between entries was written"
+        got = decode_out(store[:, : w.M].view(OUT_NP[out]).T, out)
+        nan_ref = np.isnan(ref_out)
+        assert np.array_equal(np.isnan(got) & nan_ref, nan_ref), f"{w.name}[{b}]: NaN positions"
+        inf = np.isinf(ref_out)
+        assert np.array_equal(got[inf], ref_out[inf]), f"{w.name}[{b}]: overflow differs"
+        ok = ~nan_ref & ~inf
+        err = np.abs(got[ok] - ref_out[ok])
+        tol = TOL_REL[w.dtype] * scale[ok] * lip + 2.0 ** -18 * (1 + np.abs(ref[ok])) + TOL_ABS
+        if out != "f32":
+            tol = tol + OUT_ULP_REL[out] * np.abs(ref[ok]) + OUT_ULP_ABS[out]
+        bad = ~(err <= tol)
+        if bad.any():
+            idx = np.flatnonzero(bad)[:8]
+            raise AssertionError(f"{w.name}[{b}] {ops}: {bad.sum()} of {bad.size} off; "
+                                 f"err={err[idx]} tol={tol[idx]} got={got[ok][idx]} "
+                                 f"ref={ref_out[ok][idx]}")
+        if err.size:
+            worst = max(worst, float((err / np.maximum(scale[ok], 1e-30)).max()))
+    del keep
+    return worst

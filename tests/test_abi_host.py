@@ -337,3 +337,33 @@ def test_plan_dynamic_schedule(tg):
 def test_epilogue_invalid_ops_rejected_before_cuda(tg, ops):
     st = tg.tg_gemm_epilogue(10, 10, 10, 1.0, FAKE, 10, FAKE, 10, FAKE, 10, "bf16", "f32", ops)
     assert st == tg.TG_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("args", [
+    dict(ssfa=8), dict(ssfb=512 * 7), dict(ssfa=-512), dict(sa=8), dict(sb=-1024),
+    dict(sd=90), dict(batch=-1), dict(ops=[(12, 0, 0, None)]), dict(dtype="bf16"),
+    dict(dtype="e2m1", sa=10 * 1024 + 1), dict(dtype="e2m1", sb=10 * 1024 + 16),
+    dict(opts={"split_k": 2}), dict(out=4), None,
+])
+def test_mx_batched_invalid_arguments_rejected_before_cuda(tg, args):
+    """Scale strides: 0 or a multiple of 16 at least one entry's atoms;
+    operand strides of 16-byte multiples (even, for packed FP4); outputs
+    that do not overlap."""
+    fa = tg.tg_mx_scale_bytes(10, 1024)
+    a = dict(sa=10 * 1024, ssfa=fa, sb=10 * 1024, ssfb=fa, sd=10 * 10, batch=3, dtype="e4m3",
+             out="f32", ops=[], opts=None)
+    a.update(args or {})
+    st = tg.tg_gemm_mx_batched(10, 10, 1024, 1.0, FAKE, 1024, a["sa"], FAKE, a["ssfa"], FAKE, 1024,
+                               a["sb"], FAKE, a["ssfb"], FAKE, 10, a["sd"], a["batch"], a["dtype"],
+                               a["out"], a["ops"], a["opts"])
+    if args is None:   # the unmodified call passes validation (and then needs a device)
+        assert st != tg.TG_ERR_INVALID_VALUE
+    else:
+        assert st == tg.TG_ERR_INVALID_VALUE
+
+
+def test_mx_batched_empty_is_ok_without_cuda(tg):
+    assert tg.tg_gemm_mx_batched(0, 10, 64, 1.0, None, 64, 0, None, 0, FAKE, 64, 0, FAKE, 0, None,
+                                 1, 0, 4, "e4m3", "f32") == tg.TG_OK
+    assert tg.tg_gemm_mx_batched(10, 10, 64, 1.0, FAKE, 64, 0, FAKE, 0, FAKE, 64, 0, FAKE, 0, FAKE,
+                                 10, 100, 0, "e4m3", "f32") == tg.TG_OK
