@@ -119,6 +119,7 @@ class tg_plan_info(ctypes.Structure):
         ("split_tiles", ctypes.c_int32),
         ("split_segs", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
+        ("stream_k", ctypes.c_int32),
     ]
 
 

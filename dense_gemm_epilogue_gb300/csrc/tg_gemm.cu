@@ -210,6 +210,16 @@ tg_status device_state(int *dev_out, DeviceState **out) {
 // partial-sum traffic for no gain.
 constexpr int kDefaultSplitMax = 8;
 
+// Stream-K (single-CTA tiles): a CTA's share spans at least this many K
+// blocks, so that its MMA work outweighs writing or reading one partial tile.
+constexpr int64_t kStreamKMinBlocks = 8;
+
+// Planner cost of finishing a K-split tile (flag wait, partial-sum round
+// trip through L2), in the planner's cost units: about 4 us measured, some
+// 22 K blocks of a 128 x 64 tile.  Splitting therefore pays only for long
+// K loops (1024^3 runs 8.5 us unsplit, 11.6-12.6 us split either way).
+constexpr int64_t kFixupLatency = 5632;
+
 void split_rule(int64_t tiles, int64_t pairs, int64_t nkb, int split_max, int64_t ws_tiles,
                 int64_t *rem_out, int *segs_out) {
     int64_t rem = tiles % pairs, segs = 1;
@@ -246,6 +256,7 @@ struct Plan {
     int mc = 1;         // pair kernel: pairs per cluster (2: A rows multicast)
     int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
     bool dynamic = false;  // pair kernel: one cluster per tile, launch-control stealing
+    bool stream_k = false; // single-CTA kernel: each CTA a contiguous share of all K iterations
     int64_t split_tiles = 0;
     int split_segs = 1;
     bool swap = false;
@@ -344,7 +355,10 @@ tg_status validate(const Problem &q, const tg_options *o) {
         if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
         if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->multicast < 0 || o->multicast > 2) return TG_ERR_INVALID_VALUE;
-        if (o->schedule < 0 || o->schedule > 2 || o->reserved[0]) return TG_ERR_INVALID_VALUE;
+        if (o->schedule < 0 || o->schedule > 3 || o->reserved[0]) return TG_ERR_INVALID_VALUE;
+        // Stream-K runs single-CTA tiles and splits K by definition.
+        if (o->schedule == 3 && (o->cta_pair == 2 || o->multicast == 2 || o->split_k == 1))
+            return TG_ERR_INVALID_VALUE;
         if (o->multicast == 2 && o->cta_pair == 1) return TG_ERR_INVALID_VALUE;
         // The dynamic schedule runs CTA-pair tiles, one pair per cluster, whole tiles.
         if (o->schedule == 2 && (o->cta_pair == 1 || o->multicast == 2 || o->split_k > 1))
@@ -380,21 +394,31 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     if (o->producer == 1 && !legal) return TG_ERR_INVALID_VALUE;
     p.producer = o->producer ? o->producer : (legal ? 1 : 2);
 
-    // Tile shape: the candidate with the smallest (waves x cycles per K step
-    // of one tile).  Per 16-wide K step an SM's tensor core needs BN/2 cycles
-    // (128 rows each), and its shared memory moves the A and B bytes twice
-    // (TMA write, tensor-core read) at about 128 B/cycle: 64 + BN/2 cycles for
-    // a single-CTA tile, 64 + BN/4 when a CTA pair splits B.  A tile costs the
-    // larger of the two.  Pair tiles need 16-bit or 8-bit operands on TMA.
-    // (8-bit kinds take 32 elements per 32-byte K step at twice the rate,
-    // so the same per-byte costs apply.)
+    // Tile shape and schedule: the candidate with the smallest estimated time,
+    // (K blocks run in sequence by one CTA or pair) x (cycles per K block) +
+    // the fix-up of K-split tiles.  Per 16-wide K step an SM's tensor core
+    // needs BN/2 cycles (128 rows each), and its shared memory moves the A and
+    // B bytes twice (TMA write, tensor-core read) at about 128 B/cycle: 64 +
+    // BN/2 cycles for a single-CTA tile, 64 + BN/4 when a CTA pair splits B;
+    // a K step costs the larger of the two, and a K block is four steps
+    // (8-bit kinds take 32 elements per 32-byte step at twice the rate, TF32 8
+    // per 32 bytes at half, so the same per-byte costs apply).  A K-split tile
+    // (pair split tail, stream-K) adds kFixupLatency and 8 x BN cycles per
+    // partial tile its finisher reads (128 x BN FP32 at about 64 B/cycle).
+    // Calibrated on 1024^2 x 8192, 2048 x 512 x 16384, 512 x 2048 x 4096,
+    // 256^2 x 65536, 1024^3, 4096 x 128 x 8192, 128 x 4096 x 2048 and
+    // 256 x 128 x 512 (TF32): on each it picks the measured fastest
+    // candidate or one within 3 % of it.  Pair tiles need 16-bit or 8-bit
+    // operands on TMA.
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
-    // The dynamic schedule runs CTA-pair tiles only.
+    // The dynamic schedule runs CTA-pair tiles only; stream-K single-CTA tiles.
     const bool force_pair = o->cta_pair == 2 || o->schedule == 2;
+    const bool force_single = o->cta_pair == 1 || o->schedule == 3;
     if (force_pair && !pair_ok) return TG_ERR_INVALID_VALUE;
     if (force_pair && o->block_n == 64) return TG_ERR_INVALID_VALUE;
     // Pair tiles need a few K blocks to fill their 7-stage ring.
-    const bool pair_auto = pair_ok && ceil_div(K, block_k(t)) >= 8;
+    const int64_t nkb = ceil_div(K, block_k(t));
+    const bool pair_auto = pair_ok && nkb >= 8;
     struct Cand { bool pair; int bn; };
     Cand cands[5];
     int nc = 0;
@@ -402,22 +426,63 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     for (int bn : {256, 128, 64})
         if ((!o->block_n || o->block_n == bn) && !force_pair) cands[nc++] = {false, bn};
     for (int bn : {256, 128})
-        if ((!o->block_n || o->block_n == bn) && o->cta_pair != 1 &&
+        if ((!o->block_n || o->block_n == bn) && !force_single &&
             (force_pair ? pair_ok : pair_auto))
             cands[nc++] = {true, bn};
+    int64_t cap = sms;
+    if (o->max_ctas && cap > o->max_ctas) cap = o->max_ctas;
+    if (cap < 1) cap = 1;
+    const bool sk_ok = o->split_k != 1 && (o->schedule == 0 || o->schedule == 3);
     int64_t best = -1;
     for (int i = 0; i < nc; ++i) {
         const Cand c = cands[i];
         const int rows = c.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
         const int64_t tiles = q.batch * ceil_div(p.mk, rows) * ceil_div(p.nk, c.bn);
-        const int64_t slots = c.pair ? sms / 2 : sms;
+        int64_t slots = c.pair ? cap / 2 : cap;
+        if (slots < 1) slots = 1;
         const int64_t mma = c.bn / 2;
-        const int64_t smem = c.pair ? 64 + c.bn / 4 : 64 + c.bn / 2;
-        const int64_t est = ceil_div(tiles, slots > 0 ? slots : 1) * (mma > smem ? mma : smem);
+        // TF32 stages pass through shared memory twice more (narrowed in place
+        // by other warps, one more barrier hop per stage): three times the cost.
+        const int64_t smem = (c.pair ? 64 + c.bn / 4 : 64 + c.bn / 2) * (t == TG_TF32 ? 3 : 1);
+        const int64_t kb_cost = 4 * (mma > smem ? mma : smem);
+        int64_t chain = ceil_div(tiles, slots) * nkb, fix = 0;
+        if (c.pair && tiles < slots && o->split_k != 1 && o->schedule != 2) {
+            int64_t segs = slots / tiles;
+            const int64_t smax = o->split_k ? o->split_k : kDefaultSplitMax;
+            if (segs > smax) segs = smax;
+            if (segs > nkb / tg::SPLIT_MIN_KBLOCKS) segs = nkb / tg::SPLIT_MIN_KBLOCKS;
+            if (segs > 1) {
+                chain = ceil_div(nkb, segs);
+                fix = kFixupLatency + (segs - 1) * 8 * c.bn;
+            }
+        }
+        int64_t est = chain * kb_cost + fix;
+        bool sk = false;
+        if (!c.pair && sk_ok) {
+            const int64_t iters = tiles * nkb;
+            int64_t g = iters / kStreamKMinBlocks;
+            if (g > cap) g = cap;
+            if (o->schedule == 3 || (tiles < cap && g > tiles)) {
+                if (g < 1) g = 1;
+                // CTAs over one tile: nkb / share when the shares line up
+                // with the tiles, one more when they do not.
+                int64_t share = iters / g;  // K blocks per CTA (at least)
+                if (share < 1) share = 1;
+                const int64_t segs =
+                    ceil_div(nkb, share) + ((iters % g) || (nkb % share) ? 1 : 0);
+                const int64_t est_sk = ceil_div(iters, g) * kb_cost + kFixupLatency +
+                                       (segs - 1) * 8 * c.bn;
+                if (o->schedule == 3 || est_sk < est) {
+                    est = est_sk;
+                    sk = true;
+                }
+            }
+        }
         if (best < 0 || est < best) {
             best = est;
             p.pair = c.pair;
             p.block_n = c.bn;
+            p.stream_k = sk;
         }
     }
     const int rows = p.pair ? 2 * tg::BLOCK_M : tg::BLOCK_M;
@@ -461,7 +526,6 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         if (pairs_max < 1) pairs_max = 1;
         p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 1);
         if (p.mc != 1) p.split_max = 1;  // K segments only with one pair per cluster
-        const int64_t nkb = ceil_div(K, block_k(t));
         int64_t pairs = pairs_max;
         if (p.tiles < pairs_max) {
             int64_t segs = pairs_max / p.tiles;
@@ -484,8 +548,12 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         }
     } else {
         if (o->schedule == 2) return TG_ERR_INVALID_VALUE;  // needs CTA-pair tiles
-        int64_t grid = p.tiles < sms ? p.tiles : sms;
-        if (o->max_ctas && grid > o->max_ctas) grid = o->max_ctas;
+        int64_t grid = p.tiles < cap ? p.tiles : cap;
+        if (p.stream_k) {
+            // Every CTA up to the cap, at least kStreamKMinBlocks K blocks each.
+            grid = p.tiles * nkb / kStreamKMinBlocks;
+            if (grid > cap) grid = cap;
+        }
         p.grid = (int)(grid < 1 ? 1 : grid);
     }
     // Swapped roles store each thread's 32 consecutive columns as 16-byte
@@ -631,6 +699,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
             plan.tiles_per_batch = ceil_div(plan.mk, tg::BLOCK_M) * ceil_div(plan.nk, plan.block_n);
             plan.tiles = q.batch * plan.tiles_per_batch;
             plan.grid = (int)(plan.tiles < ds->sms ? plan.tiles : ds->sms);
+            plan.stream_k = false;
         }
     }
     tg::GemmParams &p = la.p;
@@ -674,6 +743,15 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
         if (st != TG_OK) return st;
         p.split_max = plan.split_max;
         p.ws_tiles = (int32_t)w.tiles;
+        p.ws = w.ws;
+        p.flags = w.flags;
+    }
+    if (!la.pair && plan.stream_k) {
+        // One 128 x 256 FP32 slot and one flag per CTA: half a pair tile each.
+        Workspace w;
+        st = workspace_for(dev, stream, ceil_div(plan.grid, 2), &w);
+        if (st != TG_OK) return st;
+        p.stream_k = 1;
         p.ws = w.ws;
         p.flags = w.flags;
     }
@@ -953,6 +1031,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->split_tiles = (int32_t)p.split_tiles;
     out->split_segs = p.split_segs;
     out->multicast = p.pair ? p.mc : 0;
+    out->stream_k = p.stream_k ? 1 : 0;
     out->block_n = p.block_n;
     out->block_k = block_k(in_dtype);
     out->stages = p.stages;

@@ -196,6 +196,12 @@ struct GemmParams {
     // running clusters take over clusters not yet started).
     int32_t dynamic;
     int32_t swap;                   // 1: role-space rows are D's columns (operands swapped)
+    // Single-CTA kernel: 1 = stream-K.  Each CTA takes a contiguous share of
+    // the num_tiles x num_k_blocks (tile, K block) iterations; a tile cut
+    // between CTAs is finished by the CTA holding its first K block, which
+    // adds the later CTAs' FP32 partials (workspace slot = CTA index, 128 x
+    // 256 floats each; one ready flag per slot).
+    int32_t stream_k;
     EpiProgram epi;                 // composed epilogue (n = 0: alpha and ReLU only)
 };
 
@@ -306,6 +312,50 @@ __device__ __forceinline__ void batch_tile_coords(int64_t t, const GemmParams &p
     b = (int)(t / p.tiles_per_batch);
     tile_coords(t - (int64_t)b * p.tiles_per_batch, p, mb, nb);
 }
+
+// First (tile, K block) iteration of CTA c of g under stream-K.
+__device__ __forceinline__ int64_t sk_start(int64_t total, int64_t c, int64_t g) {
+    return total * c / g;
+}
+
+// The single-CTA kernel's work units, the same sequence for every role:
+// whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...; or, under stream-K,
+// this CTA's share of the iterations cut at tile boundaries.  A unit is tile
+// t, K blocks [k0, k1).
+struct TileUnits {
+    int64_t pos, end, t;
+    int32_t k0, k1;
+    __device__ __forceinline__ explicit TileUnits(const GemmParams &p) {
+        if (p.stream_k) {
+            const int64_t total = p.num_tiles * p.num_k_blocks;
+            pos = sk_start(total, blockIdx.x, gridDim.x);
+            end = sk_start(total, blockIdx.x + 1, gridDim.x);
+        } else {
+            pos = end = 0;
+        }
+        t = (int64_t)blockIdx.x - gridDim.x;
+        k0 = k1 = 0;
+    }
+    __device__ __forceinline__ bool next(const GemmParams &p) {
+        const int nkb = p.num_k_blocks;
+        if (!p.stream_k) {
+            t += gridDim.x;
+            k0 = 0;
+            k1 = nkb;
+            return t < p.num_tiles;
+        }
+        if (pos >= end) return false;
+        t = pos / nkb;
+        k0 = (int32_t)(pos - t * nkb);
+        const int64_t left = end - pos;
+        k1 = left < nkb - k0 ? k0 + (int32_t)left : nkb;
+        pos += k1 - k0;
+        return true;
+    }
+};
+
+// Stream-K workspace slot of CTA c: 128 rows x 256 columns of FP32, column-major.
+constexpr int64_t SK_SLOT_FLOATS = (int64_t)128 * 256;
 
 __device__ __forceinline__ float apply_epilogue(float x, float alpha, int relu) {
     const float y = alpha * x;
@@ -544,6 +594,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
     auto b_stage = [&](int s) -> uint32_t { return sbase + C::B_OFF + s * C::B_BYTES; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    volatile int *fin_ready = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
     const WaitCtl ctl{abort_flag, p.status, p.wait_limit_ns};
 
     if (threadIdx.x == 0) {
@@ -584,12 +635,13 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         uint32_t ph = 0;
         bool ok = true;
         constexpr int E = C::T::elem_bytes;
-        for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        TileUnits un(p);
+        while (ok && un.next(p)) {
             int bt, mb, nb;
-            batch_tile_coords(t, p, bt, mb, nb);
+            batch_tile_coords(un.t, p, bt, mb, nb);
             const uint8_t *a_src = static_cast<const uint8_t *>(p.a_ptr) + (int64_t)bt * p.stride_a * E;
             const uint8_t *b_src = static_cast<const uint8_t *>(p.b_ptr) + (int64_t)bt * p.stride_b * E;
-            for (int kb = 0; kb < nkb; ++kb) {
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                 load_stage_plain<E, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES, a_src, p.lda,
                                                  mb * BLOCK_M, p.m, kb * C::BK, p.k, ltid);
@@ -609,19 +661,20 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            TileUnits un(p);
+            while (ok && un.next(p)) {
                 int bt, mb, nb;
-                batch_tile_coords(t, p, bt, mb, nb);
+                batch_tile_coords(un.t, p, bt, mb, nb);
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
                 if (p.prefetch_k > 0) {
-                    for (int j = 0; j < p.prefetch_k && j < nkb; ++j)
+                    for (int j = un.k0; j < un.k0 + p.prefetch_k && j < un.k1; ++j)
                         tma_prefetch_l2_3d(&tmap_a, j * C::BK, mb * BLOCK_M, ab);
                 }
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (p.prefetch_k > 0 && (kb & 3) == 0) {
+                for (int kb = un.k0; kb < un.k1; ++kb) {
+                    if (p.prefetch_k > 0 && ((kb - un.k0) & 3) == 0) {
                         for (int j = 0; j < 4; ++j) {
                             const int kp = kb + p.prefetch_k + j;
-                            if (kp < nkb) tma_prefetch_l2_3d(&tmap_a, kp * C::BK, mb * BLOCK_M, ab);
+                            if (kp < un.k1) tma_prefetch_l2_3d(&tmap_a, kp * C::BK, mb * BLOCK_M, ab);
                         }
                     }
                     if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
@@ -649,7 +702,8 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             bool ok = true;
             const int wait_bar0 = C::TF32 ? C::CONV0 : C::FULL0;
             const uint32_t wait_site = C::TF32 ? SITE_CONVERTED : SITE_FULL;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++tl) {
+            TileUnits un(p);
+            for (; ok && un.next(p); ++tl) {
                 const uint32_t acc = tl & 1, use = tl >> 1;
                 if (!wait_phase(bar(C::ACCE0 + acc), (use & 1) ^ 1, ctl, SITE_ACC_EMPTY)) {
                     ok = false;
@@ -657,7 +711,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = un.k0; kb < un.k1; ++kb) {
                     if (!wait_phase(bar(wait_bar0 + s), ph, ctl, wait_site)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
@@ -665,7 +719,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
                         const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
-                        const uint32_t accumulate = (kb | kk) != 0;
+                        const uint32_t accumulate = ((kb - un.k0) | kk) != 0;
                         mma_kind<KD>(d_tmem, ad, bd, C::IDESC, accumulate);
                     }
                     mma_commit(bar(C::EMPTY0 + s));  // stage s is free once these MMAs finish
@@ -686,22 +740,92 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         const int row_in_tile = q * 32 + lane;
         constexpr int COLS = BN / (C::EPI_WARPS / 4);  // columns of this warp
         const int cbase = ((warp - 2) / 4) * COLS;
+        const int etid = threadIdx.x - 64;            // 0 .. EPI_WARPS * 32 - 1
+        constexpr uint32_t EPI_THREADS = C::EPI_WARPS * 32;
+        const int64_t sk_total = p.num_tiles * (int64_t)nkb;
         uint32_t tl = 0;
-        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tl) {
+        TileUnits un(p);
+        for (; un.next(p); ++tl) {
             int bt, mb, nb;
-            batch_tile_coords(t, p, bt, mb, nb);
+            batch_tile_coords(un.t, p, bt, mb, nb);
             const uint32_t acc = tl & 1, use = tl >> 1;
             if (!wait_phase(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
             tc_fence_after();
             const int32_t r = mb * BLOCK_M + row_in_tile;
             const bool row_ok = r < p.m;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (un.k0 > 0) {
+                // Stream-K contributor (the first unit of this CTA's share):
+                // raw FP32 partial sums to this CTA's slot, then its flag.
+                float *dst = p.ws + (int64_t)blockIdx.x * SK_SLOT_FLOATS;
 #pragma unroll 1
-            for (int c0 = cbase; c0 < cbase + COLS; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + c0, v);
-                tmem_ld_wait();
-                if (row_ok) epilogue_store(p, bt, r, nb * BN + c0, v);
+                for (int c0 = cbase; c0 < cbase + COLS; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(dst + (int64_t)(c0 + j) * BLOCK_M + row_in_tile, __uint_as_float(v[j]));
+                }
+                __threadfence();
+                named_bar_sync(1, EPI_THREADS);
+                if (etid == 0) st_release_gpu_u32(p.flags + blockIdx.x, 1u);
+            } else {
+                // Owner of the tile.  Under stream-K with the tile cut (k1 <
+                // nkb), CTAs blockIdx.x + 1, ... hold its later K blocks:
+                // wait (bounded) for their partials, then add them in CTA order.
+                const int64_t tile_end = (un.t + 1) * nkb;
+                int64_t c_last = blockIdx.x;  // last contributing CTA
+                if (un.k1 < nkb) {
+                    while (c_last + 1 < gridDim.x &&
+                           sk_start(sk_total, c_last + 1, gridDim.x) < tile_end)
+                        ++c_last;
+                }
+                bool ready = true;
+                if (c_last > blockIdx.x) {
+                    if (etid == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        for (int64_t c = blockIdx.x + 1; c <= c_last && ready; ++c) {
+                            while (ld_acquire_gpu_u32(p.flags + c) == 0u) {
+                                if (*abort_flag || globaltimer_ns() - t0 > p.wait_limit_ns) {
+                                    if (!*abort_flag) {
+                                        *abort_flag = 1;
+                                        atomicCAS(p.status, 0u, (uint32_t)SITE_PARTIAL);
+                                    }
+                                    ready = false;
+                                    break;
+                                }
+                            }
+                        }
+                        *fin_ready = ready ? 1 : 0;
+                    }
+                    named_bar_sync(1, EPI_THREADS);
+                    ready = *fin_ready != 0;
+                    if (ready)
+                        for (int64_t c = blockIdx.x + 1; c <= c_last; ++c)
+                            (void)ld_acquire_gpu_u32(p.flags + c);
+                }
+#pragma unroll 1
+                for (int c0 = cbase; ready && c0 < cbase + COLS; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c0, v);
+                    tmem_ld_wait();
+                    for (int64_t c = blockIdx.x + 1; c <= c_last; ++c) {
+                        const float *src =
+                            p.ws + c * SK_SLOT_FLOATS + (int64_t)c0 * BLOCK_M + row_in_tile;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                                   __ldcg(src + (int64_t)j * BLOCK_M));
+                    }
+                    if (row_ok) epilogue_store(p, bt, r, nb * BN + c0, v);
+                }
+                if (c_last > blockIdx.x) {
+                    // Leave the flags at zero for the next launch.
+                    named_bar_sync(1, EPI_THREADS);
+                    if (etid == 0 && ready)
+                        for (int64_t c = blockIdx.x + 1; c <= c_last; ++c) p.flags[c] = 0u;
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -716,8 +840,9 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            for (int kb = 0; kb < nkb; ++kb) {
+        TileUnits un(p);
+        while (ok && un.next(p)) {
+            for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!wait_phase(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
                 uint4 *a4 = reinterpret_cast<uint4 *>(smem + C::A_OFF + s * C::A_BYTES) + ct;
                 uint4 *b4 = reinterpret_cast<uint4 *>(smem + C::B_OFF + s * C::B_BYTES) + ct;

@@ -128,18 +128,22 @@ typedef struct {
     int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
     int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (not TF32; TMA) */
     int32_t split_k;      /* 0: planner (pair tiles fewer than pairs: split them into up to 8
-                             K segments of >= 8 K blocks); 1: never split; n >= 2: split the
-                             last, partial wave into at most n segments */
+                             K segments of >= 8 K blocks); 1: never split (nor stream-K);
+                             n >= 2: split the last, partial wave into at most n segments */
     int32_t l2_hint;      /* 0: planner (default policy); 1: default L2 policy for operand loads;
                              2: A-role rows evict-last (CTA-pair tiles) */
     int32_t prefetch_k;   /* 0: planner; -1: off; n > 0: single-CTA TMA tiles prefetch the A-role
                              rows n K blocks ahead into L2, 4 blocks per burst */
     int32_t multicast;    /* 0: planner; 1: one CTA pair per cluster; 2: two pairs per cluster
                              sharing their A-role rows by TMA multicast (CTA-pair tiles) */
-    int32_t schedule;     /* 0: planner (static); 1: static persistent tiles; 2: dynamic: one
-                             2-CTA cluster per tile, running clusters take over clusters not
-                             yet started (cluster launch control); CTA-pair tiles, no split-K,
-                             no multicast */
+    int32_t schedule;     /* 0: planner (static, or stream-K for single-CTA tiles fewer than
+                             CTAs); 1: static persistent tiles; 2: dynamic: one 2-CTA cluster
+                             per tile, running clusters take over clusters not yet started
+                             (cluster launch control); CTA-pair tiles, no split-K, no multicast;
+                             3: stream-K: single-CTA tiles, each CTA a contiguous share of all
+                             (tile, K block) iterations, at least 8 K blocks each; a tile cut
+                             between CTAs is finished by the one holding its first K block,
+                             adding the others' FP32 partials in CTA order (deterministic) */
     int32_t reserved[1];  /* must be zero */
 } tg_options;
 
@@ -163,6 +167,8 @@ typedef struct {
     int32_t split_tiles;  /* tiles of the last wave computed as K segments (0: none) */
     int32_t split_segs;   /* K segments per such tile (1: none) */
     int32_t multicast;    /* CTA pairs per cluster sharing A rows (1 or 2; 0 for single-CTA) */
+    int32_t stream_k;     /* 1 if single-CTA tiles run as stream-K (each CTA a contiguous share
+                             of all (tile, K block) iterations; cut tiles summed in CTA order) */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides

@@ -65,7 +65,9 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
     dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
-    dict(opts={"reserved": [1]}), dict(opts={"multicast": 3}), dict(opts={"schedule": 3}),
+    dict(opts={"reserved": [1]}), dict(opts={"multicast": 3}), dict(opts={"schedule": 4}),
+    dict(opts={"schedule": 3, "cta_pair": 2}), dict(opts={"schedule": 3, "split_k": 1}),
+    dict(opts={"schedule": 3, "multicast": 2}),
     dict(opts={"schedule": 2, "cta_pair": 1}), dict(opts={"schedule": 2, "multicast": 2}),
     dict(opts={"schedule": 2, "split_k": 2}),
     dict(opts={"multicast": 2, "cta_pair": 1}),
@@ -367,3 +369,38 @@ def test_mx_batched_empty_is_ok_without_cuda(tg):
                                  1, 0, 4, "e4m3", "f32") == tg.TG_OK
     assert tg.tg_gemm_mx_batched(10, 10, 64, 1.0, FAKE, 64, 0, FAKE, 0, FAKE, 64, 0, FAKE, 0, FAKE,
                                  10, 100, 0, "e4m3", "f32") == tg.TG_OK
+
+
+def test_plan_stream_k(tg):
+    """Stream-K: single-CTA tiles spread over up to every SM (at least 8 K
+    blocks each) where the shorter K chain outweighs the fix-up; schedule 1
+    or split_k 1 turn it off; schedule 3 forces it."""
+    long_k = si.Workload("long_k", 256, 256, 65536, "bf16", 1.0, True, 0, "normal")
+    p = plan(tg, long_k)
+    assert (p["stream_k"], p["cta_pair"], p["block_n"], p["grid"], p["tiles"]) == (1, 0, 64, 152, 8)
+    assert plan(tg, long_k, opts={"max_ctas": 100})["grid"] == 100
+    s = plan(tg, long_k, opts={"schedule": 1})
+    assert s["stream_k"] == 0
+    assert plan(tg, long_k, opts={"split_k": 1})["stream_k"] == 0
+    c2 = plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])
+    assert (c2["stream_k"], c2["grid"], c2["tiles"]) == (1, 8, 4)        # 2 CTAs per tile
+    # Short K chains stay whole: the fix-up would cost more than it saves.
+    for name in ("c1_bf16_65x97x73", "c5a_bf16_16384x64x4096", "c5b_bf16_64x16384x4096"):
+        assert plan(tg, si.WORKLOADS[name])["stream_k"] == 0, name
+    assert plan(tg, si.Workload("k1024", 1024, 1024, 1024, "bf16", 1.0, True, 0, "normal"))[
+        "split_segs"] == 1
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["stream_k"] == 0          # pair tiles
+    one = si.Workload("one", 128, 64, 4096, "bf16", 1.0, True, 0, "normal")
+    f = plan(tg, one, opts={"schedule": 3})
+    assert (f["stream_k"], f["grid"], f["tiles"]) == (1, 8, 1)            # 64 K blocks / 8
+    big = plan(tg, si.WORKLOADS["c3_fp16_4096"], opts={"schedule": 3})
+    assert big["stream_k"] == 1 and big["cta_pair"] == 0 and big["grid"] == 152
+
+
+def test_plan_k_split_pairs_for_mid_shapes(tg):
+    """Fewer pair tiles than pairs with a long K loop: the pair split tail
+    (K segments on otherwise idle pairs) beats one wave of narrow tiles."""
+    for (M, N, K), bn, segs in [((1024, 1024, 8192), 256, 4), ((2048, 512, 16384), 256, 4),
+                                ((4096, 128, 8192), 128, 4), ((512, 2048, 4096), 128, 2)]:
+        p = plan(tg, si.Workload("mid", M, N, K, "bf16", 1.0, True, 0, "normal"))
+        assert (p["cta_pair"], p["block_n"], p["split_segs"]) == (1, bn, segs), (M, N, K)
