@@ -35,10 +35,13 @@
  * device can address); D must not overlap A or B.  The library keeps state of
  * its own: per device a status word and cached attributes, allocated on the
  * first call on the device; and per (device, stream) a workspace of about
- * 20 MB (the partial sums of split tail tiles, plus their ready flags),
- * allocated on the first call on that stream that splits a tile and kept
- * until the process exits.  Calls on different streams never share a
- * workspace.
+ * 20 MB (the partial sums of tiles whose K loop is split across CTAs, by
+ * the pair split tail or stream-K, plus their ready flags), allocated on the
+ * first call on that stream that splits a tile and kept until the process
+ * exits.  Calls on different streams never share a workspace.  That first
+ * allocation synchronises the device, so inside a stream capture either
+ * make one call of a splitting shape on the stream beforehand, pass
+ * split_k = 1 (tg_gemm_ex), or use tg_gemm_noalloc.
  *
  * Asynchrony: tg_gemm enqueues its work on `stream` (a cudaStream_t passed as
  * void*, NULL for the legacy default stream) and returns without waiting;
