@@ -120,9 +120,12 @@ def oracle_sample_time(w: si.Workload, A, B, rows: int, cols: int, threads: int 
 
 
 def calibrate_block(w, A, B, target_s: float) -> int:
-    """Square sample size whose oracle time is about target_s."""
-    t = oracle_sample_time(w, A, B, 128, 128)
-    per_entry = max(t / (128.0 * 128.0), 1e-9)
+    """Square sample size whose oracle time is about target_s (timed first on
+    a 512 x 512 sample: smaller ones overstate the cost per entry, their
+    columns leaving host threads idle)."""
+    c = int(min(512, w.M, w.N))
+    t = oracle_sample_time(w, A, B, c, c)
+    per_entry = max(t / (float(c) * c), 1e-9)
     s = int((target_s / per_entry) ** 0.5) // 64 * 64
     return int(max(64, min(s, w.M, w.N)))
 
