@@ -749,7 +749,10 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             int bt, mb, nb;
             batch_tile_coords(un.t, p, bt, mb, nb);
             const uint32_t acc = tl & 1, use = tl >> 1;
-            if (!wait_phase(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
+            const bool got = wait_phase(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL);
+            // Stream-K units synchronise the epilogue warps on named barriers,
+            // so they leave together: if any thread's wait gave up, all stop.
+            if (p.stream_k ? named_bar_any(2, EPI_THREADS, !got) : !got) break;
             tc_fence_after();
             const int32_t r = mb * BLOCK_M + row_in_tile;
             const bool row_ok = r < p.m;

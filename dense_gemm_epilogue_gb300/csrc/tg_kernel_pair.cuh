@@ -400,7 +400,10 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             batch_tile_coords(un.tile, p, bt, mb, nbc);
             const int nb = nbc * MC + (int)pic;
             const uint32_t acc = tl & 1, use = tl >> 1;
-            if (!pair_wait(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL)) break;
+            const bool got = pair_wait(bar(C::ACCF0 + acc), use & 1, ctl, SITE_ACC_FULL);
+            // With split tiles the epilogue warps meet on named barriers, so
+            // they leave together: if any thread's wait gave up, all stop.
+            if (up.segs > 1 ? named_bar_any(2, EPI_THREADS, !got) : !got) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             // Partial tile `k` of this tail tile, this CTA's half: column-major
