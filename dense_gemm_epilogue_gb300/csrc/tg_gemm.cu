@@ -644,6 +644,18 @@ tg_status make_program(const tg_epi_op *ops, int32_t n_ops, tg::EpiProgram *prog
     return TG_OK;
 }
 
+// With TG_LOG set in the environment, one line per call: the planner's choice.
+void log_plan(const char *what, const Problem &q, const Plan &p) {
+    if (!std::getenv("TG_LOG")) return;
+    std::fprintf(stderr,
+                 "%s: M=%lld N=%lld K=%lld batch=%lld -> %s BN=%d mc=%d swap=%d producer=%d "
+                 "tiles=%lld grid=%d stages=%d group=%d split=%lldx%d stream_k=%d dynamic=%d\n",
+                 what, (long long)q.M, (long long)q.N, (long long)q.K, (long long)q.batch,
+                 p.pair ? "pair" : "single", p.block_n, p.mc, p.swap ? 1 : 0, p.producer,
+                 (long long)p.tiles, p.grid, p.stages, p.group, (long long)p.split_tiles,
+                 p.split_segs, p.stream_k ? 1 : 0, p.dynamic ? 1 : 0);
+}
+
 tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *stream_ptr,
               const tg::EpiProgram *prog = nullptr) {
     static const tg::EpiProgram kNoOps = {};
@@ -756,6 +768,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
         p.flags = w.flags;
     }
     la.grid = plan.grid;
+    log_plan("tg_gemm", q, plan);
     la.device = dev;
     la.stream = stream;
 
@@ -959,6 +972,7 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.split_max = 1;
     la.grid = plan.grid;
+    log_plan("tg_gemm_mx", q, plan);
     la.device = dev;
     la.stream = stream;
     const cudaError_t e = tg::launch_mx(la, q.t == TG_E4M3   ? Kind::E4M3

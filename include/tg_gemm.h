@@ -146,7 +146,10 @@ typedef struct {
                              3: stream-K: single-CTA tiles, each CTA a contiguous share of all
                              (tile, K block) iterations, at least 8 K blocks each; a tile cut
                              between CTAs is finished by the one holding its first K block,
-                             adding the others' FP32 partials in CTA order (deterministic) */
+                             adding the others' FP32 partials in CTA order (deterministic).
+                             Its CTAs (at most one per SM) wait on one another, so they must
+                             all fit on the device at once: where the SMs are restricted (an
+                             MPS thread limit), pass 1 */
     int32_t reserved[1];  /* must be zero */
 } tg_options;
 

@@ -288,3 +288,26 @@ def test_many_ragged_tiles_sampled():
     got = out[J, I]
     assert_within(got, ref, scale, w.dtype, w.name)
     assert np.array_equal(out[:, w.M:].view(np.uint32), D0[:, w.M:].view(np.uint32))
+
+
+def test_cross_check_against_torch_matmul():
+    """An extra signal beside the oracle: torch.matmul (cuBLAS, FP32, no TF32)
+    on the same buffers, D^T = relu(alpha * B_t A_t^T), within the same bound."""
+    import torch
+
+    w = si.Workload("xcheck", 1000, 1500, 2048, "bf16", 0.5, True, 800, "normal", ldc=1004)
+    lda, ldb, ldc = w.strides
+    A, B = si.make_operands(w)
+    D = run_tg(w, A, B, si.make_output(w))
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        At = torch.from_numpy(A.view(np.int16)).cuda().view(torch.bfloat16)[:, : w.K].float()
+        Bt = torch.from_numpy(B.view(np.int16)).cuda().view(torch.bfloat16)[:, : w.K].float()
+        ref = torch.relu(w.alpha * (Bt @ At.T))                       # (N, M)
+        scale = abs(w.alpha) * (Bt.abs() @ At.abs().T)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    got = torch.from_numpy(np.ascontiguousarray(D[:, : w.M])).cuda()
+    err = (got - ref).abs()
+    assert bool((err <= 2.0 ** -7 * scale + 1e-6).all()), float(err.max())
