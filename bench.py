@@ -143,10 +143,24 @@ def cpu_baseline(w: si.Workload, A, B, target_s: float = 15.0) -> dict:
     }
 
 
+def metric_name(w: si.Workload, nbat: int = 1, out: str = "f32") -> str:
+    """The headline metric for the benchmark workload; for any other workload
+    the same quantity (TFLOP/s) named by its type, epilogue and shape."""
+    if w.name == WORKLOAD and nbat == 1 and out == "f32":
+        return METRIC
+    return (f"{'block-scaled (32-element blocks) ' if w.block_scaled else ''}"
+            f"{w.dtype} GEMM{'+ReLU' if w.relu else ''} TFLOP/s at {w.M}x{w.N}x{w.K}"
+            + (f" x{nbat}" if nbat > 1 else "") + (f", {out} out" if out != "f32" else ""))
+
+
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, timed on the host cores
+    on a bounded square sample D[0:s, 0:s] (full K) of the chosen workload."""
     if rank != 0:
         return 0
-    w = si.WORKLOADS[WORKLOAD]
+    if args.batch != 1 or args.out != "f32":
+        raise SystemExit("--impl reference times the unbatched product with FP32 output")
+    w = si.WORKLOADS[args.workload]
     A, B = si.make_operands(w)
     import oracle
 
@@ -160,15 +174,16 @@ def run_reference(args, rank, world):
     flops = 2.0 * blk * blk * w.K
     value = flops * args.steps / total / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": metric_name(w), "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.host_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: D[0:{blk}, 0:{blk}] of the 8192^3 workload "
-                                   f"(full K), double-precision C triple loop on the host cores"},
+                         "sample": f"each step: D[0:{blk}, 0:{blk}] of the {w.M}x{w.N}x{w.K} "
+                                   f"workload (full K), double-precision C triple loop on the "
+                                   f"host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -485,10 +500,7 @@ def run_gpu(args, rank, world, local):
         traffic = load_traffic(tg.source_hash()) if args.workload == WORKLOAD and not batched else None
         default_run = args.workload == WORKLOAD and not batched
         line = {
-            "metric": METRIC if default_run else
-                      f"{'block-scaled (32-element blocks) ' if mx else ''}"
-                      f"{dt} GEMM{'+ReLU' if w.relu else ''} TFLOP/s at {w.M}x{w.N}x{w.K}"
-                      + (f" x{nbat}" if nbat > 1 else "") + (f", {out} out" if out != 'f32' else ""),
+            "metric": metric_name(w, nbat, out),
             "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
