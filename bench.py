@@ -199,15 +199,35 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # power.draw is averaged over about a second, longer than the timed region;
+    # the instantaneous reading is taken too where this nvidia-smi knows it.
+    INSTANT = "power.draw.instant"
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.t0 = self.t1 = None
+        self.instant = False
+
+    def _knows_instant(self) -> bool:
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index),
+                                f"--query-gpu={self.INSTANT}", "--format=csv,noheader,nounits"],
+                               capture_output=True, text=True, timeout=20)
+        except (OSError, subprocess.SubprocessError):
+            return False
+        try:
+            float(r.stdout.strip().splitlines()[0])
+        except (ValueError, IndexError):
+            return False
+        return r.returncode == 0
 
     def start(self):
+        self.instant = self._knows_instant()
+        query = self.QUERY + ("," + self.INSTANT if self.instant else "")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={query}",
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
@@ -241,12 +261,15 @@ class ClockSampler:
         smax = [float(s[3]) for s in use if s[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in use for i in range(4) if s[6 + i] == "Active"})
+        col = 10 if self.instant else 4
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(use),
                 "samples_in_timed_region": len(inside),
-                "power_w_max": max((float(s[4]) for s in use
-                                    if s[4].replace(".", "").isdigit()), default=None)}
+                "power_w_max": max((float(s[col]) for s in use
+                                    if len(s) > col and s[col].replace(".", "").isdigit()),
+                                   default=None),
+                "power_field": self.INSTANT if self.instant else "power.draw"}
 
 
 def load_peaks():

@@ -52,3 +52,19 @@ def test_reference_arm_rejects_batches():
     r = run_bench("--impl", "reference", "--workload", "c1_bf16_65x97x73", "--batch", "2")
     assert r.returncode != 0
     assert "unbatched" in r.stderr
+
+
+def test_metric_names():
+    sys.path.insert(0, ROOT)
+    import bench
+    import seeded_inputs as si
+
+    assert bench.metric_name(si.WORKLOADS[bench.WORKLOAD]) == bench.METRIC
+    assert bench.metric_name(si.WORKLOADS[bench.WORKLOAD], 1, "bf16") == \
+        "bf16 GEMM+ReLU TFLOP/s at 8192x8192x8192, bf16 out"
+    assert bench.metric_name(si.WORKLOADS["c3_fp16_4096"], 4, "bf16") == \
+        "fp16 GEMM+ReLU TFLOP/s at 4096x4096x4096 x4, bf16 out"
+    assert bench.metric_name(si.WORKLOADS["c2_tf32_256x128x512"]) == \
+        "tf32 GEMM TFLOP/s at 256x128x512"
+    assert bench.metric_name(si.WORKLOADS["mx_e2m1_8192"]).startswith(
+        "block-scaled (32-element blocks) e2m1 GEMM+ReLU")
