@@ -154,8 +154,12 @@ tg_status workspace_for(int dev, cudaStream_t stream, int64_t tiles, Workspace *
         cudaFree(w.ws);
         return TG_ERR_CUDA;
     }
-    if (cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * tiles) != cudaSuccess) return TG_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
+    if (cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * tiles) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(w.flags);
+        cudaFree(w.ws);
+        return TG_ERR_CUDA;
+    }
     // A smaller workspace of the same stream stays allocated (it may still be
     // in use by queued work); the larger one replaces it for later calls.
     for (Workspace &old : g_ws)
@@ -190,8 +194,12 @@ tg_status device_state(int *dev_out, DeviceState **out) {
             return TG_ERR_CUDA;
         if (s.cc_major != 10 || s.cc_minor != 3) return TG_ERR_UNSUPPORTED;
         if (cudaMalloc(&s.status, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
-        if (cudaMemset(s.status, 0, sizeof(uint32_t)) != cudaSuccess) return TG_ERR_CUDA;
-        if (cudaDeviceSynchronize() != cudaSuccess) return TG_ERR_CUDA;
+        if (cudaMemset(s.status, 0, sizeof(uint32_t)) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(s.status);
+            s.status = nullptr;
+            return TG_ERR_CUDA;
+        }
         s.ready = true;
     }
     *dev_out = dev;

@@ -8,26 +8,31 @@
 // D[r*ldc + c]; both operands are K-major, so the swap costs nothing.
 //
 // Roles per CTA (one CTA per SM, persistent over output tiles):
-//   warp 0      producer: TMA 2-D loads (or plain bounds-checked loads that
-//               write the same swizzled layout) into an S-stage ring guarded by
-//               full/empty mbarriers ("Walk through GEMM" sections 3-4: copy a
-//               K stage, consume, then release it; here the release is the
-//               tensor core's own completion signal).
+//   warp 0      producer: one thread issues TMA loads (3-D maps: K, rows,
+//               batch entry) into an S-stage ring guarded by full/empty
+//               mbarriers ("Walk through GEMM" sections 3-4: copy a K stage,
+//               consume, then release it; here the release is the tensor
+//               core's own completion signal).
 //   warp 1      tensor-memory allocator and MMA issuer: one thread issues
 //               tcgen05.mma (128 x BN x 16 for 16-bit kinds, x8 for TF32, x32
-//               for 8-bit floats) into
-//               one of two TMEM accumulators, FP32 ("Matrix Multiplication"
-//               step 3: the accumulator is wider than the inputs).
-//   warps 2-5   epilogue: tcgen05.ld TMEM -> registers, y = alpha*x, then the
-//               max with zero when ReLU is on ("Walk through GEMM" section 5),
-//               bounds-checked stores of the rows/columns inside the problem
-//               ("Matrix Multiplication", ragged sizes: the overhang is not
-//               stored).  Two accumulators let tile t's epilogue overlap tile
-//               t+1's main loop.
-//   warps 6-9   (TF32 only) narrow each landed FP32 stage in place to TF32
+//               for 8-bit floats) into one of two TMEM accumulators, FP32
+//               ("Matrix Multiplication" step 3: the accumulator is wider than
+//               the inputs).
+//   warps 2-9   epilogue (warps 2-5 for TF32): tcgen05.ld TMEM -> registers,
+//               y = alpha*x, then the max with zero when ReLU is on ("Walk
+//               through GEMM" section 5), bounds-checked stores of the
+//               rows/columns inside the problem ("Matrix Multiplication",
+//               ragged sizes: the overhang is not stored).  A warp reads the
+//               TMEM lane quarter warp % 4; with 8 warps each quarter has two,
+//               one per half of the columns.  Two accumulators let tile t's
+//               epilogue overlap tile t+1's main loop.
+//   warps 6-13  (TF32 only) narrow each landed FP32 stage in place to TF32
 //               (round to nearest, ties away from zero) before the MMA reads it
 //               ("Matrix Multiplication" step 4: convert the operand tiles to
 //               TFloat32, keep the accumulator FP32).
+//   last 4      (plain-load variant only) the producer: bounds-checked loads
+//               that write the TMA's swizzled layout, for strides or bases the
+//               TMA cannot address.
 // Out-of-range K columns of A and rows of B are read as zeros (TMA
 // out-of-bounds fill, or the plain loader's bounds check), which adds nothing
 // to the sums ("Matrix Multiplication", ragged sizes: zero padding).
