@@ -162,3 +162,33 @@ def test_grid_cap_is_respected(tg):
             assert p["grid"] <= cl * max(1, min(sms, cap) // cl)
         else:
             assert p["grid"] <= min(sms, cap)
+
+
+def test_block_scaled_plans_over_a_sweep(tg):
+    """The block-scaled planner: CTA-pair tiles 256 x 128 or 256 x 256 over
+    all pairs of the device (fewer when there are fewer tiles), TMA only
+    (strides that are not multiples of 16 bytes, or odd FP4 rows, are refused)."""
+    rng = np.random.default_rng(31)
+    for M, N, K, dtype, _, _, ldc, sms in shapes(seed=5, n=600):
+        kind = str(rng.choice(["e4m3", "e5m2", "e2m1"]))
+        if kind == "e2m1":
+            K += K & 1                                  # packed FP4: whole bytes per row
+        per16 = 32 if kind == "e2m1" else 16            # elements per 16 bytes
+        ld = cdiv(K, per16) * per16 + per16 * int(rng.integers(0, 2))
+        p = tg.tg_plan_mx(M, N, K, ld, ld, ldc, kind, None, sms)
+        swap = M < 128 and N >= 128 and N >= 2 * M
+        mk, nk = (N, M) if swap else (M, N)
+        assert p["swap_ab"] == int(swap) and p["cta_pair"] == 1 and p["producer"] == 1
+        assert p["block_m"] == 256 and p["block_n"] in (128, 256)
+        assert p["block_k"] == (256 if kind == "e2m1" else 128)
+        assert p["tiles"] == cdiv(mk, 256) * cdiv(nk, p["block_n"])
+        assert p["grid"] == 2 * min(p["tiles"], max(1, sms // 2))
+        assert 1 <= p["raster_group"] <= cdiv(mk, 256)
+        assert 0 < p["smem_bytes"] <= SMEM_LIMIT and p["stages"] >= 2
+        t = p["tmem_cols"]
+        assert 32 <= t <= 512 and t & (t - 1) == 0
+        assert p["threads"] % 32 == 0 and p["threads"] <= 1024
+        # A stride that is not a multiple of 16 bytes has no plain-load path here.
+        bad = ld + (2 if kind == "e2m1" else 1)
+        with pytest.raises(tg.TgError):
+            tg.tg_plan_mx(M, N, K, bad, ld, ldc, kind, None, sms)
