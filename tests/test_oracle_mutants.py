@@ -70,6 +70,30 @@ MUTANTS = {
     "mx_wrong_row_scale": ("Xa[i * KB + kb] = orc_decode_e8m0(SA[i * ldsa + kb]);",
                            "Xa[i * KB + kb] = orc_decode_e8m0(SA[(M - 1 - i) * ldsa + kb]);"),
     "mx_scale_abs_dropped": ("t += fabs(x) * bt;", "t += bt;"),
+    "tf32_keeps_11_bits": ("uint32_t q = sig >> 13;           /* kept: 11 (or fewer) leading bits */\n"
+                           "        uint32_t r = sig & 0x1FFFu;       /* dropped: 13 bits */\n"
+                           "        if (r >= 0x1000u) q += 1;         /* half or more: away from zero */\n"
+                           "        v = ldexp((double)q, ee - 23 + 13);",
+                           "uint32_t q = sig >> 12;\n"
+                           "        uint32_t r = sig & 0xFFFu;\n"
+                           "        if (r >= 0x800u) q += 1;\n"
+                           "        v = ldexp((double)q, ee - 23 + 12);"),
+    "tf32_no_overflow": ("if (v > ldexp(2047.0, 127 - 10)) v = INFINITY;", "if (0) v = INFINITY;"),
+    "bf16_subnormal_scale": ("v = ldexp((double)f, -126 - 7);", "v = ldexp((double)f, -127 - 7);"),
+    "fp16_bias": ("v = ldexp((double)(1024 + f), e - 15 - 10);", "v = ldexp((double)(1024 + f), e - 14 - 10);"),
+    "e5m2_bias": ("else v = ldexp((double)(4 + f), e - 15 - 2);", "else v = ldexp((double)(4 + f), e - 16 - 2);"),
+    "lda_ignored": ("Ad[i * K + k] = decode_elem(A, i * lda + k, dtype);",
+                    "Ad[i * K + k] = decode_elem(A, i * K + k, dtype);"),
+    "ldb_ignored": ("Bd[j * K + k] = decode_elem(B, k + j * ldb, dtype);",
+                    "Bd[j * K + k] = decode_elem(B, k + j * K, dtype);"),
+    "epi_sigmoid_sign": ("case ORC_EPI_SIGMOID: return 1.0 / (1.0 + exp(-y));",
+                         "case ORC_EPI_SIGMOID: return 1.0 / (1.0 + exp(y));"),
+    "epi_bias_col_by_row": ("case ORC_EPI_BIAS_COL: return y + (double)bias[j];",
+                            "case ORC_EPI_BIAS_COL: return y + (double)bias[i];"),
+    "epi_add_subtracts": ("case ORC_EPI_ADD: return y + a;", "case ORC_EPI_ADD: return y - a;"),
+    "round_bf16_extra_bit": ("case 1: y[q] = round_format(y[q], 8, -126, 127); break;",
+                             "case 1: y[q] = round_format(y[q], 9, -126, 127); break;"),
+    "round_no_subnormal_floor": ("if (ee < emin) ee = emin;", "if (0) ee = emin;"),
     "scale_signed_alpha": ("jb->scale[i + j * jb->ldd] = fabs(jb->alpha) * t;",
                            "jb->scale[i + j * jb->ldd] = jb->alpha * t;"),
 }
