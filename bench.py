@@ -7,12 +7,15 @@ A, B BF16 (seeded standard normal), D FP32 column-major, alpha = 1.  Inputs
 stay resident in HBM; A + B (268 MB) and D (268 MB) are each larger than the
 129 MB L2, so no flush is needed between steps.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead (the only other arm), on a bounded sample of the same workload.
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
+only other arm), on a bounded sample of the same workload.
 
-Multi-GPU runs (torchrun) are independent replicas: each rank computes the
-full workload on its own GPU with no collective on the data path; the value
-is the FLOPs of all ranks over the slowest rank's time ("weak" scaling).
+The library is single-GPU: some of its kernels load operand tiles with
+cluster-multicast TMA, which is used only by calls that run on one GPU.  The
+GPU arm therefore refuses to run with more than one GPU (``--gpus`` other
+than 1, or a ``WORLD_SIZE`` above 1) and exits non-zero.  The reference arm
+never touches a GPU; under a multi-rank launch rank 0 runs it and the other
+ranks exit without work.
 """
 
 from __future__ import annotations
@@ -43,7 +46,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 
 def parse():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs to use; the GPU arm runs on exactly one")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
@@ -67,6 +71,16 @@ def dist_env():
     return rank, world, local
 
 
+def single_gpu_refusal(args, world: int) -> str | None:
+    """Why the GPU arm must not run with these arguments, or None.  Both
+    --gpus and WORLD_SIZE must say one GPU: the library's multicast loads are
+    for single-GPU calls only, so there is no replica mode."""
+    if args.gpus != 1 or world != 1:
+        return (f"single-GPU library: replicas not run (--gpus {args.gpus}, WORLD_SIZE {world}); "
+                f"the GPU arm runs on exactly one GPU")
+    return None
+
+
 def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1) -> dict:
     lda, ldb, ldc = w.strides
     scales = ""
@@ -82,7 +96,7 @@ def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1
                     f"accumulate, D {out.upper()} column-major"
                     + (f", batch of {batch} (entries share one seeded draw)" if batch > 1 else ""),
         "M": w.M, "N": w.N, "K": w.K, "lda": lda, "ldb": ldb, "ldc": ldc,
-        "parallelism": "replicas" if world > 1 else "single GPU",
+        "parallelism": "single GPU",
     }
     if batch > 1:
         cfg["batch"] = batch
@@ -295,41 +309,12 @@ def load_traffic(kernel_hash: str):
     return e.get("dram_bytes_per_launch")
 
 
-def slowest_rank(dist, times_ms, device):
-    """Replicas: every rank times the same work on its own GPU; the job's time
-    is the slowest rank's (max over ranks of each entry).  No data moves
-    between ranks: this is the only collective, and only for timing."""
-    if dist is None:
-        return [float(x) for x in times_ms]
-    import torch
-
-    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(x) for x in t.tolist()]
-
-
-def replica_throughput(flops_per_rank: float, world: int, slowest_ms: float) -> float:
-    """TFLOP/s of the whole job: the FLOPs every rank did over the slowest time."""
-    return world * flops_per_rank / (slowest_ms * 1e-3) / 1e12
-
-
-def run_gpu(args, rank, world, local):
+def run_gpu(args):
     import torch
 
     import dense_gemm_epilogue_gb300 as tg
 
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_mod
-
-        dist_mod.init_process_group("nccl")
-        dist = dist_mod
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
+    torch.cuda.set_device(0)
     tg.build()
     tg.load()
     w = si.WORKLOADS[args.workload]
@@ -388,14 +373,13 @@ def run_gpu(args, rank, world, local):
             step()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(0)
     if sampler:
         sampler.start()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("t0")
@@ -408,7 +392,6 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("t1")
-    barrier()
     region_ms = region0.elapsed_time(region1)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     st, where = tg.tg_check_device_status(stream)
@@ -462,7 +445,6 @@ def run_gpu(args, rank, world, local):
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize()
-    barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
@@ -472,94 +454,89 @@ def run_gpu(args, rank, world, local):
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_wall = time.perf_counter() - t_wall0
-    barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    step_ms = region_ms / args.steps
 
-    step_ms, e2e_ms = slowest_rank(dist, [region_ms / args.steps, e2e_ms], "cuda")
-
-    if rank == 0:
-        flops = w.flops * nbat
-        e_in = si.element_bytes(w.dtype)
-        alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
-        if mx:
-            alg_bytes += (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
-        value = replica_throughput(flops, world, step_ms)
-        peaks, peak_src = load_peaks()
-        launch_avg_ms = statistics.fmean(launch_ms)
-        # Back-to-back launches for more than ~50 ms run in the power-capped
-        # regime the sustained peak was measured in; a short burst compares
-        # with the burst peak.  Both are reported.  TF32, the 8-bit and the
-        # 4-bit floats take the BF16 peak times the nominal ratio to BF16
-        # (1.1, 4.5 and 13.5 over 2.25 PFLOP/s).
-        ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
-                 "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
-        ratio_note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
-                      "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
-        sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
-        tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
-        burst_tpeak = ratio * float(peaks["bf16_tflops"])
-        hbm = float(peaks["hbm_gbs"])
-        tensor_bound = flops / alg_bytes >= tpeak * 1e12 / (hbm * 1e9)
-        first = launch_ms[: min(10, len(launch_ms))]
-        qs = sorted(launch_ms)
-        if tensor_bound:
-            unit_r = UNIT
-            achieved = flops / (launch_avg_ms * 1e-3) / 1e12
-            peak = tpeak
-            burst = {"achieved": flops / (statistics.fmean(first) * 1e-3) / 1e12,
-                     "peak": burst_tpeak}
-        else:
-            unit_r = "GB/s"
-            achieved = alg_bytes / (launch_avg_ms * 1e-3) / 1e9
-            peak = hbm
-            burst = {"achieved": alg_bytes / (statistics.fmean(first) * 1e-3) / 1e9, "peak": hbm}
-        burst["frac"] = burst["achieved"] / burst["peak"]
-        burst["launches"] = len(first)
-        dt = w.dtype
-        kname = ("tg_gemm_mx_kernel" if mx else
-                 "tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
-            f"<{dt.upper()}, {plan['block_m']}x{plan['block_n']}, " + \
-            f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>"
-        traffic = load_traffic(tg.source_hash()) if args.workload == WORKLOAD and not batched else None
-        default_run = args.workload == WORKLOAD and not batched
-        line = {
-            "metric": metric_name(w, nbat, out),
-            "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": dt, "data": "synthetic", "config": workload_config(w, world, out, nbat),
-            "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
-                         "peak": peak, "unit": unit_r,
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": (("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")
-                                         if tensor_bound else "hbm_gbs") + f" of {peak_src}" +
-                                        (ratio_note if tensor_bound else "") +
-                                        (f" (the timed region ran {region_ms:.0f} ms of back-to-back "
-                                         f"launches)" if tensor_bound and sustained else ""),
-                         "burst": burst,
-                         "kernel_ms_p10_p50_p90": [qs[len(qs) // 10], qs[len(qs) // 2],
-                                                   qs[(9 * len(qs)) // 10]],
-                         "kernel": kname,
-                         "kernel_ms_avg": launch_avg_ms,
-                         "algorithmic_flops_per_launch": flops,
-                         "algorithmic_bytes_per_launch": alg_bytes},
-            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                    "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
-                                              hB.numel() * hB.element_size() +
-                                              (hSA.numel() + hSB.numel() if mx else 0)),
-                    "d2h_bytes_per_step": int(hD.numel() * hD.element_size()),
-                    "steps": e2e_steps, "wall_s": e2e_wall,
-                    "pipelining": "2 buffer sets; H2D, compute and D2H on separate streams"},
-            "gpu_launches": args.steps,
-            "clocks": clocks,
-            "plan": plan,
-            "library_source_hash": tg.source_hash(),
-        }
-        if world == 1 and not args.no_cpu_baseline and (default_run or args.cpu_baseline):
-            line["cpu_baseline"] = cpu_baseline(w, A, B)
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    flops = w.flops * nbat
+    e_in = si.element_bytes(w.dtype)
+    alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
+    if mx:
+        alg_bytes += (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
+    value = flops / (step_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    launch_avg_ms = statistics.fmean(launch_ms)
+    # Back-to-back launches for more than ~50 ms run in the power-capped
+    # regime the sustained peak was measured in; a short burst compares
+    # with the burst peak.  Both are reported.  TF32, the 8-bit and the
+    # 4-bit floats take the BF16 peak times the nominal ratio to BF16
+    # (1.1, 4.5 and 13.5 over 2.25 PFLOP/s).
+    ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
+             "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
+    ratio_note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
+                  "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
+    sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
+    tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    burst_tpeak = ratio * float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    tensor_bound = flops / alg_bytes >= tpeak * 1e12 / (hbm * 1e9)
+    first = launch_ms[: min(10, len(launch_ms))]
+    qs = sorted(launch_ms)
+    if tensor_bound:
+        unit_r = UNIT
+        achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+        peak = tpeak
+        burst = {"achieved": flops / (statistics.fmean(first) * 1e-3) / 1e12,
+                 "peak": burst_tpeak}
+    else:
+        unit_r = "GB/s"
+        achieved = alg_bytes / (launch_avg_ms * 1e-3) / 1e9
+        peak = hbm
+        burst = {"achieved": alg_bytes / (statistics.fmean(first) * 1e-3) / 1e9, "peak": hbm}
+    burst["frac"] = burst["achieved"] / burst["peak"]
+    burst["launches"] = len(first)
+    dt = w.dtype
+    kname = ("tg_gemm_mx_kernel" if mx else
+             "tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
+        f"<{dt.upper()}, {plan['block_m']}x{plan['block_n']}, " + \
+        f"{'TMA' if plan['producer'] == 1 else 'plain loads'}>"
+    traffic = load_traffic(tg.source_hash()) if args.workload == WORKLOAD and not batched else None
+    default_run = args.workload == WORKLOAD and not batched
+    line = {
+        "metric": metric_name(w, nbat, out),
+        "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dt, "data": "synthetic", "config": workload_config(w, 1, out, nbat),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
+                     "peak": peak, "unit": unit_r,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": (("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")
+                                     if tensor_bound else "hbm_gbs") + f" of {peak_src}" +
+                                    (ratio_note if tensor_bound else "") +
+                                    (f" (the timed region ran {region_ms:.0f} ms of back-to-back "
+                                     f"launches)" if tensor_bound and sustained else ""),
+                     "burst": burst,
+                     "kernel_ms_p10_p50_p90": [qs[len(qs) // 10], qs[len(qs) // 2],
+                                               qs[(9 * len(qs)) // 10]],
+                     "kernel": kname,
+                     "kernel_ms_avg": launch_avg_ms,
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
+                                          hB.numel() * hB.element_size() +
+                                          (hSA.numel() + hSB.numel() if mx else 0)),
+                "d2h_bytes_per_step": int(hD.numel() * hD.element_size()),
+                "steps": e2e_steps, "wall_s": e2e_wall,
+                "pipelining": "2 buffer sets; H2D, compute and D2H on separate streams"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "plan": plan,
+        "library_source_hash": tg.source_hash(),
+    }
+    if not args.no_cpu_baseline and (default_run or args.cpu_baseline):
+        line["cpu_baseline"] = cpu_baseline(w, A, B)
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -568,7 +545,11 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
-    return run_gpu(args, rank, world, local)
+    why = single_gpu_refusal(args, world)
+    if why:
+        print(why, file=sys.stderr, flush=True)
+        return 2
+    return run_gpu(args)
 
 
 if __name__ == "__main__":
