@@ -47,6 +47,7 @@ EXPORTED = (
     "tg_gemm",
     "tg_gemm_ex",
     "tg_plan",
+    "tg_plan_describe",
     "tg_status_string",
     "tg_check_device_status",
     "tg_set_wait_limit_ns",
@@ -148,6 +149,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_plan.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
                                 ctypes.POINTER(tg_options), i32, ctypes.POINTER(tg_plan_info)]
         lib.tg_plan.restype = ctypes.c_int
+        lib.tg_plan_describe.argtypes = [i64, i64, i64, ctypes.c_int, i64, i64, i64, i32,
+                                         ctypes.c_char_p, ctypes.c_size_t]
+        lib.tg_plan_describe.restype = ctypes.c_int
         lib.tg_status_string.argtypes = [ctypes.c_int]
         lib.tg_status_string.restype = ctypes.c_char_p
         lib.tg_check_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -275,6 +279,16 @@ def tg_plan(M, N, K, A, lda, B, ldb, D, ldc, in_dtype, opts=None, num_sms=0):
     if st != TG_OK:
         raise TgError(st, "tg_plan")
     return {name: getattr(info, name) for name, _ in tg_plan_info._fields_}
+
+
+def tg_plan_describe(M, N, K, in_dtype, lda, ldb, ldc, num_sms=0, size=256):
+    """The planner's choice as one line of text; raises TgError on invalid
+    arguments or when the text does not fit in `size` bytes."""
+    buf = ctypes.create_string_buffer(size)
+    st = load().tg_plan_describe(M, N, K, _dtype(in_dtype), lda, ldb, ldc, num_sms, buf, size)
+    if st != TG_OK:
+        raise TgError(st, "tg_plan_describe")
+    return buf.value.decode()
 
 
 def _epi_ops(ops):

@@ -57,6 +57,24 @@ __global__ void tg_fill_empty_sum_kernel(void *d, int64_t m, int64_t n, int64_t 
     }
 }
 
+// Grid of the K == 0 fill: 1024 rows per block in x; in y, enough column
+// steps for about 16 blocks per SM (each block then loops over columns).
+static dim3 fill_grid(int64_t m, int64_t cols, int sms) {
+    const int64_t gx = (m + 1023) / 1024;
+    int64_t gy = ((int64_t)sms * 16 + gx - 1) / gx;
+    if (gy > cols) gy = cols;
+    if (gy > 65535) gy = 65535;
+    return dim3((unsigned)gx, (unsigned)(gy > 0 ? gy : 1), 1);
+}
+
+cudaError_t launch_fill_empty_sum(void *d, int64_t m, int64_t n, int64_t ldc, int64_t stride_d,
+                                  int64_t batch, int out_fmt, float alpha, int relu,
+                                  const EpiProgram &prog, int sms, cudaStream_t stream) {
+    tg_fill_empty_sum_kernel<<<fill_grid(m, n * batch, sms), 256, 0, stream>>>(
+        d, m, n, ldc, stride_d, batch, out_fmt, alpha, relu, prog);
+    return cudaGetLastError();
+}
+
 // One thread waits on a barrier that nothing completes; the bounded wait must
 // run out, record SITE_SELFTEST and return.
 __global__ void tg_selftest_wait_kernel(uint32_t *status, uint64_t limit_ns) {
@@ -623,16 +641,6 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
     return r == CUDA_SUCCESS;
 }
 
-// Grid of the K == 0 fill: 1024 rows per block in x; in y, enough column
-// steps for about 16 blocks per SM (each block then loops over columns).
-dim3 fill_grid(int64_t m, int64_t cols, int sms) {
-    const int64_t gx = ceil_div(m, 1024);
-    int64_t gy = ceil_div((int64_t)sms * 16, gx);
-    if (gy > cols) gy = cols;
-    if (gy > 65535) gy = 65535;
-    return dim3((unsigned)gx, (unsigned)(gy > 0 ? gy : 1), 1);
-}
-
 // A composed epilogue from the caller's op list (checked: count, kinds,
 // bias pointers present and float-aligned).
 tg_status make_program(const tg_epi_op *ops, int32_t n_ops, tg::EpiProgram *prog) {
@@ -680,9 +688,10 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     const int relu = epi == TG_EPILOGUE_RELU ? 1 : 0;
 
     if (q.K == 0) {
-        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N * q.batch, ds->sms), 256, 0, stream>>>(
-            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu, *prog);
-        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+        return tg::launch_fill_empty_sum(q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha,
+                                         relu, *prog, ds->sms, stream) == cudaSuccess
+                   ? TG_OK
+                   : TG_ERR_CUDA;
     }
 
     Plan plan;
@@ -920,9 +929,10 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     if (st != TG_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     if (q.K == 0) {
-        tg::tg_fill_empty_sum_kernel<<<fill_grid(q.M, q.N * q.batch, ds->sms), 256, 0, stream>>>(
-            q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha, relu, prog);
-        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+        return tg::launch_fill_empty_sum(q.D, q.M, q.N, q.ldc, q.sd, q.batch, q.out_fmt, q.alpha,
+                                         relu, prog, ds->sms, stream) == cudaSuccess
+                   ? TG_OK
+                   : TG_ERR_CUDA;
     }
     Plan plan;
     st = make_mx_plan(q, opts, ds->sms, &plan);
@@ -1067,6 +1077,31 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->tmem_cols = p.tmem_cols;
     out->vector_store = p.vector_store ? 1 : 0;
     return TG_OK;
+}
+
+tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, int64_t lda,
+                           int64_t ldb, int64_t ldc, int32_t num_sms, char *buf, size_t len) {
+    if (!buf || len == 0) return TG_ERR_INVALID_VALUE;
+    buf[0] = '\0';
+    tg_plan_info pi;
+    const tg_status st =
+        tg_plan(M, N, K, nullptr, lda, nullptr, ldb, nullptr, ldc, in_dtype, nullptr, num_sms, &pi);
+    if (st != TG_OK) return st;
+    int n;
+    if (M == 0 || N == 0 || K == 0) {
+        n = std::snprintf(buf, len, "empty");
+    } else {
+        n = std::snprintf(buf, len,
+                          "%s %dx%dx%d stages=%d producer=%s swap=%d grid=%d tiles=%lld raster=%d "
+                          "multicast=%d split=%dx%d stream_k=%d vector_store=%d threads=%d "
+                          "smem=%d tmem=%d",
+                          pi.cta_pair ? "pair" : "single", pi.block_m, pi.block_n, pi.block_k,
+                          pi.stages, pi.producer == 1 ? "tma" : "plain", pi.swap_ab, pi.grid,
+                          (long long)pi.tiles, pi.raster_group, pi.multicast, pi.split_tiles,
+                          pi.split_segs, pi.stream_k, pi.vector_store, pi.threads, pi.smem_bytes,
+                          pi.tmem_cols);
+    }
+    return (n >= 0 && (size_t)n < len) ? TG_OK : TG_ERR_INVALID_VALUE;
 }
 
 tg_status tg_gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha, const void *A,

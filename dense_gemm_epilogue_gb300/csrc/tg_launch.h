@@ -32,6 +32,12 @@ cudaError_t launch_e4m3(const LaunchArgs &a);
 cudaError_t launch_e5m2(const LaunchArgs &a);
 // Block-scaled 8-bit / packed 4-bit float kernel (CTA pairs, block_n 128 or 256).
 cudaError_t launch_mx(const LaunchArgs &a, Kind kind);
+// The K == 0 case (empty sums): D = out(epi(alpha * 0)) over `batch` M x N
+// outputs, `stride_d` output elements apart, enqueued on `stream`.  One
+// kernel launch; allocates nothing.
+cudaError_t launch_fill_empty_sum(void *d, int64_t m, int64_t n, int64_t ldc, int64_t stride_d,
+                                  int64_t batch, int out_fmt, float alpha, int relu,
+                                  const EpiProgram &prog, int sms, cudaStream_t stream);
 // Threads, shared memory, stages and tensor-memory columns of a block-scaled
 // configuration (0 when the configuration does not exist).
 void mx_config_numbers(Kind kind, int block_n, int *stages, int *smem, int *threads, int *tmem);

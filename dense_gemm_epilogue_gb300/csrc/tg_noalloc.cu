@@ -82,17 +82,6 @@ tg_status noalloc_setup(int *dev_out, NoAllocDevice **out) {
     return TG_OK;
 }
 
-// The K == 0 case (empty sums): D = epi(alpha * 0).
-__global__ void noalloc_empty_sum_kernel(float *d, int64_t m, int64_t n, int64_t ldc, float alpha,
-                                         int relu) {
-    float v = alpha * 0.0f;
-    if (relu) v = (v > 0.0f || v != v) ? v : 0.0f;
-    const int64_t total = m * n;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x)
-        d[(i % m) + (i / m) * ldc] = v;
-}
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -164,10 +153,12 @@ extern "C" tg_status tg_gemm_noalloc(int64_t M, int64_t N, int64_t K, float alph
     const int relu = epilogue == TG_EPILOGUE_RELU ? 1 : 0;
 
     if (K == 0) {
-        int64_t blocks = cdiv(M * N, 256);
-        if (blocks > (int64_t)nd->sms * 8) blocks = (int64_t)nd->sms * 8;
-        noalloc_empty_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(D, M, N, ldc, alpha, relu);
-        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+        // The empty sums, by the same fill kernel as tg_gemm (one FP32 output).
+        static const tg::EpiProgram kNoOps = {};
+        return tg::launch_fill_empty_sum(D, M, N, ldc, 0, 1, 0, alpha, relu, kNoOps, nd->sms,
+                                         stream) == cudaSuccess
+                   ? TG_OK
+                   : TG_ERR_CUDA;
     }
 
     // No split-K tail here: it would need a workspace.

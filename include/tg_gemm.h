@@ -220,6 +220,22 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
                   const tg_options *opts, int32_t num_sms, tg_plan_info *out);
 
 /*
+ * The planner's choice for tg_gemm as one line of text, for logs and tuning
+ * (a formatter over tg_plan, host only when num_sms > 0).  The operands are
+ * planned as 256-byte aligned.  Writes at most `len` bytes into `buf`,
+ * always NUL-terminated when len > 0, e.g.
+ *   "pair 256x256x64 stages=7 producer=tma swap=0 grid=152 tiles=1024
+ *    raster=8 multicast=1 split=0x1 stream_k=0 vector_store=0 threads=320
+ *    smem=230704 tmem=512"   (one line)
+ * or "empty" when M, N or K is 0.  Returns TG_OK; TG_ERR_INVALID_VALUE on
+ * the argument errors of tg_plan, when buf is NULL or len is 0, or when the
+ * text did not fit (buf then holds its truncated, NUL-terminated start).
+ */
+tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype,
+                           int64_t lda, int64_t ldb, int64_t ldc, int32_t num_sms,
+                           char *buf, size_t len);
+
+/*
  * Block-scaled (microscaling) FP8 GEMM ("Matrix Multiplication", "Where to
  * go from here": block-scaled FP8 matmuls; the pages fix no format, this is
  * the OCP Microscaling one):
@@ -379,6 +395,8 @@ tg_status tg_selftest_wait_timeout(uint64_t limit_ns, void *stream);
  * that loads the library holds until the process exits.  A plan needing more
  * scratch than that returns TG_ERR_UNSUPPORTED before launching anything
  * (no M, N, K does today: the status word does not grow with the problem).
+ * It never splits a tile's K loop across CTAs, since the partial sums would
+ * need a workspace; its K == 0 case runs tg_gemm's fill kernel.
  *
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before

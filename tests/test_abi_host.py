@@ -404,3 +404,33 @@ def test_plan_k_split_pairs_for_mid_shapes(tg):
                                 ((4096, 128, 8192), 128, 4), ((512, 2048, 4096), 128, 2)]:
         p = plan(tg, si.Workload("mid", M, N, K, "bf16", 1.0, True, 0, "normal"))
         assert (p["cta_pair"], p["block_n"], p["split_segs"]) == (1, bn, segs), (M, N, K)
+
+
+def test_plan_describe_formats_the_plan(tg):
+    w = si.WORKLOADS["c4_bf16_8192"]
+    text = tg.tg_plan_describe(w.M, w.N, w.K, w.dtype, *w.strides, 152)
+    p = plan(tg, w)
+    assert text.startswith("pair 256x256x64 stages=7 producer=tma swap=0 grid=152 tiles=1024 ")
+    fields = dict(kv.split("=") for kv in text.split()[2:])
+    assert int(fields["tiles"]) == p["tiles"] and int(fields["raster"]) == p["raster_group"]
+    assert fields["split"] == f"{p['split_tiles']}x{p['split_segs']}"
+    assert int(fields["smem"]) == p["smem_bytes"] and int(fields["tmem"]) == p["tmem_cols"]
+    c1 = si.WORKLOADS["c1_bf16_65x97x73"]
+    assert tg.tg_plan_describe(c1.M, c1.N, c1.K, c1.dtype, *c1.strides, 152).startswith(
+        "single 128x64x64 stages=8 producer=plain")
+    assert tg.tg_plan_describe(0, 5, 5, "bf16", 5, 5, 1, 152) == "empty"
+
+
+def test_plan_describe_errors(tg):
+    import ctypes
+
+    lib = tg.load()
+    small = ctypes.create_string_buffer(16)
+    # Too small: truncated, NUL-terminated, and reported.
+    assert lib.tg_plan_describe(8192, 8192, 8192, 0, 8192, 8192, 8192, 152, small, 16) == \
+        tg.TG_ERR_INVALID_VALUE
+    assert small.value == b"pair 256x256x64"
+    assert lib.tg_plan_describe(8, 8, 8, 0, 8, 8, 8, 152, None, 16) == tg.TG_ERR_INVALID_VALUE
+    assert lib.tg_plan_describe(8, 8, 8, 0, 7, 8, 8, 152, small, 16) == tg.TG_ERR_INVALID_VALUE
+    with pytest.raises(tg.TgError):
+        tg.tg_plan_describe(8, 8, 8, "bf16", 8, 8, 8, 152, size=8)
