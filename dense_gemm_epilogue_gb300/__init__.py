@@ -121,6 +121,7 @@ class tg_plan_info(ctypes.Structure):
         ("split_segs", ctypes.c_int32),
         ("multicast", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
     ]
 
 

@@ -144,8 +144,14 @@ std::mutex g_dev_mutex;
 DeviceState g_dev[kMaxDevices];
 
 // Split-K workspace of one (device, stream): room for `tiles` partial
-// 256 x 256 FP32 pair tiles and one ready flag per tile half (kept at zero
-// between launches by the kernel itself).
+// 256 x 256 FP32 pair tiles; ready flags (four per tile: one per segment and
+// tile half of a two-segment exchange) and the ticket counter after them, all
+// kept at zero between launches by the kernel itself.
+constexpr int64_t kFlagsPerTile = 4;
+constexpr int64_t kFlagWordsExtra = 32;
+int64_t flag_words(int64_t tiles) { return kFlagsPerTile * tiles + kFlagWordsExtra; }
+uint32_t *ticket_counter(uint32_t *flags, int64_t tiles) { return flags + kFlagsPerTile * tiles; }
+
 struct Workspace {
     int device;
     cudaStream_t stream;
@@ -168,11 +174,11 @@ tg_status workspace_for(int dev, cudaStream_t stream, int64_t tiles, Workspace *
     }
     Workspace w{dev, stream, nullptr, nullptr, tiles};
     if (cudaMalloc(&w.ws, sizeof(float) * kPairTileFloats * tiles) != cudaSuccess) return TG_ERR_CUDA;
-    if (cudaMalloc(&w.flags, sizeof(uint32_t) * 2 * tiles) != cudaSuccess) {
+    if (cudaMalloc(&w.flags, sizeof(uint32_t) * flag_words(tiles)) != cudaSuccess) {
         cudaFree(w.ws);
         return TG_ERR_CUDA;
     }
-    if (cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * tiles) != cudaSuccess ||
+    if (cudaMemset(w.flags, 0, sizeof(uint32_t) * flag_words(tiles)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(w.flags);
         cudaFree(w.ws);
@@ -187,11 +193,12 @@ tg_status workspace_for(int dev, cudaStream_t stream, int64_t tiles, Workspace *
     return TG_OK;
 }
 
-// After a bounded wait ran out, flags may be left raised: clear them all.
+// After a bounded wait ran out, flags may be left raised and a ticket counter
+// away from zero: clear them all.
 tg_status reset_workspace_flags(int dev) {
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     for (Workspace &w : g_ws)
-        if (w.device == dev && cudaMemset(w.flags, 0, sizeof(uint32_t) * 2 * w.tiles) != cudaSuccess)
+        if (w.device == dev && cudaMemset(w.flags, 0, sizeof(uint32_t) * flag_words(w.tiles)) != cudaSuccess)
             return TG_ERR_CUDA;
     return TG_OK;
 }
@@ -283,6 +290,7 @@ struct Plan {
     int split_max = 1;  // K segments allowed per tail tile (pair kernel only)
     bool dynamic = false;  // pair kernel: one cluster per tile, launch-control stealing
     bool stream_k = false; // single-CTA kernel: each CTA a contiguous share of all K iterations
+    bool ticket = false;   // pair kernel: first unit static, later units claimed from a counter
     int64_t split_tiles = 0;
     int split_segs = 1;
     bool swap = false;
@@ -381,7 +389,10 @@ tg_status validate(const Problem &q, const tg_options *o) {
         if (o->l2_hint < 0 || o->l2_hint > 2) return TG_ERR_INVALID_VALUE;
         if (o->prefetch_k < -1 || o->prefetch_k > 64) return TG_ERR_INVALID_VALUE;
         if (o->multicast < 0 || o->multicast > 2) return TG_ERR_INVALID_VALUE;
-        if (o->schedule < 0 || o->schedule > 3 || o->reserved[0]) return TG_ERR_INVALID_VALUE;
+        if (o->schedule < 0 || o->schedule > 4 || o->reserved[0]) return TG_ERR_INVALID_VALUE;
+        // Tickets run CTA-pair tiles, one pair per cluster, with the workspace.
+        if (o->schedule == 4 && (o->cta_pair == 1 || o->multicast == 2 || o->split_k == 1))
+            return TG_ERR_INVALID_VALUE;
         // Stream-K runs single-CTA tiles and splits K by definition.
         if (o->schedule == 3 && (o->cta_pair == 2 || o->multicast == 2 || o->split_k == 1))
             return TG_ERR_INVALID_VALUE;
@@ -438,7 +449,7 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     // operands on TMA.
     const bool pair_ok = t != TG_TF32 && p.producer == 1;
     // The dynamic schedule runs CTA-pair tiles only; stream-K single-CTA tiles.
-    const bool force_pair = o->cta_pair == 2 || o->schedule == 2;
+    const bool force_pair = o->cta_pair == 2 || o->schedule == 2 || o->schedule == 4;
     const bool force_single = o->cta_pair == 1 || o->schedule == 3;
     if (force_pair && !pair_ok) return TG_ERR_INVALID_VALUE;
     if (force_pair && o->block_n == 64) return TG_ERR_INVALID_VALUE;
@@ -519,7 +530,7 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
     // planner turns it on for short K loops (at most 32 K blocks) over several
     // waves of tiles, where each tile's loads, not its MMAs, set the pace:
     // 8191x4097x1000 ran 8 % faster, 4096^3 the same, 8192^3 4 % slower.
-    const bool mc_auto = o->multicast == 0 && o->schedule != 2 &&
+    const bool mc_auto = o->multicast == 0 && o->schedule != 2 && o->schedule != 4 &&
                          ceil_div(K, block_k(t)) <= 32 && mblocks * nblocks >= 4 * (sms / 2);
     if (p.pair) p.mc = ((o->multicast == 2 || mc_auto) && nblocks >= 2) ? 2 : 1;
     if (o->multicast == 2 && p.pair && p.mc != 2) return TG_ERR_INVALID_VALUE;
@@ -550,7 +561,20 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         int64_t pairs_max = sms / cl;
         if (o->max_ctas && pairs_max > o->max_ctas / cl) pairs_max = o->max_ctas / cl;
         if (pairs_max < 1) pairs_max = 1;
-        p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 1);
+        // Tickets: with at least a wave of tiles and one pair per cluster,
+        // pairs claim their later tiles in order, so the ones that run ahead
+        // take the tail (static: a pair's tiles are fixed, and pairs drift
+        // apart by several microseconds over a dozen tiles).  They need the
+        // workspace's counter, so not with split_k = 1.
+        const bool ticket_ok = p.mc == 1 && o->split_k != 1 && p.tiles >= pairs_max &&
+                               (o->schedule == 0 || o->schedule == 4);
+        if (o->schedule == 4 && !ticket_ok) return TG_ERR_INVALID_VALUE;
+        p.ticket = ticket_ok;
+        // K segments: up to 8 when there are fewer tiles than pairs; with
+        // tickets, a last wave at most half full is cut into two segments
+        // that exchange halves (its tiles then take half a tile's time).
+        p.split_max = o->split_k != 0 ? o->split_k
+                                      : (p.tiles < pairs_max ? kDefaultSplitMax : (p.ticket ? 2 : 1));
         if (p.mc != 1) p.split_max = 1;  // K segments only with one pair per cluster
         int64_t pairs = pairs_max;
         if (p.tiles < pairs_max) {
@@ -567,6 +591,7 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
             // many as fit and the running ones take over the rest.
             if (p.mc != 1 || p.tiles > INT32_MAX / 2) return TG_ERR_INVALID_VALUE;
             p.dynamic = true;
+            p.ticket = false;
             p.split_max = 1;
             p.split_tiles = 0;
             p.split_segs = 1;
@@ -665,11 +690,12 @@ void log_plan(const char *what, const Problem &q, const Plan &p) {
     if (!std::getenv("TG_LOG")) return;
     std::fprintf(stderr,
                  "%s: M=%lld N=%lld K=%lld batch=%lld -> %s BN=%d mc=%d swap=%d producer=%d "
-                 "tiles=%lld grid=%d stages=%d group=%d split=%lldx%d stream_k=%d dynamic=%d\n",
+                 "tiles=%lld grid=%d stages=%d group=%d split=%lldx%d stream_k=%d dynamic=%d "
+                 "ticket=%d\n",
                  what, (long long)q.M, (long long)q.N, (long long)q.K, (long long)q.batch,
                  p.pair ? "pair" : "single", p.block_n, p.mc, p.swap ? 1 : 0, p.producer,
                  (long long)p.tiles, p.grid, p.stages, p.group, (long long)p.split_tiles,
-                 p.split_segs, p.stream_k ? 1 : 0, p.dynamic ? 1 : 0);
+                 p.split_segs, p.stream_k ? 1 : 0, p.dynamic ? 1 : 0, p.ticket ? 1 : 0);
 }
 
 tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *stream_ptr,
@@ -766,14 +792,15 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.swap = plan.swap ? 1 : 0;
     p.epi = *prog;
     p.prefetch_k = (opts && opts->prefetch_k > 0) ? opts->prefetch_k : 0;
-    if (la.pair && plan.split_segs > 1) {
+    if (la.pair && (plan.split_segs > 1 || plan.ticket)) {
         Workspace w;
         st = workspace_for(dev, stream, ds->sms / 2, &w);
         if (st != TG_OK) return st;
-        p.split_max = plan.split_max;
+        p.split_max = plan.split_segs > 1 ? plan.split_max : 1;
         p.ws_tiles = (int32_t)w.tiles;
         p.ws = w.ws;
         p.flags = w.flags;
+        if (plan.ticket) p.ticket = ticket_counter(w.flags, w.tiles);
     }
     if (!la.pair && plan.stream_k) {
         // One 128 x 256 FP32 slot and one flag per CTA: half a pair tile each.
@@ -1076,6 +1103,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->smem_bytes = p.smem;
     out->tmem_cols = p.tmem_cols;
     out->vector_store = p.vector_store ? 1 : 0;
+    out->schedule = p.dynamic ? 2 : p.stream_k ? 3 : p.ticket ? 4 : 1;
     return TG_OK;
 }
 
@@ -1093,13 +1121,17 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, i
     } else {
         n = std::snprintf(buf, len,
                           "%s %dx%dx%d stages=%d producer=%s swap=%d grid=%d tiles=%lld raster=%d "
-                          "multicast=%d split=%dx%d stream_k=%d vector_store=%d threads=%d "
+                          "multicast=%d split=%dx%d schedule=%s vector_store=%d threads=%d "
                           "smem=%d tmem=%d",
                           pi.cta_pair ? "pair" : "single", pi.block_m, pi.block_n, pi.block_k,
                           pi.stages, pi.producer == 1 ? "tma" : "plain", pi.swap_ab, pi.grid,
                           (long long)pi.tiles, pi.raster_group, pi.multicast, pi.split_tiles,
-                          pi.split_segs, pi.stream_k, pi.vector_store, pi.threads, pi.smem_bytes,
-                          pi.tmem_cols);
+                          pi.split_segs,
+                          pi.schedule == 2   ? "dynamic"
+                          : pi.schedule == 3 ? "stream_k"
+                          : pi.schedule == 4 ? "ticket"
+                                             : "static",
+                          pi.vector_store, pi.threads, pi.smem_bytes, pi.tmem_cols);
     }
     return (n >= 0 && (size_t)n < len) ? TG_OK : TG_ERR_INVALID_VALUE;
 }
@@ -1180,6 +1212,7 @@ tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, 
     out->cta_pair = 1;
     out->split_segs = 1;
     out->multicast = 1;
+    out->schedule = 1;
     return TG_OK;
 }
 

@@ -200,6 +200,11 @@ struct GemmParams {
     // CTA-pair kernel: 1 = dynamic schedule (one cluster launched per tile;
     // running clusters take over clusters not yet started).
     int32_t dynamic;
+    // CTA-pair kernel, one pair per cluster: when not NULL, each pair takes
+    // its first unit statically and claims every later one in order from
+    // this counter (a word of the workspace, zero between launches: the
+    // launch's last claim puts it back to zero).
+    uint32_t *ticket;
     int32_t swap;                   // 1: role-space rows are D's columns (operands swapped)
     // Single-CTA kernel: 1 = stream-K.  Each CTA takes a contiguous share of
     // the num_tiles x num_k_blocks (tile, K block) iterations; a tile cut

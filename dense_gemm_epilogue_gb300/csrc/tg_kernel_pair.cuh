@@ -26,8 +26,13 @@
 // costs a memory barrier on the issuing thread and throttles the TMA issue.
 // With one pair per cluster (MC = 1) each CTA loads only its own rows; with
 // two (MC = 2, below) the pairs share their A rows by TMA multicast.  Work
-// is a static persistent sequence of units, or (MC = 1, p.dynamic) one
-// cluster per tile with tiles taken over through cluster launch control.
+// is a static persistent sequence of units; or (MC = 1, p.dynamic) one
+// cluster per tile with tiles taken over through cluster launch control; or
+// (MC = 1, p.ticket) a persistent grid whose pairs take their first unit
+// statically and claim every later one, in order, from a counter in global
+// memory, so that pairs that run ahead take more of the work.  The claimed
+// unit reaches every role of both CTAs through the same ring of answer slots
+// that cluster launch control fills.
 #pragma once
 
 #include <cstdint>
@@ -64,7 +69,10 @@ struct PairConfig {
     static constexpr int NUM_BARS = CLCE0 + CLC_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int CLC_OFF = (MISC_OFF + 16 + 15) / 16 * 16;
-    static constexpr int SMEM_BYTES = CLC_OFF + 16 * CLC_SLOTS + 1024;
+    // Ticket schedule: the leader writes each claimed unit here, then copies
+    // it into the answer slot of both CTAs.
+    static constexpr int TICKET_OFF = CLC_OFF + 16 * CLC_SLOTS;
+    static constexpr int SMEM_BYTES = TICKET_OFF + 16 * CLC_SLOTS + 1024;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int EPI_WARPS = 8;  // two per tensor-memory lane quarter
     static constexpr int NUM_WARPS = 2 + EPI_WARPS;
@@ -125,7 +133,14 @@ __device__ __forceinline__ void pair_pause_ns(uint64_t ns) {
 // the workspace and raise a flag; segment S-1 (on the highest-numbered of
 // those pairs, so it only waits on pairs dispatched before it) adds the
 // partials in segment order, applies the epilogue and stores D, so the
-// summation order is fixed and the result is deterministic.
+// summation order is fixed and the result is deterministic.  With S = 2 the
+// two segments instead exchange halves: each writes the partial sums of the
+// columns the other finishes, raises its flag, waits for the other's flag,
+// adds the other's partials to its own half and stores it.  Each side then
+// moves half the bytes of a one-sided finish, and both sides' stores run at
+// once.  Both segments write before they wait, and both are dispatched in
+// the same round (static) or as consecutive claims (ticket), so neither
+// waits on work that has not been handed out.
 // A K segment spans at least this many K blocks, so that a segment's MMA
 // work outweighs the finisher's read of one partial tile.
 constexpr int SPLIT_MIN_KBLOCKS = 8;
@@ -247,6 +262,11 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     // no split): this cluster's own tile, then the tile of each cluster that
     // launch control cancelled for it, until an answer says none was left.
     const bool dyn = MC == 1 && p.dynamic != 0;
+    // Ticket schedule: every pair has a first unit (units >= pairs), so each
+    // makes exactly one failing claim and the claims of a launch number
+    // exactly `units`; the last one (value units - 1) resets the counter.
+    const bool tick = MC == 1 && !dyn && p.ticket != nullptr && up.units >= num_pairs;
+    const bool ring = dyn || tick;
     const int64_t first_unit = dyn ? (int64_t)(blockIdx.x / 2) : pair;
     // Read answer `step` (waiting for it), release its slot, return the next
     // unit (-1: no more work; -2: the wait gave up).  One thread per reader.
@@ -257,8 +277,12 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                       SITE_SCHED)) {
             const volatile uint64_t *r =
                 reinterpret_cast<const volatile uint64_t *>(smem + C::CLC_OFF + 16 * slot);
-            const int32_t x = clc_cancelled_x(r[0], r[1]);
-            next = x >= 0 ? (int64_t)(x / 2) : -1;
+            if (tick) {
+                next = (int64_t)r[0];  // the claimed unit, or -1
+            } else {
+                const int32_t x = clc_cancelled_x(r[0], r[1]);
+                next = x >= 0 ? (int64_t)(x / 2) : -1;
+            }
         }
         if (leader) mbar_arrive(bar(C::CLCE0 + slot));
         else mbar_arrive_cluster(map_shared_rank(bar(C::CLCE0 + slot), lead_rank));
@@ -281,7 +305,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             bool ok = true;
             int64_t step = 0;
             for (int64_t u = first_unit; ok && u >= 0 && u < up.units;) {
-                if (dyn) {
+                if (ring) {
                     // Ask for the unit after this one (answer `step`), into a
                     // slot all readers have released.
                     const int slot = (int)(step % C::CLC_SLOTS);
@@ -293,7 +317,31 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                             ok = false;
                             break;
                         }
-                        clc_try_cancel_all(sbase + C::CLC_OFF + 16 * slot, bar(C::CLCF0 + slot));
+                        if (dyn) {
+                            clc_try_cancel_all(sbase + C::CLC_OFF + 16 * slot, bar(C::CLCF0 + slot));
+                        } else {
+                            // Claim the next unit in order; the answer lands in
+                            // both CTAs' slot as 16 transaction bytes, like a
+                            // launch-control answer.
+                            const uint32_t v = atomicAdd(p.ticket, 1u);
+                            int64_t next = num_pairs + (int64_t)v;
+                            if (next >= up.units) {
+                                next = -1;
+                                if ((int64_t)v == up.units - 1) atomicExch(p.ticket, 0u);
+                            }
+                            volatile int64_t *stg =
+                                reinterpret_cast<volatile int64_t *>(smem + C::TICKET_OFF + 16 * slot);
+                            stg[0] = next;
+                            stg[1] = 0;
+                            fence_proxy_async_smem();
+                            const uint32_t src = sbase + C::TICKET_OFF + 16 * slot;
+                            const uint32_t dst = sbase + C::CLC_OFF + 16 * slot;
+                            const uint32_t fb = bar(C::CLCF0 + slot);
+                            bulk_copy_s2cluster(map_shared_rank(dst, rank), src, 16,
+                                                map_shared_rank(fb, rank));
+                            bulk_copy_s2cluster(map_shared_rank(dst, rank ^ 1u), src, 16,
+                                                map_shared_rank(fb, rank ^ 1u));
+                        }
                     }
                 }
                 const Unit un = decode_unit(up, u, nkb);
@@ -327,7 +375,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
                 if (!ok) break;
-                u = dyn ? clc_read(step++) : u + num_pairs;
+                u = ring ? clc_read(step++) : u + num_pairs;
             }
             if (!ok && issued) {
                 // Copies already issued land within microseconds; let them
@@ -370,7 +418,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit_pair_mcast(bar(C::ACCF0 + acc), pair_ctas);
-                u = dyn ? clc_read(step++) : u + num_pairs;
+                u = ring ? clc_read(step++) : u + num_pairs;
             }
             if (!ok) {
                 mma_commit_pair_mcast(bar(C::DRAIN), (uint16_t)(1u << rank));
@@ -415,7 +463,66 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             auto flag = [&](int32_t k) -> uint32_t * {
                 return p.flags + (un.tail * (up.segs - 1) + k) * 2 + half;
             };
-            if (un.seg >= 0 && un.seg < up.segs - 1) {
+            if (un.seg >= 0 && up.segs == 2) {
+                // Exchange (two segments): this segment finishes column half
+                // `sg` of each warp's range and hands the other half over.
+                constexpr int HALF = COLS / 2;
+                const int32_t sg = un.seg, other = 1 - sg;
+                const int grp = (warp - 2) / 4;  // this warp's column range
+                // Partials of segment k: the half it hands over, column-major
+                // 128 rows x BN/2 columns of FP32 (group-major columns).
+                auto xpart = [&](int32_t k) -> float * {
+                    return p.ws + ((un.tail * 2 + half) * BN + k * (BN / 2)) * (int64_t)BLOCK_M;
+                };
+                auto xflag = [&](int32_t k) -> uint32_t * {
+                    return p.flags + (un.tail * 2 + half) * 2 + k;
+                };
+                float *mine = xpart(sg) + (int64_t)grp * HALF * BLOCK_M + row_in_half;
+#pragma unroll 1
+                for (int c0 = 0; c0 < HALF; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + cbase + other * HALF + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(mine + (int64_t)(c0 + j) * BLOCK_M, __uint_as_float(v[j]));
+                }
+                __threadfence();
+                named_bar_sync(1, EPI_THREADS);
+                if (etid == 0) st_release_gpu_u32(xflag(sg), 1u);
+                bool ready = true;
+                if (etid == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu_u32(xflag(other)) == 0u) {
+                        if (*abort_flag || globaltimer_ns() - t0 > p.wait_limit_ns) {
+                            if (!*abort_flag) pair_raise_abort(ctl, SITE_PARTIAL);
+                            ready = false;
+                            break;
+                        }
+                    }
+                    *fin_ready = ready ? 1 : 0;
+                }
+                named_bar_sync(1, EPI_THREADS);
+                ready = *fin_ready != 0;
+                if (ready) (void)ld_acquire_gpu_u32(xflag(other));
+                const int32_t r = mb * C::PAIR_M + (int32_t)half * BLOCK_M + row_in_half;
+                const bool row_ok = r < p.m;
+                const float *theirs = xpart(other) + (int64_t)grp * HALF * BLOCK_M + row_in_half;
+#pragma unroll 1
+                for (int c0 = 0; ready && c0 < HALF; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + cbase + sg * HALF + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                               __ldcg(theirs + (int64_t)(c0 + j) * BLOCK_M));
+                    if (row_ok) epilogue_store(p, bt, r, nb * BN + cbase + sg * HALF + c0, v);
+                }
+                // The other segment's flag was raised for this launch only:
+                // put it back to zero (this side is its only reader).
+                if (etid == 0 && ready) *xflag(other) = 0u;
+            } else if (un.seg >= 0 && un.seg < up.segs - 1) {
                 // Writer: raw FP32 partial sums to the workspace, then the flag.
                 float *dst = part(un.seg);
 #pragma unroll 1
@@ -488,7 +595,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 if (leader) mbar_arrive(bar(C::ACCE0 + acc));
                 else mbar_arrive_cluster_relaxed(map_shared_rank(bar(C::ACCE0 + acc), lead_rank));
             }
-            u = dyn ? clc_read_warp(step++) : u + num_pairs;
+            u = ring ? clc_read_warp(step++) : u + num_pairs;
         }
     }
 

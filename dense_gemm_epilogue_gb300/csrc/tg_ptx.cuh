@@ -348,6 +348,19 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t
                  : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory at
+// `src` to shared memory of a CTA of the cluster at `dst_cluster`,
+// completing that many transaction bytes on the destination CTA's barrier at
+// `bar_cluster` (both shared::cluster addresses; 16-byte aligned).
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32_t src,
+                                                    uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
 // Cluster launch control: ask the hardware to cancel the launch of one
 // cluster of this grid that has not started yet; the 16-byte answer lands at
 // `resp` (same offset in every CTA of this cluster), completing 16

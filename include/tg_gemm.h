@@ -36,12 +36,13 @@
  * its own: per device a status word and cached attributes, allocated on the
  * first call on the device; and per (device, stream) a workspace of about
  * 20 MB (the partial sums of tiles whose K loop is split across CTAs, by
- * the pair split tail or stream-K, plus their ready flags), allocated on the
- * first call on that stream that splits a tile and kept until the process
- * exits.  Calls on different streams never share a workspace.  That first
- * allocation synchronises the device, so inside a stream capture either
- * make one call of a splitting shape on the stream beforehand, pass
- * split_k = 1 (tg_gemm_ex), or use tg_gemm_noalloc.
+ * the pair split tail or stream-K, their ready flags, and the counter from
+ * which CTA pairs claim tiles under the ticket schedule), allocated on the
+ * first call on that stream that splits a tile or claims tiles and kept
+ * until the process exits.  Calls on different streams never share a
+ * workspace.  That first allocation synchronises the device, so inside a
+ * stream capture either make one call of such a shape on the stream
+ * beforehand, pass split_k = 1 (tg_gemm_ex), or use tg_gemm_noalloc.
  *
  * Asynchrony: tg_gemm enqueues its work on `stream` (a cudaStream_t passed as
  * void*, NULL for the legacy default stream) and returns without waiting;
@@ -139,8 +140,10 @@ typedef struct {
                              rows n K blocks ahead into L2, 4 blocks per burst */
     int32_t multicast;    /* 0: planner; 1: one CTA pair per cluster; 2: two pairs per cluster
                              sharing their A-role rows by TMA multicast (CTA-pair tiles) */
-    int32_t schedule;     /* 0: planner (static, or stream-K for single-CTA tiles fewer than
-                             CTAs); 1: static persistent tiles; 2: dynamic: one 2-CTA cluster
+    int32_t schedule;     /* 0: planner (tickets for CTA-pair tiles with one pair per cluster and
+                             at least as many tiles as pairs; stream-K for single-CTA tiles
+                             fewer than CTAs; else static); 1: static persistent tiles;
+                             2: dynamic: one 2-CTA cluster
                              per tile, running clusters take over clusters not yet started
                              (cluster launch control); CTA-pair tiles, no split-K, no multicast;
                              3: stream-K: single-CTA tiles, each CTA a contiguous share of all
@@ -149,7 +152,14 @@ typedef struct {
                              adding the others' FP32 partials in CTA order (deterministic).
                              Its CTAs (at most one per SM) wait on one another, so they must
                              all fit on the device at once: where the SMs are restricted (an
-                             MPS thread limit), pass 1 */
+                             MPS thread limit), pass 1;
+                             4: tickets: CTA-pair tiles, one pair per cluster, a persistent
+                             grid; each pair takes its first tile statically and claims every
+                             later unit in order from a counter in the stream's workspace, so
+                             pairs that run ahead take more of the work (needs the workspace:
+                             not with split_k = 1).  Tickets come with the split of a partial
+                             last wave (split_k 0: into 2 K segments when the last wave is
+                             at most half full) */
     int32_t reserved[1];  /* must be zero */
 } tg_options;
 
@@ -175,6 +185,8 @@ typedef struct {
     int32_t multicast;    /* CTA pairs per cluster sharing A rows (1 or 2; 0 for single-CTA) */
     int32_t stream_k;     /* 1 if single-CTA tiles run as stream-K (each CTA a contiguous share
                              of all (tile, K block) iterations; cut tiles summed in CTA order) */
+    int32_t schedule;     /* 1 static, 2 dynamic (cluster launch control), 3 stream-K,
+                             4 tickets (see tg_options.schedule) */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides
@@ -225,8 +237,8 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
  * planned as 256-byte aligned.  Writes at most `len` bytes into `buf`,
  * always NUL-terminated when len > 0, e.g.
  *   "pair 256x256x64 stages=7 producer=tma swap=0 grid=152 tiles=1024
- *    raster=8 multicast=1 split=0x1 stream_k=0 vector_store=0 threads=320
- *    smem=230704 tmem=512"   (one line)
+ *    raster=8 multicast=1 split=36x2 schedule=ticket vector_store=0
+ *    threads=320 smem=230768 tmem=512"   (one line)
  * or "empty" when M, N or K is 0.  Returns TG_OK; TG_ERR_INVALID_VALUE on
  * the argument errors of tg_plan, when buf is NULL or len is 0, or when the
  * text did not fit (buf then holds its truncated, NUL-terminated start).

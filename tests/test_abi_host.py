@@ -65,7 +65,9 @@ FAKE = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced here
     dict(opts={"block_n": 96}), dict(opts={"producer": 3}), dict(opts={"swap_ab": 3}),
     dict(opts={"raster_group": -1}), dict(opts={"max_ctas": -2}), dict(opts={"l2_hint": 3}),
     dict(opts={"split_k": -1}), dict(opts={"split_k": 65}), dict(opts={"prefetch_k": -2}),
-    dict(opts={"reserved": [1]}), dict(opts={"multicast": 3}), dict(opts={"schedule": 4}),
+    dict(opts={"reserved": [1]}), dict(opts={"multicast": 3}), dict(opts={"schedule": 5}),
+    dict(opts={"schedule": 4, "cta_pair": 1}), dict(opts={"schedule": 4, "multicast": 2}),
+    dict(opts={"schedule": 4, "split_k": 1}),
     dict(opts={"schedule": 3, "cta_pair": 2}), dict(opts={"schedule": 3, "split_k": 1}),
     dict(opts={"schedule": 3, "multicast": 2}),
     dict(opts={"schedule": 2, "cta_pair": 1}), dict(opts={"schedule": 2, "multicast": 2}),
@@ -112,11 +114,22 @@ def test_plan_headline_8192(tg):
 
 
 def test_plan_split_tail(tg):
-    """K segments for pair tiles: by default only when there are fewer tiles
-    than pairs; forced, the last partial wave (R = tiles mod pairs tiles) is
-    cut into S = min(pairs // R, split_k, K blocks // 8) segments."""
+    """K segments for pair tiles: up to 8 when there are fewer tiles than
+    pairs; with the ticket schedule (the default for a wave or more of pair
+    tiles) the last partial wave is cut into two segments when at most half
+    full; forced, the last partial wave (R = tiles mod pairs tiles) is cut
+    into S = min(pairs // R, split_k, K blocks // 8) segments."""
     c4 = plan(tg, si.WORKLOADS["c4_bf16_8192"])        # 1024 tiles on 76 pairs
-    assert (c4["split_tiles"], c4["split_segs"]) == (0, 1)
+    assert (c4["split_tiles"], c4["split_segs"], c4["schedule"]) == (1024 % 76, 2, 4)
+    static = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"schedule": 1})
+    assert (static["split_tiles"], static["split_segs"], static["schedule"]) == (0, 1, 1)
+    # A last wave more than half full is not split (two segments would not fit).
+    w = si.Workload("s", 256 * 12, 256 * 10, 4096, "bf16", 1.0, True, 0, "normal")
+    more = plan(tg, w)                                   # 120 tiles: 44 in the last wave
+    assert (more["split_segs"], more["schedule"]) == (1, 4)
+    # No workspace, no tickets.
+    nows = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"split_k": 1})
+    assert (nows["split_segs"], nows["schedule"]) == (1, 1)
     forced = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"split_k": 8})
     assert (forced["split_tiles"], forced["split_segs"]) == (1024 % 76, 2)
     small = plan(tg, si.Workload("s", 500, 500, 2048, "bf16", 1.0, True, 0, "normal"),
@@ -434,3 +447,20 @@ def test_plan_describe_errors(tg):
     assert lib.tg_plan_describe(8, 8, 8, 0, 7, 8, 8, 152, small, 16) == tg.TG_ERR_INVALID_VALUE
     with pytest.raises(tg.TgError):
         tg.tg_plan_describe(8, 8, 8, "bf16", 8, 8, 8, 152, size=8)
+
+
+def test_plan_ticket_schedule(tg):
+    c3 = plan(tg, si.WORKLOADS["c3_fp16_4096"])          # 256 tiles on 76 pairs
+    assert (c3["cta_pair"], c3["multicast"], c3["schedule"]) == (1, 1, 4)
+    assert (c3["split_tiles"], c3["split_segs"]) == (28, 2)
+    # Multicast clusters and fewer tiles than pairs stay static.
+    assert plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])["schedule"] == 1
+    few = plan(tg, si.Workload("f", 1000, 1000, 4096, "bf16", 1.0, True, 0, "normal"))
+    assert few["cta_pair"] == 1 and few["schedule"] == 1
+    # Forced where it cannot run (fewer tiles than pairs): refused.
+    with pytest.raises(tg.TgError):
+        plan(tg, si.Workload("f", 1000, 1000, 4096, "bf16", 1.0, True, 0, "normal"),
+             opts={"schedule": 4})
+    # Single-CTA plans report static or stream-K.
+    assert plan(tg, si.WORKLOADS["c5a_bf16_16384x64x4096"])["schedule"] == 1
+    assert plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])["schedule"] == 3

@@ -160,7 +160,10 @@ def test_pair_units_cover_every_iteration_once(tg):
         mc = p["multicast"]
         pairs = p["grid"] // (2 * mc)
         tiles, nkb = p["tiles"], cdiv(K, p["block_k"])
-        split_max = 1 if mc != 1 else (8 if tiles < max(1, sms // 2) else 1)
+        pairs_max = max(1, sms // (2 * mc))
+        ticket = mc == 1 and tiles >= pairs_max
+        assert (p["schedule"] == 4) == ticket
+        split_max = 1 if mc != 1 else (8 if tiles < pairs_max else (2 if ticket else 1))
         ws_tiles = sms // 2                      # what a fresh workspace holds
         whole, segs, units = unit_plan(tiles, pairs, nkb, split_max, ws_tiles)
         # The planner reports the same split the kernel will make.
@@ -168,24 +171,47 @@ def test_pair_units_cover_every_iteration_once(tg):
         assert (tiles - whole if segs > 1 else 0) == p["split_tiles"]
         count = np.zeros((tiles, nkb), dtype=np.int64)
         owner = {}
-        for pair in range(pairs):
-            for u in range(pair, units, pairs):
-                t, k0, k1, seg, tail = decode_unit(u, whole, segs, nkb)
-                assert k1 - k0 >= min(8, nkb) and k0 < k1
-                count[t, k0:k1] += 1
-                if seg >= 0:
-                    owner[(t, seg)] = (pair, u)
-                    # Partial index and flag inside the workspace.
-                    if seg < segs - 1:
-                        pidx = tail * (segs - 1) + seg
-                        assert pidx < ws_tiles and pidx * 2 + 1 < 2 * ws_tiles
+        if ticket:
+            # First unit of each pair static, then claims in order: claim v
+            # is unit pairs + v; claims past the end fail, one per pair, and
+            # the launch's last claim (v == units - 1) resets the counter.
+            assert units >= pairs
+            order = list(range(pairs))
+            fails = []
+            for v in range(units):
+                (order if pairs + v < units else fails).append(pairs + v if pairs + v < units else v)
+            assert len(fails) == pairs and fails[-1] == units - 1
+            dispatch = [(u, u) for u in order]          # (claim order, unit)
+        else:
+            dispatch = [(u, u) for pair in range(pairs) for u in range(pair, units, pairs)]
+        for rank, u in dispatch:
+            t, k0, k1, seg, tail = decode_unit(u, whole, segs, nkb)
+            assert k1 - k0 >= min(8, nkb) and k0 < k1
+            count[t, k0:k1] += 1
+            if seg >= 0:
+                owner[(t, seg)] = rank
+                if segs == 2:
+                    # Exchange halves: partial (tail, segment, CTA half) and
+                    # its flag inside the workspace.
+                    for half in range(2):
+                        assert (tail * 2 + half) * 2 + seg < 4 * ws_tiles
+                        assert ((tail * 2 + half) * 2 + seg + 1) * (p["block_n"] // 2) <= \
+                            ws_tiles * 2 * 256
+                elif seg < segs - 1:
+                    pidx = tail * (segs - 1) + seg
+                    assert pidx < ws_tiles and pidx * 2 + 1 < 4 * ws_tiles
         assert (count == 1).all()
         if segs > 1:
             splits += 1
             for t in range(whole, tiles):
-                # All segments of a tail tile run in the last round, and the
-                # finisher is dispatched after the segments it waits for.
-                us = [owner[(t, s)][1] for s in range(segs)]
-                assert max(us) - min(us) < pairs
-                assert owner[(t, segs - 1)][1] == max(us)
+                us = [owner[(t, s)] for s in range(segs)]
+                if ticket:
+                    # A tile's segments are consecutive claims: the two sides
+                    # of an exchange are handed out one right after the other.
+                    assert us == list(range(us[0], us[0] + segs))
+                else:
+                    # All segments of a tail tile run in the last round, and
+                    # the finisher is dispatched after the segments it waits for.
+                    assert max(us) - min(us) < pairs
+                    assert us[segs - 1] == max(us)
     assert splits >= 20
