@@ -237,11 +237,16 @@ tg_status device_state(int *dev_out, DeviceState **out) {
 // Split-K tail: the kernel cuts each of the last R = tiles mod pairs tiles
 // into S = min(pairs / R, split_max, K blocks / 8) K segments (see
 // tg_kernel_pair.cuh); the host mirrors the rule to size and report it.
-// By default the split is used only when there are fewer tiles than pairs:
-// with a full wave or more, the GPU runs at its power limit and idle SMs in
-// the last wave only raise the clock of the others, so splitting adds
-// partial-sum traffic for no gain.
+// By default: up to kDefaultSplitMax segments when there are fewer tiles
+// than pairs; with a wave or more, two segments when the last wave is at most
+// half full (the two exchange halves of their partial sums, which measured
+// 1-3 % faster than whole tiles at 4096^3 and 8192^3 in bursts of launches;
+// an earlier one-sided fix-up measured no gain under sustained load).
 constexpr int kDefaultSplitMax = 8;
+
+// The ticket schedule is the planner's choice from this many waves of
+// CTA-pair tiles up (see make_plan).
+constexpr int64_t kTicketMinWaves = 6;
 
 // Stream-K (single-CTA tiles): a CTA's share spans at least this many K
 // blocks, so that its MMA work outweighs writing or reading one partial tile.
@@ -561,20 +566,24 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
         int64_t pairs_max = sms / cl;
         if (o->max_ctas && pairs_max > o->max_ctas / cl) pairs_max = o->max_ctas / cl;
         if (pairs_max < 1) pairs_max = 1;
-        // Tickets: with at least a wave of tiles and one pair per cluster,
+        // Tickets: with one pair per cluster and at least a wave of tiles,
         // pairs claim their later tiles in order, so the ones that run ahead
-        // take the tail (static: a pair's tiles are fixed, and pairs drift
-        // apart by several microseconds over a dozen tiles).  They need the
-        // workspace's counter, so not with split_k = 1.
+        // take the tail.  Static assignment fixes a pair's tiles, and pairs
+        // drift apart by several microseconds over a dozen tiles (8192^3
+        // BF16: 7-11 us at the 14th tile); over a few waves the drift is
+        // small and the static order measured as fast or faster (4096^3
+        // FP16: 89.8 vs 91.7 us), so the planner takes tickets from
+        // kTicketMinWaves waves up.  They need the workspace's counter, so
+        // not with split_k = 1.
         const bool ticket_ok = p.mc == 1 && o->split_k != 1 && p.tiles >= pairs_max &&
                                (o->schedule == 0 || o->schedule == 4);
         if (o->schedule == 4 && !ticket_ok) return TG_ERR_INVALID_VALUE;
-        p.ticket = ticket_ok;
-        // K segments: up to 8 when there are fewer tiles than pairs; with
-        // tickets, a last wave at most half full is cut into two segments
-        // that exchange halves (its tiles then take half a tile's time).
-        p.split_max = o->split_k != 0 ? o->split_k
-                                      : (p.tiles < pairs_max ? kDefaultSplitMax : (p.ticket ? 2 : 1));
+        p.ticket = ticket_ok && (o->schedule == 4 || p.tiles >= kTicketMinWaves * pairs_max);
+        // K segments: up to 8 when there are fewer tiles than pairs; with a
+        // wave or more, a last wave at most half full is cut into two
+        // segments that exchange halves (its tiles then take half a tile's
+        // time plus a short fix-up), unless the caller asked for no workspace.
+        p.split_max = o->split_k != 0 ? o->split_k : (p.tiles < pairs_max ? kDefaultSplitMax : 2);
         if (p.mc != 1) p.split_max = 1;  // K segments only with one pair per cluster
         int64_t pairs = pairs_max;
         if (p.tiles < pairs_max) {

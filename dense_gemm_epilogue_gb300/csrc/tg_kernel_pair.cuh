@@ -508,15 +508,23 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 const int32_t r = mb * C::PAIR_M + (int32_t)half * BLOCK_M + row_in_half;
                 const bool row_ok = r < p.m;
                 const float *theirs = xpart(other) + (int64_t)grp * HALF * BLOCK_M + row_in_half;
-#pragma unroll 1
-                for (int c0 = 0; ready && c0 < HALF; c0 += 32) {
+                // All of this thread's partials are requested at once: the
+                // other segment's pair may sit on the other die, and one
+                // round trip per 32 columns would put that latency in series.
+                float pv[HALF];
+                if (ready) {
+#pragma unroll
+                    for (int j = 0; j < HALF; ++j) pv[j] = __ldcg(theirs + (int64_t)j * BLOCK_M);
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < HALF; c0 += 32) {
+                    if (!ready) break;
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(taddr + cbase + sg * HALF + c0, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        v[j] = __float_as_uint(__uint_as_float(v[j]) +
-                                               __ldcg(theirs + (int64_t)(c0 + j) * BLOCK_M));
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + pv[c0 + j]);
                     if (row_ok) epilogue_store(p, bt, r, nb * BN + cbase + sg * HALF + c0, v);
                 }
                 // The other segment's flag was raised for this launch only:

@@ -132,7 +132,9 @@ typedef struct {
     int32_t max_ctas;     /* 0: one CTA per SM; else an upper bound on the persistent grid */
     int32_t cta_pair;     /* 0: planner; 1: single-CTA tiles; 2: CTA-pair tiles (not TF32; TMA) */
     int32_t split_k;      /* 0: planner (pair tiles fewer than pairs: split them into up to 8
-                             K segments of >= 8 K blocks); 1: never split (nor stream-K);
+                             K segments of >= 8 K blocks; a wave or more: a last wave at most
+                             half full into 2 segments that exchange halves); 1: never split
+                             (nor stream-K, nor tickets: no workspace);
                              n >= 2: split the last, partial wave into at most n segments */
     int32_t l2_hint;      /* 0: planner (default policy); 1: default L2 policy for operand loads;
                              2: A-role rows evict-last (CTA-pair tiles) */
@@ -141,8 +143,8 @@ typedef struct {
     int32_t multicast;    /* 0: planner; 1: one CTA pair per cluster; 2: two pairs per cluster
                              sharing their A-role rows by TMA multicast (CTA-pair tiles) */
     int32_t schedule;     /* 0: planner (tickets for CTA-pair tiles with one pair per cluster and
-                             at least as many tiles as pairs; stream-K for single-CTA tiles
-                             fewer than CTAs; else static); 1: static persistent tiles;
+                             at least 6 waves of tiles; stream-K for single-CTA tiles fewer
+                             than CTAs; else static); 1: static persistent tiles;
                              2: dynamic: one 2-CTA cluster
                              per tile, running clusters take over clusters not yet started
                              (cluster launch control); CTA-pair tiles, no split-K, no multicast;
@@ -157,9 +159,7 @@ typedef struct {
                              grid; each pair takes its first tile statically and claims every
                              later unit in order from a counter in the stream's workspace, so
                              pairs that run ahead take more of the work (needs the workspace:
-                             not with split_k = 1).  Tickets come with the split of a partial
-                             last wave (split_k 0: into 2 K segments when the last wave is
-                             at most half full) */
+                             not with split_k = 1) */
     int32_t reserved[1];  /* must be zero */
 } tg_options;
 

@@ -122,11 +122,11 @@ def test_plan_split_tail(tg):
     c4 = plan(tg, si.WORKLOADS["c4_bf16_8192"])        # 1024 tiles on 76 pairs
     assert (c4["split_tiles"], c4["split_segs"], c4["schedule"]) == (1024 % 76, 2, 4)
     static = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"schedule": 1})
-    assert (static["split_tiles"], static["split_segs"], static["schedule"]) == (0, 1, 1)
+    assert (static["split_tiles"], static["split_segs"], static["schedule"]) == (36, 2, 1)
     # A last wave more than half full is not split (two segments would not fit).
     w = si.Workload("s", 256 * 12, 256 * 10, 4096, "bf16", 1.0, True, 0, "normal")
     more = plan(tg, w)                                   # 120 tiles: 44 in the last wave
-    assert (more["split_segs"], more["schedule"]) == (1, 4)
+    assert (more["split_segs"], more["schedule"]) == (1, 1)
     # No workspace, no tickets.
     nows = plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"split_k": 1})
     assert (nows["split_segs"], nows["schedule"]) == (1, 1)
@@ -450,9 +450,19 @@ def test_plan_describe_errors(tg):
 
 
 def test_plan_ticket_schedule(tg):
-    c3 = plan(tg, si.WORKLOADS["c3_fp16_4096"])          # 256 tiles on 76 pairs
-    assert (c3["cta_pair"], c3["multicast"], c3["schedule"]) == (1, 1, 4)
+    """Tickets from 6 waves of CTA-pair tiles up (one pair per cluster);
+    fewer waves run static, both with the exchange split of a last wave at
+    most half full."""
+    c3 = plan(tg, si.WORKLOADS["c3_fp16_4096"])          # 256 tiles on 76 pairs: 3.4 waves
+    assert (c3["cta_pair"], c3["multicast"], c3["schedule"]) == (1, 1, 1)
     assert (c3["split_tiles"], c3["split_segs"]) == (28, 2)
+    assert plan(tg, si.WORKLOADS["c3_fp16_4096"], opts={"schedule": 4})["schedule"] == 4
+    c4 = plan(tg, si.WORKLOADS["c4_bf16_8192"])          # 13.5 waves
+    assert (c4["schedule"], c4["split_tiles"], c4["split_segs"]) == (4, 36, 2)
+    six = plan(tg, si.Workload("s", 256 * 19, 256 * 24, 4096, "bf16", 1.0, True, 0, "normal"))
+    assert (six["tiles"], six["schedule"]) == (456, 4)   # exactly 6 waves of 76 pairs
+    five = plan(tg, si.Workload("s", 256 * 19, 256 * 20, 4096, "bf16", 1.0, True, 0, "normal"))
+    assert (five["tiles"], five["schedule"]) == (380, 1)
     # Multicast clusters and fewer tiles than pairs stay static.
     assert plan(tg, si.WORKLOADS["c5c_bf16_8191x4097x1000"])["schedule"] == 1
     few = plan(tg, si.Workload("f", 1000, 1000, 4096, "bf16", 1.0, True, 0, "normal"))

@@ -37,7 +37,7 @@ def find_cap(tg, w, want_segs, extra=None):
     `want_segs` K segments for the last wave."""
     lda, ldb, ldc = w.strides
     for cap in range(4, 153, 2):
-        opts = {"max_ctas": cap, "cta_pair": 2, **(extra or {})}
+        opts = {"max_ctas": cap, "cta_pair": 2, "schedule": 4, **(extra or {})}
         try:
             p = tg.tg_plan(w.M, w.N, w.K, None, lda, None, ldb, None, ldc, w.dtype, opts)
         except tg.TgError:
@@ -86,3 +86,20 @@ def test_ticket_forced_matches_static(tg):
     w = si.Workload("tk_forced", 2560, 2304, 1536, "bf16", 1.0, True, 86, "normal")
     check_full(w, opts={"schedule": 4})
     check_full(w, opts={"schedule": 1})
+
+
+def test_static_exchange_split_parity(tg):
+    """The static schedule with the two-segment exchange of a last wave at
+    most half full (the planner's choice for a few waves of pair tiles)."""
+    w = si.Workload("st_exchange", 1000, 1100, 1100, "bf16", 1.25, True, 87, "normal", lda=1104,
+                    ldb=1104, ldc=1001)
+    lda, ldb, ldc = w.strides
+    for cap in range(4, 153, 2):
+        opts = {"max_ctas": cap, "cta_pair": 2, "schedule": 1}
+        p = tg.tg_plan(w.M, w.N, w.K, None, lda, None, ldb, None, ldc, w.dtype, opts)
+        if p["split_segs"] == 2 and p["tiles"] >= p["grid"] // 2:
+            break
+    else:
+        raise AssertionError("no grid cap gives a static exchange split")
+    assert p["schedule"] == 1
+    check_full(w, opts=opts, repeats=3)

@@ -161,9 +161,9 @@ def test_pair_units_cover_every_iteration_once(tg):
         pairs = p["grid"] // (2 * mc)
         tiles, nkb = p["tiles"], cdiv(K, p["block_k"])
         pairs_max = max(1, sms // (2 * mc))
-        ticket = mc == 1 and tiles >= pairs_max
+        ticket = mc == 1 and tiles >= 6 * pairs_max
         assert (p["schedule"] == 4) == ticket
-        split_max = 1 if mc != 1 else (8 if tiles < pairs_max else (2 if ticket else 1))
+        split_max = 1 if mc != 1 else (8 if tiles < pairs_max else 2)
         ws_tiles = sms // 2                      # what a fresh workspace holds
         whole, segs, units = unit_plan(tiles, pairs, nkb, split_max, ws_tiles)
         # The planner reports the same split the kernel will make.
@@ -184,6 +184,10 @@ def test_pair_units_cover_every_iteration_once(tg):
             dispatch = [(u, u) for u in order]          # (claim order, unit)
         else:
             dispatch = [(u, u) for pair in range(pairs) for u in range(pair, units, pairs)]
+        if not ticket and segs == 2 and tiles >= pairs:
+            # Static exchange: a tail tile's two segments are consecutive
+            # units of the last round, on neighbouring pairs.
+            assert whole % pairs == 0
         for rank, u in dispatch:
             t, k0, k1, seg, tail = decode_unit(u, whole, segs, nkb)
             assert k1 - k0 >= min(8, nkb) and k0 < k1
