@@ -632,13 +632,17 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    griddep_wait();
+    // Programmatic dependent launch: every role waits for the preceding grid
+    // before its first global-memory access; the TMA producer first works
+    // out its first tile and claims its first stage, so that its first load
+    // leaves right after the wait.
     griddep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
 
     if (PLAIN_LOADS && warp >= C::NUM_WARPS) {
         // ------------------------------------------------------ plain-load producer
+        griddep_wait();
         constexpr int NT = C::LOAD_WARPS * 32;
         const int ltid = threadIdx.x - C::NUM_WARPS * 32;
         int s = 0;
@@ -671,11 +675,16 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
+            bool waited = false;
             TileUnits un(p);
             while (ok && un.next(p)) {
                 int bt, mb, nb;
                 batch_tile_coords(un.t, p, bt, mb, nb);
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
+                if (!waited && p.prefetch_k > 0) {
+                    griddep_wait();
+                    waited = true;
+                }
                 if (p.prefetch_k > 0) {
                     for (int j = un.k0; j < un.k0 + p.prefetch_k && j < un.k1; ++j)
                         tma_prefetch_l2_3d(&tmap_a, j * C::BK, mb * BLOCK_M, ab);
@@ -689,6 +698,10 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                     }
                     if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     mbar_arrive_expect_tx(bar(C::FULL0 + s), C::A_BYTES + C::B_BYTES);
+                    if (!waited) {
+                        griddep_wait();
+                        waited = true;
+                    }
                     tma_load_3d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M, ab);
                     tma_load_3d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kb * C::BK, nb * BN, bb);
                     ++issued;
@@ -703,8 +716,12 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                 }
             }
         }
+        // The warp reaches the block-wide barrier below together: the other
+        // lanes wait here for the producing lane.
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        griddep_wait();
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -746,6 +763,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         __syncwarp();
     } else if (warp < 2 + C::EPI_WARPS) {
         // ------------------------------------------------------ epilogue
+        griddep_wait();
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int row_in_tile = q * 32 + lane;
         constexpr int COLS = BN / (C::EPI_WARPS / 4);  // columns of this warp
@@ -846,6 +864,7 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
         }
     } else if constexpr (C::TF32) {
         // ------------------------------------------------------ TF32 narrowing
+        griddep_wait();
         constexpr int NT = C::CONV_THREADS;
         constexpr int NA = C::A_BYTES / 16 / NT, NB = C::B_BYTES / 16 / NT;
         static_assert(C::A_BYTES / 16 % NT == 0 && C::B_BYTES / 16 % NT == 0, "stage split");

@@ -162,7 +162,9 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
     tc_fence_before();
     cluster_sync_all();
     tc_fence_after();
-    griddep_wait();
+    // Programmatic dependent launch: each role waits for the preceding grid
+    // before its first global-memory access (the producer after working out
+    // its first tile).
     griddep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
@@ -174,9 +176,14 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
+            bool waited = false;
             for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs) {
                 int bt, mb, nb;
                 batch_tile_coords(t, p, bt, mb, nb);
+                if (!waited) {
+                    griddep_wait();
+                    waited = true;
+                }
                 const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer (leader)
+        griddep_wait();
         if (leader && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -264,6 +272,7 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue (both CTAs)
+        griddep_wait();
         const int q = warp & 3;
         const int row_in_half = q * 32 + lane;
         const int cbase = ((warp - 2) / 4) * C::COLS;

@@ -253,7 +253,9 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
     tc_fence_before();
     cluster_sync_all();  // both CTAs' barriers initialised, tensor memory allocated
     tc_fence_after();
-    griddep_wait();
+    // Programmatic dependent launch: every role waits for the preceding grid
+    // before its first global-memory access (the producer after working out
+    // its first unit, so that its first load leaves right after the wait).
     griddep_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
@@ -304,7 +306,15 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
             int64_t issued = 0;
             bool ok = true;
             int64_t step = 0;
+            bool waited = false;
             for (int64_t u = first_unit; ok && u >= 0 && u < up.units;) {
+                const Unit un = decode_unit(up, u, nkb);
+                int bt, mb, nbc;
+                batch_tile_coords(un.tile, p, bt, mb, nbc);
+                if (!waited) {
+                    griddep_wait();  // also orders the ticket claims after the previous launch
+                    waited = true;
+                }
                 if (ring) {
                     // Ask for the unit after this one (answer `step`), into a
                     // slot all readers have released.
@@ -344,9 +354,6 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                         }
                     }
                 }
-                const Unit un = decode_unit(up, u, nkb);
-                int bt, mb, nbc;
-                batch_tile_coords(un.tile, p, bt, mb, nbc);
                 const int nb = nbc * MC + (int)pic;
                 const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
@@ -387,6 +394,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer (leader)
+        griddep_wait();
         if (leader && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -434,6 +442,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue (both CTAs)
+        griddep_wait();
         const int q = warp & 3;
         const int row_in_half = q * 32 + lane;
         constexpr int EPI_THREADS = C::EPI_WARPS * 32;

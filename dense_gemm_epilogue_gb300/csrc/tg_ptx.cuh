@@ -14,11 +14,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // Programmatic dependent launch.  The kernels are launched so that the next
-// kernel of the stream may start while this one finishes; each kernel waits
-// (griddep_wait) for the preceding grid to complete, with its memory
-// visible, before its first global-memory access, and lets the next grid
-// start launching (griddep_launch) right after that wait.  Only the prologue
-// (barrier set-up, tensor-memory allocation) overlaps the previous kernel.
+// kernel of the stream may start while this one finishes; each kernel lets
+// the next grid start launching (griddep_launch) once its prologue is done,
+// and each of its threads waits (griddep_wait) for the preceding grid to
+// complete, with its memory visible, before its first global-memory access.
+// The prologue (barrier set-up, tensor-memory allocation, the producer's
+// first tile coordinates) overlaps the previous kernel.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
