@@ -122,6 +122,7 @@ class tg_plan_info(ctypes.Structure):
         ("multicast", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
+        ("k_rotate", ctypes.c_int32),
     ]
 
 

@@ -252,6 +252,13 @@ constexpr int64_t kTicketMinWaves = 6;
 // blocks, so that its MMA work outweighs writing or reading one partial tile.
 constexpr int64_t kStreamKMinBlocks = 8;
 
+// Rotated K order (single-CTA, one wave of whole tiles): the largest
+// operand shared by several tiles that the rotation still keeps in L2.
+constexpr int64_t kRotateSharedBytes = 32ll << 20;
+// ... and the shortest K loop (in K blocks) it is used for: it matters for
+// long streaming loops only.
+constexpr int64_t kRotateMinBlocks = 16;
+
 // Planner cost of finishing a K-split tile (flag wait, partial-sum round
 // trip through L2), in the planner's cost units: about 4 us measured, some
 // 22 K blocks of a 128 x 64 tile.  Splitting therefore pays only for long
@@ -310,6 +317,7 @@ struct Plan {
     int smem = 0;
     int tmem_cols = 0;
     bool vector_store = false;
+    bool k_rotate = false;   // single-CTA whole tiles: rotated K order per tile
     int64_t mk = 0, nk = 0;  // role-space rows and cols
 };
 
@@ -615,6 +623,19 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
             if (grid > cap) grid = cap;
         }
         p.grid = (int)(grid < 1 ? 1 : grid);
+        // One wave of whole tiles: each tile starts its K loop at its own
+        // offset (rotated order).  In step, every CTA reads the same K
+        // offset of rows about a megabyte apart at the same time, and on
+        // some boxes of the pool that ran 9-11 % slower at 16384 x 64 x 4096
+        // (36.5 vs 33.3 us per launch; others saw no difference).  Only where
+        // an operand that several tiles share stays in L2 anyway (one N block
+        // or a small A-role operand, one M block or a small B-role operand),
+        // since the rotated tiles no longer read it together.
+        const int64_t e_in = elem_bytes(t);
+        const bool a_ok = nblocks == 1 || p.mk * K * e_in <= kRotateSharedBytes;
+        const bool b_ok = mblocks == 1 || p.nk * K * e_in <= kRotateSharedBytes;
+        p.k_rotate = !p.stream_k && p.tiles <= p.grid && o->schedule != 1 && a_ok && b_ok &&
+                     nkb >= kRotateMinBlocks;
     }
     // Swapped roles store each thread's 32 consecutive columns as 16-byte
     // vectors when every row of every batch entry starts 16-byte aligned.
@@ -781,6 +802,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.out_fmt = q.out_fmt;
     p.alpha = q.alpha;
     p.vector_store = plan.vector_store ? 1 : 0;
+    p.k_rotate = (!la.pair && plan.k_rotate) ? 1 : 0;
     p.d = q.D;
     p.d_row_stride = plan.swap ? q.ldc : 1;
     p.d_col_stride = plan.swap ? 1 : q.ldc;
@@ -1113,6 +1135,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->tmem_cols = p.tmem_cols;
     out->vector_store = p.vector_store ? 1 : 0;
     out->schedule = p.dynamic ? 2 : p.stream_k ? 3 : p.ticket ? 4 : 1;
+    out->k_rotate = p.k_rotate ? 1 : 0;
     return TG_OK;
 }
 
@@ -1130,8 +1153,8 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, i
     } else {
         n = std::snprintf(buf, len,
                           "%s %dx%dx%d stages=%d producer=%s swap=%d grid=%d tiles=%lld raster=%d "
-                          "multicast=%d split=%dx%d schedule=%s vector_store=%d threads=%d "
-                          "smem=%d tmem=%d",
+                          "multicast=%d split=%dx%d schedule=%s k_rotate=%d vector_store=%d "
+                          "threads=%d smem=%d tmem=%d",
                           pi.cta_pair ? "pair" : "single", pi.block_m, pi.block_n, pi.block_k,
                           pi.stages, pi.producer == 1 ? "tma" : "plain", pi.swap_ab, pi.grid,
                           (long long)pi.tiles, pi.raster_group, pi.multicast, pi.split_tiles,
@@ -1140,7 +1163,7 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, i
                           : pi.schedule == 3 ? "stream_k"
                           : pi.schedule == 4 ? "ticket"
                                              : "static",
-                          pi.vector_store, pi.threads, pi.smem_bytes, pi.tmem_cols);
+                          pi.k_rotate, pi.vector_store, pi.threads, pi.smem_bytes, pi.tmem_cols);
     }
     return (n >= 0 && (size_t)n < len) ? TG_OK : TG_ERR_INVALID_VALUE;
 }

@@ -212,10 +212,24 @@ struct GemmParams {
     // adds the later CTAs' FP32 partials (workspace slot = CTA index, 128 x
     // 256 floats each; one ready flag per slot).
     int32_t stream_k;
+    // Single-CTA kernel, whole-tile units: 1 = tile t walks its K blocks
+    // starting at block (t * K_ROTATE_STEP) mod num_k_blocks (wrapping round),
+    // so that the CTAs of a wave do not all read the same K offset of their
+    // rows at the same time.  The summation order per tile stays fixed.
+    int32_t k_rotate;
     EpiProgram epi;                 // composed epilogue (n = 0: alpha and ReLU only)
 };
 
 constexpr int BLOCK_M = 128;
+constexpr int64_t K_ROTATE_STEP = 13;
+
+// The K block a whole-tile unit of tile t loads at its position kb.
+__device__ __forceinline__ int rotated_k_block(const GemmParams &p, int64_t t, int k0, int k1,
+                                               int kb, int nkb) {
+    if (!p.k_rotate || k0 != 0 || k1 != nkb) return kb;
+    int kr = kb + (int)((t * K_ROTATE_STEP) % nkb);
+    return kr >= nkb ? kr - nkb : kr;
+}
 constexpr int ROW_BYTES = 128;                   // one K-major smem row: 128 bytes
 constexpr int SMEM_LIMIT = 232448;               // max dynamic smem per CTA (227 KB)
 
@@ -657,10 +671,11 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
             const uint8_t *b_src = static_cast<const uint8_t *>(p.b_ptr) + (int64_t)bt * p.stride_b * E;
             for (int kb = un.k0; kb < un.k1; ++kb) {
                 if (!wait_phase(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                const int kr = rotated_k_block(p, un.t, un.k0, un.k1, kb, nkb);
                 load_stage_plain<E, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES, a_src, p.lda,
-                                                 mb * BLOCK_M, p.m, kb * C::BK, p.k, ltid);
+                                                 mb * BLOCK_M, p.m, kr * C::BK, p.k, ltid);
                 load_stage_plain<E, BN, NT>(smem + C::B_OFF + s * C::B_BYTES, b_src, p.ldb,
-                                            nb * BN, p.n, kb * C::BK, p.k, ltid);
+                                            nb * BN, p.n, kr * C::BK, p.k, ltid);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::FULL0 + s));
                 if (++s == S) { s = 0; ph ^= 1; }
@@ -702,8 +717,9 @@ __global__ void __launch_bounds__(Config<KD, BN>::threads(PLAIN_LOADS), 1)
                         griddep_wait();
                         waited = true;
                     }
-                    tma_load_3d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kb * C::BK, mb * BLOCK_M, ab);
-                    tma_load_3d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kb * C::BK, nb * BN, bb);
+                    const int kr = rotated_k_block(p, un.t, un.k0, un.k1, kb, nkb);
+                    tma_load_3d(a_stage(s), &tmap_a, bar(C::FULL0 + s), kr * C::BK, mb * BLOCK_M, ab);
+                    tma_load_3d(b_stage(s), &tmap_b, bar(C::FULL0 + s), kr * C::BK, nb * BN, bb);
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }

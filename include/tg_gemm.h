@@ -187,6 +187,8 @@ typedef struct {
                              of all (tile, K block) iterations; cut tiles summed in CTA order) */
     int32_t schedule;     /* 1 static, 2 dynamic (cluster launch control), 3 stream-K,
                              4 tickets (see tg_options.schedule) */
+    int32_t k_rotate;     /* 1 if each tile walks its K blocks from its own offset (one wave
+                             of single-CTA tiles; the order per tile stays fixed) */
 } tg_plan_info;
 
 /* tg_gemm with planner overrides.  Invalid or inapplicable overrides
@@ -237,8 +239,8 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
  * planned as 256-byte aligned.  Writes at most `len` bytes into `buf`,
  * always NUL-terminated when len > 0, e.g.
  *   "pair 256x256x64 stages=7 producer=tma swap=0 grid=152 tiles=1024
- *    raster=8 multicast=1 split=36x2 schedule=ticket vector_store=0
- *    threads=320 smem=230768 tmem=512"   (one line)
+ *    raster=8 multicast=1 split=36x2 schedule=ticket k_rotate=0
+ *    vector_store=0 threads=320 smem=230768 tmem=512"   (one line)
  * or "empty" when M, N or K is 0.  Returns TG_OK; TG_ERR_INVALID_VALUE on
  * the argument errors of tg_plan, when buf is NULL or len is 0, or when the
  * text did not fit (buf then holds its truncated, NUL-terminated start).

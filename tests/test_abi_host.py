@@ -474,3 +474,27 @@ def test_plan_ticket_schedule(tg):
     # Single-CTA plans report static or stream-K.
     assert plan(tg, si.WORKLOADS["c5a_bf16_16384x64x4096"])["schedule"] == 1
     assert plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])["schedule"] == 3
+
+
+def test_plan_k_rotate(tg):
+    """One wave of single-CTA whole tiles walks each tile's K blocks from its
+    own offset, where the operand the tiles share fits in L2."""
+    for name in ("c5a_bf16_16384x64x4096", "c5b_bf16_64x16384x4096"):
+        p = plan(tg, si.WORKLOADS[name])
+        assert (p["cta_pair"], p["k_rotate"]) == (0, 1)
+        assert plan(tg, si.WORKLOADS[name], opts={"schedule": 1})["k_rotate"] == 0
+        assert plan(tg, si.WORKLOADS[name], opts={"schedule": 3})["k_rotate"] == 0
+    for name in ("c4_bf16_8192", "c3_fp16_4096", "c2_tf32_256x128x512", "c1_bf16_65x97x73"):
+        assert plan(tg, si.WORKLOADS[name])["k_rotate"] == 0    # (c1: a 2-block K loop)
+    # More tiles than CTAs (several waves): no rotation.
+    many = plan(tg, si.Workload("m", 4096, 4096, 4096, "bf16", 1.0, True, 0, "normal"),
+                opts={"cta_pair": 1})
+    assert many["tiles"] > many["grid"] and many["k_rotate"] == 0
+    # One wave whose shared A-role operand is large (two N blocks of a tall A): no rotation.
+    w = si.Workload("t", 8192, 512, 8192, "bf16", 1.0, True, 0, "normal")
+    tall = plan(tg, w, opts={"cta_pair": 1, "block_n": 256, "split_k": 1})
+    assert tall["tiles"] <= tall["grid"] and tall["stream_k"] == 0 and tall["k_rotate"] == 0
+    # The same wave with a small A-role operand rotates.
+    short = plan(tg, si.with_shape(w, M=1024, K=2048, lda=2048, ldb=2048),
+                 opts={"cta_pair": 1, "block_n": 128, "split_k": 1})
+    assert short["tiles"] <= short["grid"] and short["k_rotate"] == 1

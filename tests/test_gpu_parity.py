@@ -311,3 +311,18 @@ def test_cross_check_against_torch_matmul():
     got = torch.from_numpy(np.ascontiguousarray(D[:, : w.M])).cuda()
     err = (got - ref).abs()
     assert bool((err <= 2.0 ** -7 * scale + 1e-6).all()), float(err.max())
+
+
+def test_rotated_k_order_one_wave():
+    """One wave of single-CTA tiles, each walking its K blocks from its own
+    offset (K ragged against the stage, so the wrap crosses the partial last
+    block), TMA and plain loads; bitwise repeatable."""
+    import dense_gemm_epilogue_gb300 as tg
+
+    for producer, lda in ((1, 2056), (2, 2049)):
+        w = si.Workload("rot", 1000, 500, 2049, "bf16", 1.0, True, 91 + producer, "normal",
+                        lda=lda, ldb=lda, ldc=1003)
+        opts = {"cta_pair": 1, "block_n": 128, "split_k": 1, "producer": producer}
+        p = tg.tg_plan(w.M, w.N, w.K, None, lda, None, lda, None, w.ldc, w.dtype, opts)
+        assert p["k_rotate"] == 1 and p["tiles"] <= p["grid"]
+        check_full(w, opts=opts, repeats=2)
