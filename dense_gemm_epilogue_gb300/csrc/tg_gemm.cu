@@ -868,7 +868,7 @@ bool mx_options_ok(const tg_options *o) {
     if (!o) return true;
     if (o->block_n != 0 && o->block_n != 128 && o->block_n != 256) return false;
     if (o->swap_ab < 0 || o->swap_ab > 2 || o->raster_group < 0 || o->max_ctas < 0) return false;
-    if (o->producer < 0 || o->producer > 1) return false;
+    if (o->producer < 0 || o->producer > 2) return false;
     if (o->cta_pair < 0 || o->cta_pair == 1 || o->cta_pair > 2) return false;
     if (o->split_k < 0 || o->split_k > 1) return false;
     if (o->l2_hint || o->prefetch_k < -1 || o->prefetch_k > 0) return false;
@@ -882,6 +882,16 @@ bool mx_scale_stride_ok(int64_t stride, int64_t rows, int64_t K, int64_t batch) 
     if (batch <= 1 || stride == 0) return true;
     return stride > 0 && stride % 16 == 0 && stride >= mx_scale_bytes(rows, K) &&
            stride < (int64_t)(1ull << 40);
+}
+
+// Operands of a block-scaled product the TMA can address (rows and batch
+// entries 16-byte aligned, in bytes: packed FP4 holds two elements a byte).
+bool mx_tma_legal(const Problem &q) {
+    const bool fp4 = q.t == TG_E2M1;
+    const int64_t lda_b = fp4 ? q.lda / 2 : q.lda, ldb_b = fp4 ? q.ldb / 2 : q.ldb;
+    const int64_t sa_b = fp4 ? q.sa / 2 : q.sa, sb_b = fp4 ? q.sb / 2 : q.sb;
+    return tma_legal(q.A, lda_b, 1) && tma_legal(q.B, ldb_b, 1) &&
+           tma_batch_legal(sa_b, 1, q.batch) && tma_batch_legal(sb_b, 1, q.batch);
 }
 
 tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sfb,
@@ -899,11 +909,9 @@ tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const voi
     if (!mx_scale_stride_ok(ssfa, q.M, q.K, q.batch) || !mx_scale_stride_ok(ssfb, q.N, q.K, q.batch))
         return TG_ERR_INVALID_VALUE;
     if (q.M > 0 && q.N > 0 && q.K > 0 && q.batch > 0) {
-        const int64_t lda_b = fp4 ? q.lda / 2 : q.lda, ldb_b = fp4 ? q.ldb / 2 : q.ldb;
-        const int64_t sa_b = fp4 ? q.sa / 2 : q.sa, sb_b = fp4 ? q.sb / 2 : q.sb;
-        if (!tma_legal(q.A, lda_b, 1) || !tma_legal(q.B, ldb_b, 1)) return TG_ERR_INVALID_VALUE;
-        if (!tma_batch_legal(sa_b, 1, q.batch) || !tma_batch_legal(sb_b, 1, q.batch))
-            return TG_ERR_INVALID_VALUE;
+        // Operands the TMA cannot address run on the plain-load producer;
+        // forcing the TMA producer on them is an error.
+        if (o && o->producer == 1 && !mx_tma_legal(q)) return TG_ERR_INVALID_VALUE;
         if (!sfa || !sfb || (uintptr_t)sfa % 16 || (uintptr_t)sfb % 16) return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
@@ -917,7 +925,7 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     Plan p;
     p.pair = true;
     p.mc = 1;
-    p.producer = 1;
+    p.producer = o->producer ? o->producer : (mx_tma_legal(q) ? 1 : 2);
     if (o->swap_ab == 1) p.swap = false;
     else if (o->swap_ab == 2) p.swap = true;
     else p.swap = (q.M < tg::BLOCK_M) && (q.N >= tg::BLOCK_M) && (q.N >= 2 * q.M);
@@ -929,6 +937,9 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     int64_t best = -1;
     for (int bn : {256, 128}) {
         if (o->block_n && o->block_n != bn) continue;
+        // The plain-load producer's four extra warps leave the 256-column
+        // epilogue short of registers: 128 unless asked for.
+        if (!o->block_n && p.producer == 2 && bn == 256) continue;
         const int64_t tiles =
             (q.batch > 1 ? q.batch : 1) * ceil_div(p.mk, 2 * tg::BLOCK_M) * ceil_div(p.nk, bn);
         const int64_t mma = bn / 2, smem = 64 + bn / 4;
@@ -941,8 +952,8 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     const int64_t mblocks = ceil_div(p.mk, 2 * tg::BLOCK_M);
     p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
     p.tiles = (q.batch > 1 ? q.batch : 1) * p.tiles_per_batch;
-    tg::mx_config_numbers(q.t == TG_E2M1 ? Kind::E2M1 : Kind::E4M3, p.block_n, &p.stages, &p.smem,
-                          &p.threads, &p.tmem_cols);
+    tg::mx_config_numbers(q.t == TG_E2M1 ? Kind::E2M1 : Kind::E4M3, p.block_n, p.producer == 2,
+                          &p.stages, &p.smem, &p.threads, &p.tmem_cols);
     int64_t g = o->raster_group ? o->raster_group : 8;
     if (g > mblocks) g = mblocks;
     p.group = (int)g;
@@ -1007,10 +1018,12 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     const int64_t nba = many && sa ? q.batch : 1, nbb = many && sb ? q.batch : 1;
     const int64_t nsa = many && ssa ? q.batch : 1, nsb = many && ssb ? q.batch : 1;
     const int kgs = block_k(q.t) / 128;  // scale-atom columns per K stage
-    if (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sa, tg::BLOCK_M) ||
-        !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sb, plan.block_n / 2) ||
-        !encode_scales(&la.map_sfa, sar, plan.mk, q.K, nsa, ssa, kgs, 1) ||
-        !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, nsb, ssb, kgs, plan.block_n / tg::BLOCK_M))
+    la.plain_loads = plan.producer == 2;
+    if (!la.plain_loads &&
+        (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sa, tg::BLOCK_M) ||
+         !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sb, plan.block_n / 2) ||
+         !encode_scales(&la.map_sfa, sar, plan.mk, q.K, nsa, ssa, kgs, 1) ||
+         !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, nsb, ssb, kgs, plan.block_n / tg::BLOCK_M)))
         return TG_ERR_INVALID_VALUE;
     la.block_n = plan.block_n;
     la.pair = true;
@@ -1042,6 +1055,14 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     p.b_bmul = nbb > 1 ? 1 : 0;
     p.sfa_bmul = nsa > 1 ? 1 : 0;
     p.sfb_bmul = nsb > 1 ? 1 : 0;
+    // Plain-load producer: element batch strides (0 when shared) and scale
+    // atoms with byte batch strides.
+    p.stride_a = nba > 1 ? sa : 0;
+    p.stride_b = nbb > 1 ? sb : 0;
+    p.sfa_ptr = sar;
+    p.sfb_ptr = sbr;
+    p.sfa_stride = nsa > 1 ? ssa : 0;
+    p.sfb_stride = nsb > 1 ? ssb : 0;
     p.swap = plan.swap ? 1 : 0;
     p.epi = prog;
     p.status = ds->status;
@@ -1232,7 +1253,7 @@ tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, 
     out->block_n = p.block_n;
     out->block_k = block_k(in_dtype);
     out->stages = p.stages;
-    out->producer = 1;
+    out->producer = p.producer;
     out->swap_ab = p.swap ? 1 : 0;
     out->raster_group = p.group;
     out->grid = p.grid;

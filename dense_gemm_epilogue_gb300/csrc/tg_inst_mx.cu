@@ -7,10 +7,10 @@
 
 namespace tg {
 
-template <Kind KD, int BN>
+template <Kind KD, int BN, bool PLAIN>
 static cudaError_t launch_mx_one(const LaunchArgs &a) {
     using C = MxConfig<KD, BN>;
-    auto kernel = tg_gemm_mx_kernel<KD, BN>;
+    auto kernel = tg_gemm_mx_kernel<KD, BN, PLAIN>;
     static std::atomic<uint64_t> configured{0};
     static int max_clusters[64] = {0};
     const uint64_t bit = (a.device >= 0 && a.device < 64) ? (1ull << a.device) : 0;
@@ -22,7 +22,7 @@ static cudaError_t launch_mx_one(const LaunchArgs &a) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(C::threads(PLAIN), 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = a.stream;
     cfg.attrs = attr;
@@ -45,8 +45,8 @@ static cudaError_t launch_mx_one(const LaunchArgs &a) {
     if (grid < 2) grid = 2;
     cfg.gridDim = dim3(grid, 1, 1);
     if (std::getenv("TG_LOG"))
-        std::fprintf(stderr, "tg_gemm_mx: BN=%d stages=%d grid=%d (planned %d)\n", BN, C::STAGES,
-                     grid, a.grid);
+        std::fprintf(stderr, "tg_gemm_mx: BN=%d stages=%d grid=%d (planned %d) plain=%d\n", BN,
+                     C::STAGES, grid, a.grid, PLAIN ? 1 : 0);
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a.map_a, a.map_b, a.map_sfa, a.map_sfb, a.p);
     if (e != cudaSuccess) return e;
@@ -55,8 +55,13 @@ static cudaError_t launch_mx_one(const LaunchArgs &a) {
 
 template <Kind KD>
 static cudaError_t launch_mx_kind(const LaunchArgs &a) {
-    if (a.block_n == 256) return launch_mx_one<KD, 256>(a);
-    if (a.block_n == 128) return launch_mx_one<KD, 128>(a);
+    if (a.plain_loads) {
+        if (a.block_n == 256) return launch_mx_one<KD, 256, true>(a);
+        if (a.block_n == 128) return launch_mx_one<KD, 128, true>(a);
+    } else {
+        if (a.block_n == 256) return launch_mx_one<KD, 256, false>(a);
+        if (a.block_n == 128) return launch_mx_one<KD, 128, false>(a);
+    }
     return cudaErrorInvalidValue;
 }
 
@@ -68,21 +73,22 @@ cudaError_t launch_mx(const LaunchArgs &a, Kind kind) {
 }
 
 template <Kind KD>
-static void mx_numbers(int block_n, int *stages, int *smem, int *threads, int *tmem) {
+static void mx_numbers(int block_n, bool plain, int *stages, int *smem, int *threads, int *tmem) {
     if (block_n == 256) {
         using C = MxConfig<KD, 256>;
-        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
+        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::threads(plain); *tmem = C::TMEM_COLS;
     } else if (block_n == 128) {
         using C = MxConfig<KD, 128>;
-        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::NUM_THREADS; *tmem = C::TMEM_COLS;
+        *stages = C::STAGES; *smem = C::SMEM_BYTES; *threads = C::threads(plain); *tmem = C::TMEM_COLS;
     } else {
         *stages = *smem = *threads = *tmem = 0;
     }
 }
 
-void mx_config_numbers(Kind kind, int block_n, int *stages, int *smem, int *threads, int *tmem) {
-    if (kind == Kind::E2M1) mx_numbers<Kind::E2M1>(block_n, stages, smem, threads, tmem);
-    else mx_numbers<Kind::E4M3>(block_n, stages, smem, threads, tmem);
+void mx_config_numbers(Kind kind, int block_n, bool plain, int *stages, int *smem, int *threads,
+                       int *tmem) {
+    if (kind == Kind::E2M1) mx_numbers<Kind::E2M1>(block_n, plain, stages, smem, threads, tmem);
+    else mx_numbers<Kind::E4M3>(block_n, plain, stages, smem, threads, tmem);
 }
 
 }  // namespace tg

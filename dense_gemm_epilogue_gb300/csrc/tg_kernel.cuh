@@ -197,6 +197,10 @@ struct GemmParams {
     int64_t stride_d;               // output elements between batch entries
     int32_t a_bmul, b_bmul;
     int32_t sfa_bmul, sfb_bmul;     // block-scaled kernel: scale-atom batch multipliers
+    // Block-scaled kernel with the plain-load producer: the role-space scale
+    // atoms and their batch strides in bytes (0: one set for every entry).
+    const void *sfa_ptr, *sfb_ptr;
+    int64_t sfa_stride, sfb_stride;
     // CTA-pair kernel: 1 = dynamic schedule (one cluster launched per tile;
     // running clusters take over clusters not yet started).
     int32_t dynamic;

@@ -37,6 +37,13 @@
 //     release the accumulator at once, and store from registers while the
 //     next tile's MMAs run;
 //   - no split-K tail, no multicast clusters.
+// With PLAIN = true (operand strides or bases the TMA cannot address), four
+// more warps per CTA copy each stage with bounds-checked plain loads (the
+// operands into the TMA's swizzled layout, zeros beyond K and beyond the
+// rows; the 512-byte scale atoms as they are, zeros past the last atom column
+// or row block), and every loader thread of both CTAs arrives on the pair
+// leader's stage-full barrier (the peer's remotely, with release semantics at
+// cluster scope).
 // Every wait is bounded as in the other kernels.
 #pragma once
 
@@ -87,6 +94,8 @@ struct MxConfig {
     static constexpr int EPI_WARPS = 8;
     static constexpr int NUM_WARPS = 2 + EPI_WARPS;
     static constexpr int NUM_THREADS = NUM_WARPS * 32;
+    static constexpr int LOAD_WARPS = 4;  // plain-load producer, after the others
+    static constexpr int threads(bool plain) { return (NUM_WARPS + (plain ? LOAD_WARPS : 0)) * 32; }
     static constexpr int MMAS_PER_STAGE = BK / T::umma_k;  // 4: one per scale block
     static constexpr int COLS = BN / 2;                      // columns per epilogue warp
     // Block-scaled instruction descriptor: B scale ID (bits 4-5, per MMA),
@@ -110,8 +119,27 @@ __device__ __forceinline__ uint32_t mx_idesc(uint32_t base, int kk) {
     return base | (id << 4) | (id << 29);
 }
 
-template <Kind KD, int BN>
-__global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
+// Plain-load copy of `count` 512-byte scale atoms, atom i taken from atom
+// column kg0 + (i % kgs) of row block rb0 + i / kgs of `src` (`kgroups`
+// columns, `rblocks` row blocks); atoms outside them read as zeros.  Thread
+// t of NT copies 16-byte chunks t, t + NT, ...
+template <int NT>
+__device__ __forceinline__ void load_atoms_plain(uint8_t *dst, const uint8_t *src, int count,
+                                                 int kgs, int64_t rb0, int64_t kg0,
+                                                 int64_t rblocks, int64_t kgroups, int tid) {
+    const int chunks = count * 32;  // 512 / 16 per atom
+    for (int c = tid; c < chunks; c += NT) {
+        const int i = c >> 5, w = c & 31;
+        const int64_t rb = rb0 + i / kgs, kg = kg0 + i % kgs;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (rb < rblocks && kg < kgroups)
+            v = *reinterpret_cast<const uint4 *>(src + ((rb * kgroups + kg) * 512 + w * 16));
+        *reinterpret_cast<uint4 *>(dst + c * 16) = v;
+    }
+}
+
+template <Kind KD, int BN, bool PLAIN>
+__global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
     tg_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_sfa,
@@ -142,7 +170,8 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar(C::FULL0 + s), 1);
+            // Plain loads: every loader thread of both CTAs arrives.
+            mbar_init(bar(C::FULL0 + s), PLAIN ? 2 * C::LOAD_WARPS * 32 : 1);
             mbar_init(bar(C::EMPTY0 + s), 1);
         }
         mbar_init(bar(C::ACCF), 1);
@@ -150,10 +179,12 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
         mbar_init(bar(C::DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tmap_a);
-        prefetch_tensormap(&tmap_b);
-        prefetch_tensormap(&tmap_sfa);
-        prefetch_tensormap(&tmap_sfb);
+        if (!PLAIN) {
+            prefetch_tensormap(&tmap_a);
+            prefetch_tensormap(&tmap_b);
+            prefetch_tensormap(&tmap_sfa);
+            prefetch_tensormap(&tmap_sfb);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -169,9 +200,54 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int nkb = p.num_k_blocks;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer (both CTAs)
-        if (lane == 0) {
+    if (PLAIN && warp >= C::NUM_WARPS) {
+        // ------------------------------------------------------ plain-load producer (both CTAs)
+        griddep_wait();
+        constexpr int NT = C::LOAD_WARPS * 32;
+        const int ltid = threadIdx.x - C::NUM_WARPS * 32;
+        // Operand rows and K in bytes (packed FP4: two elements per byte).
+        const int64_t lda_b = C::FP4 ? p.lda / 2 : p.lda, ldb_b = C::FP4 ? p.ldb / 2 : p.ldb;
+        const int64_t sa_b = C::FP4 ? p.stride_a / 2 : p.stride_a;
+        const int64_t sb_b = C::FP4 ? p.stride_b / 2 : p.stride_b;
+        const int32_t k_bytes = C::FP4 ? p.k / 2 : p.k;
+        const int64_t kgroups = ((int64_t)p.k + 127) / 128;  // atom columns
+        const int64_t rblocks_a = ((int64_t)p.m + BLOCK_M - 1) / BLOCK_M;
+        const int64_t rblocks_b = ((int64_t)p.n + BLOCK_M - 1) / BLOCK_M;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t t = pair; ok && t < p.num_tiles; t += num_pairs) {
+            int bt, mb, nb;
+            batch_tile_coords(t, p, bt, mb, nb);
+            const uint8_t *a_src = static_cast<const uint8_t *>(p.a_ptr) + (int64_t)bt * sa_b;
+            const uint8_t *b_src = static_cast<const uint8_t *>(p.b_ptr) + (int64_t)bt * sb_b;
+            const uint8_t *sfa_src =
+                static_cast<const uint8_t *>(p.sfa_ptr) + (int64_t)bt * p.sfa_stride;
+            const uint8_t *sfb_src =
+                static_cast<const uint8_t *>(p.sfb_ptr) + (int64_t)bt * p.sfb_stride;
+            const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
+            const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
+                load_stage_plain<1, BLOCK_M, NT>(smem + C::A_OFF + s * C::A_BYTES, a_src, lda_b,
+                                                 arow, p.m, kb * C::BK_UNITS, k_bytes, ltid);
+                load_stage_plain<1, C::B_ROWS, NT>(smem + C::B_OFF + s * C::B_BYTES, b_src, ldb_b,
+                                                   brow, p.n, kb * C::BK_UNITS, k_bytes, ltid);
+                load_atoms_plain<NT>(smem + C::SFA_OFF + s * C::SFA_BYTES, sfa_src, C::KGS, C::KGS,
+                                     mb * 2 + (int64_t)half, (int64_t)kb * C::KGS, rblocks_a,
+                                     kgroups, ltid);
+                load_atoms_plain<NT>(smem + C::SFB_OFF + s * C::SFB_BYTES, sfb_src,
+                                     C::KGS * C::SFB_ATOMS, C::KGS, (int64_t)nb * C::SFB_ATOMS,
+                                     (int64_t)kb * C::KGS, rblocks_b, kgroups, ltid);
+                fence_proxy_async_smem();
+                if (leader) mbar_arrive(bar(C::FULL0 + s));
+                else mbar_arrive_cluster(map_shared_rank(bar(C::FULL0 + s), 0));
+                if (++s == S) { s = 0; ph ^= 1; }
+            }
+        }
+    } else if (warp == 0) {
+        // ------------------------------------------------------ TMA producer (both CTAs)
+        if (!PLAIN && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int64_t issued = 0;
@@ -226,7 +302,11 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
+                    // Plain loads: the peer's loader threads completed the
+                    // phase by release arrivals at cluster scope.
+                    const bool got = PLAIN ? pair_wait_cluster(bar(C::FULL0 + s), ph, ctl, SITE_FULL)
+                                           : pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL);
+                    if (!got) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t slot = tmem_base + C::SF_COL0 + s * C::SLOT_COLS;
 #pragma unroll

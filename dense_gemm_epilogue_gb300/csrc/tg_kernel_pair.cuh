@@ -118,6 +118,22 @@ __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const P
     }
 }
 
+// pair_wait for a phase completed by release arrivals of the other CTA's
+// threads (acquire at cluster scope).
+__device__ __forceinline__ bool pair_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  const PairWaitCtl &c, uint32_t site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*c.abort_flag) return false;
+        if (globaltimer_ns() - t0 > c.limit_ns) {
+            pair_raise_abort(c, site);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void pair_pause_ns(uint64_t ns) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < ns) {

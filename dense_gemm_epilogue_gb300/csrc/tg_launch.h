@@ -17,7 +17,7 @@ struct LaunchArgs {
     CUtensorMap map_sfa; // block-scaled kernel: A-role scale atoms
     CUtensorMap map_sfb; // block-scaled kernel: B-role scale atoms
     int block_n;         // tile N: 64, 128 or 256 (single CTA); 128 or 256 (CTA pair)
-    bool plain_loads;    // plain bounds-checked loads instead of TMA (single CTA only)
+    bool plain_loads;    // plain bounds-checked loads instead of TMA (single-CTA and block-scaled kernels)
     bool pair;           // CTA-pair kernel (cta_group::2 MMA)
     int mc;              // pair kernel: pairs per cluster (1, or 2 with A multicast)
     int grid;            // persistent CTAs (even for the pair kernel)
@@ -40,6 +40,7 @@ cudaError_t launch_fill_empty_sum(void *d, int64_t m, int64_t n, int64_t ldc, in
                                   const EpiProgram &prog, int sms, cudaStream_t stream);
 // Threads, shared memory, stages and tensor-memory columns of a block-scaled
 // configuration (0 when the configuration does not exist).
-void mx_config_numbers(Kind kind, int block_n, int *stages, int *smem, int *threads, int *tmem);
+void mx_config_numbers(Kind kind, int block_n, bool plain, int *stages, int *smem, int *threads,
+                       int *tmem);
 
 }  // namespace tg

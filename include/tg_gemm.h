@@ -258,12 +258,13 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype,
  * where block kb covers k in [32*kb, 32*kb + 32) and each scale is a power of
  * two 2^(e-127) given by an 8-bit code e (e = 255 is NaN).  in_dtype is
  * TG_E4M3, TG_E5M2 or TG_E2M1 (both operands); A, B and D are laid out as for
- * tg_gemm (D of type out_dtype).  A and B must start 16-byte aligned and their
- * row strides (lda, ldb bytes) must be multiples of 16 (no plain-load
- * fallback here).  TG_E2M1 (FP4: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) is
- * packed two per byte, element 2t in the low nibble of byte t of its row;
- * lda, ldb and K count elements and must be even (so lda, ldb are multiples
- * of 32).
+ * tg_gemm (D of type out_dtype).  A and B whose base, row stride or batch
+ * stride (in bytes) is not a multiple of 16 run on a kernel variant whose
+ * producer warps load with plain bounds-checked loads (producer 2 in the
+ * plan; forcing producer 1 on them is TG_ERR_INVALID_VALUE).  TG_E2M1 (FP4:
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) is packed two per byte, element 2t
+ * in the low nibble of byte t of its row; lda, ldb, K (and batch strides)
+ * count elements and must be even.
  *
  * Scales (SFA for the M rows of A, SFB for the N columns of B) are stored as
  * "scale atoms": with R rows and KB = ceil(K/32) blocks, atom (rb, kg), for
@@ -275,10 +276,10 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype,
  * (zero is the usual fill).  tg_mx_pack_scales writes this layout from
  * row-major scales.
  *
- * opts may set block_n (128 or 256), swap_ab, raster_group and max_ctas; any
- * other field must be 0 (or the value that forces what this path does:
- * producer 1, cta_pair 2, split_k 1, multicast 1, prefetch_k -1).  Returns as
- * tg_gemm_ex.
+ * opts may set block_n (128 or 256), swap_ab, raster_group, max_ctas and
+ * producer (1 TMA, 2 plain loads); any other field must be 0 (or the value
+ * that forces what this path does: cta_pair 2, split_k 1, multicast 1,
+ * prefetch_k -1).  Returns as tg_gemm_ex.
  */
 tg_status tg_gemm_mx(int64_t M, int64_t N, int64_t K, float alpha,
                      const void *A, int64_t lda, const void *SFA,

@@ -278,10 +278,11 @@ def test_mx_scale_bytes(tg):
 
 
 @pytest.mark.parametrize("args", [
-    dict(dtype="bf16"), dict(dtype="tf32"), dict(lda=1000), dict(ldb=1000), dict(A=FAKE + 8),
+    dict(dtype="bf16"), dict(dtype="tf32"), dict(lda=1000), dict(ldb=1000),
+    dict(A=FAKE + 8, opts={"producer": 1}), dict(lda=1032, opts={"producer": 1}),
     dict(SFA=None), dict(SFB=FAKE + 4), dict(epi=2), dict(out=3), dict(ldc=9),
     dict(opts={"block_n": 64}), dict(opts={"cta_pair": 1}), dict(opts={"split_k": 2}),
-    dict(opts={"multicast": 2}), dict(opts={"producer": 2}), dict(opts={"l2_hint": 1}),
+    dict(opts={"multicast": 2}), dict(opts={"producer": 3}), dict(opts={"l2_hint": 1}),
 ])
 def test_mx_invalid_arguments_rejected_before_cuda(tg, args):
     a = dict(M=10, N=10, K=1024, A=FAKE, lda=1024, SFA=FAKE, B=FAKE, ldb=1024, SFB=FAKE, D=FAKE,
@@ -293,14 +294,16 @@ def test_mx_invalid_arguments_rejected_before_cuda(tg, args):
 
 
 @pytest.mark.parametrize("args", [
-    dict(lda=1025, ldb=1025), dict(K=1023, lda=1024, ldb=1024), dict(lda=1040), dict(ldb=1040),
+    dict(lda=1025, ldb=1025), dict(K=1023, lda=1024, ldb=1024),
+    dict(lda=1040, opts={"producer": 1}), dict(ldb=1040, opts={"producer": 1}),
 ])
 def test_mx_fp4_layout_rules(tg, args):
-    """Packed FP4: even lda, ldb and K; row strides of 16-byte multiples."""
-    a = dict(M=10, N=10, K=1024, lda=1024, ldb=1024)
+    """Packed FP4: even lda, ldb and K; the TMA producer, when forced, wants
+    row strides of 16-byte multiples."""
+    a = dict(M=10, N=10, K=1024, lda=1024, ldb=1024, opts=None)
     a.update(args)
     st = tg.tg_gemm_mx(a["M"], a["N"], a["K"], 1.0, FAKE, a["lda"], FAKE, FAKE, a["ldb"], FAKE,
-                       FAKE, 10, "e2m1", "f32", 1)
+                       FAKE, 10, "e2m1", "f32", 1, a["opts"])
     assert st == tg.TG_ERR_INVALID_VALUE
     # Only the block-scaled path takes FP4.
     assert tg.tg_gemm(10, 10, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 10, "e2m1", True) == \
@@ -326,8 +329,18 @@ def test_plan_mx(tg):
     assert s["swap_ab"] == 1
     small = tg.tg_plan_mx(300, 300, 256, 256, 256, 300, "e4m3", None, 152)
     assert small["grid"] == 2 * small["tiles"]
+    # lda not a 16-byte multiple: the plain-load producer on 256 x 128 tiles,
+    # four more warps; the TMA producer cannot be forced.
+    plain = tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", None, 152)
+    assert plain["producer"] == 2 and plain["block_n"] == 128
+    assert plain["threads"] == q["threads"] + 128
+    assert tg.tg_plan_mx(100, 100, 100, 112, 112, 100, "e4m3", None, 152)["producer"] == 1
+    fp4 = tg.tg_plan_mx(300, 200, 512, 514, 512, 300, "e2m1", None, 152)
+    assert fp4["producer"] == 2
+    wide = tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", {"block_n": 256}, 152)
+    assert wide["producer"] == 2 and wide["block_n"] == 256
     with pytest.raises(tg.TgError):
-        tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", None, 152)   # lda not 16-byte multiple
+        tg.tg_plan_mx(100, 100, 100, 100, 112, 100, "e4m3", {"producer": 1}, 152)
 
 
 def test_plan_dynamic_schedule(tg):
@@ -355,15 +368,17 @@ def test_epilogue_invalid_ops_rejected_before_cuda(tg, ops):
 
 
 @pytest.mark.parametrize("args", [
-    dict(ssfa=8), dict(ssfb=512 * 7), dict(ssfa=-512), dict(sa=8), dict(sb=-1024),
+    dict(ssfa=8), dict(ssfb=512 * 7), dict(ssfa=-512), dict(sb=-1024),
     dict(sd=90), dict(batch=-1), dict(ops=[(12, 0, 0, None)]), dict(dtype="bf16"),
-    dict(dtype="e2m1", sa=10 * 1024 + 1), dict(dtype="e2m1", sb=10 * 1024 + 16),
-    dict(opts={"split_k": 2}), dict(out=4), None,
+    dict(dtype="e2m1", sa=10 * 1024 + 1), dict(sa=8, opts={"producer": 1}),
+    dict(dtype="e2m1", sb=10 * 1024 + 16, opts={"producer": 1}),
+    dict(opts={"split_k": 2}), dict(out=4), None, dict(sa=8), dict(dtype="e2m1", sb=10 * 1024 + 16),
 ])
 def test_mx_batched_invalid_arguments_rejected_before_cuda(tg, args):
     """Scale strides: 0 or a multiple of 16 at least one entry's atoms;
-    operand strides of 16-byte multiples (even, for packed FP4); outputs
-    that do not overlap."""
+    operand batch strides even for packed FP4, and of 16-byte multiples when
+    the TMA producer is forced; outputs that do not overlap.  The last three
+    calls pass validation (and then need a device)."""
     fa = tg.tg_mx_scale_bytes(10, 1024)
     a = dict(sa=10 * 1024, ssfa=fa, sb=10 * 1024, ssfb=fa, sd=10 * 10, batch=3, dtype="e4m3",
              out="f32", ops=[], opts=None)
@@ -371,7 +386,7 @@ def test_mx_batched_invalid_arguments_rejected_before_cuda(tg, args):
     st = tg.tg_gemm_mx_batched(10, 10, 1024, 1.0, FAKE, 1024, a["sa"], FAKE, a["ssfa"], FAKE, 1024,
                                a["sb"], FAKE, a["ssfb"], FAKE, 10, a["sd"], a["batch"], a["dtype"],
                                a["out"], a["ops"], a["opts"])
-    if args is None:   # the unmodified call passes validation (and then needs a device)
+    if args is None or args in (dict(sa=8), dict(dtype="e2m1", sb=10 * 1024 + 16)):
         assert st != tg.TG_ERR_INVALID_VALUE
     else:
         assert st == tg.TG_ERR_INVALID_VALUE

@@ -132,6 +132,54 @@ def test_fp4_narrow_outputs_and_nan_scale():
     assert not np.any(np.isnan(np.delete(np.delete(got, 17, 0), 33, 1)))
 
 
+def _mx_plan(w, opts=None):
+    import dense_gemm_epilogue_gb300 as tg
+
+    lda, ldb, ldc = w.strides
+    return tg.tg_plan_mx(w.M, w.N, w.K, lda, ldb, ldc, w.dtype, opts, 0)
+
+
+@pytest.mark.parametrize("dtype,K,lda,ldb", [("e4m3", 1000, 1001, 1003), ("e5m2", 1000, 1000, 1024),
+                                             ("e2m1", 1100, 1102, 1106), ("e2m1", 384, 400, 386)])
+@pytest.mark.parametrize("block_n", [None, 256])
+def test_mx_plain_loads(dtype, K, lda, ldb, block_n):
+    """Row strides the TMA cannot address (odd byte strides included): the
+    plain-load producer warps of both CTAs fill the stages and the scale
+    atoms, ragged in every dimension; FP4 with K = 1100 and 384 leaves the
+    last stage's second atom column past the end (read as zeros)."""
+    w = si.Workload(f"mx_plain_{dtype}", 300, 390, K, dtype, 1.25, True, 530 + K + lda, "normal",
+                    lda=lda, ldb=ldb, ldc=303)
+    opts = {"block_n": block_n} if block_n else None
+    plan = _mx_plan(w, opts)
+    assert plan["producer"] == 2 and plan["block_n"] == (block_n or 128)
+    check_mx(w, opts=opts, repeats=2)
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_mx_plain_loads_swap_and_persistent(dtype):
+    """Plain loads under the role swap, and with several tiles per pair."""
+    lda = 514 if dtype == "e2m1" else 517
+    w = si.Workload("mx_plain_swap", 64, 900, 512, dtype, -0.5, False, 541, "normal", lda=lda,
+                    ldb=lda)
+    assert _mx_plan(w)["producer"] == 2 and _mx_plan(w)["swap_ab"] == 1
+    check_mx(w)
+    w = si.Workload("mx_plain_persist", 1100, 700, 768, dtype, 1.0, True, 542, "uniform",
+                    lda=lda + 256, ldb=lda + 258)
+    check_mx(w, opts={"max_ctas": 6, "raster_group": 2})
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_mx_plain_matches_tma(dtype):
+    """Forcing the plain producer on TMA-legal operands gives the TMA
+    producer's result bit for bit (the same stages, the same MMA order)."""
+    w = mx_padded(si.Workload("mx_plain_same", 520, 600, 1024, dtype, 1.0, True, 543, "normal"))
+    A, B = si.make_operands(w)
+    SA, SB = si.make_mx_scales(w)
+    _, tma = run_mx(w, A, B, SA, SB, opts={"producer": 1})
+    _, plain = run_mx(w, A, B, SA, SB, opts={"producer": 2})
+    assert np.array_equal(tma[0], plain[0])
+
+
 @pytest.mark.parametrize("name", ["mx_e4m3_8192", "mx_e2m1_8192"])
 def test_mx_8192_full(name):
     check_mx(si.WORKLOADS[name])

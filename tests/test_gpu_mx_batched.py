@@ -64,6 +64,17 @@ def test_mx_batched_tile_configs_and_swap(swap, block_n):
     check_mx_batched(w, 3, ops=CHAIN, opts={"swap_ab": swap, "block_n": block_n})
 
 
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_mx_batched_plain_loads(dtype):
+    """Batch strides the TMA cannot address (A's entries 8 bytes off a
+    16-byte boundary, B's odd rows): the plain-load producer, per-entry and
+    shared scales."""
+    ld = 522 if dtype == "e2m1" else 517
+    w = si.Workload("mxb_plain", 260, 300, 512, dtype, 0.75, False, 670, "normal", lda=ld, ldb=ld)
+    check_mx_batched(w, 3, ops=CHAIN, pad_a=16 if dtype == "e2m1" else 8, repeats=2)
+    check_mx_batched(w, 3, out="bf16", share_b=True, share_sfb=True, pad_a=32, pad_sf=48)
+
+
 def test_mx_batched_many_entries_persistent():
     """More tiles than CTA pairs: entries interleave across the persistent grid."""
     w = si.Workload("mxb_many", 512, 512, 256, "e4m3", 1.0, False, 660, "uniform")
