@@ -10,6 +10,13 @@ stay resident in HBM; A + B (268 MB) and D (268 MB) are each larger than the
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
 only other arm), on a bounded sample of the same workload.
 
+Workloads whose inputs are smaller than twice the L2 (``--workload``, and the
+other configurations the default run also times, under ``other_workloads``)
+cycle through several device copies of their inputs and outputs between
+launches, so that no launch finds its inputs in L2; where that would take
+more than 16 copies (the small latency-bound shapes) the L2 is flushed by a
+256 MB write before each launch instead, with events around every launch.
+
 The library is single-GPU: some of its kernels load operand tiles with
 cluster-multicast TMA, which is used only by calls that run on one GPU.  The
 GPU arm therefore refuses to run with more than one GPU (``--gpus`` other
@@ -24,6 +31,7 @@ import argparse
 import csv
 import io
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -42,6 +50,13 @@ WORKLOAD = "c4_bf16_8192"
 METRIC = "bf16 GEMM+ReLU TFLOP/s at 8192³; % of GB300 dense BF16 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+L2_BYTES = 129e6
+FLUSH_BYTES = 256 << 20
+MAX_COPIES = 16
+# The other configurations of the library's workload table, timed after the
+# headline in the default run (20 launches each after 5 warm-up).
+OTHER_WORKLOADS = ["c1_bf16_65x97x73", "c2_tf32_256x128x512", "c3_fp16_4096",
+                   "c5a_bf16_16384x64x4096", "c5b_bf16_64x16384x4096", "c5c_bf16_8191x4097x1000"]
 
 
 def parse():
@@ -59,6 +74,8 @@ def parse():
                     help="output type of D (bf16/fp16 go through tg_gemm_batched)")
     ap.add_argument("--batch", type=int, default=1,
                     help="batch entries of the workload per step (tg_gemm_batched)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip timing the other configurations in the default run")
     ap.add_argument("--cpu-baseline", action="store_true",
                     help="time the oracle also for a non-default workload")
     return ap.parse_args()
@@ -104,10 +121,85 @@ def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1
         cfg["out"] = out
     e = si.element_bytes(w.dtype)
     ws = batch * ((w.M * w.K + w.K * w.N) * e + w.M * w.N * (4 if out == "f32" else 2))
-    cfg["l2"] = (f"working set {ws / 1e6:.0f} MB vs 129 MB L2" +
-                 ("; larger than L2, no flush" if ws > 129e6 else
-                  "; fits in L2: consecutive steps hit warm L2"))
+    ins = batch * (w.M * w.K + w.K * w.N) * e
+    n = input_copies(ins)
+    cfg["l2"] = (f"inputs {ins / 1e6:.3g} MB, working set {ws / 1e6:.3g} MB vs 129 MB L2; " +
+                 ("inputs larger than twice the L2, no flush" if n == 1 else
+                  f"launches cycle through {n} copies of inputs and output "
+                  f"({n * ins / 1e6:.0f} MB of inputs)" if n else
+                  "L2 flushed by a 256 MB write before each launch (events around each launch)"))
     return cfg
+
+
+def input_copies(in_bytes: float) -> int:
+    """Device copies of a workload's inputs (and output) that the timed
+    launches cycle through: 1 when the inputs alone are at least twice the
+    L2; else enough copies to reach that; 0 (flush the L2 before each launch
+    instead) when that would take more than MAX_COPIES."""
+    if in_bytes >= 2 * L2_BYTES:
+        return 1
+    n = math.ceil(2 * L2_BYTES / max(in_bytes, 1.0))
+    return n if n <= MAX_COPIES else 0
+
+
+def time_launches(torch, launch, n_sets: int, steps: int, stream, flush=None):
+    """Average milliseconds per launch of `launch(i)` over `steps` launches.
+    n_sets >= 1: back-to-back launches between two events on `stream`, launch
+    i on input set i % n_sets.  n_sets == 0: `flush` (a buffer larger than
+    the L2) is overwritten before every launch and events surround each
+    launch alone; the average of those."""
+    if n_sets:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            launch(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch(i)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+
+def roofline(w: si.Workload, ms: float, peaks: dict, sustained: bool, out: str = "f32",
+             nbat: int = 1) -> dict:
+    """The workload's bound (tensor or HBM, by its arithmetic intensity
+    against the peaks' ridge point) and the fraction of that peak one launch
+    of `ms` milliseconds reaches.  TF32, the 8-bit and the 4-bit floats take
+    the BF16 peak times the nominal ratio to BF16 (1.1, 4.5 and 13.5 over
+    2.25 PFLOP/s)."""
+    flops = w.flops * nbat
+    alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * si.element_bytes(w.dtype) +
+                        w.M * w.N * (4 if out == "f32" else 2))
+    if w.block_scaled:
+        alg_bytes += nbat * (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
+    ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
+             "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
+    note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
+            "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
+    sustained = sustained and "bf16_tflops_sustained" in peaks
+    tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    tensor = flops / alg_bytes >= tpeak * 1e12 / (hbm * 1e9)
+    if tensor:
+        achieved, peak, unit = flops / (ms * 1e-3) / 1e12, tpeak, "TFLOP/s"
+        src = ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + note
+    else:
+        achieved, peak, unit = alg_bytes / (ms * 1e-3) / 1e9, hbm, "GB/s"
+        src = "hbm_gbs"
+    return {"bound": "tensor" if tensor else "hbm", "achieved": achieved, "peak": peak,
+            "unit": unit, "frac": achieved / peak, "peak_field": src,
+            "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": alg_bytes}
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -352,6 +444,15 @@ def run_gpu(args):
     else:
         plan = tg.tg_plan(w.M, w.N, w.K, dA, lda, dB, ldb, None, ldc, w.dtype)
     scale_inputs = {}
+    # Input sets the timed launches cycle through (see input_copies).
+    in_bytes = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+    n_sets = input_copies(in_bytes)
+    sets = [(dA, dB, dD)]
+    for _ in range(1, n_sets):
+        sets.append((dA.clone(), dB.clone(), torch.empty_like(dD)))
+        if mx:
+            scale_inputs[sets[-1][0].data_ptr()] = (dSA.clone(), dSB.clone())
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if n_sets == 0 else None
 
     def call(a_, b_, d_, st_):
         if mx:
@@ -363,14 +464,15 @@ def run_gpu(args):
                                       nbat, w.dtype, out, w.relu, None, st_)
         return tg.tg_gemm(w.M, w.N, w.K, w.alpha, a_, lda, b_, ldb, d_, ldc, w.dtype, w.relu, st_)
 
-    def step():
-        st = call(dA, dB, dD, stream)
+    def step(i=0):
+        a_, b_, d_ = sets[i % len(sets)]
+        st = call(a_, b_, d_, stream)
         if st != tg.TG_OK:
             raise tg.TgError(st, "tg_gemm")
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
 
     # The timed region: exactly `steps` back-to-back calls, one kernel launch
@@ -378,26 +480,16 @@ def run_gpu(args):
     # recorded between the launches, so each kernel's prologue overlaps the
     # previous one's tail (programmatic dependent launch) as in any sequence
     # of calls; the kernel's average launch duration is region / steps.
+    # (Inputs smaller than the L2: see input_copies and time_launches.)
     sampler = ClockSampler(0)
-    if sampler:
-        sampler.start()
-    region0 = torch.cuda.Event(enable_timing=True)
-    region1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark("t0")
-    region0.record(stream)
-    for i in range(args.steps):
-        step()
-    region1.record(stream)
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark("t1")
-    region_ms = region0.elapsed_time(region1)
+    sampler.start()
+    sampler.mark("t0")
+    region_ms = args.steps * time_launches(torch, step, n_sets, args.steps, stream, flush)
+    sampler.mark("t1")
     st, where = tg.tg_check_device_status(stream)
     if st != tg.TG_OK:
         raise tg.TgError(st, f"device status (wait site {where})")
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop()
 
     # A separate, untimed pass with events around every launch gives the
     # spread of single launches (an event between two launches stops the
@@ -407,7 +499,7 @@ def run_gpu(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_each)]
     for i in range(n_each):
         starts[i].record(stream)
-        step()
+        step(i)
         ends[i].record(stream)
     torch.cuda.synchronize()
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -471,41 +563,21 @@ def run_gpu(args):
     step_ms = region_ms / args.steps
 
     flops = w.flops * nbat
-    e_in = si.element_bytes(w.dtype)
-    alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * e_in + w.M * w.N * (4 if out == "f32" else 2))
-    if mx:
-        alg_bytes += (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
     value = flops / (step_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     launch_avg_ms = step_ms  # one kernel launch per step
     # Back-to-back launches for more than ~50 ms run in the power-capped
     # regime the sustained peak was measured in; a short burst compares
-    # with the burst peak.  TF32, the 8-bit and the
-    # 4-bit floats take the BF16 peak times the nominal ratio to BF16
-    # (1.1, 4.5 and 13.5 over 2.25 PFLOP/s).
-    ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
-             "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
-    ratio_note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
-                  "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
-    sustained = region_ms > 50.0 and "bf16_tflops_sustained" in peaks
-    tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
-    burst_tpeak = ratio * float(peaks["bf16_tflops"])
-    hbm = float(peaks["hbm_gbs"])
-    tensor_bound = flops / alg_bytes >= tpeak * 1e12 / (hbm * 1e9)
+    # with the burst peak.
+    sustained = region_ms > 50.0 and n_sets != 0 and "bf16_tflops_sustained" in peaks
+    rf = roofline(w, launch_avg_ms, peaks, sustained, out, nbat)
+    tensor_bound = rf["bound"] == "tensor"
     qs = sorted(launch_ms)
-    if tensor_bound:
-        unit_r = UNIT
-        achieved = flops / (launch_avg_ms * 1e-3) / 1e12
-        peak = tpeak
-    else:
-        unit_r = "GB/s"
-        achieved = alg_bytes / (launch_avg_ms * 1e-3) / 1e9
-        peak = hbm
     each = {"launches": len(launch_ms), "avg_ms": statistics.fmean(launch_ms),
             "p10_p50_p90_ms": [qs[len(qs) // 10], qs[len(qs) // 2], qs[(9 * len(qs)) // 10]],
             "how": "separate untimed pass after the timed region, events around every launch"}
     if tensor_bound and sustained:
-        each["frac_of_burst_peak"] = flops / (each["avg_ms"] * 1e-3) / 1e12 / burst_tpeak
+        each["frac_of_burst_peak"] = roofline(w, each["avg_ms"], peaks, False, out, nbat)["frac"]
     dt = w.dtype
     kname = ("tg_gemm_mx_kernel" if mx else
              "tg_gemm_pair_kernel" if plan.get("cta_pair") else "tg_gemm_kernel") + \
@@ -519,21 +591,21 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dt, "data": "synthetic", "config": workload_config(w, 1, out, nbat),
-        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
-                     "peak": peak, "unit": unit_r,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": (("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")
-                                     if tensor_bound else "hbm_gbs") + f" of {peak_src}" +
-                                    (ratio_note if tensor_bound else "") +
+        "roofline": {"bound": rf["bound"], "achieved": rf["achieved"],
+                     "peak": rf["peak"], "unit": rf["unit"],
+                     "frac": rf["frac"], "traffic": traffic,
+                     "peak_source": rf["peak_field"] + f" of {peak_src}" +
                                     (f" (the timed region ran {region_ms:.0f} ms of back-to-back "
                                      f"launches)" if tensor_bound and sustained else ""),
                      "kernel": kname,
                      "kernel_ms_avg": launch_avg_ms,
-                     "kernel_ms_how": "timed region / steps (one launch per step, events on "
-                                      "the launching stream around the region)",
+                     "kernel_ms_how": ("timed region / steps (one launch per step, events on "
+                                       "the launching stream around the region)" if n_sets else
+                                       "average of events around each launch, each after a "
+                                       "256 MB write that flushes the L2"),
                      "per_launch_events": each,
-                     "algorithmic_flops_per_launch": flops,
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     "algorithmic_flops_per_launch": rf["algorithmic_flops_per_launch"],
+                     "algorithmic_bytes_per_launch": rf["algorithmic_bytes_per_launch"]},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(hA.numel() * hA.element_size() +
                                           hB.numel() * hB.element_size() +
@@ -546,10 +618,68 @@ def run_gpu(args):
         "plan": plan,
         "library_source_hash": tg.source_hash(),
     }
+    if default_run and not args.no_others:
+        del sets, bufs, hDs
+        line["other_workloads"] = time_others(torch, tg, peaks, peak_src)
     if not args.no_cpu_baseline and (default_run or args.cpu_baseline):
         line["cpu_baseline"] = cpu_baseline(w, A, B)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def time_others(torch, tg, peaks: dict, peak_src: str, steps: int = 20, warmup: int = 5) -> dict:
+    """The other configurations through tg_gemm, each on its seeded inputs
+    (the same recipe as the headline's), `steps` launches after `warmup`,
+    timed as the headline (input copies or an L2 flush per input_copies),
+    against the burst peaks; clocks sampled over the whole pass."""
+    stream = torch.cuda.Stream()
+    sampler = ClockSampler(0)
+    sampler.start()
+    sampler.mark("t0")
+    rows = []
+    view = {"tf32": np.float32}
+    for name in OTHER_WORKLOADS:
+        w = si.WORKLOADS[name]
+        lda, ldb, ldc = w.strides
+        A, B = si.make_operands(w)
+        dA = torch.from_numpy(A.reshape(-1).view(view.get(w.dtype, np.int16))).cuda()
+        dB = torch.from_numpy(B.reshape(-1).view(view.get(w.dtype, np.int16))).cuda()
+        n_sets = input_copies(A.nbytes + B.nbytes)
+        sets = [(dA, dB, torch.empty((w.N, ldc), dtype=torch.float32, device="cuda"))]
+        for _ in range(1, n_sets):
+            sets.append((dA.clone(), dB.clone(), torch.empty_like(sets[0][2])))
+        flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if n_sets == 0
+                 else None)
+
+        def launch(i, sets=sets, w=w, lda=lda, ldb=ldb, ldc=ldc):
+            a_, b_, d_ = sets[i % len(sets)]
+            st = tg.tg_gemm(w.M, w.N, w.K, w.alpha, a_, lda, b_, ldb, d_, ldc, w.dtype, w.relu,
+                            stream)
+            if st != tg.TG_OK:
+                raise tg.TgError(st, "tg_gemm")
+
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                launch(i)
+        ms = time_launches(torch, launch, n_sets, steps, stream, flush)
+        st, where = tg.tg_check_device_status(stream)
+        if st != tg.TG_OK:
+            raise tg.TgError(st, f"device status (wait site {where})")
+        rf = roofline(w, ms, peaks, False)
+        rows.append({
+            "workload": name, "ms_per_launch": ms,
+            "value": w.flops / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac")},
+            "peak_source": rf["peak_field"] + f" of {peak_src}",
+            "l2": workload_config(w, 1)["l2"],
+            "plan": tg.tg_plan_describe(w.M, w.N, w.K, w.dtype, lda, ldb, ldc),
+        })
+        del sets, flush, dA, dB
+        torch.cuda.synchronize()
+    sampler.mark("t1")
+    return {"launches_each": steps, "warmup_each": warmup,
+            "how": "one configuration after another, after the headline's timed region",
+            "results": rows, "clocks": sampler.stop()}
 
 
 def main():
