@@ -123,6 +123,7 @@ class tg_plan_info(ctypes.Structure):
         ("stream_k", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
         ("k_rotate", ctypes.c_int32),
+        ("k_snake", ctypes.c_int32),
     ]
 
 

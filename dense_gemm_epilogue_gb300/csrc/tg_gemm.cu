@@ -318,6 +318,7 @@ struct Plan {
     int tmem_cols = 0;
     bool vector_store = false;
     bool k_rotate = false;   // single-CTA whole tiles: rotated K order per tile
+    bool k_snake = false;    // CTA-pair tiles: odd waves walk K in descending order
     int64_t mk = 0, nk = 0;  // role-space rows and cols
 };
 
@@ -614,6 +615,12 @@ tg_status make_plan(const Problem &q, const tg_options *o, int sms, Plan *plan) 
             p.split_segs = 1;
             p.grid = (int)(2 * p.tiles);
         }
+        // Many waves of 16-bit tiles: odd waves walk K downwards, so each
+        // wave starts on the K blocks the one before read last.  At 8192^3
+        // BF16 that cut DRAM reads from 0.99 to 0.87 GB per launch and the
+        // sustained launch time by 0.6 %; 4096^3 (static, 3.4 waves) and the
+        // 8-bit kinds (twice the bytes per second through L2) did not gain.
+        p.k_snake = p.ticket && elem_bytes(t) == 2;
     } else {
         if (o->schedule == 2) return TG_ERR_INVALID_VALUE;  // needs CTA-pair tiles
         int64_t grid = p.tiles < cap ? p.tiles : cap;
@@ -803,6 +810,7 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
     p.alpha = q.alpha;
     p.vector_store = plan.vector_store ? 1 : 0;
     p.k_rotate = (!la.pair && plan.k_rotate) ? 1 : 0;
+    p.k_snake = (la.pair && plan.k_snake) ? 1 : 0;
     p.d = q.D;
     p.d_row_stride = plan.swap ? q.ldc : 1;
     p.d_col_stride = plan.swap ? 1 : q.ldc;
@@ -1157,6 +1165,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, c
     out->vector_store = p.vector_store ? 1 : 0;
     out->schedule = p.dynamic ? 2 : p.stream_k ? 3 : p.ticket ? 4 : 1;
     out->k_rotate = p.k_rotate ? 1 : 0;
+    out->k_snake = p.k_snake ? 1 : 0;
     return TG_OK;
 }
 
@@ -1174,7 +1183,7 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, i
     } else {
         n = std::snprintf(buf, len,
                           "%s %dx%dx%d stages=%d producer=%s swap=%d grid=%d tiles=%lld raster=%d "
-                          "multicast=%d split=%dx%d schedule=%s k_rotate=%d vector_store=%d "
+                          "multicast=%d split=%dx%d schedule=%s k_rotate=%d k_snake=%d vector_store=%d "
                           "threads=%d smem=%d tmem=%d",
                           pi.cta_pair ? "pair" : "single", pi.block_m, pi.block_n, pi.block_k,
                           pi.stages, pi.producer == 1 ? "tma" : "plain", pi.swap_ab, pi.grid,
@@ -1184,7 +1193,8 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype, i
                           : pi.schedule == 3 ? "stream_k"
                           : pi.schedule == 4 ? "ticket"
                                              : "static",
-                          pi.k_rotate, pi.vector_store, pi.threads, pi.smem_bytes, pi.tmem_cols);
+                          pi.k_rotate, pi.k_snake, pi.vector_store, pi.threads, pi.smem_bytes,
+                          pi.tmem_cols);
     }
     return (n >= 0 && (size_t)n < len) ? TG_OK : TG_ERR_INVALID_VALUE;
 }

@@ -221,6 +221,11 @@ struct GemmParams {
     // so that the CTAs of a wave do not all read the same K offset of their
     // rows at the same time.  The summation order per tile stays fixed.
     int32_t k_rotate;
+    // CTA-pair kernel: 1 = tiles of odd waves (tile / pairs odd) walk their K
+    // blocks in descending order, so each wave starts on the K blocks the
+    // one before touched last (those most likely still in L2).  The order
+    // per tile stays fixed.
+    int32_t k_snake;
     EpiProgram epi;                 // composed epilogue (n = 0: alpha and ReLU only)
 };
 

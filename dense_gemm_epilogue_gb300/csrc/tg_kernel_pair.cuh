@@ -374,7 +374,9 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 const int32_t arow = mb * C::PAIR_M + (int32_t)half * BLOCK_M;
                 const int32_t brow = nb * BN + (int32_t)half * C::B_ROWS;
                 const int32_t ab = bt * p.a_bmul, bb = bt * p.b_bmul;
-                for (int kb = un.k0; kb < un.k1; ++kb) {
+                const bool down = p.k_snake && ((un.tile / num_pairs) & 1);
+                for (int i = 0; i < un.k1 - un.k0; ++i) {
+                    const int kb = down ? un.k1 - 1 - i : un.k0 + i;
                     if (!pair_wait(bar(C::EMPTY0 + s), ph ^ 1, ctl, SITE_EMPTY)) { ok = false; break; }
                     const uint32_t full_leader = map_shared_rank(bar(C::FULL0 + s), lead_rank);
                     if (leader) mbar_arrive_expect_tx(bar(C::FULL0 + s), 2 * (C::A_BYTES + C::B_BYTES));
@@ -426,7 +428,9 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = un.k0; kb < un.k1; ++kb) {
+                // K blocks in the producer's order (see k_snake); the first
+                // one initialises the accumulator.
+                for (int i = 0; i < un.k1 - un.k0; ++i) {
                     if (!pair_wait(bar(C::FULL0 + s), ph, ctl, SITE_FULL)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(PairConfig<KD, BN>::NUM_THREADS, 1)
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
                         mma_kind_pair<KD>(d_tmem, smem_desc_sw128(a0 + kk * 32),
                                      smem_desc_sw128(b0 + kk * 32), C::IDESC,
-                                     (kb != un.k0) || (kk != 0));
+                                     (i != 0) || (kk != 0));
                     }
                     // Every CTA of the cluster may write this stage (multicast).
                     mma_commit_pair_mcast(bar(C::EMPTY0 + s), ALL_CTAS);

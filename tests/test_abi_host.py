@@ -491,6 +491,22 @@ def test_plan_ticket_schedule(tg):
     assert plan(tg, si.WORKLOADS["c2_tf32_256x128x512"])["schedule"] == 3
 
 
+def test_plan_k_snake(tg):
+    """16-bit CTA-pair tiles under tickets alternate their K order by wave;
+    the static schedule, the 8-bit kinds, two-pair clusters and single-CTA
+    tiles keep ascending K."""
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["k_snake"] == 1
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"schedule": 1})["k_snake"] == 0
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"split_k": 1})["k_snake"] == 0
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"schedule": 2})["k_snake"] == 0
+    assert plan(tg, si.WORKLOADS["c3_fp16_4096"], opts={"schedule": 4})["k_snake"] == 1
+    for name in ("c3_fp16_4096", "f8_e4m3_8192", "c5c_bf16_8191x4097x1000",
+                 "c5a_bf16_16384x64x4096", "c1_bf16_65x97x73"):
+        assert plan(tg, si.WORKLOADS[name])["k_snake"] == 0, name
+    w = si.WORKLOADS["c4_bf16_8192"]
+    assert " k_snake=1 " in tg.tg_plan_describe(w.M, w.N, w.K, w.dtype, *w.strides, 152)
+
+
 def test_plan_k_rotate(tg):
     """One wave of single-CTA whole tiles walks each tile's K blocks from its
     own offset, where the operand the tiles share fits in L2."""

@@ -67,6 +67,9 @@ CASES = [
 def test_ticket_schedule_parity(tg, w, segs, extra):
     opts, p = find_cap(tg, w, segs, extra)
     assert p["cta_pair"] == 1 and p["multicast"] == 1
+    # 16-bit kinds: tiles of odd waves walk K downwards (k_snake).
+    assert p["k_snake"] == (1 if w.dtype in ("bf16", "fp16") else 0)
+    assert p["tiles"] >= p["grid"]  # at least one tile past the first wave
     check_full(w, opts=opts, repeats=3)
 
 

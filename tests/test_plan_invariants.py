@@ -166,8 +166,9 @@ def test_grid_cap_is_respected(tg):
 
 def test_block_scaled_plans_over_a_sweep(tg):
     """The block-scaled planner: CTA-pair tiles 256 x 128 or 256 x 256 over
-    all pairs of the device (fewer when there are fewer tiles), TMA only
-    (strides that are not multiples of 16 bytes, or odd FP4 rows, are refused)."""
+    all pairs of the device (fewer when there are fewer tiles); TMA for
+    strides of 16-byte multiples, the plain-load producer on 256 x 128 tiles
+    for the others (forcing TMA on them, or odd FP4 rows, are refused)."""
     rng = np.random.default_rng(31)
     for M, N, K, dtype, _, _, ldc, sms in shapes(seed=5, n=600):
         kind = str(rng.choice(["e4m3", "e5m2", "e2m1"]))
@@ -188,7 +189,10 @@ def test_block_scaled_plans_over_a_sweep(tg):
         t = p["tmem_cols"]
         assert 32 <= t <= 512 and t & (t - 1) == 0
         assert p["threads"] % 32 == 0 and p["threads"] <= 1024
-        # A stride that is not a multiple of 16 bytes has no plain-load path here.
+        # A stride that is not a multiple of 16 bytes: plain loads, four more warps.
         bad = ld + (2 if kind == "e2m1" else 1)
+        q = tg.tg_plan_mx(M, N, K, bad, ld, ldc, kind, None, sms)
+        assert q["producer"] == 2 and q["block_n"] == 128
+        assert q["threads"] == p["threads"] + 128 and q["tiles"] == cdiv(mk, 256) * cdiv(nk, 128)
         with pytest.raises(tg.TgError):
-            tg.tg_plan_mx(M, N, K, bad, ld, ldc, kind, None, sms)
+            tg.tg_plan_mx(M, N, K, bad, ld, ldc, kind, {"producer": 1}, sms)
