@@ -242,7 +242,7 @@ tg_status tg_plan(int64_t M, int64_t N, int64_t K,
  * planned as 256-byte aligned.  Writes at most `len` bytes into `buf`,
  * always NUL-terminated when len > 0, e.g.
  *   "pair 256x256x64 stages=7 producer=tma swap=0 grid=152 tiles=1024
- *    raster=8 multicast=1 split=36x2 schedule=ticket k_rotate=0 k_snake=1
+ *    raster=12 multicast=1 split=36x2 schedule=ticket k_rotate=0 k_snake=1
  *    vector_store=0 threads=320 smem=230768 tmem=512"   (one line)
  * or "empty" when M, N or K is 0.  Returns TG_OK; TG_ERR_INVALID_VALUE on
  * the argument errors of tg_plan, when buf is NULL or len is 0, or when the

@@ -219,7 +219,10 @@ def test_plan_overrides(tg):
     assert p["raster_group"] == 32                     # clamped to the M tile count
     p = plan(tg, w, opts={"raster_group": 1000, "cta_pair": 2})
     assert p["raster_group"] == 16                     # 256-row tiles
-    assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["raster_group"] == 8
+    # 8 M tiles per group for pair tiles; 12 under the alternating K order.
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"])["raster_group"] == 12
+    assert plan(tg, si.WORKLOADS["c4_bf16_8192"], opts={"schedule": 1})["raster_group"] == 8
+    assert plan(tg, si.WORKLOADS["c3_fp16_4096"])["raster_group"] == 8
     assert plan(tg, w, sms=7, opts={"cta_pair": 1})["grid"] == 7
     assert plan(tg, w, sms=7)["grid"] == 6             # pairs: 3 clusters of 2
 
