@@ -17,11 +17,14 @@ SOURCE = os.path.join(_HERE, "oracle_gemm.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
 
-_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
+_DTYPE_CODE = {"bf16": 0, "fp16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5, "nvf4": 5}
 _STORAGE = {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
-            "e5m2": np.uint8, "e2m1": np.uint8}
-# Elements per storage unit (E2M1: two per byte, low nibble first).
-_PER_UNIT = {"e2m1": 2}
+            "e5m2": np.uint8, "e2m1": np.uint8, "nvf4": np.uint8}
+# Elements per storage unit (E2M1: two per byte, low nibble first; "nvf4" is
+# E2M1 storage with 16-element unsigned-E4M3 block scales).
+_PER_UNIT = {"e2m1": 2, "nvf4": 2}
+# K elements per block scale.
+SCALE_BLOCK = {"e4m3": 32, "e5m2": 32, "e2m1": 32, "nvf4": 16}
 _OUT_CODE = {"f32": 0, "bf16": 1, "fp16": 2}
 EPI_KINDS = {"scale": 0, "add": 1, "relu": 2, "leaky_relu": 3, "clamp": 4, "sigmoid": 5,
              "silu": 6, "gelu_tanh": 7, "bias_row": 8, "bias_col": 9}
@@ -79,6 +82,11 @@ class Oracle:
         lib.orc_gemm_mx.restype = ip
         lib.orc_decode_e8m0_array.argtypes = [vp, i64, vp]
         lib.orc_decode_e8m0_array.restype = None
+        lib.orc_gemm_nvf4.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, vp, i64, vp, i64, ip,
+                                      vp, i64, vp, ip]
+        lib.orc_gemm_nvf4.restype = ip
+        lib.orc_decode_ue4m3_array.argtypes = [vp, i64, vp]
+        lib.orc_decode_ue4m3_array.restype = None
         lib.orc_gemm_epi.argtypes = [i64, i64, i64, dbl, vp, i64, vp, i64, ip, vp, vp, vp, vp, ip,
                                      vp, i64, vp, ip]
         lib.orc_gemm_epi.restype = ip
@@ -119,13 +127,15 @@ class Oracle:
         """Block-scaled D_ref (M, N) float64: FP8 operands as in ``gemm``, and
         one 8-bit exponent scale per 32 k, Xa(i,kb) = SA.flat[i*ldsa + kb],
         Xb(kb,j) = SB.flat[j*ldsb + kb] (uint8 codes).  For e2m1, A and B are
-        packed bytes and lda, ldb count elements (even)."""
+        packed bytes and lda, ldb count elements (even).  dtype "nvf4": packed
+        E2M1 with one unsigned-E4M3 scale per 16 k (orc_gemm_nvf4)."""
         A = _check_storage(A, dtype, "A")
         B = _check_storage(B, dtype, "B")
         per = _PER_UNIT.get(dtype, 1)
         SA = np.ascontiguousarray(SA, dtype=np.uint8)
         SB = np.ascontiguousarray(SB, dtype=np.uint8)
-        kb = (K + 31) // 32
+        blk = SCALE_BLOCK[dtype]
+        kb = (K + blk - 1) // blk
         if M and K and A.size * per < (M - 1) * lda + K:
             raise ValueError("A too small for (M, K, lda)")
         if N and K and B.size * per < (N - 1) * ldb + K:
@@ -136,19 +146,29 @@ class Oracle:
             raise ValueError("SB too small")
         Dt = np.zeros((max(N, 0), max(M, 0)), dtype=np.float64)
         St = np.zeros_like(Dt) if with_scale else None
-        rc = self.lib.orc_gemm_mx(M, N, K, float(alpha), A.ctypes.data, lda, SA.ctypes.data, ldsa,
-                                  B.ctypes.data, ldb, SB.ctypes.data, ldsb, _DTYPE_CODE[dtype],
-                                  int(bool(relu)), Dt.ctypes.data, max(M, 1),
-                                  St.ctypes.data if St is not None else None, int(threads))
+        sp = St.ctypes.data if St is not None else None
+        if dtype == "nvf4":
+            rc = self.lib.orc_gemm_nvf4(M, N, K, float(alpha), A.ctypes.data, lda, SA.ctypes.data,
+                                        ldsa, B.ctypes.data, ldb, SB.ctypes.data, ldsb,
+                                        int(bool(relu)), Dt.ctypes.data, max(M, 1), sp,
+                                        int(threads))
+        else:
+            rc = self.lib.orc_gemm_mx(M, N, K, float(alpha), A.ctypes.data, lda, SA.ctypes.data,
+                                      ldsa, B.ctypes.data, ldb, SB.ctypes.data, ldsb,
+                                      _DTYPE_CODE[dtype], int(bool(relu)), Dt.ctypes.data,
+                                      max(M, 1), sp, int(threads))
         if rc != 0:
-            raise ValueError(f"orc_gemm_mx failed with {rc}")
+            raise ValueError(f"block-scaled oracle failed with {rc}")
         return (Dt.T, St.T) if with_scale else Dt.T
 
-    def decode_scale(self, codes) -> np.ndarray:
-        """The oracle's decode of 8-bit exponent scale codes to float64."""
+    def decode_scale(self, codes, fmt: str = "e8m0") -> np.ndarray:
+        """The oracle's decode of scale codes to float64: 8-bit exponents
+        ("e8m0", the microscaling kinds) or unsigned E4M3 ("ue4m3", nvf4)."""
         x = np.ascontiguousarray(codes, dtype=np.uint8)
         out = np.zeros(x.shape, dtype=np.float64)
-        self.lib.orc_decode_e8m0_array(x.ctypes.data, x.size, out.ctypes.data)
+        fn = {"e8m0": self.lib.orc_decode_e8m0_array,
+              "ue4m3": self.lib.orc_decode_ue4m3_array}[fmt]
+        fn(x.ctypes.data, x.size, out.ctypes.data)
         return out
 
     @staticmethod
@@ -262,8 +282,8 @@ def gemm_epi(*args, **kw):
     return default().gemm_epi(*args, **kw)
 
 
-def decode_scale(codes):
-    return default().decode_scale(codes)
+def decode_scale(codes, fmt="e8m0"):
+    return default().decode_scale(codes, fmt)
 
 
 def decode(bits, dtype):

@@ -33,6 +33,10 @@
  * then apply as above.  Scales are stored one per row and block:
  *   Xa(i,kb) from SA[i*ldsa + kb],  Xb(kb,j) from SB[j*ldsb + kb],
  *   0 <= kb < ceil(K/32).
+ * orc_gemm_nvf4 is the same sum for the other published FP4 scaling (NVFP4):
+ * packed E2M1 operands, blocks of 16 consecutive k, and each scale an
+ * unsigned E4M3 code (4 exponent bits with bias 7, 3 fraction bits; code 0x7F
+ * is NaN; codes with the top bit set are not scales and are refused).
  *
  * Storage ("Walk through GEMM", section 2 "Bind runtime global arrays"):
  *   A logical (M,K), K-contiguous:  a(i,k) = A[i*lda + k]
@@ -400,8 +404,21 @@ double orc_decode_e8m0(uint8_t e) {
     return ldexp(1.0, (int)e - 127);
 }
 
+/*
+ * Unsigned E4M3 scale (NVFP4): code c = 0eeeemmm; e = 0 is subnormal,
+ * m/8 * 2^-6; otherwise (1 + m/8) * 2^(e-7); e = 15 with m = 7 is NaN.  The
+ * largest finite scale is 448, the smallest positive 2^-9.
+ */
+double orc_decode_ue4m3(uint8_t c) {
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    if (c & 0x80) return NAN;              /* not a scale code (refused by orc_gemm_nvf4) */
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) return ldexp((double)m, -9);
+    return ldexp((double)(8 + m), e - 10);
+}
+
 typedef struct {
-    int64_t M, K, KB;
+    int64_t M, K, KB, block;
     double alpha;
     int relu;
     const double *Ad, *Bd;   /* decoded, unscaled: Ad[i*K + k], Bd[j*K + k] */
@@ -422,8 +439,8 @@ static void *mx_worker(void *p) {
             const double *xa = jb->Xa + i * jb->KB;
             double s = 0.0, t = 0.0;
             for (int64_t kb = 0; kb < jb->KB; ++kb) {
-                int64_t k0 = kb * ORC_MX_BLOCK;
-                int64_t k1 = k0 + ORC_MX_BLOCK < jb->K ? k0 + ORC_MX_BLOCK : jb->K;
+                int64_t k0 = kb * jb->block;
+                int64_t k1 = k0 + jb->block < jb->K ? k0 + jb->block : jb->K;
                 double bs = 0.0, bt = 0.0;
                 for (int64_t k = k0; k < k1; ++k) {
                     bs += ai[k] * bj[k];
@@ -446,6 +463,41 @@ static void *mx_worker(void *p) {
  * scale per 32 k.  For E2M1, lda and ldb count elements and must be even.
  * Returns 0 on success, -1 on bad arguments, -2 on allocation failure.
  */
+/*
+ * The block-scaled sum over decoded operands and scales (block = k per
+ * scale), output columns split over threads; frees Ad, Bd, Xa, Xb.
+ */
+static int bs_run(int64_t M, int64_t N, int64_t K, int64_t KB, int64_t block, double alpha,
+                  int relu, double *Ad, double *Bd, double *Xa, double *Xb, double *D,
+                  int64_t ldd, double *scale, int nthreads);
+
+/* Decoded operands (K-contiguous rows of A, columns of B) and scales. */
+static int bs_decode(int64_t M, int64_t N, int64_t K, int64_t KB, const void *A, int64_t lda,
+                     const uint8_t *SA, int64_t ldsa, const void *B, int64_t ldb,
+                     const uint8_t *SB, int64_t ldsb, int dtype, double (*scale_of)(uint8_t),
+                     double **Ad, double **Bd, double **Xa, double **Xb) {
+    size_t kk = (size_t)(K ? K : 1), kbb = (size_t)(KB ? KB : 1);
+    *Ad = (double *)malloc(sizeof(double) * (size_t)M * kk);
+    *Bd = (double *)malloc(sizeof(double) * (size_t)N * kk);
+    *Xa = (double *)malloc(sizeof(double) * (size_t)M * kbb);
+    *Xb = (double *)malloc(sizeof(double) * (size_t)N * kbb);
+    if (!*Ad || !*Bd || !*Xa || !*Xb) {
+        free(*Ad); free(*Bd); free(*Xa); free(*Xb);
+        return -2;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        const int64_t row = i * lda;
+        for (int64_t k = 0; k < K; ++k) (*Ad)[i * K + k] = decode_elem(A, row + k, dtype);
+        for (int64_t kb = 0; kb < KB; ++kb) (*Xa)[i * KB + kb] = scale_of(SA[i * ldsa + kb]);
+    }
+    for (int64_t j = 0; j < N; ++j) {
+        const int64_t col = j * ldb;
+        for (int64_t k = 0; k < K; ++k) (*Bd)[j * K + k] = decode_elem(B, col + k, dtype);
+        for (int64_t kb = 0; kb < KB; ++kb) (*Xb)[j * KB + kb] = scale_of(SB[j * ldsb + kb]);
+    }
+    return 0;
+}
+
 int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
                 const void *A, int64_t lda, const uint8_t *SA, int64_t ldsa,
                 const void *B, int64_t ldb, const uint8_t *SB, int64_t ldsb,
@@ -456,22 +508,46 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
     if (dtype != ORC_E4M3 && dtype != ORC_E5M2 && dtype != ORC_E2M1) return -1;
     if (dtype == ORC_E2M1 && ((lda | ldb) & 1)) return -1;  /* rows start on whole bytes */
     if (M == 0 || N == 0) return 0;
-    size_t kk = (size_t)(K ? K : 1), kbb = (size_t)(KB ? KB : 1);
-    double *Ad = (double *)malloc(sizeof(double) * (size_t)M * kk);
-    double *Bd = (double *)malloc(sizeof(double) * (size_t)N * kk);
-    double *Xa = (double *)malloc(sizeof(double) * (size_t)M * kbb);
-    double *Xb = (double *)malloc(sizeof(double) * (size_t)N * kbb);
-    if (!Ad || !Bd || !Xa || !Xb) { free(Ad); free(Bd); free(Xa); free(Xb); return -2; }
-    for (int64_t i = 0; i < M; ++i) {
-        const int64_t row = i * lda;
-        for (int64_t k = 0; k < K; ++k) Ad[i * K + k] = decode_elem(A, row + k, dtype);
-        for (int64_t kb = 0; kb < KB; ++kb) Xa[i * KB + kb] = orc_decode_e8m0(SA[i * ldsa + kb]);
-    }
-    for (int64_t j = 0; j < N; ++j) {
-        const int64_t col = j * ldb;
-        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode_elem(B, col + k, dtype);
-        for (int64_t kb = 0; kb < KB; ++kb) Xb[j * KB + kb] = orc_decode_e8m0(SB[j * ldsb + kb]);
-    }
+    double *Ad, *Bd, *Xa, *Xb;
+    int rc = bs_decode(M, N, K, KB, A, lda, SA, ldsa, B, ldb, SB, ldsb, dtype, orc_decode_e8m0,
+                       &Ad, &Bd, &Xa, &Xb);
+    if (rc) return rc;
+    return bs_run(M, N, K, KB, ORC_MX_BLOCK, alpha, relu, Ad, Bd, Xa, Xb, D, ldd, scale,
+                  nthreads);
+}
+
+#define ORC_NV_BLOCK 16
+
+/*
+ * NVFP4 D_ref: packed E2M1 operands (lda, ldb count elements, even), one
+ * unsigned E4M3 scale per 16 k.  Returns 0, -1 on bad arguments (including
+ * a scale code with the top bit set), -2 on allocation failure.
+ */
+int orc_gemm_nvf4(int64_t M, int64_t N, int64_t K, double alpha,
+                  const void *A, int64_t lda, const uint8_t *SA, int64_t ldsa,
+                  const void *B, int64_t ldb, const uint8_t *SB, int64_t ldsb,
+                  int relu, double *D, int64_t ldd, double *scale, int nthreads) {
+    int64_t KB = (K + ORC_NV_BLOCK - 1) / ORC_NV_BLOCK;
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || ldd < M) return -1;
+    if (ldsa < KB || ldsb < KB || ((lda | ldb) & 1)) return -1;
+    if (M == 0 || N == 0) return 0;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t kb = 0; kb < KB; ++kb)
+            if (SA[i * ldsa + kb] & 0x80) return -1;
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t kb = 0; kb < KB; ++kb)
+            if (SB[j * ldsb + kb] & 0x80) return -1;
+    double *Ad, *Bd, *Xa, *Xb;
+    int rc = bs_decode(M, N, K, KB, A, lda, SA, ldsa, B, ldb, SB, ldsb, ORC_E2M1,
+                       orc_decode_ue4m3, &Ad, &Bd, &Xa, &Xb);
+    if (rc) return rc;
+    return bs_run(M, N, K, KB, ORC_NV_BLOCK, alpha, relu, Ad, Bd, Xa, Xb, D, ldd, scale,
+                  nthreads);
+}
+
+static int bs_run(int64_t M, int64_t N, int64_t K, int64_t KB, int64_t block, double alpha,
+                  int relu, double *Ad, double *Bd, double *Xa, double *Xb, double *D,
+                  int64_t ldd, double *scale, int nthreads) {
     if (nthreads <= 0) nthreads = orc_num_host_threads();
     if (nthreads > N) nthreads = (int)N;
     mx_job *jobs = (mx_job *)calloc((size_t)nthreads, sizeof(mx_job));
@@ -482,7 +558,7 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
     }
     for (int t = 0; t < nthreads; ++t) {
         mx_job *jb = &jobs[t];
-        jb->M = M; jb->K = K; jb->KB = KB; jb->alpha = alpha; jb->relu = relu;
+        jb->M = M; jb->K = K; jb->KB = KB; jb->block = block; jb->alpha = alpha; jb->relu = relu;
         jb->Ad = Ad; jb->Bd = Bd; jb->Xa = Xa; jb->Xb = Xb;
         jb->D = D; jb->ldd = ldd; jb->scale = scale;
         jb->j0 = N * t / nthreads;
@@ -585,6 +661,10 @@ int orc_gemm_epi(int64_t M, int64_t N, int64_t K, double alpha,
 /* Decode an array of scale codes (for the decode pins). */
 void orc_decode_e8m0_array(const uint8_t *src, int64_t n, double *dst) {
     for (int64_t q = 0; q < n; ++q) dst[q] = orc_decode_e8m0(src[q]);
+}
+
+void orc_decode_ue4m3_array(const uint8_t *src, int64_t n, double *dst) {
+    for (int64_t q = 0; q < n; ++q) dst[q] = orc_decode_ue4m3(src[q]);
 }
 
 /* Decode a whole array of storage elements (for the decode pins). */

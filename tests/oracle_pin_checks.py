@@ -658,6 +658,133 @@ def check_mx_nan_scale(orc):
     assert np.all(D[[0, 2]][:, [0, 1, 3]] == 32.0)
 
 
+# ---------------------------------------------------------------- NVFP4 (16-element E4M3 scales)
+
+def ue4m3_fraction(c: int) -> Fraction:
+    """Unsigned E4M3 scale code as an exact rational, from the format: 4
+    exponent bits (bias 7), 3 fraction bits, exponent 0 subnormal."""
+    e, m = (c >> 3) & 0xF, c & 7
+    if e == 0:
+        return Fraction(m, 8) * Fraction(1, 64)
+    return (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+def run_nv(orc, Alog, Blog, SAc, SBc, alpha, relu, pad_s=5, **kw):
+    """Alog (M,K), Blog (K,N) exact E2M1 values; SAc (M,KB), SBc (N,KB)
+    unsigned-E4M3 scale codes, KB = ceil(K/16).  Scale rows carry `pad_s`
+    codes of NaN (0x7F) padding, so a wrong block count or stride shows."""
+    M, K = Alog.shape
+    N = Blog.shape[1]
+    KB = SAc.shape[1]
+    A = mx_codes(Alog, "e2m1")
+    B = np.ascontiguousarray(mx_codes(Blog.T, "e2m1"))
+    ld = K + (K & 1)
+    ldsa = ldsb = KB + pad_s
+    SA = np.full((M, ldsa), 0x7F, dtype=np.uint8)
+    SB = np.full((N, ldsb), 0x7F, dtype=np.uint8)
+    SA[:, :KB] = SAc
+    SB[:, :KB] = SBc
+    return orc.gemm_mx(M, N, K, alpha, A, ld, SA, ldsa, B, ld, SB, ldsb, "nvf4", relu, **kw)
+
+
+def check_ue4m3_decode(orc):
+    """The 128 unsigned E4M3 codes against E4M3 decoded through numpy's
+    float16 (a second path), against exact rationals, and at the landmarks:
+    1 at 0x38, 448 at 0x7E, 2^-9 at 0x01, 2^-6 at 0x08, NaN at 0x7F."""
+    codes = np.arange(128, dtype=np.uint8)
+    got = orc.decode_scale(codes, "ue4m3")
+    want = e4m3_by_fp16(codes)
+    assert np.array_equal(got[:127], want[:127]) and math.isnan(got[127])
+    for c in range(127):
+        assert Fraction(got[c]) == ue4m3_fraction(c), c
+    assert (got[0x38], got[0x7E], got[0x01], got[0x08]) == (1.0, 448.0, 2.0 ** -9, 2.0 ** -6)
+    assert np.all(np.diff(got[:127]) > 0)
+
+
+def check_nvf4_bruteforce_exact(orc):
+    """Tiny problems with ragged last blocks against exact rational
+    arithmetic: 16-element blocks, each with its own pair of unsigned-E4M3
+    scales (non-powers of two included)."""
+    rng = np.random.default_rng(37)
+    for (M, N, K) in ((3, 4, 70), (2, 5, 16), (4, 3, 33), (1, 1, 2), (2, 2, 48)):
+        KB = (K + 15) // 16
+        SAc = rng.integers(0x20, 0x50, size=(M, KB)).astype(np.uint8)
+        SBc = rng.integers(0x20, 0x50, size=(N, KB)).astype(np.uint8)
+        Alog = rng.choice(FP4_GRID, size=(M, K))
+        Blog = rng.choice(FP4_GRID, size=(K, N))
+        for alpha, relu in ((1.0, False), (-0.75, True)):
+            D, S = run_nv(orc, Alog, Blog, SAc, SBc, alpha, relu, with_scale=True)
+            for i in range(M):
+                for j in range(N):
+                    s = Fraction(0)
+                    t = Fraction(0)
+                    for kb in range(KB):
+                        x = ue4m3_fraction(int(SAc[i, kb])) * ue4m3_fraction(int(SBc[j, kb]))
+                        ks = range(16 * kb, min(16 * kb + 16, K))
+                        s += x * sum((Fraction(Alog[i, k]) * Fraction(Blog[k, j]) for k in ks),
+                                     Fraction(0))
+                        t += x * sum((abs(Fraction(Alog[i, k]) * Fraction(Blog[k, j])) for k in ks),
+                                     Fraction(0))
+                    y = Fraction(alpha) * s
+                    if relu and y < 0:
+                        y = Fraction(0)
+                    assert Fraction(D[i, j]) == y, (M, N, K, i, j)
+                    assert Fraction(S[i, j]) == abs(Fraction(alpha)) * t
+
+
+def check_nvf4_block_boundaries(orc):
+    """A single nonzero in row i at column k: D(i,j) = b(k,j) * Xa(i, k // 16)
+    * Xb(k // 16, j) exactly, at every block edge."""
+    M, N, K = 2, 3, 70
+    KB = 5
+    SAc = np.array([[0x30 + 3 * kb + 5 * i for kb in range(KB)] for i in range(M)], dtype=np.uint8)
+    SBc = np.array([[0x44 - 2 * kb - 7 * j for kb in range(KB)] for j in range(N)], dtype=np.uint8)
+    for k in (0, 1, 15, 16, 17, 31, 32, 47, 48, 63, 64, 69):
+        Alog = np.zeros((M, K))
+        Alog[0, k] = 1.0
+        Alog[1, K - 1 - k] = -1.5
+        Bk = np.ones((K, N))
+        Bk[k, :] = 4.0
+        Bk[K - 1 - k, :] = 2.0 if K - 1 - k != k else 4.0
+        D = run_nv(orc, Alog, Bk, SAc, SBc, 1.0, False)
+        for j in range(N):
+            kb0, kb1 = k // 16, (K - 1 - k) // 16
+            want0 = Fraction(Bk[k, j]) * ue4m3_fraction(int(SAc[0, kb0])) * \
+                ue4m3_fraction(int(SBc[j, kb0]))
+            want1 = Fraction(-1.5) * Fraction(Bk[K - 1 - k, j]) * \
+                ue4m3_fraction(int(SAc[1, kb1])) * ue4m3_fraction(int(SBc[j, kb1]))
+            assert Fraction(D[0, j]) == want0 and Fraction(D[1, j]) == want1, (k, j)
+
+
+def check_nvf4_unit_scales_and_codes(orc):
+    """All scales 1 (code 0x38): the plain product of the E2M1 values (every
+    partial sum of these quarter-integers is exact in double, so numpy's
+    matmul gives it exactly) and the microscaling oracle with all scales 1;
+    a NaN scale (0x7F) makes its row NaN; a code with the top bit set is
+    refused."""
+    rng = np.random.default_rng(41)
+    M, N, K = 5, 4, 66
+    Alog = rng.choice(FP4_GRID, size=(M, K))
+    Blog = rng.choice(FP4_GRID, size=(K, N))
+    D = run_nv(orc, Alog, Blog, np.full((M, 5), 0x38, np.uint8), np.full((N, 5), 0x38, np.uint8),
+               1.25, False)
+    assert np.array_equal(D, 1.25 * (Alog @ Blog))
+    mx = run_mx(orc, Alog, Blog, np.full((M, 3), 127, np.uint8), np.full((N, 3), 127, np.uint8),
+                "e2m1", 1.25, False)
+    assert np.array_equal(D, mx)
+    SAc = np.full((M, 5), 0x38, np.uint8)
+    SAc[2, 4] = 0x7F
+    Dn = run_nv(orc, Alog, Blog, SAc, np.full((N, 5), 0x38, np.uint8), 1.25, False)
+    assert np.all(np.isnan(Dn[2])) and np.array_equal(np.delete(Dn, 2, 0), np.delete(D, 2, 0))
+    SAc[2, 4] = 0x80
+    try:
+        run_nv(orc, Alog, Blog, SAc, np.full((N, 5), 0x38, np.uint8), 1.25, False)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a scale code with the top bit set was accepted")
+
+
 # ---------------------------------------------------------------- composed pointwise epilogues
 
 def _epi_identity_case(vals):
@@ -769,6 +896,10 @@ ALL_CHECKS = [
     check_mx_block_boundaries,
     check_mx_scale_invariances,
     check_mx_nan_scale,
+    check_ue4m3_decode,
+    check_nvf4_bruteforce_exact,
+    check_nvf4_block_boundaries,
+    check_nvf4_unit_scales_and_codes,
     check_epi_pointwise_forms,
     check_epi_composition_and_bias,
     check_epi_nan,

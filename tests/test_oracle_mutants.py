@@ -67,8 +67,18 @@ MUTANTS = {
     "mx_only_a_scale": ("double x = xa[kb] * xb[kb];", "double x = xa[kb];"),
     "mx_block_shift": ("double x = xa[kb] * xb[kb];",
                        "double x = xa[kb] * xb[kb > 0 ? kb - 1 : 0];"),
-    "mx_wrong_row_scale": ("Xa[i * KB + kb] = orc_decode_e8m0(SA[i * ldsa + kb]);",
-                           "Xa[i * KB + kb] = orc_decode_e8m0(SA[(M - 1 - i) * ldsa + kb]);"),
+    "mx_wrong_row_scale": ("(*Xa)[i * KB + kb] = scale_of(SA[i * ldsa + kb]);",
+                           "(*Xa)[i * KB + kb] = scale_of(SA[(M - 1 - i) * ldsa + kb]);"),
+    "nv_block_32": ("#define ORC_NV_BLOCK 16", "#define ORC_NV_BLOCK 32"),
+    "nv_scales_as_exponents": ("ORC_E2M1,\n                       orc_decode_ue4m3, &Ad",
+                               "ORC_E2M1,\n                       orc_decode_e8m0, &Ad"),
+    "ue4m3_bias": ("return ldexp((double)(8 + m), e - 10);", "return ldexp((double)(8 + m), e - 11);"),
+    "ue4m3_subnormal": ("if (e == 0) return ldexp((double)m, -9);",
+                        "if (e == 0) return ldexp((double)m, -10);"),
+    "ue4m3_no_nan": ("if (e == 15 && m == 7) return NAN;", "if (0) return NAN;"),
+    "ue4m3_fraction_bits": ("return ldexp((double)(8 + m), e - 10);",
+                            "return ldexp((double)(16 + m), e - 11);"),
+    "nv_top_bit_accepted": ("if (SA[i * ldsa + kb] & 0x80) return -1;", "if (0) return -1;"),
     "mx_scale_abs_dropped": ("t += fabs(x) * bt;", "t += bt;"),
     "tf32_keeps_11_bits": ("uint32_t q = sig >> 13;           /* kept: 11 (or fewer) leading bits */\n"
                            "        uint32_t r = sig & 0x1FFFu;       /* dropped: 13 bits */\n"
