@@ -101,8 +101,12 @@ def single_gpu_refusal(args, world: int) -> str | None:
 def workload_config(w: si.Workload, world: int, out: str = "f32", batch: int = 1) -> dict:
     lda, ldb, ldc = w.strides
     scales = ""
-    if w.block_scaled:
-        lo, hi = si.MX_BENCH_SCALES
+    if w.block_scaled and w.dtype == "nvf4":
+        lo, hi = si.bench_scales(w.dtype)
+        scales = (f", one unsigned-E4M3 scale per 16 K (seeded codes 0x{lo:02X}..0x{hi:02X}: "
+                  f"0.25..4)")
+    elif w.block_scaled:
+        lo, hi = si.bench_scales(w.dtype)
         scales = (f", one 8-bit exponent scale per 32 K (seeded codes {lo}..{hi}: "
                   f"2^{lo - 127}..2^{hi - 127})")
     dist = ("N(0,1)" + (f"x{w.scale}" if w.scale != 1.0 else "") if w.dist == "normal"
@@ -181,12 +185,13 @@ def roofline(w: si.Workload, ms: float, peaks: dict, sustained: bool, out: str =
     flops = w.flops * nbat
     alg_bytes = nbat * ((w.M * w.K + w.K * w.N) * si.element_bytes(w.dtype) +
                         w.M * w.N * (4 if out == "f32" else 2))
-    if w.block_scaled:
-        alg_bytes += nbat * (w.M + w.N) * ((w.K + 31) // 32)   # one scale byte per 32 K
+    if w.block_scaled:   # one scale byte per block of K
+        alg_bytes += nbat * (w.M + w.N) * (-(-w.K // si.scale_block(w.dtype)))
     ratio = {"tf32": 1.1 / 2.25, "e4m3": 4.5 / 2.25, "e5m2": 4.5 / 2.25,
-             "e2m1": 13.5 / 2.25}.get(w.dtype, 1.0)
+             "e2m1": 13.5 / 2.25, "nvf4": 13.5 / 2.25}.get(w.dtype, 1.0)
     note = {"tf32": " x 1.1/2.25 (TF32)", "e4m3": " x 4.5/2.25 (FP8)",
-            "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
+            "e5m2": " x 4.5/2.25 (FP8)", "e2m1": " x 13.5/2.25 (FP4)",
+            "nvf4": " x 13.5/2.25 (FP4)"}.get(w.dtype, "")
     sustained = sustained and "bf16_tflops_sustained" in peaks
     tpeak = ratio * float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
     hbm = float(peaks["hbm_gbs"])
@@ -214,7 +219,7 @@ def oracle_sample_time(w: si.Workload, A, B, rows: int, cols: int, threads: int 
     As = np.ascontiguousarray(A[:rows])
     Bs = np.ascontiguousarray(B[:cols])
     if w.block_scaled:
-        SA, SB = si.make_mx_scales(si.with_shape(w, M=rows, N=cols), *si.MX_BENCH_SCALES)
+        SA, SB = si.make_mx_scales(si.with_shape(w, M=rows, N=cols))
         kb = SA.shape[1]
         t0 = time.perf_counter()
         oracle.gemm_mx(rows, cols, w.K, w.alpha, As, lda, SA, kb, Bs, ldb, SB, kb, w.dtype, w.relu,
@@ -254,7 +259,8 @@ def metric_name(w: si.Workload, nbat: int = 1, out: str = "f32") -> str:
     the same quantity (TFLOP/s) named by its type, epilogue and shape."""
     if w.name == WORKLOAD and nbat == 1 and out == "f32":
         return METRIC
-    return (f"{'block-scaled (32-element blocks) ' if w.block_scaled else ''}"
+    blocks = f"block-scaled ({si.scale_block(w.dtype)}-element blocks) " if w.block_scaled else ""
+    return (f"{blocks}"
             f"{w.dtype} GEMM{'+ReLU' if w.relu else ''} TFLOP/s at {w.M}x{w.N}x{w.K}"
             + (f" x{nbat}" if nbat > 1 else "") + (f", {out} out" if out != "f32" else ""))
 
@@ -415,7 +421,7 @@ def run_gpu(args):
     lda, ldb, ldc = w.strides
     A, B = si.make_operands(w)
     view = {"tf32": np.float32, "e4m3": np.uint8, "e5m2": np.uint8,
-            "e2m1": np.uint8}.get(w.dtype, np.int16)
+            "e2m1": np.uint8, "nvf4": np.uint8}.get(w.dtype, np.int16)
     hA = torch.from_numpy(np.tile(A.reshape(-1), nbat).view(view)).pin_memory()
     hB = torch.from_numpy(np.tile(B.reshape(-1), nbat).view(view)).pin_memory()
     dA = hA.cuda()
@@ -431,13 +437,15 @@ def run_gpu(args):
             raise SystemExit("block-scaled workloads run unbatched with FP32 output")
         # Scale atoms, packed on the device by the library from the seeded
         # row-major scales; they are inputs like A and B (uploaded in e2e).
-        SA, SB = si.make_mx_scales(w, *si.MX_BENCH_SCALES)
-        dSA = torch.empty(tg.tg_mx_scale_bytes(w.M, w.K), dtype=torch.uint8, device="cuda")
-        dSB = torch.empty(tg.tg_mx_scale_bytes(w.N, w.K), dtype=torch.uint8, device="cuda")
-        tg.check(tg.tg_mx_pack_scales(w.M, w.K, torch.from_numpy(SA).cuda(), SA.shape[1], dSA),
-                 "tg_mx_pack_scales")
-        tg.check(tg.tg_mx_pack_scales(w.N, w.K, torch.from_numpy(SB).cuda(), SB.shape[1], dSB),
-                 "tg_mx_pack_scales")
+        SA, SB = si.make_mx_scales(w)
+        dSA = torch.empty(tg.tg_bs_scale_bytes(w.M, w.K, w.dtype), dtype=torch.uint8,
+                          device="cuda")
+        dSB = torch.empty(tg.tg_bs_scale_bytes(w.N, w.K, w.dtype), dtype=torch.uint8,
+                          device="cuda")
+        tg.check(tg.tg_bs_pack_scales(w.M, w.K, w.dtype, torch.from_numpy(SA).cuda(), SA.shape[1],
+                                      dSA), "tg_bs_pack_scales")
+        tg.check(tg.tg_bs_pack_scales(w.N, w.K, w.dtype, torch.from_numpy(SB).cuda(), SB.shape[1],
+                                      dSB), "tg_bs_pack_scales")
         torch.cuda.synchronize()
         hSA, hSB = dSA.cpu().pin_memory(), dSB.cpu().pin_memory()
         plan = tg.tg_plan_mx(w.M, w.N, w.K, lda, ldb, ldc, w.dtype)

@@ -31,8 +31,9 @@ TG_TF32 = 2
 TG_E4M3 = 3
 TG_E5M2 = 4
 TG_E2M1 = 5
+TG_NVF4 = 6
 DTYPE_CODES = {"bf16": TG_BF16, "fp16": TG_FP16, "tf32": TG_TF32, "e4m3": TG_E4M3,
-               "e5m2": TG_E5M2, "e2m1": TG_E2M1}
+               "e5m2": TG_E5M2, "e2m1": TG_E2M1, "nvf4": TG_NVF4}
 
 TG_EPILOGUE_NONE = 0
 TG_EPILOGUE_RELU = 1
@@ -61,6 +62,8 @@ EXPORTED = (
     "tg_plan_mx",
     "tg_mx_scale_bytes",
     "tg_mx_pack_scales",
+    "tg_bs_scale_bytes",
+    "tg_bs_pack_scales",
 )
 
 
@@ -190,6 +193,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_mx_scale_bytes.restype = i64
         lib.tg_mx_pack_scales.argtypes = [i64, i64, vp, i64, vp, vp]
         lib.tg_mx_pack_scales.restype = ctypes.c_int
+        lib.tg_bs_scale_bytes.argtypes = [i64, i64, ctypes.c_int]
+        lib.tg_bs_scale_bytes.restype = i64
+        lib.tg_bs_pack_scales.argtypes = [i64, i64, ctypes.c_int, vp, i64, vp, vp]
+        lib.tg_bs_pack_scales.restype = ctypes.c_int
         lib.tg_version.argtypes = []
         lib.tg_version.restype = i32
         if path is None:
@@ -355,6 +362,17 @@ def tg_mx_scale_bytes(rows, K) -> int:
 def tg_mx_pack_scales(rows, K, src, ld_src, dst, stream=None) -> int:
     """Row-major scale codes (device) -> scale atoms (device)."""
     return load().tg_mx_pack_scales(rows, K, _ptr(src), ld_src, _ptr(dst), _stream(stream))
+
+
+def tg_bs_scale_bytes(rows, K, in_dtype) -> int:
+    return int(load().tg_bs_scale_bytes(rows, K, _dtype(in_dtype)))
+
+
+def tg_bs_pack_scales(rows, K, in_dtype, src, ld_src, dst, stream=None) -> int:
+    """Row-major scale codes (device) -> scale atoms (device), for in_dtype's
+    block size (32 K per scale; nvf4: 16)."""
+    return load().tg_bs_pack_scales(rows, K, _dtype(in_dtype), _ptr(src), ld_src, _ptr(dst),
+                                    _stream(stream))
 
 
 def tg_status_string(status: int) -> str:

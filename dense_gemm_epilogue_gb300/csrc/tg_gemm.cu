@@ -125,9 +125,15 @@ int elem_bytes(tg_dtype t) {
     return t == TG_TF32 ? 4 : (t == TG_E4M3 || t == TG_E5M2) ? 1 : 2;
 }
 
+// Packed 4-bit floats (two per byte), with either scaling.
+bool is_fp4(tg_dtype t) { return t == TG_E2M1 || t == TG_NVF4; }
+
 // K elements per pipeline stage: one 128-byte swizzle row of the type
 // (packed FP4: 256).
-int block_k(tg_dtype t) { return t == TG_E2M1 ? 256 : 128 / elem_bytes(t); }
+int block_k(tg_dtype t) { return is_fp4(t) ? 256 : 128 / elem_bytes(t); }
+
+// K elements per block scale (block-scaled types).
+int scale_k(tg_dtype t) { return t == TG_NVF4 ? 16 : 32; }
 
 bool known_dtype(tg_dtype t) {
     return t == TG_BF16 || t == TG_FP16 || t == TG_TF32 || t == TG_E4M3 || t == TG_E5M2;
@@ -687,7 +693,7 @@ bool encode_operand(CUtensorMap *map, tg_dtype t, const void *base, int64_t rows
                     int64_t ld, int64_t nb, int64_t sb, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    if (t == TG_E2M1) {  // packed FP4: described as bytes, two elements each
+    if (is_fp4(t)) {  // packed FP4: described as bytes, two elements each
         k = (k + 1) / 2;
         ld /= 2;
         sb /= 2;
@@ -871,8 +877,9 @@ tg_status run(const Problem &q, tg_epilogue epi, const tg_options *opts, void *s
 
 // ------------------------------------------------------------------ block-scaled products
 
-int64_t mx_scale_bytes(int64_t rows, int64_t K) {
-    return ceil_div(rows, tg::BLOCK_M) * ceil_div(K, 128) * 512;
+// Scale-atom bytes: 128 rows x 4 blocks per 512-byte atom.
+int64_t mx_scale_bytes(int64_t rows, int64_t K, tg_dtype t = TG_E4M3) {
+    return ceil_div(rows, tg::BLOCK_M) * ceil_div(K, 4 * scale_k(t)) * 512;
 }
 
 // Options the block-scaled path honours: tile N (128 or 256), role swap,
@@ -891,16 +898,16 @@ bool mx_options_ok(const tg_options *o) {
 
 // Scale-atom batch strides (bytes): 0 (one scale set for every entry), or a
 // multiple of 16 no smaller than one entry's atoms.
-bool mx_scale_stride_ok(int64_t stride, int64_t rows, int64_t K, int64_t batch) {
+bool mx_scale_stride_ok(int64_t stride, int64_t rows, int64_t K, int64_t batch, tg_dtype t) {
     if (batch <= 1 || stride == 0) return true;
-    return stride > 0 && stride % 16 == 0 && stride >= mx_scale_bytes(rows, K) &&
+    return stride > 0 && stride % 16 == 0 && stride >= mx_scale_bytes(rows, K, t) &&
            stride < (int64_t)(1ull << 40);
 }
 
 // Operands of a block-scaled product the TMA can address (rows and batch
 // entries 16-byte aligned, in bytes: packed FP4 holds two elements a byte).
 bool mx_tma_legal(const Problem &q) {
-    const bool fp4 = q.t == TG_E2M1;
+    const bool fp4 = is_fp4(q.t);
     const int64_t lda_b = fp4 ? q.lda / 2 : q.lda, ldb_b = fp4 ? q.ldb / 2 : q.ldb;
     const int64_t sa_b = fp4 ? q.sa / 2 : q.sa, sb_b = fp4 ? q.sb / 2 : q.sb;
     return tma_legal(q.A, lda_b, 1) && tma_legal(q.B, ldb_b, 1) &&
@@ -909,8 +916,8 @@ bool mx_tma_legal(const Problem &q) {
 
 tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sfb,
                       int64_t ssfb, const tg_options *o) {
-    if (q.t != TG_E4M3 && q.t != TG_E5M2 && q.t != TG_E2M1) return TG_ERR_INVALID_VALUE;
-    const bool fp4 = q.t == TG_E2M1;
+    if (q.t != TG_E4M3 && q.t != TG_E5M2 && !is_fp4(q.t)) return TG_ERR_INVALID_VALUE;
+    const bool fp4 = is_fp4(q.t);
     Problem qq = q;
     if (fp4) qq.t = TG_E4M3;  // the generic checks, on 1-byte storage
     tg_status st = validate(qq, nullptr);
@@ -919,7 +926,8 @@ tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const voi
     // Packed FP4: rows, batch entries and the reduction hold whole bytes.
     if (fp4 && ((q.lda | q.ldb | q.K) & 1)) return TG_ERR_INVALID_VALUE;
     if (fp4 && q.batch > 1 && ((q.sa | q.sb) & 1)) return TG_ERR_INVALID_VALUE;
-    if (!mx_scale_stride_ok(ssfa, q.M, q.K, q.batch) || !mx_scale_stride_ok(ssfb, q.N, q.K, q.batch))
+    if (!mx_scale_stride_ok(ssfa, q.M, q.K, q.batch, q.t) ||
+        !mx_scale_stride_ok(ssfb, q.N, q.K, q.batch, q.t))
         return TG_ERR_INVALID_VALUE;
     if (q.M > 0 && q.N > 0 && q.K > 0 && q.batch > 0) {
         // Operands the TMA cannot address run on the plain-load producer;
@@ -928,6 +936,12 @@ tg_status validate_mx(const Problem &q, const void *sfa, int64_t ssfa, const voi
         if (!sfa || !sfb || (uintptr_t)sfa % 16 || (uintptr_t)sfb % 16) return TG_ERR_INVALID_VALUE;
     }
     return TG_OK;
+}
+
+// Kernel kind of a block-scaled type.
+Kind mx_kind(tg_dtype t) {
+    return t == TG_E4M3 ? Kind::E4M3 : t == TG_E5M2 ? Kind::E5M2 : t == TG_E2M1 ? Kind::E2M1
+                                                                                : Kind::NVF4;
 }
 
 // CTA-pair tiles of 256 x 128 or 256 x 256: the candidate with the smaller
@@ -965,7 +979,7 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
     const int64_t mblocks = ceil_div(p.mk, 2 * tg::BLOCK_M);
     p.tiles_per_batch = mblocks * ceil_div(p.nk, p.block_n);
     p.tiles = (q.batch > 1 ? q.batch : 1) * p.tiles_per_batch;
-    tg::mx_config_numbers(q.t == TG_E2M1 ? Kind::E2M1 : Kind::E4M3, p.block_n, p.producer == 2,
+    tg::mx_config_numbers(mx_kind(q.t), p.block_n, p.producer == 2,
                           &p.stages, &p.smem, &p.threads, &p.tmem_cols);
     int64_t g = o->raster_group ? o->raster_group : 8;
     if (g > mblocks) g = mblocks;
@@ -982,11 +996,11 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
 // entries `stride` bytes apart (nb == 1: one entry); a box holds `box_kg` x
 // `box_rb` atoms of one entry (one K stage of one tile side), and columns or
 // row blocks past the end read as zeros.
-bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int64_t nb,
-                   int64_t stride, int box_kg, int box_rb) {
+bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int64_t atom_k,
+                   int64_t nb, int64_t stride, int box_kg, int box_rb) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const int64_t kg = ceil_div(K, 128), rb = ceil_div(rows, tg::BLOCK_M);
+    const int64_t kg = ceil_div(K, atom_k), rb = ceil_div(rows, tg::BLOCK_M);
     cuuint64_t dims[4] = {128, (cuuint64_t)kg, (cuuint64_t)rb, (cuuint64_t)nb};
     cuuint64_t strides[3] = {512, (cuuint64_t)(kg * 512),
                              (cuuint64_t)(nb > 1 ? stride : rb * kg * 512)};
@@ -1030,13 +1044,15 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     const bool many = q.batch > 1;
     const int64_t nba = many && sa ? q.batch : 1, nbb = many && sb ? q.batch : 1;
     const int64_t nsa = many && ssa ? q.batch : 1, nsb = many && ssb ? q.batch : 1;
-    const int kgs = block_k(q.t) / 128;  // scale-atom columns per K stage
+    const int atom_k = 4 * scale_k(q.t);       // K elements per scale-atom column
+    const int kgs = block_k(q.t) / atom_k;      // scale-atom columns per K stage
     la.plain_loads = plan.producer == 2;
     if (!la.plain_loads &&
         (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sa, tg::BLOCK_M) ||
          !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sb, plan.block_n / 2) ||
-         !encode_scales(&la.map_sfa, sar, plan.mk, q.K, nsa, ssa, kgs, 1) ||
-         !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, nsb, ssb, kgs, plan.block_n / tg::BLOCK_M)))
+         !encode_scales(&la.map_sfa, sar, plan.mk, q.K, atom_k, nsa, ssa, kgs, 1) ||
+         !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, atom_k, nsb, ssb, kgs,
+                        plan.block_n / tg::BLOCK_M)))
         return TG_ERR_INVALID_VALUE;
     la.block_n = plan.block_n;
     la.pair = true;
@@ -1085,9 +1101,7 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     log_plan("tg_gemm_mx", q, plan);
     la.device = dev;
     la.stream = stream;
-    const cudaError_t e = tg::launch_mx(la, q.t == TG_E4M3   ? Kind::E4M3
-                                            : q.t == TG_E5M2 ? Kind::E5M2
-                                                             : Kind::E2M1);
+    const cudaError_t e = tg::launch_mx(la, mx_kind(q.t));
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
@@ -1285,15 +1299,27 @@ tg_status tg_plan_mx(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, 
 }
 
 int64_t tg_mx_scale_bytes(int64_t rows, int64_t K) {
-    if (rows < 0 || K < 0) return -1;
-    return mx_scale_bytes(rows, K);
+    return tg_bs_scale_bytes(rows, K, TG_E4M3);
 }
 
 tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t ld_src,
                             uint8_t *dst, void *stream) {
-    const int64_t kblocks = ceil_div(K, 32);
+    return tg_bs_pack_scales(rows, K, TG_E4M3, src, ld_src, dst, stream);
+}
+
+int64_t tg_bs_scale_bytes(int64_t rows, int64_t K, tg_dtype in_dtype) {
+    if (rows < 0 || K < 0) return -1;
+    if (in_dtype != TG_E4M3 && in_dtype != TG_E5M2 && !is_fp4(in_dtype)) return -1;
+    return mx_scale_bytes(rows, K, in_dtype);
+}
+
+tg_status tg_bs_pack_scales(int64_t rows, int64_t K, tg_dtype in_dtype, const uint8_t *src,
+                            int64_t ld_src, uint8_t *dst, void *stream) {
+    if (in_dtype != TG_E4M3 && in_dtype != TG_E5M2 && !is_fp4(in_dtype))
+        return TG_ERR_INVALID_VALUE;
+    const int64_t kblocks = ceil_div(K, scale_k(in_dtype));
     if (rows < 0 || K < 0 || ld_src < (kblocks > 1 ? kblocks : 1)) return TG_ERR_INVALID_VALUE;
-    const int64_t total = mx_scale_bytes(rows, K);
+    const int64_t total = mx_scale_bytes(rows, K, in_dtype);
     if (total == 0) return TG_OK;
     if (!src || !dst) return TG_ERR_INVALID_VALUE;
     int dev = 0;
@@ -1304,7 +1330,7 @@ tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t
     const int64_t cap = (int64_t)ds->sms * 8;
     if (blocks > cap) blocks = cap;
     tg::tg_mx_pack_scales_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        src, rows, kblocks, ld_src, ceil_div(K, 128), total, dst);
+        src, rows, kblocks, ld_src, ceil_div(kblocks, 4), total, dst);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

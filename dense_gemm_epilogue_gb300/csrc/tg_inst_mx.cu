@@ -69,6 +69,7 @@ cudaError_t launch_mx(const LaunchArgs &a, Kind kind) {
     if (kind == Kind::E4M3) return launch_mx_kind<Kind::E4M3>(a);
     if (kind == Kind::E5M2) return launch_mx_kind<Kind::E5M2>(a);
     if (kind == Kind::E2M1) return launch_mx_kind<Kind::E2M1>(a);
+    if (kind == Kind::NVF4) return launch_mx_kind<Kind::NVF4>(a);
     return cudaErrorInvalidValue;
 }
 
@@ -88,6 +89,7 @@ static void mx_numbers(int block_n, bool plain, int *stages, int *smem, int *thr
 void mx_config_numbers(Kind kind, int block_n, bool plain, int *stages, int *smem, int *threads,
                        int *tmem) {
     if (kind == Kind::E2M1) mx_numbers<Kind::E2M1>(block_n, plain, stages, smem, threads, tmem);
+    else if (kind == Kind::NVF4) mx_numbers<Kind::NVF4>(block_n, plain, stages, smem, threads, tmem);
     else mx_numbers<Kind::E4M3>(block_n, plain, stages, smem, threads, tmem);
 }
 

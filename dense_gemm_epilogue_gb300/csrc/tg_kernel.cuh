@@ -50,7 +50,7 @@
 
 namespace tg {
 
-enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2, E4M3 = 3, E5M2 = 4, E2M1 = 5 };
+enum class Kind : int { BF16 = 0, FP16 = 1, TF32 = 2, E4M3 = 3, E5M2 = 4, E2M1 = 5, NVF4 = 6 };
 
 // Tensor-core instruction family of a kind.
 enum class MmaKind : int { F16, TF32, F8, F4 };
@@ -96,6 +96,14 @@ template <>
 struct KindTraits<Kind::E2M1> {
     static constexpr int block_k = 256, umma_k = 64;
     static constexpr uint32_t fmt = 1;  // E2M1 in the mxf4 format field
+    static constexpr MmaKind mma = MmaKind::F4;
+};
+// The same packed E2M1 operands with NVFP4 scaling (one unsigned-E4M3 scale
+// per 16 K elements; kind::mxf4nvf4).
+template <>
+struct KindTraits<Kind::NVF4> {
+    static constexpr int block_k = 256, umma_k = 64;
+    static constexpr uint32_t fmt = 1;  // E2M1 in the mxf4nvf4 format field
     static constexpr MmaKind mma = MmaKind::F4;
 };
 

@@ -23,6 +23,10 @@
 // column, so a stage carries one A atom per CTA and BN/128 B atoms; with
 // packed FP4 (E2M1) a stage holds 256 elements = two atom columns, and each
 // 64-wide MMA (kind::mxf4, two scales per row) reads bytes (0, 1) or (2, 3).
+// NVFP4 (Kind::NVF4: the same packed E2M1 operands, one unsigned-E4M3 scale
+// per 16 K elements) keeps the atom layout with 16-element blocks: an atom
+// column covers 64 K, a stage four of them, and each 64-wide MMA
+// (kind::mxf4nvf4, scale_vec::4X) reads all four bytes of its column's word.
 //
 // Differences from the CTA-pair kernel of tg_kernel_pair.cuh:
 //   - each stage also lands its scale atoms (TMA, 512 bytes each); each CTA
@@ -55,7 +59,8 @@ namespace tg {
 template <Kind KD, int BN>
 struct MxConfig {
     using T = KindTraits<KD>;
-    static constexpr bool FP4 = T::mma == MmaKind::F4;
+    static constexpr bool FP4 = T::mma == MmaKind::F4;   // packed E2M1 operands
+    static constexpr bool NV = KD == Kind::NVF4;         // 16-element unsigned-E4M3 scales
     static_assert(T::mma == MmaKind::F8 || FP4, "block scaling covers the 8- and 4-bit floats");
     static_assert(BN == 128 || BN == 256, "tile N: whole 128-row scale atoms");
     static constexpr int BK = T::block_k;                // K elements per stage (128 / 256)
@@ -63,7 +68,9 @@ struct MxConfig {
     static constexpr int PAIR_M = 2 * BLOCK_M;
     static constexpr int B_ROWS = BN / 2;
     static constexpr int SFB_ATOMS = BN / 128;           // B atoms per atom column
-    static constexpr int KGS = BK / 128;                 // atom columns per stage (4 blocks each)
+    static constexpr int SCALE_K = NV ? 16 : 32;         // K elements per scale
+    static constexpr int ATOM_K = 4 * SCALE_K;           // K elements per atom column
+    static constexpr int KGS = BK / ATOM_K;              // atom columns per stage (4 blocks each)
     static constexpr int ATOM_BYTES = 512;
     static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
@@ -83,9 +90,9 @@ struct MxConfig {
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
     // Tensor memory: the accumulator in columns [0, BN); then one scale slot
-    // per stage: A atoms at +4*kg .. +4*kg+3, B atoms from +8, atom column kg
-    // at +8 + 4*SFB_ATOMS*kg (+4 per row block).
-    static constexpr int SFB_COL = 8;
+    // per stage: A atoms at +4*kg .. +4*kg+3, B atoms from SFB_COL, atom
+    // column kg at SFB_COL + 4*SFB_ATOMS*kg (+4 per row block).
+    static constexpr int SFB_COL = 4 * KGS > 8 ? 4 * KGS : 8;
     static constexpr int SFB_COLS = 4 * SFB_ATOMS * KGS;
     static constexpr int SLOT_COLS = (SFB_COL + SFB_COLS + 15) / 16 * 16;
     static constexpr int SF_COL0 = BN;
@@ -100,22 +107,27 @@ struct MxConfig {
     static constexpr int COLS = BN / 2;                      // columns per epilogue warp
     // Block-scaled instruction descriptor: B scale ID (bits 4-5, per MMA),
     // A/B formats (7-9, 10-12), K-major operands (15, 16 zero), N >> 3
-    // (17-22), scale type 8-bit exponent (bit 23), M >> 4 (24-28), A scale ID
-    // (29-30, per MMA).
+    // (17-22), scale type (bit 23: 1 = 8-bit exponent, 0 = unsigned E4M3),
+    // M >> 4 (24-28), A scale ID (29-30, per MMA).
     static constexpr uint32_t IDESC = (T::fmt << 7) | (T::fmt << 10) |
-                                      ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                                      ((uint32_t)(BN >> 3) << 17) | ((NV ? 0u : 1u) << 23) |
                                       ((uint32_t)(PAIR_M >> 4) << 24);
+    // MMA kk of a stage: the atom column holding its scales, and the byte of
+    // each 32-bit scale word it starts at (its K offset inside the column, in
+    // scale blocks): FP8 byte kk of column 0; MX FP4 bytes 0 / 2 of column
+    // kk / 2; NVFP4 the whole word of column kk.
+    __host__ __device__ static constexpr int atom_col(int kk) { return kk * T::umma_k / ATOM_K; }
+    __host__ __device__ static constexpr uint32_t scale_id(int kk) {
+        return (uint32_t)((kk * T::umma_k) % ATOM_K / SCALE_K);
+    }
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
     static_assert(STAGES >= 4, "pipeline depth");
     static_assert(USED_COLS <= 512, "tensor memory");
     static_assert(4 * KGS <= SFB_COL, "A atoms fit below the B atoms");
 };
 
-// Per-MMA descriptor: scale ID kk (one scale per 32 K; FP8) or 2*(kk % 2)
-// (two per 64 K; FP4) for both operands.
-template <bool FP4>
-__device__ __forceinline__ uint32_t mx_idesc(uint32_t base, int kk) {
-    const uint32_t id = FP4 ? (uint32_t)((kk & 1) * 2) : (uint32_t)kk;
+// Per-MMA descriptor: the same scale ID for both operands.
+__device__ __forceinline__ uint32_t mx_idesc(uint32_t base, uint32_t id) {
     return base | (id << 4) | (id << 29);
 }
 
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
         const int64_t sa_b = C::FP4 ? p.stride_a / 2 : p.stride_a;
         const int64_t sb_b = C::FP4 ? p.stride_b / 2 : p.stride_b;
         const int32_t k_bytes = C::FP4 ? p.k / 2 : p.k;
-        const int64_t kgroups = ((int64_t)p.k + 127) / 128;  // atom columns
+        const int64_t kgroups = ((int64_t)p.k + C::ATOM_K - 1) / C::ATOM_K;  // atom columns
         const int64_t rblocks_a = ((int64_t)p.m + BLOCK_M - 1) / BLOCK_M;
         const int64_t rblocks_b = ((int64_t)p.n + BLOCK_M - 1) / BLOCK_M;
         int s = 0;
@@ -323,13 +335,14 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
 #pragma unroll
                     for (int kk = 0; kk < C::MMAS_PER_STAGE; ++kk) {
                         // Atom column of this MMA's scale blocks within the stage.
-                        const int g = C::FP4 ? kk >> 1 : 0;
+                        const int g = C::atom_col(kk);
                         const uint32_t sfa = slot + 4 * g;
                         const uint32_t sfb = slot + C::SFB_COL + 4 * C::SFB_ATOMS * g;
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
                         const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
-                        const uint32_t id = mx_idesc<C::FP4>(C::IDESC, kk);
-                        if constexpr (C::FP4) mma_mxf4_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
+                        const uint32_t id = mx_idesc(C::IDESC, C::scale_id(kk));
+                        if constexpr (C::NV) mma_nvf4_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
+                        else if constexpr (C::FP4) mma_mxf4_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
                         else mma_mx_pair(tmem_base, ad, bd, id, sfa, sfb, (kb | kk) != 0);
                     }
                     mma_commit_pair_mcast(bar(C::EMPTY0 + s), 0x3);

@@ -354,6 +354,21 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// Same with NVFP4 scaling (kind::mxf4nvf4, scale_vec::4X): packed 4-bit
+// float operands, 64 K elements per MMA, four 16-element scale blocks of
+// unsigned E4M3, all four bytes of each scale word.
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X "
+        "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Copy 32 rows x 16 bytes of shared memory (described by `desc`) into
 // tensor-memory columns taddr .. taddr+3 of lanes 0-31, repeated in each of
 // the four 32-lane quarters; issued for the CTA pair (each CTA's own shared

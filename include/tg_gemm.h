@@ -80,7 +80,9 @@ typedef enum {
     TG_TF32 = 2,  /* FP32 storage, narrowed to TF32 in the kernel */
     TG_E4M3 = 3,  /* 8-bit float, 4 exponent / 3 fraction bits */
     TG_E5M2 = 4,  /* 8-bit float, 5 exponent / 2 fraction bits */
-    TG_E2M1 = 5   /* 4-bit float (2 exponent / 1 fraction bits), two per byte; tg_gemm_mx only */
+    TG_E2M1 = 5,  /* 4-bit float (2 exponent / 1 fraction bits), two per byte; tg_gemm_mx only */
+    TG_NVF4 = 6   /* TG_E2M1 storage with NVFP4 scaling: one unsigned-E4M3 scale per 16 K
+                     elements; tg_gemm_mx only */
 } tg_dtype;
 
 /* Output element type of tg_gemm_batched ("Matrix Multiplication", Step 4:
@@ -261,7 +263,12 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype,
  * where block kb covers k in [32*kb, 32*kb + 32) and each scale is a power of
  * two 2^(e-127) given by an 8-bit code e (e = 255 is NaN).  in_dtype is
  * TG_E4M3, TG_E5M2 or TG_E2M1 (both operands); A, B and D are laid out as for
- * tg_gemm (D of type out_dtype).  A and B whose base, row stride or batch
+ * tg_gemm (D of type out_dtype).  TG_NVF4 is the other published FP4 scaling
+ * (NVFP4): TG_E2M1 operands, blocks of 16 consecutive K elements, and each
+ * scale an unsigned E4M3 code (4 exponent bits with bias 7, 3 fraction bits:
+ * (1 + m/8) * 2^(e-7), subnormal m/8 * 2^-6 for e = 0, code 0x7F NaN; codes
+ * with the top bit set are not scales and give undefined results) -- the
+ * sum above with 16 in place of 32.  A and B whose base, row stride or batch
  * stride (in bytes) is not a multiple of 16 run on a kernel variant whose
  * producer warps load with plain bounds-checked loads (producer 2 in the
  * plan; forcing producer 1 on them is TG_ERR_INVALID_VALUE).  TG_E2M1 (FP4:
@@ -270,14 +277,16 @@ tg_status tg_plan_describe(int64_t M, int64_t N, int64_t K, tg_dtype in_dtype,
  * count elements and must be even.
  *
  * Scales (SFA for the M rows of A, SFB for the N columns of B) are stored as
- * "scale atoms": with R rows and KB = ceil(K/32) blocks, atom (rb, kg), for
+ * "scale atoms": with R rows and KB = ceil(K/32) blocks (TG_NVF4:
+ * ceil(K/16)), atom (rb, kg), for
  * rows [128*rb, 128*rb + 128) and blocks [4*kg, 4*kg + 4), is 512 contiguous
  * bytes at byte offset (rb * ceil(KB/4) + kg) * 512, and the scale of row r,
  * block kb is at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + (kb % 4) of its
  * atom.  The buffer holds tg_mx_scale_bytes(R, K) bytes, 16-byte aligned;
- * entries for rows >= R or blocks >= KB are padding and must not be 255
- * (zero is the usual fill).  tg_mx_pack_scales writes this layout from
- * row-major scales.
+ * entries for rows >= R or blocks >= KB are padding and must not be NaN
+ * codes (zero is the usual fill).  tg_mx_pack_scales (32-element blocks) and
+ * tg_bs_pack_scales (any block-scaled type) write this layout from row-major
+ * scales; tg_mx_scale_bytes / tg_bs_scale_bytes size it.
  *
  * opts may set block_n (128 or 256), swap_ab, raster_group, max_ctas and
  * producer (1 TMA, 2 plain loads); any other field must be 0 (or the value
@@ -306,6 +315,17 @@ int64_t tg_mx_scale_bytes(int64_t rows, int64_t K);
  */
 tg_status tg_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *src, int64_t ld_src,
                             uint8_t *dst, void *stream);
+
+/* Bytes of the scale-atom buffer of in_dtype (TG_E4M3, TG_E5M2, TG_E2M1: one
+ * scale per 32 K; TG_NVF4: per 16) for `rows` rows and K; -1 on negative
+ * input or a type without block scales. */
+int64_t tg_bs_scale_bytes(int64_t rows, int64_t K, tg_dtype in_dtype);
+
+/* tg_mx_pack_scales for in_dtype's block size: row-major scales (row r,
+ * block kb at src[r*ld_src + kb], ld_src >= the block count) into
+ * tg_bs_scale_bytes(rows, K, in_dtype) bytes of scale atoms at dst. */
+tg_status tg_bs_pack_scales(int64_t rows, int64_t K, tg_dtype in_dtype, const uint8_t *src,
+                            int64_t ld_src, uint8_t *dst, void *stream);
 
 /*
  * Composed pointwise epilogue ("Walk through GEMM", section 5: the epilogue

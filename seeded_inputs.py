@@ -190,12 +190,19 @@ def pack_e2m1(codes: np.ndarray) -> np.ndarray:
 
 
 def element_bytes(dtype: str) -> float:
-    return {"bf16": 2, "fp16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e2m1": 0.5}[dtype]
+    return {"bf16": 2, "fp16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e2m1": 0.5,
+            "nvf4": 0.5}[dtype]
 
 
 def storage_numpy_dtype(dtype: str):
     return {"bf16": np.uint16, "fp16": np.uint16, "tf32": np.float32, "e4m3": np.uint8,
-            "e5m2": np.uint8, "e2m1": np.uint8}[dtype]
+            "e5m2": np.uint8, "e2m1": np.uint8, "nvf4": np.uint8}[dtype]
+
+
+def scale_block(dtype: str) -> int:
+    """K elements per block scale: 32 (8-bit exponent scales), or 16 for
+    "nvf4" (packed E2M1 with unsigned-E4M3 scales)."""
+    return 16 if dtype == "nvf4" else 32
 
 
 @dataclasses.dataclass(frozen=True)
@@ -218,7 +225,7 @@ class Workload:
     lda: int | None = None
     ldb: int | None = None
     ldc: int | None = None
-    block_scaled: bool = False  # microscaling: one 8-bit exponent scale per 32 K
+    block_scaled: bool = False  # one scale per 32 K (8-bit exponent) or per 16 K ("nvf4")
 
     @property
     def strides(self):
@@ -231,7 +238,8 @@ class Workload:
     @property
     def algorithmic_bytes(self) -> float:
         e = element_bytes(self.dtype)
-        scales = (self.M + self.N) * ((self.K + 31) // 32) if self.block_scaled else 0
+        kb = -(-self.K // scale_block(self.dtype))
+        scales = (self.M + self.N) * kb if self.block_scaled else 0
         return float((self.M * self.K + self.K * self.N) * e + scales + 4 * self.M * self.N)
 
 
@@ -260,6 +268,9 @@ WORKLOADS = {
     # The same with packed E2M1 (FP4) operands: N(0,1) rounded to E2M1.
     "mx_e2m1_8192": Workload("mx_e2m1_8192", 8192, 8192, 8192, "e2m1", 1.0, True, 9, "normal",
                              block_scaled=True),
+    # NVFP4: the same packed E2M1 operands, one unsigned-E4M3 scale per 16 K.
+    "nvf4_8192": Workload("nvf4_8192", 8192, 8192, 8192, "nvf4", 1.0, True, 10, "normal",
+                          block_scaled=True),
 }
 
 
@@ -307,7 +318,7 @@ def make_operands(w: Workload):
     stream 1 in (j, k) order.
     """
     lda, ldb, _ = w.strides
-    if w.dtype == "e2m1":
+    if w.dtype in ("e2m1", "nvf4"):
         # Packed FP4: rows of lda / 2 bytes (lda even), padding code +6.
         assert lda % 2 == 0 and ldb % 2 == 0, "E2M1 rows must hold an even number of elements"
         out = []
@@ -350,12 +361,23 @@ def scale_codes(seed: int, stream: int, rows: int, kblocks: int, lo: int, hi: in
 
 
 MX_BENCH_SCALES = (120, 134)   # codes of the benchmark's block scales: 2^-7 .. 2^7
+# Unsigned-E4M3 scale codes of "nvf4" workloads: 0x28 .. 0x48 = 0.25 .. 4,
+# every mantissa in between (0x7F would be NaN).
+NV_SCALES = (0x28, 0x48)
 
 
-def make_mx_scales(w: Workload, lo: int = 120, hi: int = 134):
-    """Row-major block scales (one per 32 K elements) for A's M rows and B's
-    N columns of workload ``w``: codes e in [lo, hi], value 2^(e-127)."""
-    kb = (w.K + 31) // 32
+def bench_scales(dtype: str):
+    return NV_SCALES if dtype == "nvf4" else MX_BENCH_SCALES
+
+
+def make_mx_scales(w: Workload, lo: int | None = None, hi: int | None = None):
+    """Row-major block scales (one per scale_block(w.dtype) K elements) for
+    A's M rows and B's N columns of workload ``w``: codes drawn uniformly from
+    [lo, hi] (default: bench_scales of the type)."""
+    dlo, dhi = bench_scales(w.dtype)
+    lo = dlo if lo is None else lo
+    hi = dhi if hi is None else hi
+    kb = -(-w.K // scale_block(w.dtype))
     return (scale_codes(w.seed, STREAM_SA, w.M, kb, lo, hi),
             scale_codes(w.seed, STREAM_SB, w.N, kb, lo, hi))
 

@@ -19,7 +19,7 @@ import numpy as np
 import seeded_inputs as si
 
 TOL_REL = {"bf16": 2.0 ** -7, "fp16": 2.0 ** -7, "tf32": 2.0 ** -9, "e4m3": 2.0 ** -7,
-           "e5m2": 2.0 ** -7, "e2m1": 2.0 ** -7}
+           "e5m2": 2.0 ** -7, "e2m1": 2.0 ** -7, "nvf4": 2.0 ** -7}
 TOL_ABS = 1e-6
 
 
@@ -201,12 +201,12 @@ def check_batched(w: si.Workload, batch: int, out: str, repeats=1, **kw):
 
 # ----------------------------------------------------------------- block-scaled (microscaling)
 
-def to_atoms(S: np.ndarray, K: int) -> np.ndarray:
-    """Row-major scale codes (R, >= ceil(K/32)) -> the scale-atom byte layout
-    of tg_gemm_mx: atom (rb, kg) at (rb * KG + kg) * 512, byte
+def to_atoms(S: np.ndarray, K: int, block: int = 32) -> np.ndarray:
+    """Row-major scale codes (R, >= ceil(K/block)) -> the scale-atom byte
+    layout of tg_gemm_mx: atom (rb, kg) at (rb * KG + kg) * 512, byte
     (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4 inside it; zero padding."""
     R = S.shape[0]
-    KB = (K + 31) // 32
+    KB = -(-K // block)
     RB, KG = -(-R // 128), -(-KB // 4)
     full = np.zeros((RB * 128, KG * 4), dtype=np.uint8)
     full[:R, :KB] = S[:, :KB]
@@ -219,7 +219,7 @@ def to_atoms(S: np.ndarray, K: int) -> np.ndarray:
 def mx_padded(w: si.Workload):
     """The workload with lda, ldb rounded up to TMA-legal strides: multiples
     of 16 bytes (16 FP8 or 32 packed FP4 elements)."""
-    q = 32 if w.dtype == "e2m1" else 16
+    q = 32 if w.dtype in ("e2m1", "nvf4") else 16
     rq = lambda x: -(-max(x, 1) // q) * q
     return si.with_shape(w, lda=w.lda or rq(w.K), ldb=w.ldb or rq(w.K))
 
@@ -233,10 +233,11 @@ def run_mx(w: si.Workload, A, B, SA, SB, out="f32", opts=None, repeats=1, D0=Non
 
     lda, ldb, ldc = w.strides
     dA, dB = torch_storage(A), torch_storage(B)
-    dSA = torch_storage(to_atoms(SA, w.K))
-    dSB = torch_storage(to_atoms(SB, w.K))
-    assert dSA.numel() == tg.tg_mx_scale_bytes(w.M, w.K)
-    assert dSB.numel() == tg.tg_mx_scale_bytes(w.N, w.K)
+    blk = si.scale_block(w.dtype)
+    dSA = torch_storage(to_atoms(SA, w.K, blk))
+    dSB = torch_storage(to_atoms(SB, w.K, blk))
+    assert dSA.numel() == tg.tg_bs_scale_bytes(w.M, w.K, w.dtype)
+    assert dSB.numel() == tg.tg_bs_scale_bytes(w.N, w.K, w.dtype)
     onp = {"f32": np.uint32, "bf16": np.uint16, "fp16": np.uint16}[out]
     if D0 is None:
         D0 = np.full((w.N, ldc), 0x7FC00002 if out == "f32" else 0x7FC3, dtype=onp)
@@ -254,7 +255,7 @@ def run_mx(w: si.Workload, A, B, SA, SB, out="f32", opts=None, repeats=1, D0=Non
     return D0, outs
 
 
-def check_mx(w: si.Workload, out="f32", opts=None, repeats=1, scale_range=(120, 134)):
+def check_mx(w: si.Workload, out="f32", opts=None, repeats=1, scale_range=None):
     """Whole-output parity of tg_gemm_mx against the oracle's block-scaled
     product: |D - D_ref| <= 2^-7 * |alpha| * sum_kb |Xa Xb| sum |a||b| + 1e-6
     (plus one output ulp for narrow outputs); padding untouched; repeats
@@ -264,11 +265,11 @@ def check_mx(w: si.Workload, out="f32", opts=None, repeats=1, scale_range=(120, 
     w = mx_padded(w)
     lda, ldb, ldc = w.strides
     A, B = si.make_operands(w)
-    SA, SB = si.make_mx_scales(w, *scale_range)
+    SA, SB = si.make_mx_scales(w, *(scale_range or (None, None)))
     D0, outs = run_mx(w, A, B, SA, SB, out=out, opts=opts, repeats=repeats)
     for o in outs[1:]:
         assert np.array_equal(o, outs[0]), "not deterministic"
-    KB = (w.K + 31) // 32
+    KB = -(-w.K // si.scale_block(w.dtype))
     ref, scale = oracle.gemm_mx(w.M, w.N, w.K, w.alpha, A, lda, SA, max(KB, 1), B, ldb, SB,
                                 max(KB, 1), w.dtype, w.relu, with_scale=True)
     store = outs[0]
@@ -392,7 +393,7 @@ def _bias_vectors(w: si.Workload, ops, bias_seed: int):
 
 def check_mx_batched(w: si.Workload, batch: int, out="f32", ops=(), share_a=False, share_b=False,
                      share_sfa=False, share_sfb=False, pad_a=0, pad_b=0, pad_sf=0, pad_d=0,
-                     opts=None, repeats=1, scale_range=(120, 134), bias_seed=7):
+                     opts=None, repeats=1, scale_range=None, bias_seed=7):
     """tg_gemm_mx_batched on `batch` entries drawn with seeds w.seed, w.seed+1,
     ... (operands and scales each either per entry or shared), against the
     oracle's block-scaled product of each entry followed by its op chain,
@@ -405,11 +406,12 @@ def check_mx_batched(w: si.Workload, batch: int, out="f32", ops=(), share_a=Fals
 
     w = mx_padded(w)
     lda, ldb, ldc = w.strides
-    per = 2 if w.dtype == "e2m1" else 1  # elements per storage byte
-    KB = (w.K + 31) // 32
+    per = 2 if w.dtype in ("e2m1", "nvf4") else 1  # elements per storage byte
+    blk = si.scale_block(w.dtype)
+    KB = -(-w.K // blk)
     ents = [si.with_shape(w, seed=w.seed + b) for b in range(batch)]
     ops_ = [si.make_operands(e) for e in ents]
-    scs = [si.make_mx_scales(e, *scale_range) for e in ents]
+    scs = [si.make_mx_scales(e, *(scale_range or (None, None))) for e in ents]
     pick = lambda lst, shared: [lst[0]] * batch if shared else lst
     A_list = pick([o[0] for o in ops_], share_a)
     B_list = pick([o[1] for o in ops_], share_b)
@@ -417,7 +419,7 @@ def check_mx_batched(w: si.Workload, batch: int, out="f32", ops=(), share_a=Fals
     SB_list = pick([s[1] for s in scs], share_sfb)
     sa = 0 if share_a else w.M * lda + pad_a
     sb = 0 if share_b else w.N * ldb + pad_b
-    fa, fb = tg.tg_mx_scale_bytes(w.M, w.K), tg.tg_mx_scale_bytes(w.N, w.K)
+    fa, fb = tg.tg_bs_scale_bytes(w.M, w.K, w.dtype), tg.tg_bs_scale_bytes(w.N, w.K, w.dtype)
     ssa = 0 if share_sfa else fa + pad_sf
     ssb = 0 if share_sfb else fb + pad_sf
     sd = w.N * ldc + pad_d
@@ -431,8 +433,8 @@ def check_mx_batched(w: si.Workload, batch: int, out="f32", ops=(), share_a=Fals
     ety = A_list[0].dtype
     A = pack(A_list, sa // per, A_list[0].size, ety)
     B = pack(B_list, sb // per, B_list[0].size, ety)
-    SA = pack([to_atoms(s, w.K) for s in SA_list], ssa, fa, np.uint8)
-    SB = pack([to_atoms(s, w.K) for s in SB_list], ssb, fb, np.uint8)
+    SA = pack([to_atoms(s, w.K, blk) for s in SA_list], ssa, fa, np.uint8)
+    SB = pack([to_atoms(s, w.K, blk) for s in SB_list], ssb, fb, np.uint8)
     host_ops, dev_ops, keep = _bias_vectors(w, ops, bias_seed)
     sentinel = {"f32": np.uint32(0x7FC00002), "bf16": np.uint16(0x7FC3), "fp16": np.uint16(0x7E03)}
     onp = np.uint32 if out == "f32" else np.uint16

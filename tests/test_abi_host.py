@@ -280,6 +280,42 @@ def test_mx_scale_bytes(tg):
     assert tg.tg_mx_scale_bytes(-1, 5) == -1
 
 
+def test_bs_scale_bytes(tg):
+    """Atoms of 128 rows x 4 blocks: 32-K blocks for the exponent-scaled
+    types, 16-K blocks for nvf4 (twice the atom columns)."""
+    for dt in ("e4m3", "e5m2", "e2m1"):
+        assert tg.tg_bs_scale_bytes(129, 129, dt) == tg.tg_mx_scale_bytes(129, 129) == 4 * 512
+    assert tg.tg_bs_scale_bytes(128, 64, "nvf4") == 512
+    assert tg.tg_bs_scale_bytes(128, 65, "nvf4") == 2 * 512
+    assert tg.tg_bs_scale_bytes(129, 129, "nvf4") == 2 * 3 * 512
+    assert tg.tg_bs_scale_bytes(8192, 8192, "nvf4") == 64 * 128 * 512
+    assert tg.tg_bs_scale_bytes(0, 100, "nvf4") == 0 and tg.tg_bs_scale_bytes(5, -1, "nvf4") == -1
+    for dt in ("bf16", "fp16", "tf32", 7):
+        assert tg.tg_bs_scale_bytes(10, 10, dt) == -1
+    assert tg.tg_bs_pack_scales(10, 64, "bf16", FAKE, 4, FAKE) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_bs_pack_scales(10, 64, "nvf4", FAKE, 3, FAKE) == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_bs_pack_scales(0, 64, "nvf4", None, 4, None) == tg.TG_OK
+
+
+@pytest.mark.parametrize("args", [
+    dict(K=1023, lda=1024, ldb=1024), dict(lda=1025, ldb=1025),
+    dict(lda=1040, opts={"producer": 1}), dict(opts={"block_n": 64}),
+])
+def test_nvf4_layout_rules(tg, args):
+    """NVFP4 takes the packed-FP4 rules: even K, lda, ldb; and only the
+    block-scaled entry points."""
+    a = dict(M=10, N=10, K=1024, lda=1024, ldb=1024, opts=None)
+    a.update(args)
+    st = tg.tg_gemm_mx(a["M"], a["N"], a["K"], 1.0, FAKE, a["lda"], FAKE, FAKE, a["ldb"], FAKE,
+                       FAKE, 10, "nvf4", "f32", 1, a["opts"])
+    assert st == tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_gemm(10, 10, 64, 1.0, FAKE, 64, FAKE, 64, FAKE, 10, "nvf4", True) == \
+        tg.TG_ERR_INVALID_VALUE
+    p = tg.tg_plan_mx(8192, 8192, 8192, 8192, 8192, 8192, "nvf4", None, 152)
+    assert (p["block_k"], p["tmem_cols"], p["cta_pair"]) == (256, 512, 1)
+    assert p["block_n"] in (128, 256) and p["stages"] >= 5
+
+
 @pytest.mark.parametrize("args", [
     dict(dtype="bf16"), dict(dtype="tf32"), dict(lda=1000), dict(ldb=1000),
     dict(A=FAKE + 8, opts={"producer": 1}), dict(lda=1032, opts={"producer": 1}),

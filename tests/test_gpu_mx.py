@@ -180,6 +180,65 @@ def test_mx_plain_matches_tma(dtype):
     assert np.array_equal(tma[0], plain[0])
 
 
-@pytest.mark.parametrize("name", ["mx_e4m3_8192", "mx_e2m1_8192"])
+@pytest.mark.parametrize("rows,K,ld", [(1, 2, 1), (200, 283, 18), (128, 64, 4), (513, 4100, 260)])
+def test_nvf4_pack_scales_matches_layout(rows, K, ld):
+    """16-element blocks: the block count and atom columns follow K / 16."""
+    import dense_gemm_epilogue_gb300 as tg
+
+    kb = (K + 15) // 16
+    S = si.scale_codes(6, 2, rows, ld, 0, 0x7E)
+    dst = torch_storage(np.full(tg.tg_bs_scale_bytes(rows, K, "nvf4"), 0xAB, dtype=np.uint8))
+    tg.check(tg.tg_bs_pack_scales(rows, K, "nvf4", torch_storage(S), ld, dst), "tg_bs_pack_scales")
+    assert np.array_equal(dst.cpu().numpy(), to_atoms(S[:, :kb], K, 16))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (1, 1, 2), (129, 65, 34), (300, 520, 1040),
+                                   (257, 255, 130), (513, 1000, 2048), (64, 1000, 512),
+                                   (300, 200, 18), (130, 260, 96), (200, 300, 4000)])
+def test_nvf4_shapes(M, N, K):
+    """NVFP4 (one unsigned-E4M3 scale per 16 K): ragged edges; K = 18, 34,
+    96 and 130 end inside an atom column (later columns of the last stage
+    read as zeros)."""
+    w = si.Workload("nvf4", M, N, K, "nvf4", 1.5, True, 800 + M + N + K, "normal", ldc=M + 3)
+    check_mx(w, repeats=2)
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("swap", [1, 2])
+def test_nvf4_tile_configs(block_n, swap):
+    w = si.Workload("nvf4_cfg", 600, 700, 1024, "nvf4", -0.75, False, 801, "normal")
+    check_mx(w, opts={"block_n": block_n, "swap_ab": swap})
+
+
+def test_nvf4_scale_range_outputs_and_nan_scale():
+    """Every finite scale code from the smallest subnormal to 448; narrow
+    outputs; a NaN scale code (0x7F) makes its row or column NaN."""
+    w = si.Workload("nvf4_out", 520, 600, 768, "nvf4", 0.5, True, 802, "normal")
+    check_mx(w, scale_range=(0x01, 0x7E))
+    check_mx(si.with_shape(w, seed=803, relu=False), out="bf16")
+    check_mx(si.with_shape(w, seed=804), out="fp16", scale_range=(0x30, 0x40))
+    w = mx_padded(si.Workload("nvf4_nan", 300, 200, 256, "nvf4", 1.0, True, 805, "normal"))
+    A, B = si.make_operands(w)
+    SA, SB = si.make_mx_scales(w)
+    SA[17, 3] = 0x7F
+    SB[33, 0] = 0x7F
+    _, outs = run_mx(w, A, B, SA, SB)
+    got = decode_out(outs[0][:, : w.M].view(np.float32).T, "f32")
+    assert np.all(np.isnan(got[17])) and np.all(np.isnan(got[:, 33]))
+    assert not np.any(np.isnan(np.delete(np.delete(got, 17, 0), 33, 1)))
+
+
+def test_nvf4_plain_loads_and_persistent():
+    """TMA-illegal rows (odd byte strides) on the plain-load producer, and
+    several tiles per CTA pair."""
+    w = si.Workload("nvf4_plain", 300, 390, 1100, "nvf4", 1.25, True, 806, "normal", lda=1102,
+                    ldb=1106, ldc=303)
+    assert _mx_plan(w)["producer"] == 2
+    check_mx(w, repeats=2)
+    w = si.Workload("nvf4_persist", 1100, 1300, 640, "nvf4", 1.0, True, 807, "normal")
+    check_mx(w, opts={"max_ctas": 6, "raster_group": 2})
+
+
+@pytest.mark.parametrize("name", ["mx_e4m3_8192", "mx_e2m1_8192", "nvf4_8192"])
 def test_mx_8192_full(name):
     check_mx(si.WORKLOADS[name])

@@ -29,7 +29,7 @@ def _library():
     tg.load()
 
 
-@pytest.mark.parametrize("dtype", ["e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2", "e2m1", "nvf4"])
 @pytest.mark.parametrize("M,N,K", [(300, 200, 320), (129, 65, 34), (257, 520, 1040)])
 def test_mx_batched_per_entry(dtype, M, N, K):
     w = si.Workload(f"mxb_{dtype}", M, N, K, dtype, 1.25, False, 610 + M + K, "normal",
