@@ -369,16 +369,17 @@ tg_status tg_gemm_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
  * Batched block-scaled GEMM with a composed epilogue: for b in [0, batch),
  *   D_b = out(op_n(... op_1(alpha * s_b)))
  * with s_b the block-scaled product of tg_gemm_mx on A_b = A + b*stride_a,
- * B_b = B + b*stride_b (elements; for TG_E2M1 the strides count elements and
- * must be even), scales SFA_b = SFA + b*stride_sfa and SFB_b = SFB +
+ * B_b = B + b*stride_b (elements; for TG_E2M1 and TG_NVF4 the strides count
+ * elements and must be even), scales SFA_b = SFA + b*stride_sfa and SFB_b = SFB +
  * b*stride_sfb (bytes), and D_b = D + b*stride_d (elements of out_dtype),
  * each as in tg_gemm_mx; ops as in tg_gemm_epilogue, the same for every
  * entry (a bias is indexed by the row or column within the entry).  Any of
  * stride_a, stride_b, stride_sfa, stride_sfb may be 0 (shared by every
  * entry); outputs may not overlap: stride_d >= ldc*N when batch > 1.  A
  * nonzero scale stride must be a multiple of 16 and at least the bytes of one
- * entry's atoms (tg_mx_scale_bytes); operand batch strides in bytes must be
- * multiples of 16.  batch == 0 launches nothing; K == 0 writes out(ops(0)).
+ * entry's atoms (tg_bs_scale_bytes); operand batch strides that are not
+ * 16-byte multiples run on the plain-load producer, as in tg_gemm_mx.
+ * batch == 0 launches nothing; K == 0 writes out(ops(0)).
  * opts as for tg_gemm_mx.  Returns as tg_gemm_mx and tg_gemm_epilogue.
  */
 tg_status tg_gemm_mx_batched(int64_t M, int64_t N, int64_t K, float alpha,
