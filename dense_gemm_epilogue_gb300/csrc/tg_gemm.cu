@@ -996,19 +996,33 @@ tg_status make_mx_plan(const Problem &q, const tg_options *o, int sms, Plan *pla
 // entries `stride` bytes apart (nb == 1: one entry); a box holds `box_kg` x
 // `box_rb` atoms of one entry (one K stage of one tile side), and columns or
 // row blocks past the end read as zeros.
+// With `rep`, a fifth dimension of four with byte stride 0 after the words:
+// one box then lands each atom four times over, the copies 512 bytes apart
+// (atom-major: the four copies of one atom, then the next row block's).
 bool encode_scales(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int64_t atom_k,
-                   int64_t nb, int64_t stride, int box_kg, int box_rb) {
+                   int64_t nb, int64_t stride, int box_kg, int box_rb, bool rep = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int64_t kg = ceil_div(K, atom_k), rb = ceil_div(rows, tg::BLOCK_M);
-    cuuint64_t dims[4] = {128, (cuuint64_t)kg, (cuuint64_t)rb, (cuuint64_t)nb};
-    cuuint64_t strides[3] = {512, (cuuint64_t)(kg * 512),
-                             (cuuint64_t)(nb > 1 ? stride : rb * kg * 512)};
-    cuuint32_t box[4] = {128, (cuuint32_t)box_kg, (cuuint32_t)box_rb, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t bstride = (cuuint64_t)(nb > 1 ? stride : rb * kg * 512);
+    CUresult r;
+    if (rep) {
+        cuuint64_t dims[5] = {128, 4, (cuuint64_t)kg, (cuuint64_t)rb, (cuuint64_t)nb};
+        cuuint64_t strides[4] = {0, 512, (cuuint64_t)(kg * 512), bstride};
+        cuuint32_t box[5] = {128, 4, (cuuint32_t)box_kg, (cuuint32_t)box_rb, 1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {128, (cuuint64_t)kg, (cuuint64_t)rb, (cuuint64_t)nb};
+        cuuint64_t strides[3] = {512, (cuuint64_t)(kg * 512), bstride};
+        cuuint32_t box[4] = {128, (cuuint32_t)box_kg, (cuuint32_t)box_rb, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -1046,13 +1060,16 @@ tg_status run_mx(const Problem &q, const void *sfa, int64_t ssfa, const void *sf
     const int64_t nsa = many && ssa ? q.batch : 1, nsb = many && ssb ? q.batch : 1;
     const int atom_k = 4 * scale_k(q.t);       // K elements per scale-atom column
     const int kgs = block_k(q.t) / atom_k;      // scale-atom columns per K stage
+    // FP8 at BN = 256: the kernel keeps each B atom four times over (its REP
+    // layout), loaded through a map with a repeating dimension.
+    const bool sfb_rep = !is_fp4(q.t) && plan.block_n == 256;
     la.plain_loads = plan.producer == 2;
     if (!la.plain_loads &&
         (!encode_operand(&la.map_a, q.t, ar, plan.mk, q.K, ldar, nba, sa, tg::BLOCK_M) ||
          !encode_operand(&la.map_b, q.t, br, plan.nk, q.K, ldbr, nbb, sb, plan.block_n / 2) ||
          !encode_scales(&la.map_sfa, sar, plan.mk, q.K, atom_k, nsa, ssa, kgs, 1) ||
          !encode_scales(&la.map_sfb, sbr, plan.nk, q.K, atom_k, nsb, ssb, kgs,
-                        plan.block_n / tg::BLOCK_M)))
+                        plan.block_n / tg::BLOCK_M, sfb_rep)))
         return TG_ERR_INVALID_VALUE;
     la.block_n = plan.block_n;
     la.pair = true;

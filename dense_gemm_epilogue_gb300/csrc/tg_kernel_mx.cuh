@@ -74,16 +74,28 @@ struct MxConfig {
     static constexpr int ATOM_BYTES = 512;
     static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;
     static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
+    // FP8 at BN = 256 (one atom column, two B row blocks): each B atom is
+    // stored four times over (2 KB: the 32 rows of the atom for each of the
+    // four 32-lane quarters), so that one 128-lane tcgen05.cp of 32-byte rows
+    // moves both B atoms -- two copies per stage instead of three, and a
+    // copy's tensor-pipe time goes by instruction, not by bytes.
+    static constexpr bool REP = !FP4 && SFB_ATOMS == 2;
+    static constexpr int REP_BYTES = 4 * ATOM_BYTES;     // one atom, four quarters
     static constexpr int SFA_BYTES = KGS * ATOM_BYTES;   // [kg][atom]
-    static constexpr int SFB_BYTES = KGS * SFB_ATOMS * ATOM_BYTES;  // [row block][kg][atom]
+    static constexpr int SFB_BYTES =                     // [row block][kg][atom] (x4 if REP)
+        KGS * SFB_ATOMS * ATOM_BYTES * (REP ? 4 : 1);
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int FIT = (SMEM_LIMIT - 2048) / STAGE_BYTES;
     static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-    static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = STAGES * A_BYTES;
-    static constexpr int SFA_OFF = B_OFF + STAGES * B_BYTES;
-    static constexpr int SFB_OFF = SFA_OFF + STAGES * SFA_BYTES;
-    static constexpr int BAR_OFF = SFB_OFF + STAGES * SFB_BYTES;
+    // Operand tiles (1024-byte aligned for the 128-byte swizzle) after the
+    // scales when REP, so that nothing a 4 KB scale copy reads lies past
+    // the end of shared memory; before them otherwise.
+    static constexpr int SCALE_REGION = STAGES * (SFA_BYTES + SFB_BYTES);
+    static constexpr int A_OFF = REP ? (SCALE_REGION + 1023) / 1024 * 1024 : 0;
+    static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+    static constexpr int SFB_OFF = REP ? 0 : B_OFF + STAGES * B_BYTES;
+    static constexpr int SFA_OFF = SFB_OFF + STAGES * SFB_BYTES;
+    static constexpr int BAR_OFF = REP ? B_OFF + STAGES * B_BYTES : SFA_OFF + STAGES * SFA_BYTES;
     static constexpr int FULL0 = 0, EMPTY0 = STAGES;
     static constexpr int ACCF = 2 * STAGES, ACCE = 2 * STAGES + 1, DRAIN = 2 * STAGES + 2;
     static constexpr int NUM_BARS = 2 * STAGES + 3;
@@ -121,6 +133,8 @@ struct MxConfig {
         return (uint32_t)((kk * T::umma_k) % ATOM_K / SCALE_K);
     }
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+    static_assert(A_OFF % 1024 == 0 && B_OFF % 1024 == 0, "swizzled operand tiles");
+    static_assert(!REP || KGS == 1, "replicated B atoms: one atom column per stage");
     static_assert(STAGES >= 4, "pipeline depth");
     static_assert(USED_COLS <= 512, "tensor memory");
     static_assert(4 * KGS <= SFB_COL, "A atoms fit below the B atoms");
@@ -248,9 +262,19 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
                 load_atoms_plain<NT>(smem + C::SFA_OFF + s * C::SFA_BYTES, sfa_src, C::KGS, C::KGS,
                                      mb * 2 + (int64_t)half, (int64_t)kb * C::KGS, rblocks_a,
                                      kgroups, ltid);
-                load_atoms_plain<NT>(smem + C::SFB_OFF + s * C::SFB_BYTES, sfb_src,
-                                     C::KGS * C::SFB_ATOMS, C::KGS, (int64_t)nb * C::SFB_ATOMS,
-                                     (int64_t)kb * C::KGS, rblocks_b, kgroups, ltid);
+                if constexpr (C::REP) {
+                    for (int a = 0; a < C::SFB_ATOMS; ++a)
+                        for (int c = 0; c < 4; ++c)
+                            load_atoms_plain<NT>(smem + C::SFB_OFF + s * C::SFB_BYTES +
+                                                     a * C::REP_BYTES + c * C::ATOM_BYTES,
+                                                 sfb_src, 1, 1, (int64_t)nb * C::SFB_ATOMS + a,
+                                                 (int64_t)kb, rblocks_b, kgroups, ltid);
+                } else {
+                    load_atoms_plain<NT>(smem + C::SFB_OFF + s * C::SFB_BYTES, sfb_src,
+                                         C::KGS * C::SFB_ATOMS, C::KGS,
+                                         (int64_t)nb * C::SFB_ATOMS, (int64_t)kb * C::KGS,
+                                         rblocks_b, kgroups, ltid);
+                }
                 fence_proxy_async_smem();
                 if (leader) mbar_arrive(bar(C::FULL0 + s));
                 else mbar_arrive_cluster(map_shared_rank(bar(C::FULL0 + s), 0));
@@ -287,11 +311,19 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
                     tma_load_3d_pair(a_stage(s), &tmap_a, full_leader, kb * C::BK_UNITS, arow, ab);
                     tma_load_3d_pair(b_stage(s), &tmap_b, full_leader, kb * C::BK_UNITS, brow, bb);
                     // One box per operand: the stage's KGS atom columns of the
-                    // CTA's A row block, and of the tile's SFB_ATOMS B row blocks.
+                    // CTA's A row block, and of the tile's SFB_ATOMS B row blocks
+                    // (REP: each B atom four times, one atom per box).
                     tma_load_4d_pair(sfa_stage(s), &tmap_sfa, full_leader, 0, kb * C::KGS, sfa_rb,
                                      sfa_b);
-                    tma_load_4d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, kb * C::KGS, sfb_rb,
-                                     sfb_b);
+                    if constexpr (C::REP) {
+                        // The map repeats each atom four times (a dimension of
+                        // stride 0): both B atoms, four copies each, in one box.
+                        tma_load_5d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, 0, kb, sfb_rb,
+                                         sfb_b);
+                    } else {
+                        tma_load_4d_pair(sfb_stage(s), &tmap_sfb, full_leader, 0, kb * C::KGS,
+                                         sfb_rb, sfb_b);
+                    }
                     ++issued;
                     if (++s == S) { s = 0; ph ^= 1; }
                 }
@@ -321,15 +353,25 @@ __global__ void __launch_bounds__(MxConfig<KD, BN>::threads(PLAIN), 1)
                     if (!got) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t slot = tmem_base + C::SF_COL0 + s * C::SLOT_COLS;
+                    if constexpr (C::REP) {
+                        // Both B atoms in one copy: lane L takes 32 bytes, row
+                        // L % 32 of atom 0 (columns +0..3) and of atom 1 (+4..7),
+                        // from the atoms' four-quarter copies 2 KB apart.
+                        tmem_cp_32x128b_x4_pair(slot, smem_desc_rows16(sfa_stage(s)));
+                        tmem_cp_128x256b_pair(slot + C::SFB_COL,
+                                              smem_desc_k2(sfb_stage(s), C::REP_BYTES));
+                    } else {
 #pragma unroll
-                    for (int g = 0; g < C::KGS; ++g) {
-                        tmem_cp_32x128b_x4_pair(slot + 4 * g,
-                                                smem_desc_rows16(sfa_stage(s) + g * C::ATOM_BYTES));
-#pragma unroll
-                        for (int a = 0; a < C::SFB_ATOMS; ++a)
+                        for (int g = 0; g < C::KGS; ++g) {
                             tmem_cp_32x128b_x4_pair(
-                                slot + C::SFB_COL + 4 * (g * C::SFB_ATOMS + a),
-                                smem_desc_rows16(sfb_stage(s) + (a * C::KGS + g) * C::ATOM_BYTES));
+                                slot + 4 * g, smem_desc_rows16(sfa_stage(s) + g * C::ATOM_BYTES));
+#pragma unroll
+                            for (int a = 0; a < C::SFB_ATOMS; ++a)
+                                tmem_cp_32x128b_x4_pair(
+                                    slot + C::SFB_COL + 4 * (g * C::SFB_ATOMS + a),
+                                    smem_desc_rows16(sfb_stage(s) +
+                                                     (a * C::KGS + g) * C::ATOM_BYTES));
+                        }
                     }
                     const uint32_t a0 = a_stage(s), b0 = b_stage(s);
 #pragma unroll

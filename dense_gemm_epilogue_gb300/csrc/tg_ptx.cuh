@@ -225,6 +225,18 @@ __device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
     return d;                            // layout type 0: no swizzle
 }
 
+// The same for rows of 32 bytes held as two 16-byte columns `col_bytes`
+// apart, each a dense block of 16-byte rows (leading byte offset: the next
+// 16 bytes of a row; stride byte offset: the next 8 rows).
+__device__ __forceinline__ uint64_t smem_desc_k2(uint32_t saddr, uint32_t col_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((col_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 }  // namespace tg
 
 // ------------------------------------------------------------------ clusters / CTA pairs
@@ -367,6 +379,14 @@ __device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, 
         "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
+}
+
+// Copy 128 rows x 32 bytes of shared memory (described by `desc`) into
+// tensor-memory columns taddr .. taddr+7 of lanes 0-127 (row L to lane L);
+// issued for the CTA pair.
+__device__ __forceinline__ void tmem_cp_128x256b_pair(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(desc)
+                 : "memory");
 }
 
 // Copy 32 rows x 16 bytes of shared memory (described by `desc`) into
@@ -523,6 +543,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
 }
 
 // 4-D CTA-pair load: coordinates (c0, c1, c2, c3), innermost first.
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, int32_t c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar_cluster, int32_t c0, int32_t c1,
                                                  int32_t c2, int32_t c3) {
