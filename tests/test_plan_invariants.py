@@ -118,6 +118,10 @@ def check_plan(p, M, N, K, dtype, lda, ldb, ldc, sms):
     assert p["stages"] >= 2
     if p["vector_store"]:
         assert swap
+    # Alternating K order: 16-bit pair tiles under tickets, and nowhere else.
+    assert p["k_snake"] == int(pair and p["schedule"] == 4 and dtype in ("bf16", "fp16"))
+    if p["k_rotate"]:
+        assert not pair and not p["stream_k"] and p["tiles"] <= g
 
 
 def test_plans_over_a_sweep_of_shapes(tg):
@@ -171,17 +175,18 @@ def test_block_scaled_plans_over_a_sweep(tg):
     for the others (forcing TMA on them, or odd FP4 rows, are refused)."""
     rng = np.random.default_rng(31)
     for M, N, K, dtype, _, _, ldc, sms in shapes(seed=5, n=600):
-        kind = str(rng.choice(["e4m3", "e5m2", "e2m1"]))
-        if kind == "e2m1":
+        kind = str(rng.choice(["e4m3", "e5m2", "e2m1", "nvf4"]))
+        fp4 = kind in ("e2m1", "nvf4")
+        if fp4:
             K += K & 1                                  # packed FP4: whole bytes per row
-        per16 = 32 if kind == "e2m1" else 16            # elements per 16 bytes
+        per16 = 32 if fp4 else 16                       # elements per 16 bytes
         ld = cdiv(K, per16) * per16 + per16 * int(rng.integers(0, 2))
         p = tg.tg_plan_mx(M, N, K, ld, ld, ldc, kind, None, sms)
         swap = M < 128 and N >= 128 and N >= 2 * M
         mk, nk = (N, M) if swap else (M, N)
         assert p["swap_ab"] == int(swap) and p["cta_pair"] == 1 and p["producer"] == 1
         assert p["block_m"] == 256 and p["block_n"] in (128, 256)
-        assert p["block_k"] == (256 if kind == "e2m1" else 128)
+        assert p["block_k"] == (256 if fp4 else 128)
         assert p["tiles"] == cdiv(mk, 256) * cdiv(nk, p["block_n"])
         assert p["grid"] == 2 * min(p["tiles"], max(1, sms // 2))
         assert 1 <= p["raster_group"] <= cdiv(mk, 256)
@@ -190,7 +195,7 @@ def test_block_scaled_plans_over_a_sweep(tg):
         assert 32 <= t <= 512 and t & (t - 1) == 0
         assert p["threads"] % 32 == 0 and p["threads"] <= 1024
         # A stride that is not a multiple of 16 bytes: plain loads, four more warps.
-        bad = ld + (2 if kind == "e2m1" else 1)
+        bad = ld + (2 if fp4 else 1)
         q = tg.tg_plan_mx(M, N, K, bad, ld, ldc, kind, None, sms)
         assert q["producer"] == 2 and q["block_n"] == 128
         assert q["threads"] == p["threads"] + 128 and q["tiles"] == cdiv(mk, 256) * cdiv(nk, 128)
